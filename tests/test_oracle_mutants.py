@@ -1,0 +1,79 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check that
+each one trips at least one pin. A pin set that a mistake slips through is not
+pinning that part of the oracle."""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import pins
+from oracle import core
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
+                   "gqa_oracle.c")
+
+# (name, text in gqa_oracle.c, replacement). Each replacement keeps every memory
+# access inside its buffer, so a mutant can only give wrong numbers.
+MUTANTS = [
+    ("head mapping h % Hkv", "int kvh = h / G;", "int kvh = h % s->Hkv;"),
+    ("causal: own position excluded", "int n = base_len[b] - seq_q + i + 1;",
+     "int n = base_len[b] - seq_q + i + (i > 0 ? 0 : 1);"),
+    ("causal: row index ignored", "int n = base_len[b] - seq_q + i + 1;",
+     "int n = base_len[b] - seq_q + 1;"),
+    ("scale divides", "w[j] = scale * dot;", "w[j] = (scale != 0.0 ? dot / scale : dot);"),
+    ("scale dropped", "w[j] = scale * dot;", "w[j] = dot;"),
+    ("no normalisation", "out[c] = num / den;", "out[c] = num;"),
+    ("value rows reversed", "num += w[j] * ld(s->v, row_index(s, b, kvh, j, s->dv, c), s->et);",
+     "num += w[j] * ld(s->v, row_index(s, b, kvh, n - 1 - j, s->dv, c), s->et);"),
+    ("value columns reversed", "num += w[j] * ld(s->v, row_index(s, b, kvh, j, s->dv, c), s->et);",
+     "num += w[j] * ld(s->v, row_index(s, b, kvh, j, s->dv, s->dv - 1 - c), s->et);"),
+    ("paged: rows reversed in block", "+ (j % s->bs)) * (size_t)d + c;",
+     "+ (s->bs - 1 - j % s->bs)) * (size_t)d + c;"),
+    ("rope: sign flipped", "x0 * cos(a) - x1 * sin(a)", "x0 * cos(a) + x1 * sin(a)"),
+    ("rope: exponent over pairs", "pow(theta, -2.0 * pr / rot_dim)", "pow(theta, -1.0 * pr / rot_dim)"),
+    ("rope: half-split pairs", "double x0 = ld(x, row + 2 * pr, et), x1 = ld(x, row + 2 * pr + 1, et);\n"
+     "          st(x, row + 2 * pr, et, x0 * cos(a) - x1 * sin(a));\n"
+     "          st(x, row + 2 * pr + 1, et, x0 * sin(a) + x1 * cos(a));",
+     "double x0 = ld(x, row + pr, et), x1 = ld(x, row + pr + rot_dim / 2, et);\n"
+     "          st(x, row + pr, et, x0 * cos(a) - x1 * sin(a));\n"
+     "          st(x, row + pr + rot_dim / 2, et, x0 * sin(a) + x1 * cos(a));"),
+    ("append: rotated at p+1", "int32_t pos = p;", "int32_t pos = p + 1;"),
+    ("append: next slot", "size_t dst_k = (((size_t)blk * Hkv + kvh) * bs + p % bs) * (size_t)dk;",
+     "size_t dst_k = (((size_t)blk * Hkv + kvh) * bs + (p + 1) % bs) * (size_t)dk;"),
+    ("append: length not advanced", "seq_lens_out[b] = p + 1;", "seq_lens_out[b] = p;"),
+    ("bf16: truncating round", "double r = nearbyint(ldexp(ax, -shift));",
+     "double r = floor(ldexp(ax, -shift));"),
+    ("bf16: ties away from zero", "double r = nearbyint(ldexp(ax, -shift));",
+     "double r = round(ldexp(ax, -shift));"),
+    ("bf16: widened with a shift of 15", "uint32_t u = (uint32_t)h << 16;",
+     "uint32_t u = (uint32_t)h << 15;"),
+]
+
+
+@pytest.fixture(scope="module")
+def mutant_dir():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+    core.bind()  # back to the real oracle
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(mutant_dir, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site not unique or missing: {old!r}"
+    path = os.path.join(mutant_dir, f"m{MUTANTS.index((name, old, new))}")
+    open(path + ".c", "w").write(src.replace(old, new))
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", path + ".so",
+                    path + ".c", "-lm"], check=True)
+    core.bind(path + ".so")
+    try:
+        failed = []
+        for pin in pins.ALL_PINS:
+            try:
+                pin(core)
+            except (AssertionError, ValueError, FloatingPointError):
+                failed.append(pin.__name__)
+        assert failed, f"planted mistake '{name}' passed every pin"
+    finally:
+        core.bind()
