@@ -1,0 +1,69 @@
+// internal.h -- host-side declarations shared by the translation units of
+// libgqa_attn.so (not part of the public ABI; see include/gqa_attn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gqa {
+
+// Bits of the device error word.
+enum : unsigned { kErrBounds = 1u, kErrTimeout = 2u };
+
+// Rows of one split-K work item. Split boundaries are multiples of this, a
+// fixed number independent of the layout and of the rest of the batch, so the
+// paged and contiguous decodes of one history do identical arithmetic.
+constexpr int kSplitRows = 1024;
+
+// Parameters of the SIMT attention kernel (decode, and prefill shapes that the
+// tensor-core kernel does not take). All pointers are device pointers.
+struct RowsParams {
+  const void* q;            // [B, seq_q, H, DK]
+  const void* k;            // contiguous [B, Hkv, max_len, DK-DROT] or pool [nb, Hkv, bs, DK]
+  const void* v;            // contiguous [B, Hkv, max_len, DV] or pool [nb, Hkv, bs, DV]
+  const void* k_rot;        // contiguous only: [B, max_len, DROT]
+  void* out;                // [B, seq_q, H, DV]
+  float* partial;           // [B*seq_q*H, max_splits, DV+2] when max_splits > 1
+  const int32_t* kv_len;    // [B] keys present (decode), or NULL: offsets[b] + seq_q
+  const int32_t* offsets;   // [B] or NULL (prefill)
+  const int32_t* tables;    // paged: [B, mbps]
+  unsigned* err;            // device error word
+  int paged;
+  int B, seq_q, H, Hkv, G;  // G = H / Hkv
+  int GH, QR;               // query heads and query rows per work item (GH*QR = NV)
+  int n_hchunks, n_rblocks; // G / GH, ceil(seq_q / QR)
+  int max_len;              // contiguous rows per (b, kvh); 0 when paged
+  int capacity;             // largest valid key count of one sequence
+  int mbps, bs, num_blocks; // paged
+  int split_rows;           // rows per split (kSplitRows, or >= capacity for no split)
+  int max_splits;
+  float qscale;             // attention_scale * log2(e)
+  int debug_withhold;       // test hook: withhold tile 0 of every item
+};
+
+// Dispatch of the SIMT kernel by element type and head widths; NV = GH * QR.
+// Returns cudaErrorNotSupported when there is no instantiation.
+cudaError_t launch_attn_rows_f32(const RowsParams& p, int dk, int dv, int drot, int nv, cudaStream_t st);
+cudaError_t launch_attn_rows_bf16(const RowsParams& p, int dk, int dv, int drot, int nv, cudaStream_t st);
+// Largest NV the instantiation set offers for these widths (0 = unsupported).
+int rows_max_nv(int bf16, int dk, int dv, int drot);
+
+cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStream_t st);
+
+cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int heads, int d, int heads_outer,
+                        int rot_offset, int rot_dim, double theta, int bf16, cudaStream_t st);
+
+cudaError_t launch_append(void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                          const int32_t* tables, const int32_t* lens_in, int32_t* lens_out, int B, int mbps,
+                          int num_blocks, int bs, int H, int Hkv, int dk, int dv, double theta, int rot_offset,
+                          int rot_dim, int bf16, unsigned* err, cudaStream_t st);
+
+// tcgen05 causal prefill (bf16, d_k = d_v = 64). Returns cudaErrorNotSupported
+// for other shapes.
+cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
+                              int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv,
+                              float qscale, unsigned* err, cudaStream_t st);
+bool prefill_tc_supported(int bf16, int dk, int dv);
+
+}  // namespace gqa

@@ -1,0 +1,211 @@
+// kernels_aux.cu -- split combine, interleaved RoPE, paged KV append, and the
+// dispatch of the SIMT attention instantiations.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gqa {
+
+cudaError_t rows_dispatch_f32_small(const RowsParams&, int, int, int, int, cudaStream_t);
+cudaError_t rows_dispatch_f32_large(const RowsParams&, int, int, int, int, cudaStream_t);
+cudaError_t rows_dispatch_bf16_small(const RowsParams&, int, int, int, int, cudaStream_t);
+cudaError_t rows_dispatch_bf16_d128(const RowsParams&, int, int, int, int, cudaStream_t);
+cudaError_t rows_dispatch_bf16_large(const RowsParams&, int, int, int, int, cudaStream_t);
+
+int rows_max_nv(int /*bf16*/, int dk, int dv, int drot) {
+  if (drot == 0 && dk == dv && (dk == 16 || dk == 32 || dk == 64)) return 8;
+  if (drot == 0 && dk == 128 && dv == 128) return 4;
+  if (drot == 0 && dk == 256 && dv == 256) return 2;
+  if (dk == 192 && dv == 128 && (drot == 0 || drot == 64)) return 2;
+  return 0;
+}
+
+cudaError_t launch_attn_rows_f32(const RowsParams& p, int dk, int dv, int drot, int nv, cudaStream_t st) {
+  if (dk <= 64 && dk == dv) return rows_dispatch_f32_small(p, dk, dv, drot, nv, st);
+  return rows_dispatch_f32_large(p, dk, dv, drot, nv, st);
+}
+
+cudaError_t launch_attn_rows_bf16(const RowsParams& p, int dk, int dv, int drot, int nv, cudaStream_t st) {
+  if (dk <= 64 && dk == dv) return rows_dispatch_bf16_small(p, dk, dv, drot, nv, st);
+  if (dk == 128 && dv == 128) return rows_dispatch_bf16_d128(p, dk, dv, drot, nv, st);
+  return rows_dispatch_bf16_large(p, dk, dv, drot, nv, st);
+}
+
+// ---------------------------------------------------------------------------
+// Split combine: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the
+// splits of one (sequence, head), M = max_s m_s, in split order. Empty splits
+// (m = -inf) weigh zero. One warp per output row.
+
+template <typename ET>
+__global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, int DV) {
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.B * p.seq_q * p.H) return;
+  const int b = wid / (p.seq_q * p.H);
+  const int kv_len = p.kv_len ? p.kv_len[b] : (p.offsets ? p.offsets[b] : 0) + p.seq_q;
+  if (!(kv_len >= p.seq_q && kv_len >= 1 && kv_len <= p.capacity)) return;  // attention wrote zeros
+  const int n = (kv_len + p.split_rows - 1) / p.split_rows;  // seq_q == 1 whenever splitting
+  if (n <= 1) return;  // attention wrote the output itself
+  const int stride = DV + 2;
+  const float* P = p.partial + (size_t)wid * p.max_splits * stride;
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, P[(size_t)s * stride]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  ET* out = reinterpret_cast<ET*>(p.out) + (size_t)wid * DV;
+  if (M == -INFINITY) {
+    for (int d = lane; d < DV; d += 32) out[d] = Elem<ET>::from_f32(0.f);
+    return;
+  }
+  float den = 0.f;
+  for (int s = 0; s < n; ++s) {
+    const float ms = P[(size_t)s * stride];
+    const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+    den = fmaf(w, P[(size_t)s * stride + 1], den);
+  }
+  for (int d = lane; d < DV; d += 32) {
+    float acc = 0.f;
+    for (int s = 0; s < n; ++s) {
+      const float ms = P[(size_t)s * stride];
+      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      acc = fmaf(w, P[(size_t)s * stride + 2 + d], acc);
+    }
+    out[d] = Elem<ET>::from_f32(den > 0.f ? acc / den : 0.f);
+  }
+}
+
+cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStream_t st) {
+  const long long rows = (long long)p.B * p.seq_q * p.H;
+  if (rows <= 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  const unsigned blocks = (unsigned)((rows + warps_per_block - 1) / warps_per_block);
+  if (bf16)
+    split_combine_kernel<__nv_bfloat16><<<blocks, 32 * warps_per_block, 0, st>>>(p, dv);
+  else
+    split_combine_kernel<float><<<blocks, 32 * warps_per_block, 0, st>>>(p, dv);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Interleaved RoPE. The angle pos * theta^(-2t/rot_dim) is formed in fp64 and
+// reduced modulo 2*pi in fp64 (positions reach 32k, where an fp32 angle would
+// be off by ~2e-3 rad); sine and cosine of the reduced angle come from the
+// fp32 sincosf, the rotation is done in fp32 and rounded once on store.
+
+__device__ __forceinline__ void rope_angle(double pos, int pair, int rot_dim, double theta, float* c, float* s) {
+  const double w = pow(theta, -2.0 * pair / rot_dim);
+  const double a = remainder(pos * w, 6.283185307179586476925286766559);
+  sincosf((float)a, s, c);
+}
+
+template <typename ET>
+__device__ __forceinline__ void rotate_pair(ET* x, float c, float s) {
+  const float x0 = Elem<ET>::to_f32(x[0]), x1 = Elem<ET>::to_f32(x[1]);
+  x[0] = Elem<ET>::from_f32(fmaf(x0, c, -x1 * s));
+  x[1] = Elem<ET>::from_f32(fmaf(x0, s, x1 * c));
+}
+
+template <typename ET>
+__global__ void __launch_bounds__(256) rope_kernel(ET* x, const int32_t* positions, int B, int T, int heads, int d,
+                                                   int heads_outer, int rot_offset, int rot_dim, double theta) {
+  const int npairs = rot_dim / 2;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)B * T * npairs) return;
+  const int pr = (int)(idx % npairs);
+  const long long tok = idx / npairs;  // b * T + t
+  const int b = (int)(tok / T), t = (int)(tok % T);
+  float c, s;
+  rope_angle((double)positions[tok], pr, rot_dim, theta, &c, &s);
+  for (int h = 0; h < heads; ++h) {
+    const size_t row = heads_outer ? (((size_t)b * heads + h) * T + t) : ((size_t)tok * heads + h);
+    rotate_pair(x + row * d + rot_offset + 2 * pr, c, s);
+  }
+}
+
+cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int heads, int d, int heads_outer,
+                        int rot_offset, int rot_dim, double theta, int bf16, cudaStream_t st) {
+  const long long total = (long long)B * T * (rot_dim / 2);
+  if (total <= 0 || heads <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((total + 255) / 256);
+  if (bf16)
+    rope_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(x), positions, B, T, heads,
+                                                        d, heads_outer, rot_offset, rot_dim, theta);
+  else
+    rope_kernel<float><<<blocks, 256, 0, st>>>(reinterpret_cast<float*>(x), positions, B, T, heads, d, heads_outer,
+                                               rot_offset, rot_dim, theta);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Paged append of one row per sequence (one CTA per sequence): position
+// p = lens_in[b] is read before anything is written; q (all heads) and the new
+// k (all KV heads) are rotated at p; k and v go to slot p % bs of block
+// tables[b][p / bs]; lens_out[b] = p + 1.
+
+template <typename ET>
+__global__ void __launch_bounds__(128) append_kernel(ET* q, const ET* k_new, const ET* v_new, ET* k_pool, ET* v_pool,
+                                                     const int32_t* tables, const int32_t* lens_in, int32_t* lens_out,
+                                                     int mbps, int num_blocks, int bs, int H, int Hkv, int dk, int dv,
+                                                     double theta, int rot_offset, int rot_dim, unsigned* err) {
+  const int b = blockIdx.x;
+  const int p = lens_in[b];
+  const bool pos_ok = p >= 0 && (long long)p < (long long)mbps * bs;
+  const int blk = pos_ok ? tables[(size_t)b * mbps + p / bs] : -1;
+  const bool ok = pos_ok && blk >= 0 && blk < num_blocks;
+  __syncthreads();  // every thread has read lens_in[b] (lens_out may alias it)
+  if (!ok) {
+    if (threadIdx.x == 0) {
+      raise_error(err, kErrBounds);
+      lens_out[b] = p;
+    }
+    return;
+  }
+  const int row = p % bs;
+  const bool rope = theta > 0.0 && rot_dim > 0;
+  if (rope) {
+    for (int pr = threadIdx.x; pr < rot_dim / 2; pr += blockDim.x) {
+      float c, s;
+      rope_angle((double)p, pr, rot_dim, theta, &c, &s);
+      const int e = rot_offset + 2 * pr;
+      for (int h = 0; h < H; ++h) rotate_pair(q + ((size_t)b * H + h) * dk + e, c, s);
+      for (int kh = 0; kh < Hkv; ++kh) {
+        ET pair[2] = {k_new[((size_t)b * Hkv + kh) * dk + e], k_new[((size_t)b * Hkv + kh) * dk + e + 1]};
+        rotate_pair(pair, c, s);
+        ET* dst = k_pool + (((size_t)blk * Hkv + kh) * bs + row) * dk + e;
+        dst[0] = pair[0];
+        dst[1] = pair[1];
+      }
+    }
+  }
+  for (int idx = threadIdx.x; idx < Hkv * dk; idx += blockDim.x) {
+    const int kh = idx / dk, e = idx % dk;
+    if (rope && e >= rot_offset && e < rot_offset + rot_dim) continue;  // written rotated above
+    k_pool[(((size_t)blk * Hkv + kh) * bs + row) * dk + e] = k_new[((size_t)b * Hkv + kh) * dk + e];
+  }
+  for (int idx = threadIdx.x; idx < Hkv * dv; idx += blockDim.x) {
+    const int kh = idx / dv, e = idx % dv;
+    v_pool[(((size_t)blk * Hkv + kh) * bs + row) * dv + e] = v_new[((size_t)b * Hkv + kh) * dv + e];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) lens_out[b] = p + 1;
+}
+
+cudaError_t launch_append(void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                          const int32_t* tables, const int32_t* lens_in, int32_t* lens_out, int B, int mbps,
+                          int num_blocks, int bs, int H, int Hkv, int dk, int dv, double theta, int rot_offset,
+                          int rot_dim, int bf16, unsigned* err, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  if (bf16)
+    append_kernel<__nv_bfloat16><<<B, 128, 0, st>>>(
+        reinterpret_cast<__nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
+        reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__nv_bfloat16*>(k_pool),
+        reinterpret_cast<__nv_bfloat16*>(v_pool), tables, lens_in, lens_out, mbps, num_blocks, bs, H, Hkv, dk, dv,
+        theta, rot_offset, rot_dim, err);
+  else
+    append_kernel<float><<<B, 128, 0, st>>>(reinterpret_cast<float*>(q), reinterpret_cast<const float*>(k_new),
+                                            reinterpret_cast<const float*>(v_new), reinterpret_cast<float*>(k_pool),
+                                            reinterpret_cast<float*>(v_pool), tables, lens_in, lens_out, mbps,
+                                            num_blocks, bs, H, Hkv, dk, dv, theta, rot_offset, rot_dim, err);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

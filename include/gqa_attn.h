@@ -1,0 +1,185 @@
+/*
+ * gqa_attn.h -- C ABI of libgqa_attn.so: causal grouped-query attention of new
+ * query rows against a KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (kopitiam-runtime 0.2.4 src/attention.rs, module doc,
+ * `repeat_kv_heads`, `causal_mask`, `attention_forward`):
+ *   query head h reads KV head h / (H / Hkv);
+ *   query row i sits at absolute position position_offset + i and sees keys
+ *   0 ..= position_offset + i, never later ones;
+ *   out = softmax_j(attention_scale * q . k_j) weighted sum of v_j.
+ * One rule covers a multi-row prefill (offset 0) and a single-row decode step
+ * (offset = rows cached before the step).
+ *
+ * Conventions shared by every call:
+ *  - Every tensor argument is a DEVICE pointer on the current CUDA device,
+ *    owned by the caller. The library neither keeps nor frees any of them and
+ *    allocates no device memory. `stream` is a cudaStream_t (NULL = the legacy
+ *    default stream); every call is asynchronous on it.
+ *  - Element type: `dt` gives the type of q, k, v, pools and out alike
+ *    (GQA_F32 = float, GQA_BF16 = bfloat16). Arithmetic is fp32 whatever `dt`.
+ *  - Layouts are dense row-major with the shapes given below; head and row
+ *    widths d_k, d_v must be multiples of 8 and every tensor pointer 16-byte
+ *    aligned.
+ *  - Supported head widths (d_k, d_v): (16,16), (32,32), (64,64), (128,128),
+ *    (256,256), (192,128); others return GQA_ERR_UNSUPPORTED.
+ *  - Errors a host check can see (null pointer, H % Hkv != 0, bad size or
+ *    alignment, small workspace) are returned before anything is launched.
+ *  - Errors only the device can see (a block-table entry outside
+ *    [0, num_blocks), a sequence length outside its valid range, a bounded
+ *    wait that ran out) skip the affected work without any out-of-range access
+ *    and set a sticky device error word; attn_get_device_error() reads and
+ *    clears it. Outputs of the affected sequences are then unspecified.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1,    /* a host-checkable argument is wrong */
+  GQA_ERR_UNSUPPORTED = 2,    /* valid, but a shape this library has no kernel for */
+  GQA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+  GQA_ERR_WORKSPACE = 4,      /* workspace missing or smaller than required */
+  GQA_ERR_DEVICE_BOUNDS = 5,  /* device saw an index or length out of range */
+  GQA_ERR_DEVICE_TIMEOUT = 6  /* a bounded device wait gave up */
+} gqa_status;
+
+typedef enum { GQA_F32 = 0, GQA_BF16 = 1 } gqa_dtype;
+
+/*
+ * Causal prefill: seq_q new rows per sequence attend to the cache that already
+ * holds them (kopitiam-runtime src/attention.rs, `attention_forward` and
+ * `causal_mask`; position_offset is an explicit argument, never re-derived from
+ * the cache, as that page's `attention_forward` doc requires).
+ *
+ *   q    [B, seq_q, H, d_k]           (token-major; heads are a reshape of the hidden axis)
+ *   k    [B, Hkv, seq_kv_max, d_k]    (head-major, kopitiam's per-layer [n_kv, seq, d])
+ *   v    [B, Hkv, seq_kv_max, d_v]
+ *   position_offset  int32 [B] on the device, or NULL for all zeros
+ *   out  [B, seq_q, H, d_v]
+ * Row i of sequence b sees keys 0..=position_offset[b] + i; it requires
+ * position_offset[b] + seq_q <= seq_kv_max (checked on the device).
+ * bf16 with d_k == d_v == 64 runs on the tcgen05 tensor-core kernel; every
+ * other shape and f32 run on the SIMT kernel. No workspace.
+ */
+gqa_status attn_prefill_causal(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
+                               int seq_kv_max, const int32_t* position_offset, int H, int Hkv, int d_k,
+                               int d_v, float attention_scale, gqa_dtype dt, void* stream);
+
+/*
+ * Single-row decode against contiguous per-sequence caches (frink-models
+ * src/decoder/attn_block.rs, `push_and_attend_row`, contiguous arms: the row
+ * is pushed first, then the sequence attends over all it holds).
+ *
+ *   q        [B, H, d_k]
+ *   k_cache  [B, Hkv, max_len, d_k - d_rot]
+ *   v_cache  [B, Hkv, max_len, d_v]
+ *   k_rot_shared  NULL (d_rot = 0), or [B, max_len, d_rot]: one rotated vector per
+ *            position shared by every KV head, so that key row j of head h is
+ *            concat(k_cache[b, h, j, :], k_rot_shared[b, j, :]) -- the MLA shape of
+ *            frink-models src/mla/mod.rs (`naive_attention`, module doc point 2).
+ *            Supported for (d_k, d_v, d_rot) = (192, 128, 64).
+ *   seq_lens int32 [B]: rows present, the query's own row included; the query
+ *            sits at position seq_lens[b] - 1. Valid range 1..max_len.
+ *   out      [B, H, d_v]
+ * workspace: device scratch of at least attn_decode_workspace_bytes(B, H, d_v,
+ * max_len) bytes (may be NULL when that is 0); its contents need no
+ * initialisation and are clobbered.
+ */
+gqa_status attn_decode_contig(const void* q, const void* k_cache, const void* v_cache,
+                              const void* k_rot_shared, int d_rot, const int32_t* seq_lens, void* out,
+                              int B, int max_len, int H, int Hkv, int d_k, int d_v,
+                              float attention_scale, gqa_dtype dt, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * Single-row decode against a paged pool shared by all sequences (frink-models
+ * src/decoder/attn_block.rs, `push_and_attend_row`, paged arm: paging changes
+ * where rows live and nothing else, so the result is bit-identical to
+ * attn_decode_contig on the same history).
+ *
+ *   k_pool        [num_blocks, Hkv, block_size, d_k]
+ *   v_pool        [num_blocks, Hkv, block_size, d_v]
+ *   block_tables  int32 [B, max_blocks_per_seq]: row j of sequence b lives in
+ *                 block block_tables[b][j / block_size], slot j % block_size.
+ *                 Entries past the sequence's last block are never read.
+ *   seq_lens      int32 [B], as for attn_decode_contig; valid range
+ *                 1..max_blocks_per_seq * block_size.
+ *   q [B, H, d_k], out [B, H, d_v]; workspace as for attn_decode_contig with
+ *   max_len = max_blocks_per_seq * block_size.
+ */
+gqa_status attn_decode_paged(const void* q, const void* k_pool, const void* v_pool,
+                             const int32_t* block_tables, const int32_t* seq_lens, void* out, int B,
+                             int max_blocks_per_seq, int num_blocks, int block_size, int H, int Hkv,
+                             int d_k, int d_v, float attention_scale, gqa_dtype dt, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
+ * Paged append of one new row per sequence, with interleaved RoPE on q and k
+ * (frink-models src/decoder/attn_block.rs, `attn_block_tail` then
+ * `push_and_attend_row`: per-head RoPE at the row's position, the position read
+ * before the push, then the push).
+ *
+ *   q      [B, H, d_k]     rotated in place at p = seq_lens_in[b]
+ *   k_new  [B, Hkv, d_k]   rotated at p, then written to k_pool
+ *   v_new  [B, Hkv, d_v]   written to v_pool unrotated
+ *   written slot: block block_tables[b][p / block_size], row p % block_size
+ *   seq_lens_out[b] = p + 1 (seq_lens_out may alias seq_lens_in)
+ * RoPE: rope_theta <= 0 disables it; otherwise the rotated slice is
+ * [rot_offset, rot_offset + rot_dim) of every head, pairs (2t, 2t+1) turned by
+ * p * rope_theta^(-2t / rot_dim) (the angle is formed and reduced in fp64).
+ * A sequence whose position or block entry is out of range is skipped (its
+ * seq_lens_out[b] = seq_lens_in[b]) and the device error word is set.
+ */
+gqa_status kv_append_paged(void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                           const int32_t* block_tables, const int32_t* seq_lens_in,
+                           int32_t* seq_lens_out, int B, int max_blocks_per_seq, int num_blocks,
+                           int block_size, int H, int Hkv, int d_k, int d_v, double rope_theta,
+                           int rot_offset, int rot_dim, gqa_dtype dt, void* stream);
+
+/*
+ * Interleaved RoPE in place (frink-models src/mla/mod.rs, module doc point 2 and
+ * `rotate_pe`: adjacent pairs, ggml NORM layout; frink-models
+ * src/decoder/attn_block.rs, per-head RoPE in `attn_block_tail`).
+ *
+ *   x          heads_outer == 0: [B, T, heads, d]; heads_outer == 1: [B, heads, T, d]
+ *   positions  int32 [B, T]: the absolute position of token t of sequence b
+ * The slice [rot_offset, rot_offset + rot_dim) of every head is rotated pairwise
+ * by pos * theta^(-2t / rot_dim), t < rot_dim / 2. rot_dim must be even, theta > 0.
+ */
+gqa_status attn_rope_interleaved(void* x, const int32_t* positions, int B, int T, int heads, int d,
+                                 int heads_outer, int rot_offset, int rot_dim, double theta,
+                                 gqa_dtype dt, void* stream);
+
+/* Bytes of workspace attn_decode_contig / attn_decode_paged need for B
+ * sequences of at most max_len_upper_bound rows (0 when no sequence that long
+ * is split). Host only; launches nothing. */
+size_t attn_decode_workspace_bytes(int B, int H, int d_v, int max_len_upper_bound);
+
+/* Synchronises `stream`, then returns and clears the device error word of the
+ * current device: GQA_OK, GQA_ERR_DEVICE_TIMEOUT (takes precedence) or
+ * GQA_ERR_DEVICE_BOUNDS; GQA_ERR_CUDA if the stream reports a CUDA error. */
+gqa_status attn_get_device_error(void* stream);
+
+/* Static, NUL-terminated text of a status code. */
+const char* gqa_status_string(gqa_status status);
+
+/* Test hook for the bounded waits: while enabled, each decode launch withholds
+ * the first K/V tile of every work item, so that the consumers' wait on it runs
+ * out (after about one second), the device error word records
+ * GQA_ERR_DEVICE_TIMEOUT and the kernel returns. Outputs are then garbage.
+ * Never enable outside tests. Returns the previous setting. */
+int gqa_debug_withhold_first_tile(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

@@ -1,0 +1,75 @@
+"""The C ABI library (CPU only): it loads, exports every symbol include/gqa_attn.h
+declares, and rejects host-checkable bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_gqa_attention_row_gb300 import build
+    build.build()
+    import causal_gqa_attention_row_gb300 as g
+    return g.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gqa_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) - {"if", "sizeof"}
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"attn_prefill_causal", "attn_decode_contig", "attn_decode_paged", "kv_append_paged",
+            "attn_rope_interleaved", "attn_decode_workspace_bytes", "attn_get_device_error"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    import causal_gqa_attention_row_gb300 as g
+    assert names <= set(g.EXPORTS)
+
+
+def test_status_strings(lib):
+    import causal_gqa_attention_row_gb300 as g
+    for s in range(7):
+        assert g.gqa_status_string(s) == g.STATUS[s]
+
+
+def test_workspace_size(lib):
+    import causal_gqa_attention_row_gb300 as g
+    assert g.attn_decode_workspace_bytes(256, 32, 128, 1024) == 0          # one split: none needed
+    assert g.attn_decode_workspace_bytes(256, 32, 128, 2049 * 16) == 256 * 32 * 33 * 130 * 4
+    assert g.attn_decode_workspace_bytes(0, 32, 128, 5000) == 0
+
+
+def test_bad_arguments_rejected_before_launch(lib):
+    """Each call below fails a host check, so it returns before any CUDA call."""
+    P = ctypes.c_void_p(16)  # a non-null, 16-byte aligned stand-in: never dereferenced
+    N = None
+    inv = 1
+    # H % Hkv != 0
+    assert lib.attn_decode_contig(P, P, P, N, 0, P, P, 2, 64, 6, 4, 128, 128, 0.1, 1, N, 0, N) == inv
+    # d_k not a multiple of 8
+    assert lib.attn_decode_paged(P, P, P, P, P, P, 2, 4, 10, 16, 8, 2, 100, 100, 0.1, 1, N, 0, N) == inv
+    # null q
+    assert lib.attn_decode_paged(N, P, P, P, P, P, 2, 4, 10, 16, 8, 2, 128, 128, 0.1, 1, N, 0, N) == inv
+    # unknown dtype
+    assert lib.attn_prefill_causal(P, P, P, P, 1, 8, 8, N, 4, 2, 16, 16, 0.25, 7, N) == inv
+    # seq_q > seq_kv_max
+    assert lib.attn_prefill_causal(P, P, P, P, 1, 9, 8, N, 4, 2, 16, 16, 0.25, 0, N) == inv
+    # k_rot given without d_rot
+    assert lib.attn_decode_contig(P, P, P, P, 0, P, P, 2, 64, 8, 8, 192, 128, 0.1, 1, N, 0, N) == inv
+    # misaligned pointer
+    assert lib.attn_decode_contig(ctypes.c_void_p(18), P, P, N, 0, P, P, 2, 64, 8, 8, 128, 128, 0.1, 1, N, 0,
+                                  N) == inv
+    # odd rot_dim, theta <= 0
+    assert lib.attn_rope_interleaved(P, P, 1, 4, 2, 64, 0, 0, 63, 1e4, 1, N) == inv
+    assert lib.attn_rope_interleaved(P, P, 1, 4, 2, 64, 0, 0, 64, 0.0, 1, N) == inv
+    # rotated slice past the head
+    assert lib.kv_append_paged(P, P, P, P, P, P, P, P, 2, 4, 10, 16, 8, 2, 64, 64, 1e4, 16, 64, 1, N) == inv
+    # empty batches are no-ops
+    assert lib.attn_decode_contig(N, N, N, N, 0, N, N, 0, 64, 8, 2, 128, 128, 0.1, 1, N, 0, N) == 0
