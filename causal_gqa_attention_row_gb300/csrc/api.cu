@@ -170,7 +170,7 @@ gqa_status attn_prefill_causal(const void* q, const void* k, const void* v, void
   unsigned* err = error_word();
   if (!err) return GQA_ERR_CUDA;
   const float qscale = attention_scale * 1.4426950408889634f;
-  if (gqa::prefill_tc_supported(bf16, d_k, d_v))
+  if (gqa::prefill_tc_supported(bf16, d_k, d_v) && attention_scale > 0.f)
     return from_cuda(gqa::launch_prefill_tc(q, k, v, out, B, seq_q, seq_kv_max, position_offset, H, Hkv, d_k, d_v,
                                             qscale, err, st));
   const int nvmax = gqa::rows_max_nv(bf16, d_k, d_v, 0);

@@ -1,0 +1,74 @@
+"""The tcgen05 causal prefill (bf16, d = 64) against the fp64 oracle (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import core
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run(g, c):
+    B, S, H, _ = c.q.shape
+    out = torch.full((B, S, H, c.v.shape[-1]), float("nan"), dtype=torch.bfloat16, device=DEV)
+    g.attn_prefill_causal(c.q.to(DEV), c.k.to(DEV), c.v.to(DEV), out, c.scale, position_offset=c.offsets.to(DEV))
+    assert g.attn_get_device_error() == g.OK
+    return out
+
+
+@pytest.mark.parametrize("B,S,H,Hkv,offs", [
+    (1, 128, 2, 1, [0]), (1, 256, 4, 2, [0]), (1, 300, 14, 2, [0]), (2, 200, 6, 3, [0, 37]),
+    (1, 1, 2, 2, [5]), (2, 129, 8, 1, [128, 3]), (1, 520, 4, 4, [0])])
+def test_prefill_tc_matches_oracle(gpu_lib, B, S, H, Hkv, offs):
+    g = gpu_lib
+    extra = max(offs)
+    c = W.make_prefill(B=B, S=S, H=H, Hkv=Hkv, dk=64, dv=64, seed=70 + S, S_kv=S + extra + 5, offsets=offs)
+    out = run(g, c)
+    want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
+    err = np.abs(out.float().cpu().numpy() - want).max()
+    assert err <= 2e-2, err
+
+
+def test_prefill_tc_full_size_config(gpu_lib):
+    """The causal prefill workload at full size: B=1, H=14, Hkv=2, d=64, 2048 rows,
+    interleaved RoPE (theta 1e6) applied to q and k first; every output checked."""
+    g = gpu_lib
+    c = W.make_prefill(B=1, S=2048, H=14, Hkv=2, dk=64, dv=64, seed=1)
+    pos = torch.arange(2048, dtype=torch.int32)[None]
+    q, k = c.q.to(DEV), c.k.to(DEV)
+    g.attn_rope_interleaved(q, pos.to(DEV), 1e6)
+    g.attn_rope_interleaved(k, pos.to(DEV), 1e6, heads_outer=True)
+    out = torch.empty(1, 2048, 14, 64, dtype=torch.bfloat16, device=DEV)
+    g.attn_prefill_causal(q, k, c.v.to(DEV), out, c.scale)
+    assert g.attn_get_device_error() == g.OK
+    # oracle: its own RoPE of the raw inputs, rounded to bf16 as the cache stores them
+    qo = core.rope_interleaved(W.to_oracle(c.q), W.to_oracle(pos), 0, 64, 1e6)
+    ko = np.ascontiguousarray(core.rope_interleaved(np.ascontiguousarray(W.to_oracle(c.k).transpose(0, 2, 1, 3)),
+                                                    W.to_oracle(pos), 0, 64, 1e6).transpose(0, 2, 1, 3))
+    want = core.prefill_causal(qo, ko, W.to_oracle(c.v), c.scale)
+    err = np.abs(out.float().cpu().numpy() - want).max()
+    assert err <= 2e-2, err
+
+
+def test_prefill_tc_zero_keys_give_prefix_mean(gpu_lib):
+    """K = 0: every visible key scores 0, so row i is the mean of V[0..=i]."""
+    g = gpu_lib
+    c = W.make_prefill(B=1, S=300, H=4, Hkv=2, dk=64, dv=64, seed=71)
+    c.k.zero_()
+    out = run(g, c)
+    v = c.v.float()[0]                                       # [Hkv, S, d]
+    mean = torch.cumsum(v, dim=1) / torch.arange(1, 301)[None, :, None]
+    want = mean.repeat_interleave(2, dim=0).permute(1, 0, 2)  # [S, H, d]
+    assert (out[0].float().cpu() - want).abs().max().item() <= 2e-2
+
+
+def test_prefill_tc_decode_step_is_last_row(gpu_lib):
+    g = gpu_lib
+    c = W.make_prefill(B=1, S=640, H=8, Hkv=2, dk=64, dv=64, seed=72)
+    out = run(g, c)
+    dec = torch.empty(1, 8, 64, dtype=torch.bfloat16, device=DEV)
+    g.attn_decode_contig(c.q[:, 639].contiguous().to(DEV), c.k.to(DEV), c.v.to(DEV),
+                         torch.tensor([640], dtype=torch.int32, device=DEV), dec, c.scale)
+    assert (dec.float() - out[:, 639].float()).abs().max().item() <= 2e-2
