@@ -22,7 +22,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE_BOUNDS
 
 EXPORTS = ("attn_prefill_causal", "attn_decode_contig", "attn_decode_paged", "kv_append_paged",
            "attn_rope_interleaved", "attn_decode_workspace_bytes", "attn_get_device_error",
-           "gqa_status_string", "gqa_debug_withhold_first_tile")
+           "gqa_status_string", "gqa_debug_withhold_first_tile", "attn_decode_paged_static_workspace")
+
+STATIC_WORKSPACE_BYTES = 16 << 20  # GQA_STATIC_WORKSPACE_BYTES
 
 _lib = None
 
@@ -47,6 +49,7 @@ def load(path: str = None):
         "attn_prefill_causal": [P, P, P, P, I, I, I, P, I, I, I, I, F, I, P],
         "attn_decode_contig": [P, P, P, P, I, P, P, I, I, I, I, I, I, F, I, P, S, P],
         "attn_decode_paged": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, S, P],
+        "attn_decode_paged_static_workspace": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P],
         "kv_append_paged": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, I, I, I, P],
         "attn_rope_interleaved": [P, P, I, I, I, I, I, I, I, D, I, P],
         "attn_get_device_error": [P],
@@ -145,6 +148,22 @@ def attn_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, out, attention_
                                     B, block_tables.shape[1], nb, bs, H, Hkv, dk, dv, float(attention_scale),
                                     _dtype(q, k_pool, v_pool, out), _p(workspace), ws, _stream(stream)),
            "attn_decode_paged")
+    return out
+
+
+def attn_decode_paged_static_workspace(q, k_pool, v_pool, block_tables, seq_lens, out, attention_scale,
+                                       stream=None):
+    """attn_decode_paged with the library's fixed device scratch instead of a
+    caller-allocated workspace (for callers that cannot allocate device memory;
+    see include/gqa_attn.h). Raises GqaError(ERR_WORKSPACE) when the problem needs
+    more than STATIC_WORKSPACE_BYTES of scratch."""
+    B, H, dk = q.shape
+    nb, Hkv, bs, dv = v_pool.shape
+    _check(load().attn_decode_paged_static_workspace(_p(q), _p(k_pool), _p(v_pool), _i32(block_tables),
+                                                     _i32(seq_lens), _p(out), B, block_tables.shape[1], nb, bs, H,
+                                                     Hkv, dk, dv, float(attention_scale),
+                                                     _dtype(q, k_pool, v_pool, out), _stream(stream)),
+           "attn_decode_paged_static_workspace")
     return out
 
 

@@ -121,6 +121,38 @@ gqa_status attn_decode_paged(const void* q, const void* k_pool, const void* v_po
                              int d_k, int d_v, float attention_scale, gqa_dtype dt, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* Size of the fixed device scratch behind attn_decode_paged_static_workspace. */
+#define GQA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+
+/*
+ * attn_decode_paged without a caller-supplied workspace, for callers that cannot
+ * allocate device memory: a program whose GPU memory is all handed out up front
+ * by another component (a serving engine that reserves the free HBM for its KV
+ * pool, say), a plugin in a framework that exposes no allocator, or a loop that
+ * must not risk the implicit synchronisation cudaMalloc/cudaFree can bring. The
+ * pages have no counterpart of this call; it exists for such callers only.
+ *
+ * Arguments, layouts, results and errors are those of attn_decode_paged. The
+ * split-K scratch is a fixed GQA_STATIC_WORKSPACE_BYTES array in the library's
+ * device data, held by every GPU that loads the library until the process
+ * exits; the call allocates nothing and calls no allocating routine. A problem
+ * that needs more scratch than that (attn_decode_workspace_bytes(B, H, d_v,
+ * max_blocks_per_seq * block_size) > GQA_STATIC_WORKSPACE_BYTES) is rejected
+ * with GQA_ERR_WORKSPACE before anything is launched.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture begins. Every call shares the one array per device: two calls whose
+ * kernels overlap on the GPU (different streams, no ordering between them) race
+ * on it and may return wrong results. Calls ordered on one stream are safe; no
+ * contents need clearing between them.
+ */
+gqa_status attn_decode_paged_static_workspace(const void* q, const void* k_pool, const void* v_pool,
+                                              const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                                              int B, int max_blocks_per_seq, int num_blocks, int block_size,
+                                              int H, int Hkv, int d_k, int d_v, float attention_scale,
+                                              gqa_dtype dt, void* stream);
+
 /*
  * Paged append of one new row per sequence, with interleaved RoPE on q and k
  * (frink-models src/decoder/attn_block.rs, `attn_block_tail` then
