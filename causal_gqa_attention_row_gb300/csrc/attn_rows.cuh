@@ -12,27 +12,34 @@
 // (frink-models src/decoder/attn_block.rs and kopitiam's module doc: every
 // query head of a group genuinely shares its KV head).
 //
-// Data path: one producer warp streams K/V tiles of kTileRows rows into a
-// kStages-deep shared-memory ring with 1-D bulk copies (cp.async.bulk, the TMA
-// engine) completing on mbarriers. Contiguous caches need one copy per tile and
+// Data path: one producer warp streams K/V tiles of T rows into an NS-deep
+// shared-memory ring with 1-D bulk copies (cp.async.bulk, the TMA engine)
+// completing on mbarriers. Contiguous caches need one copy per tile and
 // operand; paged caches one per block segment, the block-table gather done by
 // the copy engine (frink-models src/decoder/attn_block.rs, `push_and_attend_row`,
 // paged arm). Four compute warps consume the ring.
 //
 // Compute mapping: a "row group" of L lanes owns one key row at a time; lane li
 // holds the 16-byte chunks li, li+L, li+2L, ... of q (fp32, pre-scaled by
-// scale*log2 e) for each virtual head and of its own output accumulators. A row's
-// scores are L-lane dot products finished by a butterfly of warp shuffles. Each
-// row group keeps its own online-softmax state (running reference max m,
-// denominator l, accumulator o), with lazy rescaling: o and l are rescaled only
-// when a score exceeds m by more than 2^8, which keeps every term <= 256 and
-// leaves o / l unchanged. At the end the row groups are merged in shared memory
-// in a fixed order (log-sum-exp), then written as the output (one split) or as
-// a partial (m, l, o) that the combine kernel merges, again in a fixed order.
+// scale*log2 e) for each virtual head and of its own output accumulators, as
+// float2 pairs for the paired FFMA2 instruction. A row's NV scores are L-lane
+// partial dot products finished by a halving ("transpose") butterfly: each
+// shuffle step also halves the number of heads a lane carries, so the lane ends
+// up owning ONE head's full score. That lane alone runs the online softmax of
+// its head (reference max m, denominator l) and the probability p is broadcast
+// to the group with one shuffle per head.
+//
+// Each row group takes the 2 rows it owns in a tile as one chunk: two
+// independent dot products, one max/rescale check, two exponentials. Rescaling
+// is lazy: o and l move to a new reference max only when a score exceeds the
+// current one by more than 2^8, which keeps every term <= 256 and leaves o / l
+// unchanged. At the end the row groups are merged through shared memory in a
+// fixed order (log-sum-exp), then written as the output (one split) or as a
+// partial (m, l, o) that the combine kernel merges, again in a fixed order.
 //
 // Determinism: split boundaries are multiples of kSplitRows, tiles multiples of
-// kTileRows from the split start, and the row -> row-group assignment a function
-// of the key index only. The arithmetic on a key row therefore does not depend on
+// T rows from the split start, and the row -> row-group assignment a function of
+// the key index only. The arithmetic on a key row therefore does not depend on
 // where the row lives (contiguous or paged), on the block table, or on the other
 // sequences of the batch: paged and contiguous results are bit-identical.
 #pragma once
@@ -44,13 +51,13 @@ namespace gqa {
 
 constexpr int kRowsWarps = 4;  // compute warps
 constexpr int kRowsThreads = (kRowsWarps + 1) * 32;
-constexpr int kTileRows = 32;
 constexpr int kMaxStages = 4;
 constexpr int kRingBudget = 128 * 1024;  // shared-memory ring per CTA (two CTAs per SM)
 constexpr float kRescaleLog2 = 8.0f;
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
+constexpr int clog2(int x) { return x <= 1 ? 0 : 1 + clog2(x / 2); }
 
 template <typename ET, int DK, int DV, int DROT, int NV>
 struct RowsCfg {
@@ -63,19 +70,95 @@ struct RowsCfg {
   static constexpr int EK = QK * CH, EV = QV * CH;   // elements per lane
   static constexpr int RGW = 32 / L;                 // row groups per warp
   static constexpr int NRG = kRowsWarps * RGW;
-  static constexpr int T = kTileRows;
+  static constexpr int T = 2 * NRG;                  // rows per tile: two per row group
   static constexpr int kN = T * DN * ES, kR = T * DROT * ES, kV = T * DV * ES;
   static constexpr int stage_bytes = kN + kR + kV;
   static constexpr int row_bytes = (DN + DROT + DV) * ES;
   static constexpr int NS = cmax(2, cmin(kMaxStages, kRingBudget / stage_bytes));  // ring depth
   static constexpr int merge_bytes = NRG * NV * (DV + 2) * 4;
   static constexpr int data_bytes = cmax(NS * stage_bytes, merge_bytes);
-  static constexpr int kHeader = 128;  // mbarriers + abort flag
+  static constexpr int kHeader = 128;  // mbarriers + flags
   static constexpr int smem_bytes = kHeader + data_bytes;
   static_assert(DK % CH == 0 && DV % CH == 0 && DN % CH == 0, "head widths must be whole 16-byte chunks");
   static_assert(KCH % L == 0 && VCH % L == 0 && NCH % L == 0, "chunks must split evenly over a row group");
   static_assert(32 % L == 0, "row groups must tile a warp");
+  static_assert(NV <= L, "a row group needs at least one lane per virtual head");
+  static_assert(kSplitRows % T == 0, "split boundaries must fall on tile boundaries");
 };
+
+// Head owned by lane li of a row group after the halving butterfly: at the
+// step with offset L >> (k+1) the lanes with that bit set keep the upper half
+// of the heads they carried.
+template <int NV, int L>
+__device__ __forceinline__ int owned_head(int li) {
+  int h = 0;
+#pragma unroll
+  for (int k = 0, n = NV; n > 1; ++k, n >>= 1)
+    if (li & (L >> (k + 1))) h += n >> 1;
+  return h;
+}
+
+// Lowest lane of a row group that owns head h (inverse of owned_head).
+template <int NV, int L>
+__host__ __device__ constexpr int owner_lane(int h) {
+  int li = 0;
+  for (int k = 0, n = NV; n > 1; ++k, n >>= 1)
+    if (h & (n >> 1)) li |= L >> (k + 1);
+  return li;
+}
+
+// Sum NV per-lane partial scores over the L lanes of a row group; each lane
+// returns the full score of its owned head.
+template <int NV, int L>
+__device__ __forceinline__ float reduce_own(const float (&v)[NV], int li) {
+  float cur[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) cur[i] = v[i];
+  int off = L >> 1;
+#pragma unroll
+  for (int n = NV; n > 1; n >>= 1) {
+    const bool upper = (li & off) != 0;
+    const int half = n >> 1;
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) {
+      if (i < half) {
+        const float keep = upper ? cur[i + half] : cur[i];
+        const float send = upper ? cur[i] : cur[i + half];
+        cur[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+    off >>= 1;
+  }
+  float s = cur[0];
+#pragma unroll
+  for (; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return s;
+}
+
+// 2^x on the special-function unit (the PTX ex2.approx instruction, flushing
+// subnormal results to zero; exp2(-inf) = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename ET>
+__device__ __forceinline__ void chunk_to_f2(const uint4 u, float2* f);
+
+template <>
+__device__ __forceinline__ void chunk_to_f2<__nv_bfloat16>(const uint4 u, float2* f) {
+  f[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+  f[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  f[2] = make_float2(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u));
+  f[3] = make_float2(__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u));
+}
+
+template <>
+__device__ __forceinline__ void chunk_to_f2<float>(const uint4 u, float2* f) {
+  f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+  f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+}
 
 // Warp-uniform bounded wait. On a timeout (or an abort raised elsewhere in the
 // CTA) every lane returns false and the abort flag and error word are set.
@@ -94,6 +177,7 @@ template <typename ET, int DK, int DV, int DROT, int NV>
 __global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsParams p) {
   using C = RowsCfg<ET, DK, DV, DROT, NV>;
   constexpr int CH = C::CH, L = C::L, T = C::T, kStages = C::NS;
+  constexpr int H2K = C::EK / 2, H2V = C::EV / 2;  // float2 pairs per lane
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kStages;
@@ -183,17 +267,15 @@ __global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsPa
 
   const int ntiles = (r1 - r0 + T - 1) / T;
   const int rgw = lane / L, li = lane % L;
+  const int own = owned_head<NV, L>(li);  // the virtual head whose softmax this lane runs
 
-  // online-softmax state of this lane's row group, one entry per virtual head
-  float o[NV][C::EV];
-  float m[NV], l[NV];
+  // output accumulators (all heads, this lane's chunks) and the owned head's state
+  float2 o2[NV][H2V];
 #pragma unroll
-  for (int vh = 0; vh < NV; ++vh) {
-    m[vh] = -INFINITY;
-    l[vh] = 0.f;
+  for (int vh = 0; vh < NV; ++vh)
 #pragma unroll
-    for (int e = 0; e < C::EV; ++e) o[vh][e] = 0.f;
-  }
+    for (int e = 0; e < H2V; ++e) o2[vh][e] = make_float2(0.f, 0.f);
+  float m_ref = -INFINITY, l_sum = 0.f;
 
   if (warp == kRowsWarps) {
     // ================= producer warp =================
@@ -260,23 +342,27 @@ __global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsPa
     }
   } else {
     // ================= compute warps =================
-    float qf[NV][C::EK];
-    int lim[NV];
+    float2 q2[NV][H2K];
+    int lim_own = 0;
 #pragma unroll
     for (int vh = 0; vh < NV; ++vh) {
       const int iq = i0 + vh / p.GH;
       const int h = kvh * p.G + hc * p.GH + vh % p.GH;
       const bool active = iq <= i_last;
-      lim[vh] = active ? kv_len - p.seq_q + iq + 1 : 0;
+      if (vh == own) lim_own = active ? kv_len - p.seq_q + iq + 1 : 0;
       const ET* qrow = reinterpret_cast<const ET*>(p.q) + (((size_t)b * p.seq_q + (active ? iq : i0)) * p.H + h) * DK;
+      const float qs = active ? p.qscale : 0.f;
 #pragma unroll
       for (int qk = 0; qk < C::QK; ++qk) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(qrow + (li + L * qk) * CH));
-        Elem<ET>::chunk_to_f32(u, &qf[vh][qk * CH]);
-      }
+        float2 f[CH / 2];
+        chunk_to_f2<ET>(__ldg(reinterpret_cast<const uint4*>(qrow + (li + L * qk) * CH)), f);
 #pragma unroll
-      for (int e = 0; e < C::EK; ++e) qf[vh][e] = active ? qf[vh][e] * p.qscale : 0.f;
+        for (int e = 0; e < CH / 2; ++e) q2[vh][qk * (CH / 2) + e] = make_float2(f[e].x * qs, f[e].y * qs);
+      }
     }
+    const int gbase = rgw * L;  // first lane of this row group
+    const int rg = warp * C::RGW + rgw;
+
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % kStages;
       if (!warp_wait(&full[s], (t / kStages) & 1, abort_flag, p.err)) break;
@@ -286,58 +372,84 @@ __global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsPa
       const ET* sKn = reinterpret_cast<const ET*>(st);
       const ET* sKr = reinterpret_cast<const ET*>(st + C::kN);
       const ET* sV = reinterpret_cast<const ET*>(st + C::kN + C::kR);
-      for (int rbase = warp * C::RGW; rbase < n; rbase += C::NRG) {  // warp-uniform
-        const int r = rbase + rgw;
-        const bool valid = r < n;
-        const int rr = valid ? r : rbase;
-        float kf[C::EK];
+      // the two rows of this row group in the tile
+      const int ra = rg, rb2 = rg + C::NRG;
+      const bool va = ra < n, vb = rb2 < n;
+      const int rra = va ? ra : 0, rrb = vb ? rb2 : 0;
+      if (__any_sync(0xffffffffu, va)) {  // warp-uniform: some row of this warp is in the tile
+        // ---- scores: NV partial dot products per row
+        float pa[NV], pb[NV];
+#pragma unroll
+        for (int vh = 0; vh < NV; ++vh) pa[vh] = pb[vh] = 0.f;
 #pragma unroll
         for (int qk = 0; qk < C::QK; ++qk) {
           const int c = li + L * qk;
-          const ET* src = (DROT == 0 || qk < C::NCH / L) ? sKn + rr * C::DN + c * CH
-                                                          : sKr + rr * DROT + (c - C::NCH) * CH;
-          Elem<ET>::chunk_to_f32(*reinterpret_cast<const uint4*>(src), &kf[qk * CH]);
-        }
-        float sc[NV];
+          const ET* srcA = (DROT == 0 || qk < C::NCH / L) ? sKn + rra * C::DN + c * CH
+                                                           : sKr + rra * DROT + (c - C::NCH) * CH;
+          const ET* srcB = (DROT == 0 || qk < C::NCH / L) ? sKn + rrb * C::DN + c * CH
+                                                           : sKr + rrb * DROT + (c - C::NCH) * CH;
+          float2 ka[CH / 2], kb[CH / 2];
+          chunk_to_f2<ET>(*reinterpret_cast<const uint4*>(srcA), ka);
+          chunk_to_f2<ET>(*reinterpret_cast<const uint4*>(srcB), kb);
 #pragma unroll
-        for (int vh = 0; vh < NV; ++vh) {
-          float a0 = 0.f, a1 = 0.f;
+          for (int vh = 0; vh < NV; ++vh) {
+            float2 acc_a = make_float2(0.f, 0.f), acc_b = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < C::EK; e += 2) {
-            a0 = fmaf(qf[vh][e], kf[e], a0);
-            a1 = fmaf(qf[vh][e + 1], kf[e + 1], a1);
-          }
-          sc[vh] = a0 + a1;
-        }
-#pragma unroll
-        for (int off = L / 2; off >= 1; off >>= 1)
-#pragma unroll
-          for (int vh = 0; vh < NV; ++vh) sc[vh] += __shfl_xor_sync(0xffffffffu, sc[vh], off);
-        const int j = tr0 + rr;
-        float pv[NV];
-#pragma unroll
-        for (int vh = 0; vh < NV; ++vh) {
-          pv[vh] = 0.f;
-          if (valid && j < lim[vh]) {
-            if (sc[vh] > m[vh] + kRescaleLog2) {
-              const float f = exp2f(m[vh] - sc[vh]);  // 0 while m = -inf
-              l[vh] *= f;
-#pragma unroll
-              for (int e = 0; e < C::EV; ++e) o[vh][e] *= f;
-              m[vh] = sc[vh];
+            for (int e = 0; e < CH / 2; ++e) {
+              acc_a = __ffma2_rn(q2[vh][qk * (CH / 2) + e], ka[e], acc_a);
+              acc_b = __ffma2_rn(q2[vh][qk * (CH / 2) + e], kb[e], acc_b);
             }
-            pv[vh] = exp2f(sc[vh] - m[vh]);
-            l[vh] += pv[vh];
+            pa[vh] += acc_a.x + acc_a.y;
+            pb[vh] += acc_b.x + acc_b.y;
           }
+        }
+        const float sa = reduce_own<NV, L>(pa, li);
+        const float sb = reduce_own<NV, L>(pb, li);
+        // ---- online softmax of the owned head over the two rows
+        const bool visa = va && tr0 + ra < lim_own;
+        const bool visb = vb && tr0 + rb2 < lim_own;
+        const float mx = fmaxf(visa ? sa : -INFINITY, visb ? sb : -INFINITY);
+        const bool grow = mx > m_ref + kRescaleLog2;
+        float f = 1.f;
+        if (grow) {
+          f = ex2(m_ref - mx);  // 0 while m_ref = -inf
+          l_sum *= f;
+          m_ref = mx;
+        }
+        const float ea = visa ? ex2(sa - m_ref) : 0.f;
+        const float eb = visb ? ex2(sb - m_ref) : 0.f;
+        l_sum += ea + eb;
+        if (__any_sync(0xffffffffu, grow)) {  // rare: move every head's accumulators to its new max
+#pragma unroll
+          for (int vh = 0; vh < NV; ++vh) {
+            const float fh = NV == 1 ? f : __shfl_sync(0xffffffffu, f, gbase + owner_lane<NV, L>(vh));
+#pragma unroll
+            for (int e = 0; e < H2V; ++e) o2[vh][e] = make_float2(o2[vh][e].x * fh, o2[vh][e].y * fh);
+          }
+        }
+        // ---- probabilities to every lane of the group, then P.V
+        float2 pp[NV];
+#pragma unroll
+        for (int vh = 0; vh < NV; ++vh) {
+          const float xa = NV == 1 ? ea : __shfl_sync(0xffffffffu, ea, gbase + owner_lane<NV, L>(vh));
+          const float xb = NV == 1 ? eb : __shfl_sync(0xffffffffu, eb, gbase + owner_lane<NV, L>(vh));
+          pp[vh] = make_float2(xa, xb);
         }
 #pragma unroll
         for (int qv = 0; qv < C::QV; ++qv) {
-          float vf[CH];
-          Elem<ET>::chunk_to_f32(*reinterpret_cast<const uint4*>(sV + rr * DV + (li + L * qv) * CH), vf);
+          float2 fa[CH / 2], fb[CH / 2];
+          chunk_to_f2<ET>(*reinterpret_cast<const uint4*>(sV + rra * DV + (li + L * qv) * CH), fa);
+          chunk_to_f2<ET>(*reinterpret_cast<const uint4*>(sV + rrb * DV + (li + L * qv) * CH), fb);
 #pragma unroll
-          for (int vh = 0; vh < NV; ++vh)
+          for (int vh = 0; vh < NV; ++vh) {
+            const float2 wa = make_float2(pp[vh].x, pp[vh].x), wb = make_float2(pp[vh].y, pp[vh].y);
 #pragma unroll
-            for (int e = 0; e < CH; ++e) o[vh][qv * CH + e] = fmaf(pv[vh], vf[e], o[vh][qv * CH + e]);
+            for (int e = 0; e < CH / 2; ++e) {
+              float2& acc = o2[vh][qv * (CH / 2) + e];
+              acc = __ffma2_rn(wa, fa[e], acc);
+              acc = __ffma2_rn(wb, fb[e], acc);
+            }
+          }
         }
       }
       __syncwarp();
@@ -353,19 +465,19 @@ __global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsPa
   float* mo = ml + C::NRG * NV;                // [NRG][NV][DV]
   if (warp < kRowsWarps) {
     const int rg = warp * C::RGW + rgw;
+    if (li == owner_lane<NV, L>(own)) {
+      mm[rg * NV + own] = m_ref;
+      ml[rg * NV + own] = l_sum;
+    }
 #pragma unroll
-    for (int vh = 0; vh < NV; ++vh) {
-      if (li == 0) {
-        mm[rg * NV + vh] = m[vh];
-        ml[rg * NV + vh] = l[vh];
-      }
+    for (int vh = 0; vh < NV; ++vh)
 #pragma unroll
       for (int qv = 0; qv < C::QV; ++qv)
 #pragma unroll
-        for (int e = 0; e < CH; e += 4)
-          *reinterpret_cast<float4*>(&mo[(rg * NV + vh) * DV + (li + L * qv) * CH + e]) =
-              make_float4(o[vh][qv * CH + e], o[vh][qv * CH + e + 1], o[vh][qv * CH + e + 2], o[vh][qv * CH + e + 3]);
-    }
+        for (int e = 0; e < CH / 2; e += 2)
+          *reinterpret_cast<float4*>(&mo[(rg * NV + vh) * DV + (li + L * qv) * CH + 2 * e]) =
+              make_float4(o2[vh][qv * (CH / 2) + e].x, o2[vh][qv * (CH / 2) + e].y,
+                          o2[vh][qv * (CH / 2) + e + 1].x, o2[vh][qv * (CH / 2) + e + 1].y);
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < NV * DV; idx += blockDim.x) {
@@ -379,7 +491,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsPa
     if (M != -INFINITY) {
       for (int g = 0; g < C::NRG; ++g) {
         const float mg = mm[g * NV + vh];
-        const float w = (mg == -INFINITY) ? 0.f : exp2f(mg - M);
+        const float w = (mg == -INFINITY) ? 0.f : ex2(mg - M);
         ls = fmaf(w, ml[g * NV + vh], ls);
         os = fmaf(w, mo[(g * NV + vh) * DV + d], os);
       }

@@ -11,8 +11,12 @@ cudaError_t rows_dispatch_bf16_small(const RowsParams&, int, int, int, int, cuda
 cudaError_t rows_dispatch_bf16_d128(const RowsParams&, int, int, int, int, cudaStream_t);
 cudaError_t rows_dispatch_bf16_large(const RowsParams&, int, int, int, int, cudaStream_t);
 
-int rows_max_nv(int /*bf16*/, int dk, int dv, int drot) {
-  if (drot == 0 && dk == dv && (dk == 16 || dk == 32 || dk == 64)) return 8;
+// Largest NV instantiated for these widths: at most the lanes of a row group
+// (one lane per virtual head) and a register budget of ~128 floats for q and o.
+int rows_max_nv(int bf16, int dk, int dv, int drot) {
+  if (drot == 0 && dk == dv && dk == 16) return bf16 ? 2 : 4;
+  if (drot == 0 && dk == dv && dk == 32) return bf16 ? 4 : 8;
+  if (drot == 0 && dk == dv && dk == 64) return 8;
   if (drot == 0 && dk == 128 && dv == 128) return 4;
   if (drot == 0 && dk == 256 && dv == 256) return 2;
   if (dk == 192 && dv == 128 && (drot == 0 || drot == 64)) return 2;

@@ -8,7 +8,6 @@ cudaError_t rows_dispatch_f32_small(const RowsParams& p, int dk, int dv, int dro
     if (nv == 1) return launch_rows_inst<float, 16, 16, 0, 1>(p, st);
     if (nv == 2) return launch_rows_inst<float, 16, 16, 0, 2>(p, st);
     if (nv == 4) return launch_rows_inst<float, 16, 16, 0, 4>(p, st);
-    if (nv == 8) return launch_rows_inst<float, 16, 16, 0, 8>(p, st);
   }
   if (dk == 32 && dv == 32 && drot == 0) {
     if (nv == 1) return launch_rows_inst<float, 32, 32, 0, 1>(p, st);
