@@ -6,19 +6,29 @@
 // softmax(scale * q.k); everything else weighs exactly zero.
 //
 // One CTA = one (sequence, query head, 128-row query tile); CTAs are ordered
-// longest-first (the causal work of a tile grows with its index). Roles:
-//   warp 0      TMA producer: the Q tile once, then 128-key K and V tiles into a
-//               two-stage ring (128-byte swizzle, the layout the MMA reads).
-//   warp 1      allocates TMEM; one thread issues every tcgen05.mma:
-//               S = Q K^T (M=128, N=128, K=64) into TMEM columns [0,128), and
-//               O += P V (M=128, N=64, K=128) into TMEM columns [128,192).
-//   warps 2-5   softmax: thread t owns query row t (TMEM lane t). It reads its S
-//               row from TMEM, applies the causal mask (only tiles that cross the
-//               diagonal), keeps an online softmax with lazy rescaling (O is
-//               rescaled in TMEM only when the row maximum grows by more than
-//               2^8), writes P as bf16 into shared memory in the swizzled K-major
-//               layout, and finally normalises O and stores the output rows.
-// S is computed for tile j+1 while the softmax works on tile j.
+// longest-first (the causal work of a tile grows with its index). Roles, one
+// warpgroup each, with registers moved from the control warpgroup to the two
+// softmax warpgroups (setmaxnreg: 88 and 208 per thread from 168 at launch):
+//   warps 0-3   softmax warpgroup 0: key tiles 0, 2, 4, ...
+//   warps 4-7   softmax warpgroup 1: key tiles 1, 3, 5, ...
+//   warp 8      TMA producer: the Q tile once, then 128-key K and V tiles into a
+//               four-stage ring (128-byte swizzle, the layout the MMA reads).
+//   warps 9, 10 one thread each issues the tcgen05.mma of one softmax warpgroup
+//               (warp 9 also allocates and frees TMEM); warp 11 idles.
+// Warpgroup w owns S_w = Q K^T (M=128, N=128, K=64; TMEM columns 128w..),
+// O_w += P_w V (M=128, N=64, K=128; TMEM columns 256 + 64w..), and its P_w tile
+// in shared memory. Thread t of a warpgroup owns query row t (TMEM lane t).
+//
+// Softmax with lazy rescaling: p = 2^((s - m) * scale * log2 e) against a
+// reference max m that only moves when a score exceeds it by more than 2^8 in
+// p, which keeps every p <= 256 and leaves O / l unchanged. So after a row's
+// first tile, one pass over S computes p directly and tracks the tile max; in
+// the rare case the max moved that far, O_w is rescaled in TMEM and the pass is
+// redone with the new reference. The first tile takes the max first. Keys past
+// a row's position (only in tiles that cross the diagonal) weigh exactly zero.
+// The two warpgroups take turns for the exponential pass, so that one computes
+// while the tensor core runs the other's MMAs. At the end warpgroup 0 merges
+// the two partial (m, l, O) rows and stores bf16.
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
@@ -29,18 +39,26 @@ namespace {
 constexpr int kD = 64;     // head width (d_k = d_v)
 constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // keys per tile
-constexpr int kStagesKV = 2;
-constexpr int kThreads = 192;
+constexpr int kStagesKV = 4;
+constexpr int kWG = 2;     // softmax warpgroups
+constexpr int kThreads = (kWG + 1) * 128;  // two softmax warpgroups + one control warpgroup
+constexpr int kProducerWarp = 8, kMmaWarp0 = 9;
+// Registers per thread: 168 at launch (384 threads); the control warpgroup
+// gives up 80 per thread and the softmax warpgroups take 40 more:
+// 128 * 88 + 256 * 208 = 384 * 168.
+constexpr int kLaunchRegs = 168, kCtrlRegs = 88, kSoftmaxRegs = 208;
+static_assert(128 * kCtrlRegs + kWG * 128 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split over budget");
 constexpr int kTile = kBM * kD * 2;  // 16 KiB: one Q, K or V tile (128 rows x 128 bytes)
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColO = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256;  // S_w at 128w, O_w at 256 + 64w
 constexpr float kRescaleLog2 = 8.0f;
 
 // shared-memory map (from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kTile;                              // stage s: K at +0, V at +kTile
-constexpr int kOffP = kOffKV + kStagesKV * 2 * kTile;      // P: two 64-key halves
-constexpr int kOffBar = kOffP + 2 * kTile;
+constexpr int kOffP = kOffKV + kStagesKV * 2 * kTile;      // P_w: two 64-key halves each
+constexpr int kOffML = kOffP + kWG * 2 * kTile;            // warpgroup 1's row max and sum
+constexpr int kOffBar = kOffML + 2 * kBM * 4;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;           // + alignment slack
 
 struct TcParams {
@@ -52,17 +70,133 @@ struct TcParams {
 };
 
 struct Bars {
-  uint64_t q_full, kv_full[kStagesKV], kv_empty[kStagesKV], s_full, s_free, p_full, o_done, mma_final;
+  uint64_t q_full, kv_full[kStagesKV], kv_empty[kStagesKV];
+  uint64_t s_full[kWG], s_free[kWG], p_full[kWG], o_done[kWG], mma_final[kWG];
+  uint64_t turn[kWG];  // turn[w]: the other warpgroup finished an exponential pass
   uint32_t tmem_base;
   int abort_flag;
 };
 
+__device__ __forceinline__ bool aborted(Bars* bars) { return *reinterpret_cast<volatile int*>(&bars->abort_flag); }
+
+// Single-thread wait of the producer and MMA issuers: a spin, so that the next
+// TMA load or MMA goes out as soon as its barrier completes.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
-  if (*reinterpret_cast<volatile int*>(&bars->abort_flag)) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (aborted(bars)) return false;
+  if (mbar_spin(bar, parity)) return true;
   *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
   raise_error(err, kErrTimeout);
   return false;
+}
+
+// Whole-warp version: every lane agrees on the outcome.
+__device__ __forceinline__ bool warp_wait_tc(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
+  bool ok = !aborted(bars) && mbar_wait(bar, parity);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0) {
+    *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
+    raise_error(err, kErrTimeout);
+  }
+  return ok;
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^x for two bf16 values at once (special-function unit, subnormals flushed;
+// 2^-inf = 0).
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Row max of one S row (raw scores; masked keys excluded), from TMEM.
+__device__ __forceinline__ float row_max(uint32_t tS, bool diag, int j0, int pos) {
+  float mx8[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < kBN / 32; c += 2) {  // two loads in flight per wait
+    uint32_t v[2][32];
+    tc::tmem_ld_32x32b_x32(tS + c * 32, v[0]);
+    tc::tmem_ld_32x32b_x32(tS + (c + 1) * 32, v[1]);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float x = (diag && j0 + (c + u) * 32 + e > pos) ? -INFINITY : __uint_as_float(v[u][e]);
+        mx8[e & 7] = fmaxf(mx8[e & 7], x);
+      }
+  }
+  return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])), fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+}
+
+// One pass over an S row: p = 2^(s*qs - mq) written as bf16 into row r of P
+// (two 64-key halves, 128-byte swizzle: 16-byte chunk index XOR row % 8, the
+// K-major layout the PV MMA reads). Returns the sum of p; *tile_max gets the
+// row max of the raw scores (masked keys excluded).
+__device__ __forceinline__ float exp_pass(uint32_t tS, bool diag, int j0, int pos, float qs, float mq,
+                                          unsigned char* sP, int r, float* tile_max) {
+  const float2 qs2 = make_float2(qs, qs), nmq2 = make_float2(-mq, -mq);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t v[32];
+    tc::tmem_ld_32x32b_x32(tS + c * 32, v);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int q8 = 0; q8 < 4; ++q8) {
+      uint32_t w4[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int e = q8 * 8 + 2 * t;
+        float s0 = __uint_as_float(v[e]), s1 = __uint_as_float(v[e + 1]);
+        if (diag) {
+          if (j0 + c * 32 + e > pos) s0 = -INFINITY;
+          if (j0 + c * 32 + e + 1 > pos) s1 = -INFINITY;
+        }
+        mx4[t] = fmaxf(mx4[t], fmaxf(s0, s1));
+        // exponent argument in fp32, rounded to bf16x2, exponentiated two lanes at a
+        // time: the result is already the bf16 pair P stores; the row sum is taken
+        // from the same bf16 values, so numerator and denominator agree
+        const float2 x = __ffma2_rn(make_float2(s0, s1), qs2, nmq2);
+        const uint32_t pb = ex2_bf16x2(pack_bf16(x.x, x.y));
+        acc[t] = __fadd2_rn(acc[t], make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)));
+        w4[t] = pb;
+      }
+      const int cidx = c * 4 + q8;  // 16-byte chunk of the 256-byte P row
+      const int half = cidx / 8, ch = cidx % 8;
+      *reinterpret_cast<uint4*>(sP + half * kTile + r * 128 + ((ch ^ (r & 7)) * 16)) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+  }
+  *tile_max = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  return a.x + a.y;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -97,15 +231,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 128);
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->mma_final, 1);
+    for (int w = 0; w < kWG; ++w) {
+      mbar_init(&bars->s_full[w], 1);
+      mbar_init(&bars->s_free[w], 4);  // one arrival per softmax warp
+      mbar_init(&bars->p_full[w], 4);
+      mbar_init(&bars->o_done[w], 1);
+      mbar_init(&bars->mma_final[w], 1);
+      mbar_init(&bars->turn[w], 4);
+    }
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp0) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -114,7 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
+  if (warp >= kProducerWarp) {
+    regs_dec<kCtrlRegs>();  // the whole control warpgroup, right at the top of its branch
+  if (warp == kProducerWarp) {
     // ================= TMA producer =================
     if (lane == 0) {
       tc::prefetch_tmap(&tm_q);
@@ -122,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::prefetch_tmap(&tm_v);
       mbar_arrive_expect_tx(&bars->q_full, kTile);
       tc::tma_load_4d(smem + kOffQ, &tm_q, 0, h, i0, b, &bars->q_full);
-      int issued_last[kStagesKV] = {-1, -1};
+      int issued_last[kStagesKV] = {-1, -1, -1, -1};
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % kStagesKV;
         if (j >= kStagesKV && !wait_or_abort(&bars->kv_empty[st], ((j / kStagesKV) - 1) & 1, bars, p.err)) break;
@@ -137,180 +276,184 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued_last[st] >= 0 && !mbar_wait(&bars->kv_full[st], (issued_last[st] / kStagesKV) & 1))
           raise_error(p.err, kErrTimeout);
     }
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
+  } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+    // ================= MMA issuers: warp 9 for warpgroup 0, warp 10 for warpgroup 1 =================
+    const int w = warp - kMmaWarp0;
     if (lane == 0) {
+      const int n_mine = (n_kv - w + 1) / 2;
       const uint32_t idS = tc::idesc_bf16_f32(kBM, kBN, false);
       const uint32_t idO = tc::idesc_bf16_f32(kBM, kD, true);
-      const uint32_t sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP);
-      bool ok = wait_or_abort(&bars->q_full, 0, bars, p.err);
-      auto issue_s = [&](int j) -> bool {
+      // descriptors: constant high part + (shared address >> 4) in the low bits
+      constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);
+      const uint64_t dQ = kHi | (smem_u32(smem + kOffQ) >> 4);
+      const uint64_t dKV0 = kHi | (smem_u32(smem + kOffKV) >> 4);
+      const uint64_t dP = kHi | (smem_u32(smem + kOffP + w * 2 * kTile) >> 4);
+      const uint32_t dS = tmem + kColS + w * kBN, dO = tmem + kColO + w * kD;
+      auto issue_s = [&](int j) -> bool {  // S_w = Q K_j^T
         const int st = j % kStagesKV;
         if (!wait_or_abort(&bars->kv_full[st], (j / kStagesKV) & 1, bars, p.err)) return false;
         tc::fence_after_sync();
-        const uint32_t sK = smem_u32(smem + kOffKV + st * 2 * kTile);
+        const uint64_t dK = dKV0 + (uint64_t)((st * 2 * kTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          tc::mma_f16_ss(tmem + kColS, tc::smem_desc_sw128(sQ + kk * 32, 0, 1024),
-                         tc::smem_desc_sw128(sK + kk * 32, 0, 1024), idS, kk > 0);
-        tc::mma_commit(&bars->s_full);
+        for (int kk = 0; kk < kD / 16; ++kk) tc::mma_f16_ss(dS, dQ + kk * 2, dK + kk * 2, idS, kk > 0);
+        tc::mma_commit(&bars->s_full[w]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          ok = wait_or_abort(&bars->s_free, j & 1, bars, p.err) && issue_s(j + 1);
-          if (!ok) break;
-        }
-        if (!wait_or_abort(&bars->p_full, j & 1, bars, p.err)) break;
+      bool ok = n_mine > 0 && wait_or_abort(&bars->q_full, 0, bars, p.err) && issue_s(w);
+      for (int k = 0; ok && k < n_mine; ++k) {
+        const int j = 2 * k + w;
+        if (!wait_or_abort(&bars->p_full[w], k & 1, bars, p.err)) break;
         tc::fence_after_sync();
         const int st = j % kStagesKV;
-        const uint32_t sV = smem_u32(smem + kOffKV + st * 2 * kTile + kTile);
+        const uint64_t dV = dKV0 + (uint64_t)((st * 2 * kTile + kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_f16_ss(tmem + kColO, tc::smem_desc_sw128(sP + (kk / 4) * kTile + (kk % 4) * 32, 0, 1024),
-                         tc::smem_desc_sw128(sV + kk * 2048, 0, 1024), idO, (j > 0 || kk > 0));
-        tc::mma_commit(&bars->o_done);
-        tc::mma_commit(&bars->kv_empty[st]);
+          tc::mma_f16_ss(dO, dP + (((kk / 4) * kTile + (kk % 4) * 32) >> 4), dV + kk * (2048 >> 4), idO,
+                         (k > 0 || kk > 0));
+        tc::mma_commit(&bars->o_done[w]);
+        tc::mma_commit(&bars->kv_empty[st]);  // stage st only ever holds tiles of this warpgroup's parity
+        if (k + 1 < n_mine)  // S_w is free once the warpgroup has read it (before it published P_j)
+          ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
       }
       // every MMA issued above has completed before TMEM is released
-      tc::mma_commit(&bars->mma_final);
-      if (!mbar_wait(&bars->mma_final, 0)) raise_error(p.err, kErrTimeout);
+      tc::mma_commit(&bars->mma_final[w]);
+      if (!mbar_wait(&bars->mma_final[w], 0)) raise_error(p.err, kErrTimeout);
     }
+  }
   } else {
-    // ================= softmax warps (2..5) =================
-    const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int r = quarter * 32 + lane;       // query row within the tile
+    // ================= softmax warpgroups =================
+    regs_inc<kSoftmaxRegs>();  // both softmax warpgroups, right at the top of their branch
+    const int wg = warp >> 2;  // 0 or 1
+    const int quarter = warp & 3;                     // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;                // query row within the tile
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const int pos = off + i0 + r;            // absolute position of this row
+    const int pos = off + i0 + r;                     // absolute position of this row
     const float qs = p.qscale;
     const float th = kRescaleLog2 / qs;
-    float m_ref = -INFINITY, l = 0.f;
-    unsigned char* sP = smem + kOffP;
+    float m_ref = -INFINITY, l_sum = 0.f;
+    unsigned char* sP = smem + kOffP + wg * 2 * kTile;
+    const uint32_t tS = tmem + lane_addr + kColS + wg * kBN;
+    const uint32_t tO = tmem + lane_addr + kColO + wg * kD;
+    const int n_mine = (n_kv - wg + 1) / 2;  // key tiles this warpgroup handles
     bool alive = true;
-    for (int j = 0; j < n_kv && alive; ++j) {
-      bool ok = mbar_wait(&bars->s_full, j & 1) && !*reinterpret_cast<volatile int*>(&bars->abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        if (lane == 0) {
-          *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
-          raise_error(p.err, kErrTimeout);
-        }
+    for (int k = 0; k < n_mine; ++k) {
+      const int j = 2 * k + wg;
+      const int j0 = j * kBN;
+      const bool diag = j0 + kBN - 1 > off + i0;  // this tile crosses the diagonal of some row
+      if (!warp_wait_tc(&bars->s_full[wg], k & 1, bars, p.err)) {
         alive = false;
         break;
       }
       tc::fence_after_sync();
-      float s[kBN];
-      {
-        uint32_t v[32];
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          tc::tmem_ld_32x32b_x32(tmem + lane_addr + kColS + c * 32, v);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
-        }
-      }
-      tc::fence_before_sync();
-      mbar_arrive(&bars->s_free);
-
-      const int j0 = j * kBN;
-      if (j0 + kBN - 1 > off + i0) {  // this tile crosses the diagonal of some row
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (j0 + c > pos) s[c] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-      float f = 1.f;
-      const bool grow = mx > m_ref + th;
-      if (grow) {
-        f = exp2f((m_ref - mx) * qs);  // 0 while m_ref = -inf
-        l *= f;
-        m_ref = mx;
-      }
-      const float mq = m_ref * qs;
-      float sum = 0.f;
-      uint32_t pk[kBN / 2];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float p0 = exp2f(fmaf(s[c], qs, -mq));
-        const float p1 = exp2f(fmaf(s[c + 1], qs, -mq));
-        sum += p0 + p1;
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        pk[c / 2] = *reinterpret_cast<const uint32_t*>(&pb);
-      }
-      l += sum;
-
-      if (j > 0) {  // PV of tile j-1 done: P may be overwritten and O is stable
-        ok = mbar_wait(&bars->o_done, (j - 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) {
-          if (lane == 0) raise_error(p.err, kErrTimeout);
-          alive = false;
-          break;
-        }
+      if (k == 0) {
+        m_ref = row_max(tS, diag, j0, pos);  // first tile: the max first (nothing to rescale yet)
+      } else if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
+        alive = false;  // P_w is free and O_w stable once this warpgroup's previous PV is done
+        break;
+      } else {
         tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, grow)) {  // rescale O in TMEM (rare)
+      }
+      // The two warpgroups take turns for the exponential pass (warpgroup 0's pass
+      // k, then warpgroup 1's pass k, then warpgroup 0's pass k+1, ...), so one
+      // computes exponentials while the tensor core runs the other's PV and S.
+      if (!(wg == 0 && k == 0) &&
+          !warp_wait_tc(&bars->turn[wg], (wg == 0 ? k - 1 : k) & 1, bars, p.err)) {
+        alive = false;
+        break;
+      }
+      float tsum = 0.f;
+      for (int pass = 0; pass < 2; ++pass) {
+        float tile_max;
+        const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
+        tsum = exp_pass(tS, diag, j0, pos, qs, mq, sP, r, &tile_max);
+        const bool grow = tile_max > m_ref + th;
+        if (!__any_sync(0xffffffffu, grow)) break;
+        // rare: move to the new reference max, rescale O_w and l, then redo the pass
+        float f = 1.f;
+        if (grow) {
+          f = ex2f((m_ref - tile_max) * qs);  // 0 while m_ref = -inf
+          l_sum *= f;
+          m_ref = tile_max;
+        }
+        if (k > 0) {
           uint32_t o[32];
 #pragma unroll
           for (int c = 0; c < kD / 32; ++c) {
-            tc::tmem_ld_32x32b_x32(tmem + lane_addr + kColO + c * 32, o);
+            tc::tmem_ld_32x32b_x32(tO + c * 32, o);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tc::tmem_st_32x32b_x32(tmem + lane_addr + kColO + c * 32, o);
+            tc::tmem_st_32x32b_x32(tO + c * 32, o);
           }
           tc::tmem_st_wait();
         }
       }
-      // P row r, 128 keys as two 64-key halves, 128-byte swizzle (16-byte chunk
-      // index XOR row % 8) -- the K-major layout the PV MMA reads.
-#pragma unroll
-      for (int cidx = 0; cidx < kBN / 8; ++cidx) {
-        const int half = cidx / 8, ch = cidx % 8;
-        uint4* dst = reinterpret_cast<uint4*>(sP + half * kTile + r * 128 + ((ch ^ (r & 7)) * 16));
-        *dst = make_uint4(pk[cidx * 4], pk[cidx * 4 + 1], pk[cidx * 4 + 2], pk[cidx * 4 + 3]);
+      l_sum += tsum;
+      tc::fence_before_sync();  // this thread's reads of S_w are done
+      tc::fence_async_smem();   // this thread's P_w writes visible to the tensor core
+      __syncwarp();             // ... for every lane of the warp; one lane signals
+      if (lane == 0) {
+        mbar_arrive(&bars->turn[wg ^ 1]);
+        mbar_arrive(&bars->s_free[wg]);
+        mbar_arrive(&bars->p_full[wg]);
       }
-      tc::fence_async_smem();
-      tc::fence_before_sync();
-      mbar_arrive(&bars->p_full);
     }
-    // ---- epilogue: O / l -> bf16 rows
-    if (alive) {
-      const bool ok = mbar_wait(&bars->o_done, (n_kv - 1) & 1);
-      if (__all_sync(0xffffffffu, ok)) {
-        tc::fence_after_sync();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.out + (((size_t)b * p.S + i0 + r) * p.H + h) * kD;
+    // ---- this warpgroup's last PV, then warpgroup 1 hands (m, l) to warpgroup 0
+    bool have_o = alive && n_mine > 0;
+    if (have_o) {
+      have_o = warp_wait_tc(&bars->o_done[wg], (n_mine - 1) & 1, bars, p.err);
+      tc::fence_after_sync();
+    }
+    float* sm = reinterpret_cast<float*>(smem + kOffML);
+    if (wg == 1) {
+      sm[r] = have_o ? m_ref : -INFINITY;
+      sm[kBM + r] = have_o ? l_sum : 0.f;
+    }
+    tc::fence_before_sync();  // order warpgroup 1's view of its finished O_1 before the hand-off
+    named_bar_sync(1, kWG * 128);
+    tc::fence_after_sync();
+    if (wg == 0 && have_o) {
+      const float m1 = sm[r], l1 = sm[kBM + r];
+      const bool use1 = n_kv > 1 && l1 > 0.f;  // warpgroup 1 wrote O_1 and saw a visible key
+      const float M = use1 ? fmaxf(m_ref, m1) : m_ref;
+      const float a0 = (m_ref == -INFINITY) ? 0.f : ex2f((m_ref - M) * qs);
+      const float a1 = use1 ? ex2f((m1 - M) * qs) : 0.f;
+      const float l = a0 * l_sum + a1 * l1;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float c0 = a0 * inv, c1 = a1 * inv;
+      __nv_bfloat16* orow = p.out + (((size_t)b * p.S + i0 + r) * p.H + h) * kD;
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
-          uint32_t o[32];
-          tc::tmem_ld_32x32b_x32(tmem + lane_addr + kColO + c * 32, o);
-          tc::tmem_ld_wait();
-          if (r < rows) {
+      for (int c = 0; c < kD / 16; ++c) {
+        uint32_t o0[16], o1[16];
+        tc::tmem_ld_32x32b_x16(tmem + lane_addr + kColO + c * 16, o0);
+        if (n_kv > 1) tc::tmem_ld_32x32b_x16(tmem + lane_addr + kColO + kD + c * 16, o1);
+        tc::tmem_ld_wait();
+        if (r < rows) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint32_t w[4];
+          for (int e = 0; e < 16; e += 8) {
+            uint32_t w4[4];
 #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(o[e + 2 * t]) * inv,
-                                                                __uint_as_float(o[e + 2 * t + 1]) * inv);
-                w[t] = *reinterpret_cast<const uint32_t*>(&v2);
+            for (int t = 0; t < 4; ++t) {
+              float x0 = __uint_as_float(o0[e + 2 * t]) * c0, x1 = __uint_as_float(o0[e + 2 * t + 1]) * c0;
+              if (use1) {
+                x0 = fmaf(__uint_as_float(o1[e + 2 * t]), c1, x0);
+                x1 = fmaf(__uint_as_float(o1[e + 2 * t + 1]), c1, x1);
               }
-              *reinterpret_cast<uint4*>(orow + c * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
+              w4[t] = pack_bf16(x0, x1);
             }
+            *reinterpret_cast<uint4*>(orow + c * 16 + e) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
-      } else if (lane == 0) {
-        raise_error(p.err, kErrTimeout);
       }
+    } else if (wg == 0 && lane == 0 && !have_o) {
+      raise_error(p.err, kErrTimeout);
     }
   }
 
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -370,7 +513,14 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
   cudaGetDevice(&dev);
   static unsigned long long attr_done = 0;
   if (dev < 64 && !(attr_done >> dev & 1ull)) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // The register hand-over inside the kernel assumes exactly kLaunchRegs per
+    // thread at launch; with any other allocation it could wait forever, so
+    // such a build is refused here instead of launched.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorNotSupported;
+    e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << dev;
   }
