@@ -1,5 +1,7 @@
 // kernels_aux.cu -- split combine, interleaved RoPE, paged KV append, and the
 // dispatch of the SIMT attention instantiations.
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -95,10 +97,30 @@ cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStre
 // be off by ~2e-3 rad); sine and cosine of the reduced angle come from the
 // fp32 sincosf, the rotation is done in fp32 and rounded once on store.
 
-__device__ __forceinline__ void rope_angle(double pos, int pair, int rot_dim, double theta, float* c, float* s) {
-  const double w = pow(theta, -2.0 * pair / rot_dim);
-  const double a = remainder(pos * w, 6.283185307179586476925286766559);
-  sincosf((float)a, s, c);
+// 2*pi split into a double and the double nearest to its remainder (Cody and
+// Waite's reduction): a - n*HI - n*LO keeps ~1e-15 rad for |n| < 2^20.
+constexpr double kTwoPiHi = 6.283185307179586;
+constexpr double kTwoPiLo = 2.4492935982947064e-16;
+constexpr double kInvTwoPi = 0.15915494309189535;
+
+__device__ __forceinline__ void rope_cos_sin(double pos, double w, float* c, float* s) {
+  const double a = pos * w;
+  const double n = rint(a * kInvTwoPi);
+  const double r = fma(-n, kTwoPiLo, fma(-n, kTwoPiHi, a));
+  sincosf((float)r, s, c);
+}
+
+// The rot_dim/2 frequencies theta^(-2t/rot_dim), t < rot_dim/2, computed once
+// per call on the host in double and passed by value (they depend only on the
+// call's scalar arguments).
+struct RopeFreqs {
+  double w[128];
+};
+
+RopeFreqs rope_freqs(int rot_dim, double theta) {
+  RopeFreqs f{};
+  for (int t = 0; t < rot_dim / 2 && t < 128; ++t) f.w[t] = std::pow(theta, -2.0 * t / rot_dim);
+  return f;
 }
 
 template <typename ET>
@@ -108,9 +130,10 @@ __device__ __forceinline__ void rotate_pair(ET* x, float c, float s) {
   x[1] = Elem<ET>::from_f32(fmaf(x0, s, x1 * c));
 }
 
+// One thread per (token, pair), looping over the heads.
 template <typename ET>
 __global__ void __launch_bounds__(256) rope_kernel(ET* x, const int32_t* positions, int B, int T, int heads, int d,
-                                                   int heads_outer, int rot_offset, int rot_dim, double theta) {
+                                                   int heads_outer, int rot_offset, int rot_dim, const RopeFreqs fr) {
   const int npairs = rot_dim / 2;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)B * T * npairs) return;
@@ -118,7 +141,7 @@ __global__ void __launch_bounds__(256) rope_kernel(ET* x, const int32_t* positio
   const long long tok = idx / npairs;  // b * T + t
   const int b = (int)(tok / T), t = (int)(tok % T);
   float c, s;
-  rope_angle((double)positions[tok], pr, rot_dim, theta, &c, &s);
+  rope_cos_sin((double)positions[tok], fr.w[pr], &c, &s);
   for (int h = 0; h < heads; ++h) {
     const size_t row = heads_outer ? (((size_t)b * heads + h) * T + t) : ((size_t)tok * heads + h);
     rotate_pair(x + row * d + rot_offset + 2 * pr, c, s);
@@ -129,13 +152,15 @@ cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int hea
                         int rot_offset, int rot_dim, double theta, int bf16, cudaStream_t st) {
   const long long total = (long long)B * T * (rot_dim / 2);
   if (total <= 0 || heads <= 0) return cudaSuccess;
+  if (rot_dim > 256) return cudaErrorNotSupported;
   const unsigned blocks = (unsigned)((total + 255) / 256);
+  const RopeFreqs fr = rope_freqs(rot_dim, theta);
   if (bf16)
     rope_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(x), positions, B, T, heads,
-                                                        d, heads_outer, rot_offset, rot_dim, theta);
+                                                        d, heads_outer, rot_offset, rot_dim, fr);
   else
     rope_kernel<float><<<blocks, 256, 0, st>>>(reinterpret_cast<float*>(x), positions, B, T, heads, d, heads_outer,
-                                               rot_offset, rot_dim, theta);
+                                               rot_offset, rot_dim, fr);
   return cudaGetLastError();
 }
 
@@ -149,7 +174,8 @@ template <typename ET>
 __global__ void __launch_bounds__(128) append_kernel(ET* q, const ET* k_new, const ET* v_new, ET* k_pool, ET* v_pool,
                                                      const int32_t* tables, const int32_t* lens_in, int32_t* lens_out,
                                                      int mbps, int num_blocks, int bs, int H, int Hkv, int dk, int dv,
-                                                     double theta, int rot_offset, int rot_dim, unsigned* err) {
+                                                     bool rope, const RopeFreqs fr, int rot_offset, int rot_dim,
+                                                     unsigned* err) {
   const int b = blockIdx.x;
   const int p = lens_in[b];
   const bool pos_ok = p >= 0 && (long long)p < (long long)mbps * bs;
@@ -164,11 +190,10 @@ __global__ void __launch_bounds__(128) append_kernel(ET* q, const ET* k_new, con
     return;
   }
   const int row = p % bs;
-  const bool rope = theta > 0.0 && rot_dim > 0;
   if (rope) {
     for (int pr = threadIdx.x; pr < rot_dim / 2; pr += blockDim.x) {
       float c, s;
-      rope_angle((double)p, pr, rot_dim, theta, &c, &s);
+      rope_cos_sin((double)p, fr.w[pr], &c, &s);
       const int e = rot_offset + 2 * pr;
       for (int h = 0; h < H; ++h) rotate_pair(q + ((size_t)b * H + h) * dk + e, c, s);
       for (int kh = 0; kh < Hkv; ++kh) {
@@ -198,17 +223,20 @@ cudaError_t launch_append(void* q, const void* k_new, const void* v_new, void* k
                           int num_blocks, int bs, int H, int Hkv, int dk, int dv, double theta, int rot_offset,
                           int rot_dim, int bf16, unsigned* err, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
+  const bool rope = theta > 0.0 && rot_dim > 0;
+  if (rope && rot_dim > 256) return cudaErrorNotSupported;
+  const RopeFreqs fr = rope_freqs(rope ? rot_dim : 0, theta);
   if (bf16)
     append_kernel<__nv_bfloat16><<<B, 128, 0, st>>>(
         reinterpret_cast<__nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
         reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__nv_bfloat16*>(k_pool),
         reinterpret_cast<__nv_bfloat16*>(v_pool), tables, lens_in, lens_out, mbps, num_blocks, bs, H, Hkv, dk, dv,
-        theta, rot_offset, rot_dim, err);
+        rope, fr, rot_offset, rot_dim, err);
   else
     append_kernel<float><<<B, 128, 0, st>>>(reinterpret_cast<float*>(q), reinterpret_cast<const float*>(k_new),
                                             reinterpret_cast<const float*>(v_new), reinterpret_cast<float*>(k_pool),
                                             reinterpret_cast<float*>(v_pool), tables, lens_in, lens_out, mbps,
-                                            num_blocks, bs, H, Hkv, dk, dv, theta, rot_offset, rot_dim, err);
+                                            num_blocks, bs, H, Hkv, dk, dv, rope, fr, rot_offset, rot_dim, err);
   return cudaGetLastError();
 }
 
