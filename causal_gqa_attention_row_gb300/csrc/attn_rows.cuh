@@ -79,6 +79,7 @@ struct RowsCfg {
   static constexpr int data_bytes = cmax(NS * stage_bytes, merge_bytes);
   static constexpr int kHeader = 128;  // mbarriers + flags
   static constexpr int smem_bytes = kHeader + data_bytes;
+  static constexpr int MIN_CTAS = 2;  // CTAs per SM the register budget targets
   static_assert(DK % CH == 0 && DV % CH == 0 && DN % CH == 0, "head widths must be whole 16-byte chunks");
   static_assert(KCH % L == 0 && VCH % L == 0 && NCH % L == 0, "chunks must split evenly over a row group");
   static_assert(32 % L == 0, "row groups must tile a warp");
@@ -174,7 +175,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <typename ET, int DK, int DV, int DROT, int NV>
-__global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsParams p) {
+__global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::MIN_CTAS)
+    attn_rows_kernel(const RowsParams p) {
   using C = RowsCfg<ET, DK, DV, DROT, NV>;
   constexpr int CH = C::CH, L = C::L, T = C::T, kStages = C::NS;
   constexpr int H2K = C::EK / 2, H2V = C::EV / 2;  // float2 pairs per lane
@@ -378,9 +380,9 @@ __global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsPa
       const int rra = va ? ra : 0, rrb = vb ? rb2 : 0;
       if (__any_sync(0xffffffffu, va)) {  // warp-uniform: some row of this warp is in the tile
         // ---- scores: NV partial dot products per row
-        float pa[NV], pb[NV];
+        float2 acc_a[NV], acc_b[NV];  // paired partial sums, folded once per row
 #pragma unroll
-        for (int vh = 0; vh < NV; ++vh) pa[vh] = pb[vh] = 0.f;
+        for (int vh = 0; vh < NV; ++vh) acc_a[vh] = acc_b[vh] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int qk = 0; qk < C::QK; ++qk) {
           const int c = li + L * qk;
@@ -392,16 +394,18 @@ __global__ void __launch_bounds__(kRowsThreads, 2) attn_rows_kernel(const RowsPa
           chunk_to_f2<ET>(*reinterpret_cast<const uint4*>(srcA), ka);
           chunk_to_f2<ET>(*reinterpret_cast<const uint4*>(srcB), kb);
 #pragma unroll
-          for (int vh = 0; vh < NV; ++vh) {
-            float2 acc_a = make_float2(0.f, 0.f), acc_b = make_float2(0.f, 0.f);
+          for (int vh = 0; vh < NV; ++vh)
 #pragma unroll
             for (int e = 0; e < CH / 2; ++e) {
-              acc_a = __ffma2_rn(q2[vh][qk * (CH / 2) + e], ka[e], acc_a);
-              acc_b = __ffma2_rn(q2[vh][qk * (CH / 2) + e], kb[e], acc_b);
+              acc_a[vh] = __ffma2_rn(q2[vh][qk * (CH / 2) + e], ka[e], acc_a[vh]);
+              acc_b[vh] = __ffma2_rn(q2[vh][qk * (CH / 2) + e], kb[e], acc_b[vh]);
             }
-            pa[vh] += acc_a.x + acc_a.y;
-            pb[vh] += acc_b.x + acc_b.y;
-          }
+        }
+        float pa[NV], pb[NV];
+#pragma unroll
+        for (int vh = 0; vh < NV; ++vh) {
+          pa[vh] = acc_a[vh].x + acc_a[vh].y;
+          pb[vh] = acc_b[vh].x + acc_b[vh].y;
         }
         const float sa = reduce_own<NV, L>(pa, li);
         const float sb = reduce_own<NV, L>(pb, li);
