@@ -52,6 +52,10 @@ gqa_status from_cuda(cudaError_t e) {
 }
 
 gqa_status launch_rows(const gqa::RowsParams& p, int bf16, int dk, int dv, int drot, int nv, cudaStream_t st) {
+  if (p.sched) {
+    const cudaError_t ep = gqa::launch_plan_units(p, st);
+    if (ep != cudaSuccess) return from_cuda(ep);
+  }
   cudaError_t e = bf16 ? gqa::launch_attn_rows_bf16(p, dk, dv, drot, nv, st)
                        : gqa::launch_attn_rows_f32(p, dk, dv, drot, nv, st);
   if (e != cudaSuccess) return from_cuda(e);
@@ -66,7 +70,8 @@ extern "C" {
 size_t attn_decode_workspace_bytes(int B, int H, int d_v, int max_len_upper_bound) {
   if (B <= 0 || H <= 0 || d_v <= 0 || max_len_upper_bound <= gqa::kSplitRows) return 0;
   const size_t splits = (size_t)ceil_div(max_len_upper_bound, gqa::kSplitRows);
-  return (size_t)B * (size_t)H * splits * (size_t)(d_v + 2) * sizeof(float);
+  const size_t units = (size_t)B * (size_t)H * splits;  // at least the (item, split) units of a call
+  return gqa::plan_bytes(units) + units * (size_t)(d_v + 2) * sizeof(float);
 }
 
 static gqa_status decode_common(gqa::RowsParams& p, int bf16, int d_k, int d_v, int d_rot, void* workspace,
@@ -86,7 +91,12 @@ static gqa_status decode_common(gqa::RowsParams& p, int bf16, int d_k, int d_v, 
     if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_INVALID_ARG;
   }
-  p.partial = static_cast<float*>(workspace);
+  if (need > 0) {
+    const size_t units = (size_t)p.B * (size_t)p.H * (size_t)p.max_splits;
+    p.sched = static_cast<int*>(workspace);
+    p.units = reinterpret_cast<int2*>(static_cast<char*>(workspace) + gqa::kPlanHeaderBytes);
+    p.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + gqa::plan_bytes(units));
+  }
   p.err = error_word();
   if (!p.err) return GQA_ERR_CUDA;
   p.debug_withhold = g_withhold_first_tile;

@@ -5,24 +5,40 @@
 // i at position offset + i sees keys 0..=offset + i; softmax over the visible
 // keys of scale * q.k, then the weighted sum of V.
 //
-// One CTA is one work item: (sequence b, KV head kvh, a chunk of GH of that KV
-// head's G query heads, a block of QR query rows, a split of the key range).
-// Its GH*QR = NV "virtual heads" (query row, query head) all read the SAME K/V
+// Work units: (sequence b, KV head kvh, a chunk of GH of that KV head's G
+// query heads, a block of QR query rows, a split of the key range). A unit's
+// GH*QR = NV "virtual heads" (query row, query head) all read the SAME K/V
 // rows, so each K/V row crosses HBM once per KV head however large the group
 // (frink-models src/decoder/attn_block.rs and kopitiam's module doc: every
 // query head of a group genuinely shares its KV head).
+//
+// Scheduling: the kernel is persistent, one CTA per resident slot. With a
+// split-K workspace, a one-CTA plan kernel first lists the units that have keys
+// (every full split, then every item's final partial split) and the CTAs take
+// units from that list one at a time through an atomic ticket, so the work
+// balances to within one unit whatever the length mix. Without one (a single
+// split per item) CTA c takes items c, c + grid, ... The producer warp alone
+// fetches units; each tile it passes through the ring carries the unit's
+// coordinates, so the compute warps simply follow the ring, and the copies of
+// the next unit stream in while they merge the current one. A unit's first tile
+// also brings its query rows into shared memory.
 //
 // Data path: one producer warp streams K/V tiles of T rows into an NS-deep
 // shared-memory ring with 1-D bulk copies (cp.async.bulk, the TMA engine)
 // completing on mbarriers. Contiguous caches need one copy per tile and
 // operand; paged caches one per block segment, the block-table gather done by
 // the copy engine (frink-models src/decoder/attn_block.rs, `push_and_attend_row`,
-// paged arm). Four compute warps consume the ring.
+// paged arm). Four compute warps consume the ring. A unit whose block-table
+// entries are out of range is caught by the producer before any of its copies;
+// the producer then writes the unit's empty result itself.
 //
 // Compute mapping: a "row group" of L lanes owns one key row at a time; lane li
-// holds the 16-byte chunks li, li+L, li+2L, ... of q (fp32, pre-scaled by
-// scale*log2 e) for each virtual head and of its own output accumulators, as
-// float2 pairs for the paired FFMA2 instruction. A row's NV scores are L-lane
+// works on the 16-byte chunks li, li+L, li+2L, ... of each row. It keeps its
+// chunks of the output accumulators of every virtual head in registers, as
+// float2 pairs for the paired FFMA2 instruction, and reads the matching chunks of
+// q (fp32, pre-scaled by scale*log2 e) from its warp's copy in shared memory (the
+// warp's row groups read the same addresses: 4-way broadcasts). Keeping q out of
+// the registers lets three CTAs share an SM. A row's NV scores are L-lane
 // partial dot products finished by a halving ("transpose") butterfly: each
 // shuffle step also halves the number of heads a lane carries, so the lane ends
 // up owning ONE head's full score. That lane alone runs the online softmax of
@@ -33,15 +49,18 @@
 // independent dot products, one max/rescale check, two exponentials. Rescaling
 // is lazy: o and l move to a new reference max only when a score exceeds the
 // current one by more than 2^8, which keeps every term <= 256 and leaves o / l
-// unchanged. At the end the row groups are merged through shared memory in a
-// fixed order (log-sum-exp), then written as the output (one split) or as a
-// partial (m, l, o) that the combine kernel merges, again in a fixed order.
+// unchanged. At the end of a unit the row groups of each warp are merged in
+// registers (xor butterflies), then the warps through a shared-memory area of
+// their own (not the ring), always in the same order (log-sum-exp); the result
+// is written as the output (one split) or as a partial (m, l, o) that the
+// combine kernel merges, again in a fixed order.
 //
 // Determinism: split boundaries are multiples of kSplitRows, tiles multiples of
 // T rows from the split start, and the row -> row-group assignment a function of
 // the key index only. The arithmetic on a key row therefore does not depend on
-// where the row lives (contiguous or paged), on the block table, or on the other
-// sequences of the batch: paged and contiguous results are bit-identical.
+// where the row lives (contiguous or paged), on the block table, on the other
+// sequences of the batch or on which CTA takes the unit: paged and contiguous
+// results are bit-identical, and so are repeated calls.
 #pragma once
 
 #include "common.cuh"
@@ -52,12 +71,26 @@ namespace gqa {
 constexpr int kRowsWarps = 4;  // compute warps
 constexpr int kRowsThreads = (kRowsWarps + 1) * 32;
 constexpr int kMaxStages = 4;
-constexpr int kRingBudget = 128 * 1024;  // shared-memory ring per CTA (two CTAs per SM)
+constexpr int kSmemBudget = 74 * 1024;  // shared memory per CTA (three CTAs per SM)
+constexpr int kSmemPerSM = 228 * 1024;  // shared memory of one SM
+constexpr int kSmemPerCTAReserved = 1024;
 constexpr float kRescaleLog2 = 8.0f;
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 constexpr int clog2(int x) { return x <= 1 ? 0 : 1 + clog2(x / 2); }
+
+// Shared-memory header of the attention kernel.
+struct RowsHeader {
+  uint64_t full[kMaxStages];   // a tile has landed in the stage
+  uint64_t empty[kMaxStages];  // the compute warps are done with the stage
+  uint64_t merge[2];           // merge area: written / read by every compute warp
+  int abort_flag;
+  int pad_;
+  // Per stage, the tile it holds: {item (-1: no more work), split, first key row,
+  // rows | first tile of its unit << 16 | last tile << 17}.
+  int4 tile[kMaxStages];
+};
 
 template <typename ET, int DK, int DV, int DROT, int NV>
 struct RowsCfg {
@@ -72,19 +105,24 @@ struct RowsCfg {
   static constexpr int NRG = kRowsWarps * RGW;
   static constexpr int T = 2 * NRG;                  // rows per tile: two per row group
   static constexpr int kN = T * DN * ES, kR = T * DROT * ES, kV = T * DV * ES;
-  static constexpr int stage_bytes = kN + kR + kV;
+  static constexpr int kQ = NV * DK * ES;  // the unit's query rows, carried by its first tile
+  static constexpr int stage_bytes = kN + kR + kV + kQ;
   static constexpr int row_bytes = (DN + DROT + DV) * ES;
-  static constexpr int NS = cmax(2, cmin(kMaxStages, kRingBudget / stage_bytes));  // ring depth
-  static constexpr int merge_bytes = NRG * NV * (DV + 2) * 4;
-  static constexpr int data_bytes = cmax(NS * stage_bytes, merge_bytes);
-  static constexpr int kHeader = 128;  // mbarriers + flags
-  static constexpr int smem_bytes = kHeader + data_bytes;
-  static constexpr int MIN_CTAS = 2;  // CTAs per SM the register budget targets
+  static constexpr int kHeader = 256;  // RowsHeader
+  static constexpr int merge_bytes = kRowsWarps * NV * (DV + 2) * 4;  // one (m, l, o) per warp and head
+  static constexpr int qbuf_bytes = kRowsWarps * NV * DK * 4;         // each warp's fp32 queries
+  static constexpr int NS = cmax(
+      2, cmin(kMaxStages, (kSmemBudget - kHeader - merge_bytes - qbuf_bytes) / stage_bytes));  // ring depth
+  static constexpr int ring_bytes = NS * stage_bytes;
+  static constexpr int smem_bytes = kHeader + ring_bytes + qbuf_bytes + merge_bytes;
+  // CTAs per SM the register budget targets: three where shared memory allows.
+  static constexpr int MIN_CTAS = cmax(1, cmin(3, kSmemPerSM / (smem_bytes + kSmemPerCTAReserved)));
   static_assert(DK % CH == 0 && DV % CH == 0 && DN % CH == 0, "head widths must be whole 16-byte chunks");
   static_assert(KCH % L == 0 && VCH % L == 0 && NCH % L == 0, "chunks must split evenly over a row group");
   static_assert(32 % L == 0, "row groups must tile a warp");
   static_assert(NV <= L, "a row group needs at least one lane per virtual head");
   static_assert(kSplitRows % T == 0, "split boundaries must fall on tile boundaries");
+  static_assert(sizeof(RowsHeader) <= kHeader, "the header must fit its reserved space");
 };
 
 // Head owned by lane li of a row group after the halving butterfly: at the
@@ -174,6 +212,52 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
+// One work unit: split `split` of item `item` (sequence, KV head, head chunk,
+// query-row block).
+struct Unit {
+  int b, kvh, hc, split;
+  int kv_len, i0, i_last;
+  int r0, r1, nsplit;  // key rows [r0, r1) of this split; splits of the item
+  bool len_ok;
+};
+
+__device__ __forceinline__ Unit decode_unit(const RowsParams& p, int item, int split) {
+  Unit u;
+  u.split = split;
+  const int rb = item % p.n_rblocks;
+  item /= p.n_rblocks;
+  u.hc = item % p.n_hchunks;
+  item /= p.n_hchunks;
+  u.kvh = item % p.Hkv;
+  u.b = item / p.Hkv;
+  u.kv_len = p.kv_len ? __ldg(p.kv_len + u.b) : (p.offsets ? __ldg(p.offsets + u.b) : 0) + p.seq_q;
+  u.i0 = rb * p.QR;
+  u.i_last = min(u.i0 + p.QR, p.seq_q) - 1;
+  u.len_ok = u.kv_len >= p.seq_q && u.kv_len >= 1 && u.kv_len <= p.capacity;
+  const int kv_hi = u.len_ok ? u.kv_len - p.seq_q + u.i_last + 1 : 0;  // keys the last row sees
+  u.nsplit = (kv_hi + p.split_rows - 1) / p.split_rows;
+  u.r0 = split * p.split_rows;
+  u.r1 = min(u.r0 + p.split_rows, kv_hi);
+  return u;
+}
+
+// Output row of virtual head vh of a unit (query row, query head).
+__device__ __forceinline__ size_t unit_out_row(const RowsParams& p, const Unit& u, int vh) {
+  const int iq = u.i0 + vh / p.GH;
+  const int h = u.kvh * p.G + u.hc * p.GH + vh % p.GH;
+  return ((size_t)u.b * p.seq_q + iq) * p.H + h;
+}
+
+// Bounded barrier of the compute warps on an mbarrier that counts one arrival
+// per warp. A warp that has given up never arrives, so the others give up too
+// (after the bounded wait) instead of hanging.
+__device__ __forceinline__ bool compute_sync(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned* err) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  return warp_wait(bar, parity, abort_flag, err);
+}
+
 template <typename ET, int DK, int DV, int DROT, int NV>
 __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::MIN_CTAS)
     attn_rows_kernel(const RowsParams p) {
@@ -181,196 +265,240 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
   constexpr int CH = C::CH, L = C::L, T = C::T, kStages = C::NS;
   constexpr int H2K = C::EK / 2, H2V = C::EV / 2;  // float2 pairs per lane
   extern __shared__ __align__(1024) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
-  volatile int* bad_table = abort_flag + 1;
+  RowsHeader* hdr = reinterpret_cast<RowsHeader*>(smem);
+  volatile int* abort_flag = &hdr->abort_flag;
   unsigned char* data = smem + C::kHeader;
+  float* qbuf = reinterpret_cast<float*>(smem + C::kHeader + C::ring_bytes);  // [warp][NV][DK]
+  float* mm = qbuf + kRowsWarps * NV * DK;                                    // merge area: m [warp][NV]
+  float* ml = mm + kRowsWarps * NV;                                           // l [warp][NV]
+  float* mo = ml + kRowsWarps * NV;                                           // o [warp][NV][DV]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- the work item
-  const int split = blockIdx.y;
-  int item = blockIdx.x;
-  const int rb = item % p.n_rblocks;
-  item /= p.n_rblocks;
-  const int hc = item % p.n_hchunks;
-  item /= p.n_hchunks;
-  const int kvh = item % p.Hkv;
-  const int b = item / p.Hkv;
-
-  const int kv_len = p.kv_len ? p.kv_len[b] : (p.offsets ? p.offsets[b] : 0) + p.seq_q;
-  const int i0 = rb * p.QR;
-  const int i_last = min(i0 + p.QR, p.seq_q) - 1;
-  const bool len_ok = kv_len >= p.seq_q && kv_len >= 1 && kv_len <= p.capacity;
-  const int kv_hi = len_ok ? kv_len - p.seq_q + i_last + 1 : 0;  // keys the last row sees
-  const int nsplit = (kv_hi + p.split_rows - 1) / p.split_rows;
-  const int r0 = split * p.split_rows;
-  const int r1 = min(r0 + p.split_rows, kv_hi);
-
-  if (!len_ok) {
-    // Length out of range: record it, write zeros once, touch no K/V.
-    if (split == 0) {
-      if (threadIdx.x == 0 && kvh == 0 && hc == 0 && rb == 0) raise_error(p.err, kErrBounds);
-      for (int idx = threadIdx.x; idx < NV * DV; idx += blockDim.x) {
-        const int vh = idx / DV, d = idx % DV;
-        const int iq = i0 + vh / p.GH;
-        if (iq >= p.seq_q) continue;
-        const int h = kvh * p.G + hc * p.GH + vh % p.GH;
-        reinterpret_cast<ET*>(p.out)[(((size_t)b * p.seq_q + iq) * p.H + h) * DV + d] = Elem<ET>::from_f32(0.f);
-      }
-    }
-    return;
-  }
-  if (r0 >= r1) return;  // this split lies past the last visible key
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kRowsWarps);
+      mbar_init(&hdr->full[s], 1);
+      mbar_init(&hdr->empty[s], kRowsWarps);
     }
+    mbar_init(&hdr->merge[0], kRowsWarps);
+    mbar_init(&hdr->merge[1], kRowsWarps);
     *abort_flag = 0;
-    *bad_table = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
-  // ---- paged: check every block-table entry this item reads before any copy
-  if (p.paged) {
-    const int blk0 = r0 / p.bs, blk1 = (r1 - 1) / p.bs;
-    for (int bi = blk0 + (int)threadIdx.x; bi <= blk1; bi += blockDim.x) {
-      const int e = p.tables[(size_t)b * p.mbps + bi];
-      if (e < 0 || e >= p.num_blocks) *bad_table = 1;
-    }
-    __syncthreads();
-    if (*bad_table) {
-      if (threadIdx.x == 0) raise_error(p.err, kErrBounds);
-      // An empty partial (m = -inf, l = 0) or zeros: no K/V row is read.
-      for (int idx = threadIdx.x; idx < NV * DV; idx += blockDim.x) {
-        const int vh = idx / DV, d = idx % DV;
-        const int iq = i0 + vh / p.GH;
-        if (iq >= p.seq_q) continue;
-        const int h = kvh * p.G + hc * p.GH + vh % p.GH;
-        const size_t row = ((size_t)b * p.seq_q + iq) * p.H + h;
-        if (nsplit == 1) {
-          reinterpret_cast<ET*>(p.out)[row * DV + d] = Elem<ET>::from_f32(0.f);
-        } else {
-          float* P = p.partial + (row * p.max_splits + split) * (DV + 2);
-          if (d == 0) {
-            P[0] = -INFINITY;
-            P[1] = 0.f;
-          }
-          P[2 + d] = 0.f;
-        }
-      }
-      return;
-    }
-  }
-
-  const int ntiles = (r1 - r0 + T - 1) / T;
-  const int rgw = lane / L, li = lane % L;
-  const int own = owned_head<NV, L>(li);  // the virtual head whose softmax this lane runs
-
-  // output accumulators (all heads, this lane's chunks) and the owned head's state
-  float2 o2[NV][H2V];
-#pragma unroll
-  for (int vh = 0; vh < NV; ++vh)
-#pragma unroll
-    for (int e = 0; e < H2V; ++e) o2[vh][e] = make_float2(0.f, 0.f);
-  float m_ref = -INFINITY, l_sum = 0.f;
-
   if (warp == kRowsWarps) {
     // ================= producer warp =================
     const uint64_t pol = l2_policy_evict_first();
+    const int n_items = p.B * p.Hkv * p.n_hchunks * p.n_rblocks;
+    const int n_units = p.sched ? __ldcg(p.sched + 1) : n_items;
     int last_issued[kStages];
 #pragma unroll
     for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t % kStages;
-      if (t >= kStages) {
-        bool ok = true;
-        if (lane == 0) ok = (*abort_flag == 0) && mbar_wait(&empty[s], ((t / kStages) - 1) & 1);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          if (lane == 0) {
-            *abort_flag = 1;
-            raise_error(p.err, kErrTimeout);
+    int gt = 0;  // tiles through the ring so far, across units
+    int next_static = blockIdx.x;
+    bool stop = false;
+    while (!stop) {
+      // ---- the next unit
+      int item, split;
+      if (p.sched) {
+        int k = 0;
+        if (lane == 0) k = atomicAdd(p.sched, 1);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        if (k >= n_units) break;
+        const int2 uu = __ldcg(p.units + k);
+        item = uu.x;
+        split = uu.y;
+      } else {
+        if (next_static >= n_items) break;
+        item = next_static;
+        split = 0;
+        next_static += gridDim.x;
+      }
+      const Unit u = decode_unit(p, item, split);
+      if (!u.len_ok) {
+        // Length out of range: record it, write zeros, touch no K/V.
+        if (lane == 0 && split == 0 && item % (p.Hkv * p.n_hchunks * p.n_rblocks) == 0)
+          raise_error(p.err, kErrBounds);
+        for (int idx = lane; idx < NV * DV; idx += 32) {
+          const int vh = idx / DV;
+          if (u.i0 + vh / p.GH >= p.seq_q) continue;
+          reinterpret_cast<ET*>(p.out)[unit_out_row(p, u, vh) * DV + idx % DV] = Elem<ET>::from_f32(0.f);
+        }
+        continue;
+      }
+      if (p.paged) {
+        // every block-table entry of the unit is checked before any copy
+        const int blk0 = u.r0 / p.bs, blk1 = (u.r1 - 1) / p.bs;
+        bool bad = false;
+        for (int bi = blk0 + lane; bi <= blk1; bi += 32) {
+          const int e = __ldg(p.tables + (size_t)u.b * p.mbps + bi);
+          if (e < 0 || e >= p.num_blocks) bad = true;
+        }
+        if (__any_sync(0xffffffffu, bad)) {
+          // An empty partial (m = -inf, l = 0) or zeros: no K/V row is read.
+          if (lane == 0) raise_error(p.err, kErrBounds);
+          for (int idx = lane; idx < NV * DV; idx += 32) {
+            const int vh = idx / DV, d = idx % DV;
+            if (u.i0 + vh / p.GH > u.i_last) continue;
+            const size_t row = unit_out_row(p, u, vh);
+            if (u.nsplit == 1) {
+              reinterpret_cast<ET*>(p.out)[row * DV + d] = Elem<ET>::from_f32(0.f);
+            } else {
+              float* P = p.partial + (row * p.max_splits + u.split) * (DV + 2);
+              if (d == 0) {
+                P[0] = -INFINITY;
+                P[1] = 0.f;
+              }
+              P[2 + d] = 0.f;
+            }
           }
+          continue;
+        }
+      }
+      const int ntiles = (u.r1 - u.r0 + T - 1) / T;
+      const int qrows = u.i_last - u.i0 + 1;
+      for (int t = 0; t < ntiles; ++t, ++gt) {
+        const int s = gt % kStages;
+        if (gt >= kStages) {
+          bool ok = true;
+          if (lane == 0) ok = (*abort_flag == 0) && mbar_wait(&hdr->empty[s], ((gt / kStages) - 1) & 1);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              raise_error(p.err, kErrTimeout);
+            }
+            stop = true;
+            break;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
+          stop = true;
           break;
         }
-      }
-      if (*abort_flag) break;
-      const int tr0 = r0 + t * T;
-      const int n = min(T, r1 - tr0);
-      if (p.debug_withhold && t == 0) continue;  // test hook: this tile never arrives
+        if (p.debug_withhold && gt == 0) continue;  // test hook: this tile never arrives
 #pragma unroll
-      for (int s2 = 0; s2 < kStages; ++s2)
-        if (s2 == s) last_issued[s2] = t;
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(n * C::row_bytes));
-      __syncwarp();
-      unsigned char* st = data + s * C::stage_bytes;
-      if (!p.paged) {
-        const size_t base = ((size_t)b * p.Hkv + kvh) * (size_t)p.max_len + tr0;
-        if (lane == 0)
-          bulk_g2s(st, reinterpret_cast<const ET*>(p.k) + base * C::DN, (uint32_t)(n * C::DN * C::ES), &full[s], pol);
-        if (DROT > 0 && lane == 1)
-          bulk_g2s(st + C::kN, reinterpret_cast<const ET*>(p.k_rot) + ((size_t)b * p.max_len + tr0) * DROT,
-                   (uint32_t)(n * DROT * C::ES), &full[s], pol);
-        if (lane == 2)
-          bulk_g2s(st + C::kN + C::kR, reinterpret_cast<const ET*>(p.v) + base * DV, (uint32_t)(n * DV * C::ES),
-                   &full[s], pol);
-      } else {
-        const int blk0 = tr0 / p.bs, blk1 = (tr0 + n - 1) / p.bs;
-        for (int bi = blk0 + lane; bi <= blk1; bi += 32) {
-          const int ra = max(tr0, bi * p.bs), rz = min(tr0 + n, (bi + 1) * p.bs);
-          const int e = p.tables[(size_t)b * p.mbps + bi];
-          const size_t src_row = ((size_t)e * p.Hkv + kvh) * p.bs + (ra - bi * p.bs);
-          bulk_g2s(st + (ra - tr0) * C::DN * C::ES, reinterpret_cast<const ET*>(p.k) + src_row * DK,
-                   (uint32_t)((rz - ra) * DK * C::ES), &full[s], pol);
-          bulk_g2s(st + C::kN + C::kR + (ra - tr0) * DV * C::ES, reinterpret_cast<const ET*>(p.v) + src_row * DV,
-                   (uint32_t)((rz - ra) * DV * C::ES), &full[s], pol);
+        for (int s2 = 0; s2 < kStages; ++s2)
+          if (s2 == s) last_issued[s2] = gt;
+        const int tr0 = u.r0 + t * T;
+        const int n = min(T, u.r1 - tr0);
+        unsigned char* st = data + s * C::stage_bytes;
+        if (lane == 0) {
+          hdr->tile[s] = make_int4(item, split, tr0, n | (t == 0 ? 1 << 16 : 0) | (t == ntiles - 1 ? 1 << 17 : 0));
+          const uint32_t qb = t == 0 ? (uint32_t)(qrows * p.GH * DK * C::ES) : 0u;
+          mbar_arrive_expect_tx(&hdr->full[s], (uint32_t)(n * C::row_bytes) + qb);
+        }
+        __syncwarp();
+        if (!p.paged) {
+          const size_t base = ((size_t)u.b * p.Hkv + u.kvh) * (size_t)p.max_len + tr0;
+          if (lane == 0)
+            bulk_g2s(st, reinterpret_cast<const ET*>(p.k) + base * C::DN, (uint32_t)(n * C::DN * C::ES),
+                     &hdr->full[s], pol);
+          if (DROT > 0 && lane == 1)
+            bulk_g2s(st + C::kN, reinterpret_cast<const ET*>(p.k_rot) + ((size_t)u.b * p.max_len + tr0) * DROT,
+                     (uint32_t)(n * DROT * C::ES), &hdr->full[s], pol);
+          if (lane == 2)
+            bulk_g2s(st + C::kN + C::kR, reinterpret_cast<const ET*>(p.v) + base * DV, (uint32_t)(n * DV * C::ES),
+                     &hdr->full[s], pol);
+        } else {
+          const int blk0 = tr0 / p.bs, blk1 = (tr0 + n - 1) / p.bs;
+          for (int bi = blk0 + lane; bi <= blk1; bi += 32) {
+            const int ra = max(tr0, bi * p.bs), rz = min(tr0 + n, (bi + 1) * p.bs);
+            const int e = __ldg(p.tables + (size_t)u.b * p.mbps + bi);
+            const size_t src_row = ((size_t)e * p.Hkv + u.kvh) * p.bs + (ra - bi * p.bs);
+            bulk_g2s(st + (ra - tr0) * C::DN * C::ES, reinterpret_cast<const ET*>(p.k) + src_row * DK,
+                     (uint32_t)((rz - ra) * DK * C::ES), &hdr->full[s], pol);
+            bulk_g2s(st + C::kN + C::kR + (ra - tr0) * DV * C::ES, reinterpret_cast<const ET*>(p.v) + src_row * DV,
+                     (uint32_t)((rz - ra) * DV * C::ES), &hdr->full[s], pol);
+          }
+        }
+        if (t == 0 && lane < qrows) {
+          // query row i0 + lane: the unit's GH heads of it, contiguous
+          const ET* src = reinterpret_cast<const ET*>(p.q) +
+                          (((size_t)u.b * p.seq_q + u.i0 + lane) * p.H + u.kvh * p.G + u.hc * p.GH) * DK;
+          bulk_g2s(st + C::kN + C::kR + C::kV + lane * p.GH * DK * C::ES, src, (uint32_t)(p.GH * DK * C::ES),
+                   &hdr->full[s], pol);
         }
       }
+    }
+    if (!stop) {
+      // end of work: one more tile descriptor, carrying no data
+      const int s = gt % kStages;
+      bool ok = true;
+      if (lane == 0) {
+        if (gt >= kStages) ok = (*abort_flag == 0) && mbar_wait(&hdr->empty[s], ((gt / kStages) - 1) & 1);
+        if (ok) {
+          hdr->tile[s] = make_int4(-1, 0, 0, 0);
+          mbar_arrive(&hdr->full[s]);
+        } else {
+          *abort_flag = 1;
+          raise_error(p.err, kErrTimeout);
+        }
+      }
+      // The marker completes a phase of its stage: the drain below must wait
+      // on that phase, not on the one before it (a parity wait cannot tell a
+      // phase from the one two later).
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+#pragma unroll
+      for (int s2 = 0; s2 < kStages; ++s2)
+        if (ok && s2 == s) last_issued[s2] = gt;
     }
     // Never leave with a copy in flight: wait (bounded) for the last tile
     // issued into each stage. On the normal path these have all completed.
     if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < kStages; ++s)
-        if (last_issued[s] >= 0 && !mbar_wait(&full[s], (last_issued[s] / kStages) & 1)) {
+        if (last_issued[s] >= 0 && !mbar_wait(&hdr->full[s], (last_issued[s] / kStages) & 1)) {
           *abort_flag = 1;
           raise_error(p.err, kErrTimeout);
         }
     }
-  } else {
-    // ================= compute warps =================
-    float2 q2[NV][H2K];
-    int lim_own = 0;
-#pragma unroll
-    for (int vh = 0; vh < NV; ++vh) {
-      const int iq = i0 + vh / p.GH;
-      const int h = kvh * p.G + hc * p.GH + vh % p.GH;
-      const bool active = iq <= i_last;
-      if (vh == own) lim_own = active ? kv_len - p.seq_q + iq + 1 : 0;
-      const ET* qrow = reinterpret_cast<const ET*>(p.q) + (((size_t)b * p.seq_q + (active ? iq : i0)) * p.H + h) * DK;
-      const float qs = active ? p.qscale : 0.f;
-#pragma unroll
-      for (int qk = 0; qk < C::QK; ++qk) {
-        float2 f[CH / 2];
-        chunk_to_f2<ET>(__ldg(reinterpret_cast<const uint4*>(qrow + (li + L * qk) * CH)), f);
-#pragma unroll
-        for (int e = 0; e < CH / 2; ++e) q2[vh][qk * (CH / 2) + e] = make_float2(f[e].x * qs, f[e].y * qs);
-      }
-    }
-    const int gbase = rgw * L;  // first lane of this row group
-    const int rg = warp * C::RGW + rgw;
+    return;
+  }
 
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t % kStages;
-      if (!warp_wait(&full[s], (t / kStages) & 1, abort_flag, p.err)) break;
-      const int tr0 = r0 + t * T;
-      const int n = min(T, r1 - tr0);
-      const unsigned char* st = data + s * C::stage_bytes;
+  // ================= compute warps =================
+  const int rgw = lane / L, li = lane % L;
+  const int own = owned_head<NV, L>(li);  // the virtual head whose softmax this lane runs
+  const int gbase = rgw * L;              // first lane of this row group
+  const int rg = warp * C::RGW + rgw;
+  const int ctid = threadIdx.x;           // 0 .. 32*kRowsWarps-1
+
+  // This warp's copy of the unit's queries, fp32 and pre-scaled by scale*log2 e;
+  // the four row groups read it as 4-way broadcasts.
+  float* qw = qbuf + warp * NV * DK;
+  // output accumulators (all heads, this lane's chunks) and the owned head's state
+  float2 o2[NV][H2V];
+  float m_ref = -INFINITY, l_sum = 0.f;
+  int lim_own = 0;
+  int merges = 0;
+  for (int gt = 0;; ++gt) {
+    const int s = gt % kStages;
+    if (!warp_wait(&hdr->full[s], (gt / kStages) & 1, abort_flag, p.err)) break;
+    const int4 dsc = hdr->tile[s];
+    if (dsc.x < 0) break;  // no more work
+    const int tr0 = dsc.z, n = dsc.w & 0xffff;
+    const unsigned char* st = data + s * C::stage_bytes;
+    if (dsc.w & (1 << 16)) {
+      // first tile of a unit: fresh state, queries from the stage into qw
+      const Unit u = decode_unit(p, dsc.x, dsc.y);
+      const ET* sQ = reinterpret_cast<const ET*>(st + C::kN + C::kR + C::kV);
+      for (int idx = lane; idx < NV * DK; idx += 32) {
+        const bool active = u.i0 + (idx / DK) / p.GH <= u.i_last;
+        qw[idx] = active ? Elem<ET>::to_f32(sQ[idx]) * p.qscale : 0.f;
+      }
+#pragma unroll
+      for (int vh = 0; vh < NV; ++vh) {
+#pragma unroll
+        for (int e = 0; e < H2V; ++e) o2[vh][e] = make_float2(0.f, 0.f);
+        const int iq = u.i0 + vh / p.GH;
+        if (vh == own) lim_own = iq <= u.i_last ? u.kv_len - p.seq_q + iq + 1 : 0;
+      }
+      m_ref = -INFINITY;
+      l_sum = 0.f;
+      __syncwarp();
+    }
+    {
       const ET* sKn = reinterpret_cast<const ET*>(st);
       const ET* sKr = reinterpret_cast<const ET*>(st + C::kN);
       const ET* sV = reinterpret_cast<const ET*>(st + C::kN + C::kR);
@@ -394,12 +522,17 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
           chunk_to_f2<ET>(*reinterpret_cast<const uint4*>(srcA), ka);
           chunk_to_f2<ET>(*reinterpret_cast<const uint4*>(srcB), kb);
 #pragma unroll
-          for (int vh = 0; vh < NV; ++vh)
+          for (int vh = 0; vh < NV; ++vh) {
+            const float4* qp = reinterpret_cast<const float4*>(qw + vh * DK + c * CH);
 #pragma unroll
-            for (int e = 0; e < CH / 2; ++e) {
-              acc_a[vh] = __ffma2_rn(q2[vh][qk * (CH / 2) + e], ka[e], acc_a[vh]);
-              acc_b[vh] = __ffma2_rn(q2[vh][qk * (CH / 2) + e], kb[e], acc_b[vh]);
+            for (int j = 0; j < CH / 4; ++j) {
+              const float4 qq = qp[j];
+              acc_a[vh] = __ffma2_rn(make_float2(qq.x, qq.y), ka[2 * j], acc_a[vh]);
+              acc_b[vh] = __ffma2_rn(make_float2(qq.x, qq.y), kb[2 * j], acc_b[vh]);
+              acc_a[vh] = __ffma2_rn(make_float2(qq.z, qq.w), ka[2 * j + 1], acc_a[vh]);
+              acc_b[vh] = __ffma2_rn(make_float2(qq.z, qq.w), kb[2 * j + 1], acc_b[vh]);
             }
+          }
         }
         float pa[NV], pb[NV];
 #pragma unroll
@@ -456,81 +589,121 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
-  }
-  // Every copy has landed and every compute warp is done with the ring.
-  __syncthreads();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&hdr->empty[s]);
+    if (!(dsc.w & (1 << 17))) continue;
 
-  // ---- merge the row groups (fixed order) through shared memory
-  float* mm = reinterpret_cast<float*>(data);  // [NRG][NV]
-  float* ml = mm + C::NRG * NV;                // [NRG][NV]
-  float* mo = ml + C::NRG * NV;                // [NRG][NV][DV]
-  if (warp < kRowsWarps) {
-    const int rg = warp * C::RGW + rgw;
-    if (li == owner_lane<NV, L>(own)) {
-      mm[rg * NV + own] = m_ref;
-      ml[rg * NV + own] = l_sum;
-    }
+    // ---- last tile of the unit: merge, in a fixed order. First the RGW row
+    // groups of this warp, in registers: xor butterflies over the lane bits
+    // above the row group, after which every lane holds the same sums.
+    float Mw[NV], lw[NV];
 #pragma unroll
-    for (int vh = 0; vh < NV; ++vh)
+    for (int vh = 0; vh < NV; ++vh) {
+      const float mg = NV == 1 ? m_ref : __shfl_sync(0xffffffffu, m_ref, gbase + owner_lane<NV, L>(vh));
+      const float lg = NV == 1 ? l_sum : __shfl_sync(0xffffffffu, l_sum, gbase + owner_lane<NV, L>(vh));
+      float M = mg;
 #pragma unroll
-      for (int qv = 0; qv < C::QV; ++qv)
+      for (int off = L; off < 32; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float w = (mg == -INFINITY) ? 0.f : ex2(mg - M);
+      float lsum = w * lg;
 #pragma unroll
-        for (int e = 0; e < CH / 2; e += 2)
-          *reinterpret_cast<float4*>(&mo[(rg * NV + vh) * DV + (li + L * qv) * CH + 2 * e]) =
-              make_float4(o2[vh][qv * (CH / 2) + e].x, o2[vh][qv * (CH / 2) + e].y,
-                          o2[vh][qv * (CH / 2) + e + 1].x, o2[vh][qv * (CH / 2) + e + 1].y);
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < NV * DV; idx += blockDim.x) {
-    const int vh = idx / DV, d = idx % DV;
-    const int iq = i0 + vh / p.GH;
-    if (iq > i_last) continue;
-    const int h = kvh * p.G + hc * p.GH + vh % p.GH;
-    float M = -INFINITY;
-    for (int g = 0; g < C::NRG; ++g) M = fmaxf(M, mm[g * NV + vh]);
-    float ls = 0.f, os = 0.f;
-    if (M != -INFINITY) {
-      for (int g = 0; g < C::NRG; ++g) {
-        const float mg = mm[g * NV + vh];
-        const float w = (mg == -INFINITY) ? 0.f : ex2(mg - M);
-        ls = fmaf(w, ml[g * NV + vh], ls);
-        os = fmaf(w, mo[(g * NV + vh) * DV + d], os);
+      for (int off = L; off < 32; off <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      Mw[vh] = M;
+      lw[vh] = lsum;
+#pragma unroll
+      for (int e = 0; e < H2V; ++e) {
+        float ox = o2[vh][e].x * w, oy = o2[vh][e].y * w;
+#pragma unroll
+        for (int off = L; off < 32; off <<= 1) {
+          ox += __shfl_xor_sync(0xffffffffu, ox, off);
+          oy += __shfl_xor_sync(0xffffffffu, oy, off);
+        }
+        o2[vh][e] = make_float2(ox, oy);
       }
     }
-    const size_t row = ((size_t)b * p.seq_q + iq) * p.H + h;
-    if (nsplit == 1) {
-      reinterpret_cast<ET*>(p.out)[row * DV + d] = Elem<ET>::from_f32(ls > 0.f ? os / ls : 0.f);
-    } else {
-      float* P = p.partial + (row * p.max_splits + split) * (DV + 2);
-      if (d == 0) {
-        P[0] = M;
-        P[1] = ls;
+    // Then the warps, through the merge area.
+    const uint32_t par = merges & 1;
+    ++merges;
+    // every warp is done reading the previous unit's merge area
+    if (!compute_sync(&hdr->merge[0], par, abort_flag, p.err)) break;
+    if (rgw == 0) {
+      if (li == 0) {
+#pragma unroll
+        for (int vh = 0; vh < NV; ++vh) {
+          mm[warp * NV + vh] = Mw[vh];
+          ml[warp * NV + vh] = lw[vh];
+        }
       }
-      P[2 + d] = os;
+#pragma unroll
+      for (int vh = 0; vh < NV; ++vh)
+#pragma unroll
+        for (int qv = 0; qv < C::QV; ++qv)
+#pragma unroll
+          for (int e = 0; e < CH / 2; e += 2)
+            *reinterpret_cast<float4*>(&mo[(warp * NV + vh) * DV + (li + L * qv) * CH + 2 * e]) =
+                make_float4(o2[vh][qv * (CH / 2) + e].x, o2[vh][qv * (CH / 2) + e].y,
+                            o2[vh][qv * (CH / 2) + e + 1].x, o2[vh][qv * (CH / 2) + e + 1].y);
+    }
+    if (!compute_sync(&hdr->merge[1], par, abort_flag, p.err)) break;
+    const Unit u = decode_unit(p, dsc.x, dsc.y);
+    for (int idx = ctid; idx < NV * DV; idx += kRowsWarps * 32) {
+      const int vh = idx / DV, d = idx % DV;
+      if (u.i0 + vh / p.GH > u.i_last) continue;
+      float M = -INFINITY;
+      for (int g = 0; g < kRowsWarps; ++g) M = fmaxf(M, mm[g * NV + vh]);
+      float ls = 0.f, os = 0.f;
+      if (M != -INFINITY) {
+        for (int g = 0; g < kRowsWarps; ++g) {
+          const float mg = mm[g * NV + vh];
+          const float wg = (mg == -INFINITY) ? 0.f : ex2(mg - M);
+          ls = fmaf(wg, ml[g * NV + vh], ls);
+          os = fmaf(wg, mo[(g * NV + vh) * DV + d], os);
+        }
+      }
+      const size_t row = unit_out_row(p, u, vh);
+      if (u.nsplit == 1) {
+        reinterpret_cast<ET*>(p.out)[row * DV + d] = Elem<ET>::from_f32(ls > 0.f ? os / ls : 0.f);
+      } else {
+        float* P = p.partial + (row * p.max_splits + u.split) * (DV + 2);
+        if (d == 0) {
+          P[0] = M;
+          P[1] = ls;
+        }
+        P[2 + d] = os;
+      }
     }
   }
 }
 
-// Host launcher of one instantiation.
+// Host launcher of one instantiation: a persistent grid of one CTA per
+// resident slot (SMs x CTAs per SM), capped at the number of units.
 template <typename ET, int DK, int DV, int DROT, int NV>
 cudaError_t launch_rows_inst(const RowsParams& p, cudaStream_t st) {
   using C = RowsCfg<ET, DK, DV, DROT, NV>;
   auto kern = attn_rows_kernel<ET, DK, DV, DROT, NV>;
   int dev = 0;
-  cudaGetDevice(&dev);
-  static unsigned long long attr_done = 0;  // one bit per device
-  if (dev < 64 && !(attr_done >> dev & 1ull)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static int slots_cache[64] = {};  // per device, 0 = not yet known
+  int slots = dev < 64 ? slots_cache[dev] : 0;
+  if (slots == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes);
     if (e != cudaSuccess) return e;
-    attr_done |= 1ull << dev;
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowsThreads, C::smem_bytes);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+    slots = per_sm * sms;
+    if (dev < 64) slots_cache[dev] = slots;
   }
   const long long items = (long long)p.B * p.Hkv * p.n_hchunks * p.n_rblocks;
-  if (items <= 0) return cudaSuccess;
-  if (items > 0x7fffffffLL || p.max_splits > 65535) return cudaErrorInvalidConfiguration;
-  dim3 grid((unsigned)items, (unsigned)p.max_splits);
+  if (items <= 0 || p.max_splits <= 0) return cudaSuccess;
+  const long long units = p.sched ? items * p.max_splits : items;  // an upper bound with a plan
+  if (items * p.max_splits > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int grid = (int)(units < slots ? units : slots);
   kern<<<grid, kRowsThreads, C::smem_bytes, st>>>(p);
   return cudaGetLastError();
 }

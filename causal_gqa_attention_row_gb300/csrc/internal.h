@@ -14,7 +14,7 @@ enum : unsigned { kErrBounds = 1u, kErrTimeout = 2u };
 // Rows of one split-K work item. Split boundaries are multiples of this, a
 // fixed number independent of the layout and of the rest of the batch, so the
 // paged and contiguous decodes of one history do identical arithmetic.
-constexpr int kSplitRows = 1024;
+constexpr int kSplitRows = 2048;
 
 // Parameters of the SIMT attention kernel (decode, and prefill shapes that the
 // tensor-core kernel does not take). All pointers are device pointers.
@@ -25,6 +25,8 @@ struct RowsParams {
   const void* k_rot;        // contiguous only: [B, max_len, DROT]
   void* out;                // [B, seq_q, H, DV]
   float* partial;           // [B*seq_q*H, max_splits, DV+2] when max_splits > 1
+  int* sched;               // split-K plan: [0] ticket counter, [1] units listed; NULL without a workspace
+  int2* units;              // split-K plan: the listed (item, split) units
   const int32_t* kv_len;    // [B] keys present (decode), or NULL: offsets[b] + seq_q
   const int32_t* offsets;   // [B] or NULL (prefill)
   const int32_t* tables;    // paged: [B, mbps]
@@ -39,7 +41,7 @@ struct RowsParams {
   int split_rows;           // rows per split (kSplitRows, or >= capacity for no split)
   int max_splits;
   float qscale;             // attention_scale * log2(e)
-  int debug_withhold;       // test hook: withhold tile 0 of every item
+  int debug_withhold;       // test hook: withhold the first tile of every CTA
 };
 
 // Dispatch of the SIMT kernel by element type and head widths; NV = GH * QR.
@@ -50,6 +52,16 @@ cudaError_t launch_attn_rows_bf16(const RowsParams& p, int dk, int dv, int drot,
 int rows_max_nv(int bf16, int dk, int dv, int drot);
 
 cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStream_t st);
+
+// The split-K plan: lists the units with keys into p.units and resets the
+// ticket counter (p.sched must be set).
+cudaError_t launch_plan_units(const RowsParams& p, cudaStream_t st);
+
+// Split-K workspace layout: the plan (ticket counter and total, then the unit
+// list), then the partial results.
+constexpr size_t kPlanHeaderBytes = 256;
+inline size_t round_up256(size_t n) { return (n + 255) / 256 * 256; }
+inline size_t plan_bytes(size_t units_max) { return kPlanHeaderBytes + round_up256(units_max * 8); }
 
 cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int heads, int d, int heads_outer,
                         int rot_offset, int rot_dim, double theta, int bf16, cudaStream_t st);

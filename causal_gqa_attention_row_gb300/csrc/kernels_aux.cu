@@ -37,6 +37,98 @@ cudaError_t launch_attn_rows_bf16(const RowsParams& p, int dk, int dv, int drot,
 }
 
 // ---------------------------------------------------------------------------
+// Split-K plan. Items are (sequence, KV head, head chunk, query-row block); an
+// item with kv_hi visible keys has kv_hi / split_rows full splits and, when
+// split_rows does not divide kv_hi, one partial split. The list holds every
+// full split (item by item), then every partial split, so the smallest units
+// come last and the tail of the dynamic schedule is short. An item whose length
+// is out of range contributes one unit (split 0), on which the attention
+// kernel writes its zeros. One CTA of 1024 threads.
+
+constexpr int kPlanThreads = 1024;
+
+// Exclusive prefix sum over the CTA; `total` receives the CTA-wide sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  total = warp_sums[(blockDim.x >> 5) - 1];
+  const int before = (warp == 0 ? 0 : warp_sums[warp - 1]) + x - v;
+  __syncthreads();  // warp_sums is reused by the next call
+  return before;
+}
+
+__device__ __forceinline__ void item_split_counts(const RowsParams& p, int item, int& full, int& part) {
+  const int rb = item % p.n_rblocks;
+  const int b = item / (p.n_rblocks * p.n_hchunks * p.Hkv);
+  const int kv_len = p.kv_len ? p.kv_len[b] : (p.offsets ? p.offsets[b] : 0) + p.seq_q;
+  const bool len_ok = kv_len >= p.seq_q && kv_len >= 1 && kv_len <= p.capacity;
+  if (!len_ok) {
+    full = 1;
+    part = 0;
+    return;
+  }
+  const int i_last = min(rb * p.QR + p.QR, p.seq_q) - 1;
+  const int kv_hi = kv_len - p.seq_q + i_last + 1;
+  full = kv_hi / p.split_rows;
+  part = (kv_hi % p.split_rows) != 0;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_units_kernel(const RowsParams p) {
+  __shared__ int warp_sums[32];
+  const int n_items = p.B * p.Hkv * p.n_hchunks * p.n_rblocks;
+  // pass 1: the number of full units, where the partial units start
+  int n_full = 0;
+  for (int base = 0; base < n_items; base += kPlanThreads) {
+    const int item = base + (int)threadIdx.x;
+    int full = 0, part = 0;
+    if (item < n_items) item_split_counts(p, item, full, part);
+    int tot;
+    block_exclusive_scan(full, warp_sums, tot);
+    n_full += tot;
+  }
+  // pass 2: write the list
+  int at_full = 0, at_part = n_full;
+  for (int base = 0; base < n_items; base += kPlanThreads) {
+    const int item = base + (int)threadIdx.x;
+    int full = 0, part = 0;
+    if (item < n_items) item_split_counts(p, item, full, part);
+    int tot_full, tot_part;
+    const int of = block_exclusive_scan(full, warp_sums, tot_full);
+    const int op = block_exclusive_scan(part, warp_sums, tot_part);
+    for (int s = 0; s < full; ++s) p.units[at_full + of + s] = make_int2(item, s);
+    if (part) p.units[at_part + op] = make_int2(item, full);
+    at_full += tot_full;
+    at_part += tot_part;
+  }
+  if (threadIdx.x == 0) {
+    p.sched[0] = 0;
+    p.sched[1] = at_part;
+  }
+}
+
+cudaError_t launch_plan_units(const RowsParams& p, cudaStream_t st) {
+  plan_units_kernel<<<1, kPlanThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Split combine: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the
 // splits of one (sequence, head), M = max_s m_s, in split order. Empty splits
 // (m = -inf) weigh zero. One warp per output row.

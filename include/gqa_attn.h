@@ -192,7 +192,9 @@ gqa_status attn_rope_interleaved(void* x, const int32_t* positions, int B, int T
 
 /* Bytes of workspace attn_decode_contig / attn_decode_paged need for B
  * sequences of at most max_len_upper_bound rows (0 when no sequence that long
- * is split). Host only; launches nothing. */
+ * is split). With S = ceil(max_len_upper_bound / 2048) splits and U = B*H*S:
+ * a 256-byte scheduling header, the split list (8*U bytes rounded up to 256),
+ * then the partial results (U * (d_v + 2) floats). Host only; launches nothing. */
 size_t attn_decode_workspace_bytes(int B, int H, int d_v, int max_len_upper_bound);
 
 /* Synchronises `stream`, then returns and clears the device error word of the
@@ -204,9 +206,10 @@ gqa_status attn_get_device_error(void* stream);
 const char* gqa_status_string(gqa_status status);
 
 /* Test hook for the bounded waits: while enabled, each decode launch withholds
- * the first K/V tile of every work item, so that the consumers' wait on it runs
- * out (after about one second), the device error word records
- * GQA_ERR_DEVICE_TIMEOUT and the kernel returns. Outputs are then garbage.
+ * the first K/V tile that every CTA of the (persistent) attention kernel would
+ * stream, so that the consumers' wait on it runs out (after about one second),
+ * the device error word records GQA_ERR_DEVICE_TIMEOUT and the kernel returns.
+ * Outputs are then garbage.
  * Never enable outside tests. Returns the previous setting. */
 int gqa_debug_withhold_first_tile(int enable);
 

@@ -41,8 +41,10 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     import causal_gqa_attention_row_gb300 as g
-    assert g.attn_decode_workspace_bytes(256, 32, 128, 1024) == 0          # one split: none needed
-    assert g.attn_decode_workspace_bytes(256, 32, 128, 2049 * 16) == 256 * 32 * 33 * 130 * 4
+    assert g.attn_decode_workspace_bytes(256, 32, 128, 2048) == 0          # one split: none needed
+    units = 256 * 32 * 17                       # (sequence, head, split) slots, 2048-row splits
+    plan = 256 + (units * 8 + 255) // 256 * 256  # ticket header + split list
+    assert g.attn_decode_workspace_bytes(256, 32, 128, 2049 * 16) == plan + units * 130 * 4
     assert g.attn_decode_workspace_bytes(0, 32, 128, 5000) == 0
 
 

@@ -92,10 +92,11 @@ def test_tiny_decode_appended_ninth_row_contig_and_paged(gpu_lib):
                                      (6, 3, 128), (4, 2, 256)])
 def test_decode_contig(gpu_lib, dtype, H, Hkv, d):
     g = gpu_lib
-    lens = [1, 31, 1024, 1025, 2900]
-    c = W.make_contig(B=len(lens), H=H, Hkv=Hkv, dk=d, dv=d, max_len=3000, lens=lens, dtype=dtype, seed=20)
+    # lengths around the 2048-row split boundary and past two of them
+    lens = [1, 31, 1024, 2047, 2048, 2049, 4500]
+    c = W.make_contig(B=len(lens), H=H, Hkv=Hkv, dk=d, dv=d, max_len=4600, lens=lens, dtype=dtype, seed=20)
     out = torch.empty(len(lens), H, d, dtype=dtype, device=DEV)
-    ws = g.decode_workspace(len(lens), H, d, 3000)
+    ws = g.decode_workspace(len(lens), H, d, 4600)
     g.attn_decode_contig(c.q.to(DEV), c.k.to(DEV), c.v.to(DEV), c.seq_lens.to(DEV), out, c.scale, workspace=ws)
     ok(g)
     want = core.decode_contig(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), lens, c.scale)
@@ -105,8 +106,8 @@ def test_decode_contig(gpu_lib, dtype, H, Hkv, d):
 @pytest.mark.parametrize("bs", [16, 4, 5, 64])
 def test_decode_paged_matches_oracle_and_contig_bits(gpu_lib, bs):
     g = gpu_lib
-    lens = [1, 16, 17, 1023, 1024, 1025, 2600]
-    B, H, Hkv, d, L = len(lens), 32, 8, 128, 2600
+    lens = [1, 16, 17, 1023, 2047, 2048, 2049, 4200]
+    B, H, Hkv, d, L = len(lens), 32, 8, 128, 4200
     c = W.make_contig(B=B, H=H, Hkv=Hkv, dk=d, dv=d, max_len=L, lens=lens, seed=21)
     mbps = (L + bs - 1) // bs + 1
     need = sum((n + bs - 1) // bs for n in lens)
