@@ -15,19 +15,26 @@
 //               four-stage ring (128-byte swizzle, the layout the MMA reads).
 //   warps 9, 10 one thread each issues the tcgen05.mma of one softmax warpgroup
 //               (warp 9 also allocates and frees TMEM); warp 11 idles.
-// Warpgroup w owns S_w = Q K^T (M=128, N=128, K=64; TMEM columns 128w..),
-// O_w += P_w V (M=128, N=64, K=128; TMEM columns 256 + 64w..), and its P_w tile
-// in shared memory. Thread t of a warpgroup owns query row t (TMEM lane t).
+// Warpgroup w owns, in tensor memory (TMEM), S_w = Q K^T (M=128, N=128, K=64;
+// columns 128w..) and [O_w | L_w] += P_w [V | 1] (M=128, N=64+16, K=128;
+// columns 256 + 80w..): the row sums L_w come out of the same MMAs as O_w, the
+// tensor core adding up the very bf16 p that multiply V. The ones are a
+// constant 16 KiB tile in shared memory that each stage's V descriptor reaches
+// as its second 64-column group (leading byte offset). P_w is written to shared
+// memory in the layout the PV MMA reads. Thread t of a warpgroup owns query row
+// t (TMEM lane t).
+//
+// Pipeline per warpgroup and key tile j: the softmax threads load their S_j row
+// into registers and release S_w at once, so the MMA thread issues S_{j+2}
+// while the exponentials of tile j are still being computed; PV_j follows as
+// soon as P_j is in shared memory and overlaps the next tile's load and max.
 //
 // Softmax with lazy rescaling: p = 2^((s - m) * scale * log2 e) against a
 // reference max m that only moves when a score exceeds it by more than 2^8 in
-// p, which keeps every p <= 256 and leaves O / l unchanged. So after a row's
-// first tile, one pass over S computes p directly and tracks the tile max; in
-// the rare case the max moved that far, O_w is rescaled in TMEM and the pass is
-// redone with the new reference. The first tile takes the max first. Keys past
-// a row's position (only in tiles that cross the diagonal) weigh exactly zero.
-// The two warpgroups take turns for the exponential pass, so that one computes
-// while the tensor core runs the other's MMAs. At the end warpgroup 0 merges
+// p, which keeps every p <= 256 and leaves O / l unchanged. Keys past the row's
+// position (only in tiles that cross the diagonal) weigh exactly zero. In the
+// rare case the reference must move, O_w and L_w are rescaled in TMEM. The two
+// warpgroups take turns for the exponential pass. At the end warpgroup 0 merges
 // the two partial (m, l, O) rows and stores bf16.
 #include <cudaTypedefs.h>
 
@@ -39,7 +46,7 @@ namespace {
 constexpr int kD = 64;     // head width (d_k = d_v)
 constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // keys per tile
-constexpr int kStagesKV = 4;
+constexpr int kStagesKV = 4;  // even: stage s only ever holds key tiles of warpgroup s % 2
 constexpr int kWG = 2;     // softmax warpgroups
 constexpr int kThreads = (kWG + 1) * 128;  // two softmax warpgroups + one control warpgroup
 constexpr int kProducerWarp = 8, kMmaWarp0 = 9;
@@ -48,18 +55,24 @@ constexpr int kProducerWarp = 8, kMmaWarp0 = 9;
 // 128 * 88 + 256 * 208 = 384 * 168.
 constexpr int kLaunchRegs = 168, kCtrlRegs = 88, kSoftmaxRegs = 208;
 static_assert(128 * kCtrlRegs + kWG * 128 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split over budget");
+static_assert(kStagesKV % kWG == 0, "a stage must only ever hold one warpgroup's tiles");
 constexpr int kTile = kBM * kD * 2;  // 16 KiB: one Q, K or V tile (128 rows x 128 bytes)
+constexpr int kSumN = 16;            // row-sum columns appended to O (the smallest N step)
+constexpr int kOW = kD + kSumN;      // 80: TMEM columns of [O_w | L_w]
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;  // S_w at 128w, O_w at 256 + 64w
+constexpr uint32_t kColS = 0, kColO = 256;  // S_w at 128w, [O_w | L_w] at 256 + 80w
 constexpr float kRescaleLog2 = 8.0f;
 
 // shared-memory map (from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kTile;                              // stage s: K at +0, V at +kTile
-constexpr int kOffP = kOffKV + kStagesKV * 2 * kTile;      // P_w: two 64-key halves each
+constexpr int kStageBytes = 2 * kTile;                     // K, then V
+constexpr int kOffKV = kTile;
+constexpr int kOffOnes = kOffKV + kStagesKV * kStageBytes;  // columns 64..79 of every [V | 1]
+constexpr int kOffP = kOffOnes + kTile;                    // P_w: two 64-key halves each
 constexpr int kOffML = kOffP + kWG * 2 * kTile;            // warpgroup 1's row max and sum
 constexpr int kOffBar = kOffML + 2 * kBM * 4;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;           // + alignment slack
+static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
 
 struct TcParams {
   int B, S, H, Hkv, G, S_kv, n_qtiles;
@@ -79,11 +92,11 @@ struct Bars {
 
 __device__ __forceinline__ bool aborted(Bars* bars) { return *reinterpret_cast<volatile int*>(&bars->abort_flag); }
 
-// Single-thread wait of the producer and MMA issuers: a spin, so that the next
-// TMA load or MMA goes out as soon as its barrier completes.
+// Single-thread wait of the producer and MMA issuers (suspends on the
+// mbarrier; bounded).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
   if (aborted(bars)) return false;
-  if (mbar_spin(bar, parity)) return true;
+  if (mbar_wait(bar, parity)) return true;
   *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
   raise_error(err, kErrTimeout);
   return false;
@@ -119,6 +132,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// 2^(s*qs - mq) for two scores, the exponent rounded to bf16 first: the result
+// is the bf16 pair that P stores.
+__device__ __forceinline__ uint32_t exp2_pair(float s0, float s1, float2 qs2, float2 nmq2) {
+  const float2 x = __ffma2_rn(make_float2(s0, s1), qs2, nmq2);
+  return ex2_bf16x2(pack_bf16(x.x, x.y));
+}
+
 template <int N>
 __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
@@ -130,73 +150,6 @@ __device__ __forceinline__ void regs_inc() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Row max of one S row (raw scores; masked keys excluded), from TMEM.
-__device__ __forceinline__ float row_max(uint32_t tS, bool diag, int j0, int pos) {
-  float mx8[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-#pragma unroll
-  for (int c = 0; c < kBN / 32; c += 2) {  // two loads in flight per wait
-    uint32_t v[2][32];
-    tc::tmem_ld_32x32b_x32(tS + c * 32, v[0]);
-    tc::tmem_ld_32x32b_x32(tS + (c + 1) * 32, v[1]);
-    tc::tmem_ld_wait();
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float x = (diag && j0 + (c + u) * 32 + e > pos) ? -INFINITY : __uint_as_float(v[u][e]);
-        mx8[e & 7] = fmaxf(mx8[e & 7], x);
-      }
-  }
-  return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])), fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-}
-
-// One pass over an S row: p = 2^(s*qs - mq) written as bf16 into row r of P
-// (two 64-key halves, 128-byte swizzle: 16-byte chunk index XOR row % 8, the
-// K-major layout the PV MMA reads). Returns the sum of p; *tile_max gets the
-// row max of the raw scores (masked keys excluded).
-__device__ __forceinline__ float exp_pass(uint32_t tS, bool diag, int j0, int pos, float qs, float mq,
-                                          unsigned char* sP, int r, float* tile_max) {
-  const float2 qs2 = make_float2(qs, qs), nmq2 = make_float2(-mq, -mq);
-  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int c = 0; c < kBN / 32; ++c) {
-    uint32_t v[32];
-    tc::tmem_ld_32x32b_x32(tS + c * 32, v);
-    tc::tmem_ld_wait();
-#pragma unroll
-    for (int q8 = 0; q8 < 4; ++q8) {
-      uint32_t w4[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int e = q8 * 8 + 2 * t;
-        float s0 = __uint_as_float(v[e]), s1 = __uint_as_float(v[e + 1]);
-        if (diag) {
-          if (j0 + c * 32 + e > pos) s0 = -INFINITY;
-          if (j0 + c * 32 + e + 1 > pos) s1 = -INFINITY;
-        }
-        mx4[t] = fmaxf(mx4[t], fmaxf(s0, s1));
-        // exponent argument in fp32, rounded to bf16x2, exponentiated two lanes at a
-        // time: the result is already the bf16 pair P stores; the row sum is taken
-        // from the same bf16 values, so numerator and denominator agree
-        const float2 x = __ffma2_rn(make_float2(s0, s1), qs2, nmq2);
-        const uint32_t pb = ex2_bf16x2(pack_bf16(x.x, x.y));
-        acc[t] = __fadd2_rn(acc[t], make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)));
-        w4[t] = pb;
-      }
-      const int cidx = c * 4 + q8;  // 16-byte chunk of the 256-byte P row
-      const int half = cidx / 8, ch = cidx % 8;
-      *reinterpret_cast<uint4*>(sP + half * kTile + r * 128 + ((ch ^ (r & 7)) * 16)) =
-          make_uint4(w4[0], w4[1], w4[2], w4[3]);
-    }
-  }
-  *tile_max = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-  return a.x + a.y;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -242,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort_flag = 0;
     fence_barrier_init();
   }
+  // the constant all-ones tile (any swizzle of ones is ones)
+  for (int i = threadIdx.x; i < kTile / 16; i += blockDim.x)
+    *reinterpret_cast<uint4*>(smem + kOffOnes + i * 16) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  tc::fence_async_smem();
   if (warp == kMmaWarp0) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
     tc::tmem_relinquish();
@@ -266,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % kStagesKV;
         if (j >= kStagesKV && !wait_or_abort(&bars->kv_empty[st], ((j / kStagesKV) - 1) & 1, bars, p.err)) break;
         mbar_arrive_expect_tx(&bars->kv_full[st], 2 * kTile);
-        tc::tma_load_4d(smem + kOffKV + st * 2 * kTile, &tm_k, 0, j * kBN, kvh, b, &bars->kv_full[st]);
-        tc::tma_load_4d(smem + kOffKV + st * 2 * kTile + kTile, &tm_v, 0, j * kBN, kvh, b, &bars->kv_full[st]);
+        tc::tma_load_4d(smem + kOffKV + st * kStageBytes, &tm_k, 0, j * kBN, kvh, b, &bars->kv_full[st]);
+        tc::tma_load_4d(smem + kOffKV + st * kStageBytes + kTile, &tm_v, 0, j * kBN, kvh, b, &bars->kv_full[st]);
         issued_last[st] = j;
       }
       // never exit with a load in flight
@@ -282,18 +239,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int n_mine = (n_kv - w + 1) / 2;
       const uint32_t idS = tc::idesc_bf16_f32(kBM, kBN, false);
-      const uint32_t idO = tc::idesc_bf16_f32(kBM, kD, true);
+      const uint32_t idO = tc::idesc_bf16_f32(kBM, kOW, true);
       // descriptors: constant high part + (shared address >> 4) in the low bits
       constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);
       const uint64_t dQ = kHi | (smem_u32(smem + kOffQ) >> 4);
       const uint64_t dKV0 = kHi | (smem_u32(smem + kOffKV) >> 4);
       const uint64_t dP = kHi | (smem_u32(smem + kOffP + w * 2 * kTile) >> 4);
-      const uint32_t dS = tmem + kColS + w * kBN, dO = tmem + kColO + w * kD;
+      // [V | 1] of each stage: MN-major, 8-key groups 1024 bytes apart, the ones
+      // tile (columns 64..79) at the leading byte offset from the stage's V
+      uint64_t dV[kStagesKV];
+#pragma unroll
+      for (int st = 0; st < kStagesKV; ++st) {
+        const uint32_t v = smem_u32(smem + kOffKV + st * kStageBytes + kTile);
+        dV[st] = tc::desc_sw128_hi(smem_u32(smem + kOffOnes) - v, 1024) | (v >> 4);
+      }
+      const uint32_t dS = tmem + kColS + w * kBN, dO = tmem + kColO + w * kOW;
       auto issue_s = [&](int j) -> bool {  // S_w = Q K_j^T
         const int st = j % kStagesKV;
         if (!wait_or_abort(&bars->kv_full[st], (j / kStagesKV) & 1, bars, p.err)) return false;
         tc::fence_after_sync();
-        const uint64_t dK = dKV0 + (uint64_t)((st * 2 * kTile) >> 4);
+        const uint64_t dK = dKV0 + (uint64_t)((st * kStageBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) tc::mma_f16_ss(dS, dQ + kk * 2, dK + kk * 2, idS, kk > 0);
         tc::mma_commit(&bars->s_full[w]);
@@ -302,18 +267,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = n_mine > 0 && wait_or_abort(&bars->q_full, 0, bars, p.err) && issue_s(w);
       for (int k = 0; ok && k < n_mine; ++k) {
         const int j = 2 * k + w;
-        if (!wait_or_abort(&bars->p_full[w], k & 1, bars, p.err)) break;
+        // S_{j+2} as soon as the softmax threads have read S_j into registers
+        if (k + 1 < n_mine) ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
+        if (!ok || !wait_or_abort(&bars->p_full[w], k & 1, bars, p.err)) break;
         tc::fence_after_sync();
         const int st = j % kStagesKV;
-        const uint64_t dV = dKV0 + (uint64_t)((st * 2 * kTile + kTile) >> 4);
+        // [O_w | L_w] += P_j [V_j | 1]: 16 keys per instruction
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_f16_ss(dO, dP + (((kk / 4) * kTile + (kk % 4) * 32) >> 4), dV + kk * (2048 >> 4), idO,
+          tc::mma_f16_ss(dO, dP + (((kk / 4) * kTile + (kk % 4) * 32) >> 4), dV[st] + kk * (2048 >> 4), idO,
                          (k > 0 || kk > 0));
         tc::mma_commit(&bars->o_done[w]);
         tc::mma_commit(&bars->kv_empty[st]);  // stage st only ever holds tiles of this warpgroup's parity
-        if (k + 1 < n_mine)  // S_w is free once the warpgroup has read it (before it published P_j)
-          ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
       }
       // every MMA issued above has completed before TMEM is released
       tc::mma_commit(&bars->mma_final[w]);
@@ -330,10 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = off + i0 + r;                     // absolute position of this row
     const float qs = p.qscale;
     const float th = kRescaleLog2 / qs;
-    float m_ref = -INFINITY, l_sum = 0.f;
+    float m_ref = -INFINITY;
     unsigned char* sP = smem + kOffP + wg * 2 * kTile;
     const uint32_t tS = tmem + lane_addr + kColS + wg * kBN;
-    const uint32_t tO = tmem + lane_addr + kColO + wg * kD;
+    const uint32_t tO = tmem + lane_addr + kColO + wg * kOW;
+    const uint32_t tL = tO + kD;  // L_w: the first of the 16 row-sum columns
+    const float2 qs2 = make_float2(qs, qs);
     const int n_mine = (n_kv - wg + 1) / 2;  // key tiles this warpgroup handles
     bool alive = true;
     for (int k = 0; k < n_mine; ++k) {
@@ -345,35 +312,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      if (k == 0) {
-        m_ref = row_max(tS, diag, j0, pos);  // first tile: the max first (nothing to rescale yet)
-      } else if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
-        alive = false;  // P_w is free and O_w stable once this warpgroup's previous PV is done
-        break;
-      } else {
+      // ---- the S row into registers; S_w is then free for S_{j+2}
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld_32x32b_x32(tS + c * 32, sv[c]);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free[wg]);
+      if (diag) {  // only the tile that crosses the diagonal has keys past some row's position
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (j0 + c * 32 + e > pos) sv[c][e] = __float_as_uint(-INFINITY);
+      }
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // P_w is free and O_w, L_w stable once this warpgroup's previous PV is done
+      if (k > 0) {
+        if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
         tc::fence_after_sync();
       }
-      // The two warpgroups take turns for the exponential pass (warpgroup 0's pass
-      // k, then warpgroup 1's pass k, then warpgroup 0's pass k+1, ...), so one
-      // computes exponentials while the tensor core runs the other's PV and S.
-      if (!(wg == 0 && k == 0) &&
-          !warp_wait_tc(&bars->turn[wg], (wg == 0 ? k - 1 : k) & 1, bars, p.err)) {
-        alive = false;
-        break;
-      }
-      float tsum = 0.f;
-      for (int pass = 0; pass < 2; ++pass) {
-        float tile_max;
-        const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
-        tsum = exp_pass(tS, diag, j0, pos, qs, mq, sP, r, &tile_max);
-        const bool grow = tile_max > m_ref + th;
-        if (!__any_sync(0xffffffffu, grow)) break;
-        // rare: move to the new reference max, rescale O_w and l, then redo the pass
+      // ---- rare: move the reference max and rescale O_w and L_w
+      const bool grow = mx > m_ref + th;
+      if (__any_sync(0xffffffffu, grow)) {
         float f = 1.f;
         if (grow) {
-          f = ex2f((m_ref - tile_max) * qs);  // 0 while m_ref = -inf
-          l_sum *= f;
-          m_ref = tile_max;
+          f = ex2f((m_ref - mx) * qs);  // 0 while m_ref = -inf
+          m_ref = mx;
         }
         if (k > 0) {
           uint32_t o[32];
@@ -385,24 +362,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
             tc::tmem_st_32x32b_x32(tO + c * 32, o);
           }
+          const uint32_t l0 = tc::tmem_ld_32x32b_x1(tL);
+          tc::tmem_ld_wait();
+          tc::tmem_st_32x32b_x1(tL, __float_as_uint(__uint_as_float(l0) * f));
           tc::tmem_st_wait();
         }
       }
-      l_sum += tsum;
-      tc::fence_before_sync();  // this thread's reads of S_w are done
+      // The two warpgroups take turns for the exponential pass (warpgroup 0's pass
+      // k, then warpgroup 1's pass k, then warpgroup 0's pass k+1, ...).
+      if (!(wg == 0 && k == 0) &&
+          !warp_wait_tc(&bars->turn[wg], (wg == 0 ? k - 1 : k) & 1, bars, p.err)) {
+        alive = false;
+        break;
+      }
+      // ---- p = 2^(s*qs - m*qs) as bf16 pairs into P_w (128-byte swizzle: 16-byte
+      // chunk index XOR row % 8, the K-major layout the PV MMA reads)
+      const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
+      const float2 nmq2 = make_float2(-mq, -mq);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int e = q8 * 8 + 2 * t;
+            w4[t] = exp2_pair(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]), qs2, nmq2);
+          }
+          const int cidx = c * 4 + q8;  // 16-byte chunk of the 256-byte P row
+          *reinterpret_cast<uint4*>(sP + (cidx / 8) * kTile + r * 128 + (((cidx % 8) ^ (r & 7)) * 16)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      tc::fence_before_sync();  // this thread's TMEM accesses are done
       tc::fence_async_smem();   // this thread's P_w writes visible to the tensor core
       __syncwarp();             // ... for every lane of the warp; one lane signals
       if (lane == 0) {
         mbar_arrive(&bars->turn[wg ^ 1]);
-        mbar_arrive(&bars->s_free[wg]);
         mbar_arrive(&bars->p_full[wg]);
       }
     }
     // ---- this warpgroup's last PV, then warpgroup 1 hands (m, l) to warpgroup 0
     bool have_o = alive && n_mine > 0;
+    float l_sum = 0.f;
     if (have_o) {
       have_o = warp_wait_tc(&bars->o_done[wg], (n_mine - 1) & 1, bars, p.err);
       tc::fence_after_sync();
+    }
+    if (have_o) {
+      l_sum = __uint_as_float(tc::tmem_ld_32x32b_x1(tL));
+      tc::tmem_ld_wait();
     }
     float* sm = reinterpret_cast<float*>(smem + kOffML);
     if (wg == 1) {
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kD / 16; ++c) {
         uint32_t o0[16], o1[16];
         tc::tmem_ld_32x32b_x16(tmem + lane_addr + kColO + c * 16, o0);
-        if (n_kv > 1) tc::tmem_ld_32x32b_x16(tmem + lane_addr + kColO + kD + c * 16, o1);
+        if (n_kv > 1) tc::tmem_ld_32x32b_x16(tmem + lane_addr + kColO + kOW + c * 16, o1);
         tc::tmem_ld_wait();
         if (r < rows) {
 #pragma unroll
