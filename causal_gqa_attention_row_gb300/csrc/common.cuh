@@ -84,6 +84,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Like mbar_wait, but each probe suspends the thread for at most `hint_ns`
+// nanoseconds, so that a waiter on a critical path wakes up soon after the
+// phase completes.
+__device__ __forceinline__ bool mbar_test_parity_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  if (mbar_test_parity_hint(bar, parity, hint_ns)) return true;
+  const long long t0 = clock64();
+  while (!mbar_test_parity_hint(bar, parity, hint_ns)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
 // L2 eviction policy for data read exactly once (K/V streams).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;

@@ -11,31 +11,34 @@
 // softmax warpgroups (setmaxnreg: 88 and 208 per thread from 168 at launch):
 //   warps 0-3   softmax warpgroup 0: key tiles 0, 2, 4, ...
 //   warps 4-7   softmax warpgroup 1: key tiles 1, 3, 5, ...
-//   warp 8      TMA producer: the Q tile once, then 128-key K and V tiles into a
-//               four-stage ring (128-byte swizzle, the layout the MMA reads).
+//   warp 8      TMA producer of Q (once) and of the 128-key K tiles (two-stage
+//               ring; 128-byte swizzle, the layout the MMA reads)
 //   warps 9, 10 one thread each issues the tcgen05.mma of one softmax warpgroup
-//               (warp 9 also allocates and frees TMEM); warp 11 idles.
+//               (warp 9 also allocates and frees TMEM)
+//   warp 11     TMA producer of the V tiles (two-stage ring)
 // Warpgroup w owns, in tensor memory (TMEM), S_w = Q K^T (M=128, N=128, K=64;
 // columns 128w..) and [O_w | L_w] += P_w [V | 1] (M=128, N=64+16, K=128;
 // columns 256 + 80w..): the row sums L_w come out of the same MMAs as O_w, the
 // tensor core adding up the very bf16 p that multiply V. The ones are a
 // constant 16 KiB tile in shared memory that each stage's V descriptor reaches
 // as its second 64-column group (leading byte offset). P_w is written to shared
-// memory in the layout the PV MMA reads. Thread t of a warpgroup owns query row
-// t (TMEM lane t).
+// memory in the layout the PV MMA reads, in two buffers that alternate by tile.
+// Thread t of a warpgroup owns query row t (TMEM lane t).
 //
 // Pipeline per warpgroup and key tile j: the softmax threads load their S_j row
 // into registers and release S_w at once, so the MMA thread issues S_{j+2}
-// while the exponentials of tile j are still being computed; PV_j follows as
-// soon as P_j is in shared memory and overlaps the next tile's load and max.
+// while the exponentials of tile j are still being computed. P_j goes to the
+// buffer PV_{j-4} read, so the softmax never waits for the PV of the tile
+// before: PV runs behind it, off its critical path. K and V have rings of their
+// own: a K stage is free as soon as its S MMA is done, a V stage once its PV is.
 //
 // Softmax with lazy rescaling: p = 2^((s - m) * scale * log2 e) against a
 // reference max m that only moves when a score exceeds it by more than 2^8 in
 // p, which keeps every p <= 256 and leaves O / l unchanged. Keys past the row's
 // position (only in tiles that cross the diagonal) weigh exactly zero. In the
-// rare case the reference must move, O_w and L_w are rescaled in TMEM. The two
-// warpgroups take turns for the exponential pass. At the end warpgroup 0 merges
-// the two partial (m, l, O) rows and stores bf16.
+// rare case the reference must move, O_w and L_w are rescaled in TMEM (after
+// every PV issued so far has completed). At the end warpgroup 0 merges the two
+// partial (m, l, O) rows and stores bf16.
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
@@ -46,16 +49,17 @@ namespace {
 constexpr int kD = 64;     // head width (d_k = d_v)
 constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // keys per tile
-constexpr int kStagesKV = 4;  // even: stage s only ever holds key tiles of warpgroup s % 2
+constexpr int kStagesKV = 2;  // per ring (K and V): stage s only ever holds key tiles of warpgroup s
+constexpr int kPBufs = 2;     // P buffers per warpgroup
 constexpr int kWG = 2;     // softmax warpgroups
 constexpr int kThreads = (kWG + 1) * 128;  // two softmax warpgroups + one control warpgroup
-constexpr int kProducerWarp = 8, kMmaWarp0 = 9;
+constexpr int kProducerWarp = 8, kMmaWarp0 = 9, kProducerVWarp = 11;
 // Registers per thread: 168 at launch (384 threads); the control warpgroup
 // gives up 80 per thread and the softmax warpgroups take 40 more:
 // 128 * 88 + 256 * 208 = 384 * 168.
 constexpr int kLaunchRegs = 168, kCtrlRegs = 88, kSoftmaxRegs = 208;
 static_assert(128 * kCtrlRegs + kWG * 128 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split over budget");
-static_assert(kStagesKV % kWG == 0, "a stage must only ever hold one warpgroup's tiles");
+static_assert(kStagesKV == kWG, "stage s must only ever hold warpgroup s's tiles");
 constexpr int kTile = kBM * kD * 2;  // 16 KiB: one Q, K or V tile (128 rows x 128 bytes)
 constexpr int kSumN = 16;            // row-sum columns appended to O (the smallest N step)
 constexpr int kOW = kD + kSumN;      // 80: TMEM columns of [O_w | L_w]
@@ -65,11 +69,12 @@ constexpr float kRescaleLog2 = 8.0f;
 
 // shared-memory map (from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
-constexpr int kStageBytes = 2 * kTile;                     // K, then V
-constexpr int kOffKV = kTile;
-constexpr int kOffOnes = kOffKV + kStagesKV * kStageBytes;  // columns 64..79 of every [V | 1]
-constexpr int kOffP = kOffOnes + kTile;                    // P_w: two 64-key halves each
-constexpr int kOffML = kOffP + kWG * 2 * kTile;            // warpgroup 1's row max and sum
+constexpr int kOffK = kTile;                               // K ring
+constexpr int kOffV = kOffK + kStagesKV * kTile;           // V ring
+constexpr int kOffOnes = kOffV + kStagesKV * kTile;        // columns 64..79 of every [V | 1]
+constexpr int kPBytes = 2 * kTile;                         // one P buffer: two 64-key halves
+constexpr int kOffP = kOffOnes + kTile;                    // P[w][buffer]
+constexpr int kOffML = kOffP + kWG * kPBufs * kPBytes;     // warpgroup 1's row max and sum
 constexpr int kOffBar = kOffML + 2 * kBM * 4;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;           // + alignment slack
 static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
@@ -83,20 +88,25 @@ struct TcParams {
 };
 
 struct Bars {
-  uint64_t q_full, kv_full[kStagesKV], kv_empty[kStagesKV];
-  uint64_t s_full[kWG], s_free[kWG], p_full[kWG], o_done[kWG], mma_final[kWG];
-  uint64_t turn[kWG];  // turn[w]: the other warpgroup finished an exponential pass
+  uint64_t q_full, k_full[kStagesKV], k_empty[kStagesKV], v_full[kStagesKV], v_empty[kStagesKV];
+  uint64_t s_full[kWG], s_free[kWG], p_full[kWG], mma_final[kWG];
+  uint64_t o_done[kWG][kPBufs];  // the PV that read P buffer b of warpgroup w is done
   uint32_t tmem_base;
   int abort_flag;
 };
 
 __device__ __forceinline__ bool aborted(Bars* bars) { return *reinterpret_cast<volatile int*>(&bars->abort_flag); }
 
-// Single-thread wait of the producer and MMA issuers (suspends on the
-// mbarrier; bounded).
+// The waits of this kernel sit on its critical path (MMA -> softmax -> MMA):
+// each probe of the mbarrier suspends a waiter for at most this long, so it
+// resumes within tens of nanoseconds of the phase completing.
+constexpr uint32_t kWaitHintNs = 20;
+
+
+// Single-thread wait of the producer and MMA issuers (bounded).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
   if (aborted(bars)) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait_hint(bar, parity, kWaitHintNs)) return true;
   *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
   raise_error(err, kErrTimeout);
   return false;
@@ -104,7 +114,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 
 // Whole-warp version: every lane agrees on the outcome.
 __device__ __forceinline__ bool warp_wait_tc(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
-  bool ok = !aborted(bars) && mbar_wait(bar, parity);
+  bool ok = !aborted(bars) && mbar_wait_hint(bar, parity, kWaitHintNs);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && (threadIdx.x & 31) == 0) {
     *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
@@ -137,6 +147,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 __device__ __forceinline__ uint32_t exp2_pair(float s0, float s1, float2 qs2, float2 nmq2) {
   const float2 x = __ffma2_rn(make_float2(s0, s1), qs2, nmq2);
   return ex2_bf16x2(pack_bf16(x.x, x.y));
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 template <int N>
@@ -181,16 +198,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kStagesKV; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int w = 0; w < kWG; ++w) {
       mbar_init(&bars->s_full[w], 1);
       mbar_init(&bars->s_free[w], 4);  // one arrival per softmax warp
       mbar_init(&bars->p_full[w], 4);
-      mbar_init(&bars->o_done[w], 1);
       mbar_init(&bars->mma_final[w], 1);
-      mbar_init(&bars->turn[w], 4);
+      for (int b2 = 0; b2 < kPBufs; ++b2) mbar_init(&bars->o_done[w][b2], 1);
     }
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -210,27 +228,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kProducerWarp) {
     regs_dec<kCtrlRegs>();  // the whole control warpgroup, right at the top of its branch
-  if (warp == kProducerWarp) {
-    // ================= TMA producer =================
+  if (warp == kProducerWarp || warp == kProducerVWarp) {
+    // ================= TMA producers: Q and K (warp 8), V (warp 11) =================
+    const bool is_k = warp == kProducerWarp;
     if (lane == 0) {
-      tc::prefetch_tmap(&tm_q);
-      tc::prefetch_tmap(&tm_k);
-      tc::prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, kTile);
-      tc::tma_load_4d(smem + kOffQ, &tm_q, 0, h, i0, b, &bars->q_full);
-      int issued_last[kStagesKV] = {-1, -1, -1, -1};
+      const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+      uint64_t* full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+      unsigned char* ring = smem + (is_k ? kOffK : kOffV);
+      tc::prefetch_tmap(tm);
+      if (is_k) {
+        tc::prefetch_tmap(&tm_q);
+        mbar_arrive_expect_tx(&bars->q_full, kTile);
+        tc::tma_load_4d(smem + kOffQ, &tm_q, 0, h, i0, b, &bars->q_full);
+      }
+      int issued_last[kStagesKV] = {-1, -1};
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % kStagesKV;
-        if (j >= kStagesKV && !wait_or_abort(&bars->kv_empty[st], ((j / kStagesKV) - 1) & 1, bars, p.err)) break;
-        mbar_arrive_expect_tx(&bars->kv_full[st], 2 * kTile);
-        tc::tma_load_4d(smem + kOffKV + st * kStageBytes, &tm_k, 0, j * kBN, kvh, b, &bars->kv_full[st]);
-        tc::tma_load_4d(smem + kOffKV + st * kStageBytes + kTile, &tm_v, 0, j * kBN, kvh, b, &bars->kv_full[st]);
+        if (j >= kStagesKV && !wait_or_abort(&empty[st], ((j / kStagesKV) - 1) & 1, bars, p.err)) break;
+        mbar_arrive_expect_tx(&full[st], kTile);
+        tc::tma_load_4d(ring + st * kTile, tm, 0, j * kBN, kvh, b, &full[st]);
         issued_last[st] = j;
       }
       // never exit with a load in flight
-      if (!mbar_wait(&bars->q_full, 0)) raise_error(p.err, kErrTimeout);
+      if (is_k && !mbar_wait(&bars->q_full, 0)) raise_error(p.err, kErrTimeout);
       for (int st = 0; st < kStagesKV; ++st)
-        if (issued_last[st] >= 0 && !mbar_wait(&bars->kv_full[st], (issued_last[st] / kStagesKV) & 1))
+        if (issued_last[st] >= 0 && !mbar_wait(&full[st], (issued_last[st] / kStagesKV) & 1))
           raise_error(p.err, kErrTimeout);
     }
   } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
@@ -243,25 +266,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // descriptors: constant high part + (shared address >> 4) in the low bits
       constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);
       const uint64_t dQ = kHi | (smem_u32(smem + kOffQ) >> 4);
-      const uint64_t dKV0 = kHi | (smem_u32(smem + kOffKV) >> 4);
-      const uint64_t dP = kHi | (smem_u32(smem + kOffP + w * 2 * kTile) >> 4);
+      const uint64_t dK0 = kHi | (smem_u32(smem + kOffK) >> 4);
+      const uint64_t dP0 = kHi | (smem_u32(smem + kOffP + w * kPBufs * kPBytes) >> 4);
       // [V | 1] of each stage: MN-major, 8-key groups 1024 bytes apart, the ones
       // tile (columns 64..79) at the leading byte offset from the stage's V
       uint64_t dV[kStagesKV];
 #pragma unroll
       for (int st = 0; st < kStagesKV; ++st) {
-        const uint32_t v = smem_u32(smem + kOffKV + st * kStageBytes + kTile);
+        const uint32_t v = smem_u32(smem + kOffV + st * kTile);
         dV[st] = tc::desc_sw128_hi(smem_u32(smem + kOffOnes) - v, 1024) | (v >> 4);
       }
       const uint32_t dS = tmem + kColS + w * kBN, dO = tmem + kColO + w * kOW;
       auto issue_s = [&](int j) -> bool {  // S_w = Q K_j^T
         const int st = j % kStagesKV;
-        if (!wait_or_abort(&bars->kv_full[st], (j / kStagesKV) & 1, bars, p.err)) return false;
+        if (!wait_or_abort(&bars->k_full[st], (j / kStagesKV) & 1, bars, p.err)) return false;
         tc::fence_after_sync();
-        const uint64_t dK = dKV0 + (uint64_t)((st * kStageBytes) >> 4);
+        const uint64_t dK = dK0 + (uint64_t)((st * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) tc::mma_f16_ss(dS, dQ + kk * 2, dK + kk * 2, idS, kk > 0);
         tc::mma_commit(&bars->s_full[w]);
+        tc::mma_commit(&bars->k_empty[st]);  // the K stage is free once S_j is done
         return true;
       };
       bool ok = n_mine > 0 && wait_or_abort(&bars->q_full, 0, bars, p.err) && issue_s(w);
@@ -270,15 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_{j+2} as soon as the softmax threads have read S_j into registers
         if (k + 1 < n_mine) ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
         if (!ok || !wait_or_abort(&bars->p_full[w], k & 1, bars, p.err)) break;
-        tc::fence_after_sync();
         const int st = j % kStagesKV;
+        if (!wait_or_abort(&bars->v_full[st], (j / kStagesKV) & 1, bars, p.err)) break;
+        tc::fence_after_sync();
+        const uint64_t dP = dP0 + (uint64_t)(((k % kPBufs) * kPBytes) >> 4);
         // [O_w | L_w] += P_j [V_j | 1]: 16 keys per instruction
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           tc::mma_f16_ss(dO, dP + (((kk / 4) * kTile + (kk % 4) * 32) >> 4), dV[st] + kk * (2048 >> 4), idO,
                          (k > 0 || kk > 0));
-        tc::mma_commit(&bars->o_done[w]);
-        tc::mma_commit(&bars->kv_empty[st]);  // stage st only ever holds tiles of this warpgroup's parity
+        tc::mma_commit(&bars->o_done[w][k % kPBufs]);
+        tc::mma_commit(&bars->v_empty[st]);
       }
       // every MMA issued above has completed before TMEM is released
       tc::mma_commit(&bars->mma_final[w]);
@@ -296,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float qs = p.qscale;
     const float th = kRescaleLog2 / qs;
     float m_ref = -INFINITY;
-    unsigned char* sP = smem + kOffP + wg * 2 * kTile;
+    unsigned char* sP0 = smem + kOffP + wg * kPBufs * kPBytes;
     const uint32_t tS = tmem + lane_addr + kColS + wg * kBN;
     const uint32_t tO = tmem + lane_addr + kColO + wg * kOW;
     const uint32_t tL = tO + kD;  // L_w: the first of the 16 row-sum columns
@@ -333,18 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
+        for (int e = 0; e < 32; e += 2)
+          mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // P_w is free and O_w, L_w stable once this warpgroup's previous PV is done
-      if (k > 0) {
-        if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
-        tc::fence_after_sync();
-      }
-      // ---- rare: move the reference max and rescale O_w and L_w
+      // ---- rare: move the reference max and rescale O_w and L_w, once every PV
+      // issued so far (the last one, PV of tile k-1, read buffer (k-1) % 2) is done
       const bool grow = mx > m_ref + th;
       if (__any_sync(0xffffffffu, grow)) {
         float f = 1.f;
@@ -353,6 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mx;
         }
         if (k > 0) {
+          if (!warp_wait_tc(&bars->o_done[wg][(k - 1) % kPBufs], ((k - 1) / kPBufs) & 1, bars, p.err)) {
+            alive = false;
+            break;
+          }
+          tc::fence_after_sync();
           uint32_t o[32];
 #pragma unroll
           for (int c = 0; c < kD / 32; ++c) {
@@ -368,13 +393,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st_wait();
         }
       }
-      // The two warpgroups take turns for the exponential pass (warpgroup 0's pass
-      // k, then warpgroup 1's pass k, then warpgroup 0's pass k+1, ...).
-      if (!(wg == 0 && k == 0) &&
-          !warp_wait_tc(&bars->turn[wg], (wg == 0 ? k - 1 : k) & 1, bars, p.err)) {
-        alive = false;
-        break;
+      // P buffer k % 2 is free once the PV of tile k-2 (which read it) is done
+      if (k >= kPBufs) {
+        if (!warp_wait_tc(&bars->o_done[wg][k % kPBufs], ((k - kPBufs) / kPBufs) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
       }
+      unsigned char* sP = sP0 + (k % kPBufs) * kPBytes;
       // ---- p = 2^(s*qs - m*qs) as bf16 pairs into P_w (128-byte swizzle: 16-byte
       // chunk index XOR row % 8, the K-major layout the PV MMA reads)
       const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
@@ -396,16 +422,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();  // this thread's TMEM accesses are done
       tc::fence_async_smem();   // this thread's P_w writes visible to the tensor core
       __syncwarp();             // ... for every lane of the warp; one lane signals
-      if (lane == 0) {
-        mbar_arrive(&bars->turn[wg ^ 1]);
-        mbar_arrive(&bars->p_full[wg]);
-      }
+      if (lane == 0) mbar_arrive(&bars->p_full[wg]);
     }
     // ---- this warpgroup's last PV, then warpgroup 1 hands (m, l) to warpgroup 0
     bool have_o = alive && n_mine > 0;
     float l_sum = 0.f;
-    if (have_o) {
-      have_o = warp_wait_tc(&bars->o_done[wg], (n_mine - 1) & 1, bars, p.err);
+    if (have_o) {  // the last PV (in-order completion: every earlier one too)
+      have_o = warp_wait_tc(&bars->o_done[wg][(n_mine - 1) % kPBufs], ((n_mine - 1) / kPBufs) & 1, bars, p.err);
       tc::fence_after_sync();
     }
     if (have_o) {
