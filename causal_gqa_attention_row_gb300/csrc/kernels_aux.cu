@@ -93,33 +93,30 @@ __device__ __forceinline__ void item_split_counts(const RowsParams& p, int item,
 __global__ void __launch_bounds__(kPlanThreads) plan_units_kernel(const RowsParams p) {
   __shared__ int warp_sums[32];
   const int n_items = p.B * p.Hkv * p.n_hchunks * p.n_rblocks;
-  // pass 1: the number of full units, where the partial units start
-  int n_full = 0;
-  for (int base = 0; base < n_items; base += kPlanThreads) {
-    const int item = base + (int)threadIdx.x;
-    int full = 0, part = 0;
-    if (item < n_items) item_split_counts(p, item, full, part);
-    int tot;
-    block_exclusive_scan(full, warp_sums, tot);
-    n_full += tot;
+  // thread t owns the contiguous items [lo, hi): one scan for the full units, one
+  // for the partial ones, in item order (the list order does not depend on the
+  // thread count)
+  const int per = (n_items + kPlanThreads - 1) / kPlanThreads;
+  const int lo = min(n_items, (int)threadIdx.x * per), hi = min(n_items, lo + per);
+  int my_full = 0, my_part = 0;
+  for (int item = lo; item < hi; ++item) {
+    int full, part;
+    item_split_counts(p, item, full, part);
+    my_full += full;
+    my_part += part;
   }
-  // pass 2: write the list
-  int at_full = 0, at_part = n_full;
-  for (int base = 0; base < n_items; base += kPlanThreads) {
-    const int item = base + (int)threadIdx.x;
-    int full = 0, part = 0;
-    if (item < n_items) item_split_counts(p, item, full, part);
-    int tot_full, tot_part;
-    const int of = block_exclusive_scan(full, warp_sums, tot_full);
-    const int op = block_exclusive_scan(part, warp_sums, tot_part);
-    for (int s = 0; s < full; ++s) p.units[at_full + of + s] = make_int2(item, s);
-    if (part) p.units[at_part + op] = make_int2(item, full);
-    at_full += tot_full;
-    at_part += tot_part;
+  int n_full, n_part;
+  int at_full = block_exclusive_scan(my_full, warp_sums, n_full);
+  int at_part = n_full + block_exclusive_scan(my_part, warp_sums, n_part);
+  for (int item = lo; item < hi; ++item) {
+    int full, part;
+    item_split_counts(p, item, full, part);
+    for (int s = 0; s < full; ++s) p.units[at_full++] = make_int2(item, s);
+    if (part) p.units[at_part++] = make_int2(item, full);
   }
   if (threadIdx.x == 0) {
     p.sched[0] = 0;
-    p.sched[1] = at_part;
+    p.sched[1] = n_full + n_part;
   }
 }
 

@@ -44,12 +44,14 @@ def _declare(_lib):
         _lib.oracle_rope_interleaved.argtypes = [P, P, I, I, I, I, I, I, D, I]
         _lib.oracle_kv_append_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, I,
                                                 I, I]
+        _lib.oracle_attention_arms.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D, I, D, P, P, I, I]
         _lib.orc_double_to_bf16_bits.argtypes = [D]
         _lib.orc_double_to_bf16_bits.restype = ctypes.c_uint16
         _lib.orc_bf16_bits_to_double.argtypes = [ctypes.c_uint16]
         _lib.orc_bf16_bits_to_double.restype = D
         for f in ("oracle_prefill_causal", "oracle_decode_contig", "oracle_decode_paged",
-                  "oracle_rope_interleaved", "oracle_kv_append_paged", "orc_max_threads"):
+                  "oracle_rope_interleaved", "oracle_kv_append_paged", "orc_max_threads",
+                  "oracle_attention_arms"):
             getattr(_lib, f).restype = ctypes.c_int
 
 
@@ -116,6 +118,30 @@ def decode_contig(q, k, v, seq_lens, scale, nthreads=0):
     _check(lib().oracle_decode_contig(_ptr(q), _ptr(k), _ptr(v), _ptr(lens), _ptr(out), B, max_len, H,
                                       Hkv, dk, dv, float(scale), et, nthreads))
     return out
+
+
+def attention_arms(q, k, v, base_len, scale, window=0, softcap=0.0, sinks=None, slopes=None, nthreads=0):
+    """Query rows with the arms (gqa_oracle.c, `oracle_attention_arms`):
+    q [B, seq_q, H, dk] (or [B, H, dk] for one row), k [B, Hkv, max_len, dk],
+    v [B, Hkv, max_len, dv]; base_len[b] = keys present after this pass's rows
+    (row i sits at position base_len[b] - seq_q + i). window <= 0 and softcap
+    <= 0 switch those arms off; sinks and slopes are [H] or None. Returns f64
+    with q's leading shape and d_v last."""
+    q, k, v = _c(q), _c(k), _c(v)
+    one_row = q.ndim == 3
+    q4 = q.reshape(q.shape[0], 1, q.shape[1], q.shape[2]) if one_row else q
+    B, seq_q, H, dk = q4.shape
+    _, Hkv, max_len, dv = v.shape
+    et = _same_et(q4, k, v)
+    base = _c(np.asarray(base_len), np.int32)
+    sk = None if sinks is None else _c(np.asarray(sinks, np.float64), np.float64)
+    sl = None if slopes is None else _c(np.asarray(slopes, np.float64), np.float64)
+    out = np.empty((B, seq_q, H, dv), np.float64)
+    _check(lib().oracle_attention_arms(_ptr(q4), _ptr(k), _ptr(v), _ptr(base), _ptr(out), B, seq_q, max_len, H,
+                                       Hkv, dk, dv, float(scale), int(window), float(softcap),
+                                       None if sk is None else _ptr(sk), None if sl is None else _ptr(sl), et,
+                                       nthreads))
+    return out.reshape(B, H, dv) if one_row else out
 
 
 def decode_paged(q, k_pool, v_pool, tables, seq_lens, scale, nthreads=0):

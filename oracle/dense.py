@@ -64,3 +64,36 @@ def probabilities(q: np.ndarray, k_full: np.ndarray, position_offset: int, scale
     k_rep = repeat_kv_heads(k_full, H // Hkv)
     scores = np.matmul(np.transpose(q, (1, 0, 2)), np.transpose(k_rep, (0, 2, 1))) * scale
     return softmax_last(scores + causal_mask(seq_q, k_full.shape[1], position_offset))
+
+
+def attention_arms(q: np.ndarray, k_full: np.ndarray, v_full: np.ndarray, position_offset: int, scale: float,
+                   window: int = 0, softcap: float = 0.0, sinks=None, slopes=None) -> np.ndarray:
+    """`attention` with the arms of the attention row, as one additive bias matrix
+    and one extra key: per head, scores = q k^T * scale; softcap c > 0 maps them
+    to c * tanh(scores / c); ALiBi adds slope_h * (j - p); the mask takes keys
+    past the row's position and, with a window W > 0, keys at or before p - W;
+    a sink z_h is one more key column with logit z_h and a zero value vector.
+    Shapes as in `attention`."""
+    seq_q, H, _ = q.shape
+    Hkv, seq_kv, dv = v_full.shape
+    group = H // Hkv
+    qh = np.transpose(q, (1, 0, 2))
+    k_rep = repeat_kv_heads(k_full, group)
+    v_rep = repeat_kv_heads(v_full, group)
+    scores = np.matmul(qh, np.transpose(k_rep, (0, 2, 1))) * scale          # [H, seq_q, seq_kv]
+    if softcap > 0:
+        scores = softcap * np.tanh(scores / softcap)
+    pos = position_offset + np.arange(seq_q)[:, None]                          # [seq_q, 1]
+    keys = np.arange(seq_kv)[None, :]                                          # [1, seq_kv]
+    if slopes is not None:
+        scores = scores + np.asarray(slopes, np.float64)[:, None, None] * (keys - pos)[None]
+    visible = keys <= pos
+    if window > 0:
+        visible = visible & (keys > pos - window)
+    scores = np.where(visible[None], scores, -np.inf)
+    if sinks is not None:  # the extra key: logit z_h for every row, value 0
+        z = np.broadcast_to(np.asarray(sinks, np.float64)[:, None, None], (H, seq_q, 1))
+        scores = np.concatenate([scores, z], axis=2)
+        v_rep = np.concatenate([v_rep, np.zeros((H, 1, dv))], axis=1)
+    probs = softmax_last(scores)
+    return np.transpose(np.matmul(probs, v_rep), (1, 0, 2))

@@ -269,6 +269,93 @@ int oracle_decode_paged(const void* q, const void* k_pool, const void* v_pool, c
   return run_rows(q, &s, seq_lens, out, B, 1, H, scale, nthreads);
 }
 
+/* ---- the arms of the attention row ------------------------------------------
+ *
+ * frink-models src/decoder/attn_block.rs, `push_and_attend_row`: one kernel
+ * serves plain, windowed, softcapped and sink-bearing layers, and takes ALiBi
+ * slopes too (`causal_gqa_attention_row(..., window, sinks, softcap, alibi)` and
+ * `causal_gqa_attention_paged_sinks(...)`). The pages print no formula for the
+ * arms; the readings used here:
+ *   window W > 0   the query at position p sees keys j with p - W < j <= p
+ *                  (W keys, its own included);
+ *   softcap c > 0  s_j <- c * tanh(s_j / c), on the scaled score;
+ *   ALiBi slope a  s_j <- s_j + a_h * (j - p)  (zero for the query's own key,
+ *                  falling off with distance);
+ *   sink z         one more term exp(z_h - m) in the softmax denominator and
+ *                  none in the numerator, m = max(max_j s_j, z_h).
+ * Order: scale, softcap, ALiBi, then the causal and window mask, then the
+ * softmax with the sink.
+ */
+static void attend_arms(const double* qv, const kv_source* s, int b, int kvh, int p, int lo, double scale,
+                        double softcap, const double* sink, double slope, double* out, double* w) {
+  double m = sink ? *sink : -INFINITY;
+  for (int j = lo; j <= p; ++j) {
+    double dot = 0.0;
+    for (int c = 0; c < s->dk; ++c) dot += qv[c] * ld(s->k, row_index(s, b, kvh, j, s->dk, c), s->et);
+    double sj = scale * dot;
+    if (softcap > 0.0) sj = softcap * tanh(sj / softcap);
+    sj += slope * (double)(j - p);
+    w[j - lo] = sj;
+    if (sj > m) m = sj;
+  }
+  double total = sink ? exp(*sink - m) : 0.0;
+  for (int j = lo; j <= p; ++j) {
+    w[j - lo] = exp(w[j - lo] - m);
+    total += w[j - lo];
+  }
+  for (int c = 0; c < s->dv; ++c) {
+    double num = 0.0;
+    for (int j = lo; j <= p; ++j) num += w[j - lo] * ld(s->v, row_index(s, b, kvh, j, s->dv, c), s->et);
+    out[c] = num / total;
+  }
+}
+
+/* Query rows against contiguous caches with the arms: q [B, seq_q, H, dk],
+ * k [B, Hkv, max_len, dk], v [B, Hkv, max_len, dv]; base_len[b] = keys present
+ * after this pass's rows, so row i sits at position base_len[b] - seq_q + i
+ * (decode: seq_q = 1, base_len = seq_lens). window <= 0: none; softcap <= 0:
+ * none; sinks, slopes: [H] or NULL. out f64 [B, seq_q, H, dv]. */
+int oracle_attention_arms(const void* q, const void* k, const void* v, const int32_t* base_len, double* out,
+                          int B, int seq_q, int max_len, int H, int Hkv, int dk, int dv, double scale,
+                          int window, double softcap, const double* sinks, const double* slopes, int et,
+                          int nthreads) {
+  if (B < 0 || seq_q < 1 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || dk <= 0 || dv <= 0) return ORC_BAD_ARG;
+  kv_source s = {0, k, v, max_len, NULL, 0, 0, 0, Hkv, dk, dv, et};
+  for (int b = 0; b < B; ++b) {
+    int n = base_len[b];
+    if (n < seq_q || n < 1) return ORC_BAD_ARG;
+    if (check_rows(&s, b, n) != ORC_OK) return ORC_BAD_INDEX;
+  }
+  const int G = H / Hkv;
+  set_threads(nthreads);
+  const long total = (long)B * seq_q * H;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* qv = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* w = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    if (!qv || !w) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (long r = 0; r < total; ++r) {
+        int h = (int)(r % H);
+        int i = (int)((r / H) % seq_q);
+        int b = (int)(r / ((long)H * seq_q));
+        int pos = base_len[b] - seq_q + i;
+        int lo = (window > 0 && pos - window + 1 > 0) ? pos - window + 1 : 0;
+        for (int c = 0; c < dk; ++c) qv[c] = ld(q, (size_t)r * dk + c, et);
+        attend_arms(qv, &s, b, h / G, pos, lo, scale, softcap, sinks ? sinks + h : NULL, slopes ? slopes[h] : 0.0,
+                    out + (size_t)r * dv, w);
+      }
+    }
+    free(qv);
+    free(w);
+  }
+  return failed ? ORC_NO_MEMORY : ORC_OK;
+}
+
 /* Interleaved RoPE in place on x [B, T, heads, d] stored as `et`; positions
  * [B, T]. The rotated slice is x[..., rot_offset : rot_offset + rot_dim]. */
 int oracle_rope_interleaved(void* x, const int32_t* positions, int B, int T, int heads, int d,

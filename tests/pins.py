@@ -371,4 +371,75 @@ def pin_bf16_storage_widens_exactly(core):
                           core.prefill_causal(wide(qb), wide(kb), wide(vb), 0.3))
 
 
+# ---- the arms of the attention row (window, sink logits, softcap, ALiBi) ---
+# The pages print no formula for these; the readings are stated in
+# oracle/gqa_oracle.c (`oracle_attention_arms`).
+
+def _arms_case(seed, B=2, S=5, H=4, Hkv=2, d=8, L=12):
+    r = rng(seed)
+    return r.standard_normal((B, S, H, d)), r.standard_normal((B, Hkv, L, d)), r.standard_normal((B, Hkv, L, d))
+
+
+def pin_arms_loops_equal_mask_matrix(core):
+    """The loops with every combination of arms equal the mask-matrix form with one
+    bias matrix and the sink as an extra key of zero value (oracle/dense.py)."""
+    from oracle import dense
+    q, k, v = _arms_case(31)
+    S = q.shape[1]
+    sinks, slopes = np.array([0.4, -1.2, 2.0, 0.0]), np.array([0.25, 0.125, 0.0625, 0.5])
+    base = [9, 12]
+    for window, cap, sk, sl in [(3, 0.0, None, None), (0, 1.7, None, None), (0, 0.0, sinks, None),
+                                (0, 0.0, None, slopes), (4, 2.5, sinks, slopes), (1, 0.9, sinks, slopes)]:
+        out = core.attention_arms(q, k, v, base, 0.35, window, cap, sk, sl)
+        for b in range(2):
+            ref = dense.attention_arms(q[b], k[b, :, :base[b]], v[b, :, :base[b]], base[b] - S, 0.35, window, cap,
+                                       sk, sl)
+            assert np.abs(out[b] - ref).max() <= 1e-12
+
+
+def pin_arms_vanish_at_their_limits(core):
+    """No arms equals the plain oracle; a window wider than the history, a sink of
+    -inf, an infinite cap and a zero slope each change nothing."""
+    q, k, v = _arms_case(32)
+    S, H = q.shape[1], q.shape[2]
+    base = np.array([9, 12], np.int32)
+    plain = core.attention_arms(q, k, v, base, 0.5)
+    assert np.abs(plain - core.prefill_causal(q, k, v, 0.5, offsets=base - S)).max() <= 1e-13
+    assert np.abs(core.attention_arms(q, k, v, base, 0.5, window=100) - plain).max() <= 1e-13
+    assert np.abs(core.attention_arms(q, k, v, base, 0.5, sinks=[-1e300] * H) - plain).max() <= 1e-13
+    assert np.abs(core.attention_arms(q, k, v, base, 0.5, softcap=1e9) - plain).max() <= 1e-9
+    assert np.abs(core.attention_arms(q, k, v, base, 0.5, slopes=[0.0] * H) - plain).max() <= 1e-13
+
+
+def pin_arms_closed_forms(core):
+    """One or two visible keys: window 1 gives v_p; window 2 with ALiBi weighs key
+    p-1 by e^(s - a); a sink z gives v_p / (1 + e^(z - s)); a softcap c maps s to
+    c tanh(s / c) and leaves the sink alone."""
+    q, k, v = _arms_case(33)
+    B, S, H, _ = q.shape
+    G = H // k.shape[1]
+    base, scale, cap = [9, 12], 0.45, 0.8
+    slopes, sinks = np.array([0.3, 0.7, 1.1, 0.05]), np.array([0.5, -0.7, 1.9, 0.0])
+    w1 = core.attention_arms(q, k, v, base, scale, window=1)
+    w2 = core.attention_arms(q, k, v, base, scale, window=2, slopes=slopes)
+    ws = core.attention_arms(q, k, v, base, scale, window=1, sinks=sinks)
+    wc = core.attention_arms(q, k, v, base, scale, window=1, sinks=sinks, softcap=cap)
+    sc = lambda b, i, h, j: scale * float(np.dot(q[b, i, h], k[b, h // G, j]))
+    for b in range(B):
+        for i in range(S):
+            p = base[b] - S + i
+            for h in range(H):
+                vp = v[b, h // G, p]
+                assert np.abs(w1[b, i, h] - vp).max() <= 1e-14
+                s = sc(b, i, h, p)
+                assert np.abs(ws[b, i, h] - vp / (1.0 + math.exp(sinks[h] - s))).max() <= 1e-13
+                assert np.abs(wc[b, i, h] - vp / (1.0 + math.exp(sinks[h] - cap * math.tanh(s / cap)))).max() <= 1e-13
+                if p > 0:
+                    s0, s1 = sc(b, i, h, p - 1) - slopes[h], s
+                    mx = max(s0, s1)
+                    e0, e1 = math.exp(s0 - mx), math.exp(s1 - mx)
+                    want = (e0 * v[b, h // G, p - 1] + e1 * vp) / (e0 + e1)
+                    assert np.abs(w2[b, i, h] - want).max() <= 1e-13
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -48,6 +48,12 @@ MUTANTS = [
      "double r = round(ldexp(ax, -shift));"),
     ("bf16: widened with a shift of 15", "uint32_t u = (uint32_t)h << 16;",
      "uint32_t u = (uint32_t)h << 15;"),
+    ("arms: ALiBi sign flipped", "sj += slope * (double)(j - p);", "sj += slope * (double)(p - j);"),
+    ("arms: sink left out of the denominator", "double total = sink ? exp(*sink - m) : 0.0;", "double total = 0.0;"),
+    ("arms: window one key wider", "int lo = (window > 0 && pos - window + 1 > 0) ? pos - window + 1 : 0;",
+     "int lo = (window > 0 && pos - window > 0) ? pos - window : 0;"),
+    ("arms: softcap after the bias", "if (softcap > 0.0) sj = softcap * tanh(sj / softcap);\n    sj += slope * (double)(j - p);",
+     "sj += slope * (double)(j - p);\n    if (softcap > 0.0) sj = softcap * tanh(sj / softcap);"),
 ]
 
 
