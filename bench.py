@@ -212,9 +212,41 @@ def run_paged(args, rank, world):
            "append_bytes": app_bytes, "clocks": clk.summary(), "sample": sample, "rows": int(lens_after.sum())}
     if not args.no_e2e:
         res["e2e"] = run_paged_e2e(args, g, c, tables, lens_in, lens_out, out, ws, dec_bytes + app_bytes, world)
+    if not args.no_secondary:
+        res["arms"] = run_paged_arms(args, g, c, qs[0], tables, lens_out, out, ws, lens_after)
     del c, qs, kns, vns
     torch.cuda.empty_cache()
     return res
+
+
+def run_paged_arms(args, g, c, q, tables, lens, out, ws, lens_after, window=4096):
+    """The paged decode with every arm on (a 4096-row sliding window, sink logits,
+    ALiBi slopes, a logit softcap) over the same pool and lengths. Algorithmic
+    bytes: the K/V rows inside each sequence's window, their table entries, q
+    and out."""
+    B, H, d = q.shape
+    Hkv, bs = c.k_pool.shape[1], c.k_pool.shape[2]
+    dev = q.device
+    sinks = W.randn((H,), W.generator(123, dev), torch.float32, dev)
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32, device=dev)
+    arms = dict(window=window, softcap=30.0, sinks=sinks, alibi_slopes=slopes)
+    vis = np.minimum(lens_after, window)
+    first_blk = (lens_after - vis) // bs
+    last_blk = (lens_after - 1) // bs
+    nbytes = int(vis.sum()) * Hkv * 2 * d * 2 + int((last_blk - first_blk + 1).sum()) * 4 + B * H * 2 * d * 2
+    st = torch.cuda.current_stream()
+
+    def step(_):
+        g.attn_decode_paged(q, c.k_pool, c.v_pool, tables, lens, out, c.scale, workspace=ws, **arms)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    ms = timed(step, max(5, args.steps), st)
+    assert g.attn_get_device_error() == g.OK
+    return {"workload": f"paged decode bf16 as above with window {window}, sink logits, ALiBi slopes and "
+                        "softcap 30 (every arm on)", "gbs": nbytes / (ms * 1e-3) / 1e9, "ms": ms, "bytes": nbytes,
+            "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9}}
 
 
 def run_paged_e2e(args, g, c, tables, lens_in, lens_out, out, ws, step_bytes, world):
@@ -469,6 +501,11 @@ def main():
     if not args.no_secondary and args.only is None:
         secondary = {"prefill": run_prefill(args, peaks, peak_kind), "contig": run_contig(args, peaks, peak_kind),
                      "mla": run_mla(args, peaks, peak_kind)}
+    if res.get("arms"):
+        arms = res["arms"]
+        arms["roofline"].update({"peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": arms["gbs"] / peaks["hbm_gbs"],
+                                 "peak_kind": peak_kind})
+        secondary["paged_arms"] = arms
     if rank != 0:
         return
     cpu = None

@@ -22,7 +22,14 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE_BOUNDS
 
 EXPORTS = ("attn_prefill_causal", "attn_decode_contig", "attn_decode_paged", "kv_append_paged",
            "attn_rope_interleaved", "attn_decode_workspace_bytes", "attn_get_device_error",
-           "gqa_status_string", "gqa_debug_withhold_first_tile", "attn_decode_paged_static_workspace")
+           "gqa_status_string", "gqa_debug_withhold_first_tile", "attn_decode_paged_static_workspace",
+           "attn_prefill_causal_ex", "attn_decode_contig_ex", "attn_decode_paged_ex")
+
+
+class GqaArms(ctypes.Structure):
+    """`gqa_arms` (include/gqa_attn.h): window, softcap, sinks, ALiBi slopes."""
+    _fields_ = [("window", ctypes.c_int), ("softcap", ctypes.c_float), ("sinks", ctypes.c_void_p),
+                ("alibi_slopes", ctypes.c_void_p)]
 
 STATIC_WORKSPACE_BYTES = 16 << 20  # GQA_STATIC_WORKSPACE_BYTES
 
@@ -53,6 +60,9 @@ def load(path: str = None):
         "kv_append_paged": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, I, I, I, P],
         "attn_rope_interleaved": [P, P, I, I, I, I, I, I, I, D, I, P],
         "attn_get_device_error": [P],
+        "attn_prefill_causal_ex": [P, P, P, P, I, I, I, P, I, I, I, I, F, I, P, P],
+        "attn_decode_contig_ex": [P, P, P, P, I, P, P, I, I, I, I, I, I, F, I, P, S, P, P],
+        "attn_decode_paged_ex": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, S, P, P],
         "gqa_debug_withhold_first_tile": [I],
     }
     for name, args in sig.items():
@@ -103,13 +113,29 @@ def _check(status, what):
         raise GqaError(status, what)
 
 
-def attn_prefill_causal(q, k, v, out, attention_scale, position_offset=None, stream=None):
-    """q [B, S, H, dk], k [B, Hkv, S_kv, dk], v [B, Hkv, S_kv, dv], out [B, S, H, dv]."""
+def _arms(window, softcap, sinks, alibi_slopes):
+    """The `gqa_arms` struct (by reference), or None when every arm is off."""
+    if not window and not softcap and sinks is None and alibi_slopes is None:
+        return None
+    for t in (sinks, alibi_slopes):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("sinks and alibi_slopes must be float32 [H]")
+    return ctypes.byref(GqaArms(int(window or 0), float(softcap or 0.0), _p(sinks), _p(alibi_slopes)))
+
+
+def attn_prefill_causal(q, k, v, out, attention_scale, position_offset=None, stream=None, window=0, softcap=0.0,
+                        sinks=None, alibi_slopes=None):
+    """q [B, S, H, dk], k [B, Hkv, S_kv, dk], v [B, Hkv, S_kv, dv], out [B, S, H, dv].
+    window / softcap / sinks / alibi_slopes: the arms (include/gqa_attn.h, `gqa_arms`)."""
     B, S, H, dk = q.shape
     _, Hkv, S_kv, dv = v.shape
-    _check(load().attn_prefill_causal(_p(q), _p(k), _p(v), _p(out), B, S, S_kv, _i32(position_offset), H, Hkv,
-                                      dk, dv, float(attention_scale), _dtype(q, k, v, out), _stream(stream)),
-           "attn_prefill_causal")
+    arms = _arms(window, softcap, sinks, alibi_slopes)
+    args = (_p(q), _p(k), _p(v), _p(out), B, S, S_kv, _i32(position_offset), H, Hkv, dk, dv, float(attention_scale),
+            _dtype(q, k, v, out))
+    if arms is None:
+        _check(load().attn_prefill_causal(*args, _stream(stream)), "attn_prefill_causal")
+    else:
+        _check(load().attn_prefill_causal_ex(*args, arms, _stream(stream)), "attn_prefill_causal_ex")
     return out
 
 
@@ -124,30 +150,38 @@ def decode_workspace(B, H, d_v, max_len, device="cuda"):
 
 
 def attn_decode_contig(q, k_cache, v_cache, seq_lens, out, attention_scale, workspace=None, k_rot_shared=None,
-                       stream=None):
+                       stream=None, window=0, softcap=0.0, sinks=None, alibi_slopes=None):
     """q [B, H, dk]; k_cache [B, Hkv, L, dk - d_rot]; v_cache [B, Hkv, L, dv];
-    k_rot_shared None or [B, L, d_rot]; seq_lens int32 [B]; out [B, H, dv]."""
+    k_rot_shared None or [B, L, d_rot]; seq_lens int32 [B]; out [B, H, dv];
+    window / softcap / sinks / alibi_slopes: the arms (`gqa_arms`)."""
     B, H, dk = q.shape
     _, Hkv, L, dv = v_cache.shape
     d_rot = 0 if k_rot_shared is None else k_rot_shared.shape[-1]
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().attn_decode_contig(_p(q), _p(k_cache), _p(v_cache), _p(k_rot_shared), d_rot, _i32(seq_lens),
-                                     _p(out), B, L, H, Hkv, dk, dv, float(attention_scale),
-                                     _dtype(q, k_cache, v_cache, out, k_rot_shared), _p(workspace), ws,
-                                     _stream(stream)), "attn_decode_contig")
+    arms = _arms(window, softcap, sinks, alibi_slopes)
+    args = (_p(q), _p(k_cache), _p(v_cache), _p(k_rot_shared), d_rot, _i32(seq_lens), _p(out), B, L, H, Hkv, dk, dv,
+            float(attention_scale), _dtype(q, k_cache, v_cache, out, k_rot_shared), _p(workspace), ws)
+    if arms is None:
+        _check(load().attn_decode_contig(*args, _stream(stream)), "attn_decode_contig")
+    else:
+        _check(load().attn_decode_contig_ex(*args, arms, _stream(stream)), "attn_decode_contig_ex")
     return out
 
 
 def attn_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, out, attention_scale, workspace=None,
-                      stream=None):
-    """q [B, H, dk]; pools [num_blocks, Hkv, bs, d]; block_tables int32 [B, mbps]."""
+                      stream=None, window=0, softcap=0.0, sinks=None, alibi_slopes=None):
+    """q [B, H, dk]; pools [num_blocks, Hkv, bs, d]; block_tables int32 [B, mbps];
+    window / softcap / sinks / alibi_slopes: the arms (`gqa_arms`)."""
     B, H, dk = q.shape
     nb, Hkv, bs, dv = v_pool.shape
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().attn_decode_paged(_p(q), _p(k_pool), _p(v_pool), _i32(block_tables), _i32(seq_lens), _p(out),
-                                    B, block_tables.shape[1], nb, bs, H, Hkv, dk, dv, float(attention_scale),
-                                    _dtype(q, k_pool, v_pool, out), _p(workspace), ws, _stream(stream)),
-           "attn_decode_paged")
+    arms = _arms(window, softcap, sinks, alibi_slopes)
+    args = (_p(q), _p(k_pool), _p(v_pool), _i32(block_tables), _i32(seq_lens), _p(out), B, block_tables.shape[1], nb,
+            bs, H, Hkv, dk, dv, float(attention_scale), _dtype(q, k_pool, v_pool, out), _p(workspace), ws)
+    if arms is None:
+        _check(load().attn_decode_paged(*args, _stream(stream)), "attn_decode_paged")
+    else:
+        _check(load().attn_decode_paged_ex(*args, arms, _stream(stream)), "attn_decode_paged_ex")
     return out
 
 

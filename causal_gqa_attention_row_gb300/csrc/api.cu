@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libgqa_attn.so (include/gqa_attn.h):
 // host-side argument checks, work decomposition, and launches. No device
 // memory is allocated here; the only device state is the error word below.
+#include <cmath>
 #include <climits>
 #include <cstdint>
 
@@ -63,6 +64,22 @@ gqa_status launch_rows(const gqa::RowsParams& p, int bf16, int dk, int dv, int d
   return GQA_OK;
 }
 
+// The arms of the attention row into the kernel parameters; true when any is on.
+gqa_status apply_arms(gqa::RowsParams& p, const gqa_arms* arms, bool* active) {
+  *active = false;
+  if (!arms) return GQA_OK;
+  if (!std::isfinite(arms->softcap)) return GQA_ERR_INVALID_ARG;
+  if ((arms->sinks && reinterpret_cast<uintptr_t>(arms->sinks) % 4) ||
+      (arms->alibi_slopes && reinterpret_cast<uintptr_t>(arms->alibi_slopes) % 4))
+    return GQA_ERR_INVALID_ARG;
+  p.window = arms->window > 0 ? arms->window : 0;
+  p.softcap2 = arms->softcap > 0.f ? arms->softcap * gqa::kLog2e : 0.f;
+  p.sinks = arms->sinks;
+  p.alibi = arms->alibi_slopes;
+  *active = p.window > 0 || p.softcap2 > 0.f || p.sinks || p.alibi;
+  return GQA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -103,10 +120,10 @@ static gqa_status decode_common(gqa::RowsParams& p, int bf16, int d_k, int d_v, 
   return launch_rows(p, bf16, d_k, d_v, d_rot, p.GH, st);
 }
 
-gqa_status attn_decode_contig(const void* q, const void* k_cache, const void* v_cache, const void* k_rot_shared,
-                              int d_rot, const int32_t* seq_lens, void* out, int B, int max_len, int H, int Hkv,
-                              int d_k, int d_v, float attention_scale, gqa_dtype dt, void* workspace,
-                              size_t workspace_bytes, void* stream) {
+gqa_status attn_decode_contig_ex(const void* q, const void* k_cache, const void* v_cache, const void* k_rot_shared,
+                                 int d_rot, const int32_t* seq_lens, void* out, int B, int max_len, int H, int Hkv,
+                                 int d_k, int d_v, float attention_scale, gqa_dtype dt, void* workspace,
+                                 size_t workspace_bytes, const gqa_arms* arms, void* stream) {
   const int bf16 = dtype_flag(dt);
   if (bf16 < 0 || B < 0 || max_len <= 0 || !heads_ok(H, Hkv) || !width_ok(d_k) || !width_ok(d_v))
     return GQA_ERR_INVALID_ARG;
@@ -131,13 +148,17 @@ gqa_status attn_decode_contig(const void* q, const void* k_cache, const void* v_
   p.max_len = max_len;
   p.capacity = max_len;
   p.qscale = attention_scale * 1.4426950408889634f;
+  bool arms_on;
+  const gqa_status sa = apply_arms(p, arms, &arms_on);
+  if (sa != GQA_OK) return sa;
   return decode_common(p, bf16, d_k, d_v, d_rot, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
-gqa_status attn_decode_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
-                             const int32_t* seq_lens, void* out, int B, int max_blocks_per_seq, int num_blocks,
-                             int block_size, int H, int Hkv, int d_k, int d_v, float attention_scale, gqa_dtype dt,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+gqa_status attn_decode_paged_ex(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                                const int32_t* seq_lens, void* out, int B, int max_blocks_per_seq, int num_blocks,
+                                int block_size, int H, int Hkv, int d_k, int d_v, float attention_scale,
+                                gqa_dtype dt, void* workspace, size_t workspace_bytes, const gqa_arms* arms,
+                                void* stream) {
   const int bf16 = dtype_flag(dt);
   if (bf16 < 0 || B < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0 || !heads_ok(H, Hkv) ||
       !width_ok(d_k) || !width_ok(d_v))
@@ -163,12 +184,15 @@ gqa_status attn_decode_paged(const void* q, const void* k_pool, const void* v_po
   p.bs = block_size;
   p.num_blocks = num_blocks;
   p.qscale = attention_scale * 1.4426950408889634f;
+  bool arms_on;
+  const gqa_status sa = apply_arms(p, arms, &arms_on);
+  if (sa != GQA_OK) return sa;
   return decode_common(p, bf16, d_k, d_v, 0, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
-gqa_status attn_prefill_causal(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
-                               int seq_kv_max, const int32_t* position_offset, int H, int Hkv, int d_k, int d_v,
-                               float attention_scale, gqa_dtype dt, void* stream) {
+gqa_status attn_prefill_causal_ex(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
+                                  int seq_kv_max, const int32_t* position_offset, int H, int Hkv, int d_k, int d_v,
+                                  float attention_scale, gqa_dtype dt, const gqa_arms* arms, void* stream) {
   const int bf16 = dtype_flag(dt);
   if (bf16 < 0 || B < 0 || seq_q < 0 || seq_kv_max <= 0 || seq_q > seq_kv_max || !heads_ok(H, Hkv) ||
       !width_ok(d_k) || !width_ok(d_v))
@@ -180,12 +204,15 @@ gqa_status attn_prefill_causal(const void* q, const void* k, const void* v, void
   unsigned* err = error_word();
   if (!err) return GQA_ERR_CUDA;
   const float qscale = attention_scale * 1.4426950408889634f;
-  if (gqa::prefill_tc_supported(bf16, d_k, d_v) && attention_scale > 0.f)
+  gqa::RowsParams p{};
+  bool arms_on;
+  const gqa_status sa = apply_arms(p, arms, &arms_on);
+  if (sa != GQA_OK) return sa;
+  if (!arms_on && gqa::prefill_tc_supported(bf16, d_k, d_v) && attention_scale > 0.f)
     return from_cuda(gqa::launch_prefill_tc(q, k, v, out, B, seq_q, seq_kv_max, position_offset, H, Hkv, d_k, d_v,
                                             qscale, err, st));
   const int nvmax = gqa::rows_max_nv(bf16, d_k, d_v, 0);
   if (nvmax == 0) return GQA_ERR_UNSUPPORTED;
-  gqa::RowsParams p{};
   p.q = q;
   p.k = k;
   p.v = v;
@@ -209,6 +236,31 @@ gqa_status attn_prefill_causal(const void* q, const void* k, const void* v, void
   p.qscale = qscale;
   p.err = err;
   return launch_rows(p, bf16, d_k, d_v, 0, p.GH * p.QR, st);
+}
+
+// The plain calls: the _ex calls with no arms.
+gqa_status attn_decode_contig(const void* q, const void* k_cache, const void* v_cache, const void* k_rot_shared,
+                              int d_rot, const int32_t* seq_lens, void* out, int B, int max_len, int H, int Hkv,
+                              int d_k, int d_v, float attention_scale, gqa_dtype dt, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return attn_decode_contig_ex(q, k_cache, v_cache, k_rot_shared, d_rot, seq_lens, out, B, max_len, H, Hkv, d_k, d_v,
+                               attention_scale, dt, workspace, workspace_bytes, nullptr, stream);
+}
+
+gqa_status attn_decode_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                             const int32_t* seq_lens, void* out, int B, int max_blocks_per_seq, int num_blocks,
+                             int block_size, int H, int Hkv, int d_k, int d_v, float attention_scale, gqa_dtype dt,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_decode_paged_ex(q, k_pool, v_pool, block_tables, seq_lens, out, B, max_blocks_per_seq, num_blocks,
+                              block_size, H, Hkv, d_k, d_v, attention_scale, dt, workspace, workspace_bytes, nullptr,
+                              stream);
+}
+
+gqa_status attn_prefill_causal(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
+                               int seq_kv_max, const int32_t* position_offset, int H, int Hkv, int d_k, int d_v,
+                               float attention_scale, gqa_dtype dt, void* stream) {
+  return attn_prefill_causal_ex(q, k, v, out, B, seq_q, seq_kv_max, position_offset, H, Hkv, d_k, d_v,
+                                attention_scale, dt, nullptr, stream);
 }
 
 gqa_status kv_append_paged(void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,

@@ -217,7 +217,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 struct Unit {
   int b, kvh, hc, split;
   int kv_len, i0, i_last;
-  int r0, r1, nsplit;  // key rows [r0, r1) of this split; splits of the item
+  int r0, r1;   // key rows [r0, r1) of this split
+  int lo;       // first key the unit's first row sees (the window's lower end)
+  int nsplit;   // splits of the item that hold a visible key
   bool len_ok;
 };
 
@@ -235,7 +237,8 @@ __device__ __forceinline__ Unit decode_unit(const RowsParams& p, int item, int s
   u.i_last = min(u.i0 + p.QR, p.seq_q) - 1;
   u.len_ok = u.kv_len >= p.seq_q && u.kv_len >= 1 && u.kv_len <= p.capacity;
   const int kv_hi = u.len_ok ? u.kv_len - p.seq_q + u.i_last + 1 : 0;  // keys the last row sees
-  u.nsplit = (kv_hi + p.split_rows - 1) / p.split_rows;
+  u.lo = u.len_ok ? first_visible_key(u.kv_len - p.seq_q + u.i0, p.window) : 0;
+  u.nsplit = (kv_hi + p.split_rows - 1) / p.split_rows - u.lo / p.split_rows;
   u.r0 = split * p.split_rows;
   u.r1 = min(u.r0 + p.split_rows, kv_hi);
   return u;
@@ -258,7 +261,9 @@ __device__ __forceinline__ bool compute_sync(uint64_t* bar, uint32_t parity, vol
   return warp_wait(bar, parity, abort_flag, err);
 }
 
-template <typename ET, int DK, int DV, int DROT, int NV>
+// ARMS: the window / softcap / sink / ALiBi code is compiled in (a plain call
+// runs the instantiation without it, at the plain kernel's register count).
+template <typename ET, int DK, int DV, int DROT, int NV, bool ARMS>
 __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::MIN_CTAS)
     attn_rows_kernel(const RowsParams p) {
   using C = RowsCfg<ET, DK, DV, DROT, NV>;
@@ -329,7 +334,7 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
       }
       if (p.paged) {
         // every block-table entry of the unit is checked before any copy
-        const int blk0 = u.r0 / p.bs, blk1 = (u.r1 - 1) / p.bs;
+        const int blk0 = max(u.r0, u.lo) / p.bs, blk1 = (u.r1 - 1) / p.bs;  // entries below the window go unread
         bool bad = false;
         for (int bi = blk0 + lane; bi <= blk1; bi += 32) {
           const int e = __ldg(p.tables + (size_t)u.b * p.mbps + bi);
@@ -357,8 +362,11 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
         }
       }
       const int ntiles = (u.r1 - u.r0 + T - 1) / T;
+      // tiles stay aligned to the split start (the arithmetic on a key row must
+      // not depend on the window); the first one holds the window's lower end
+      const int t0 = u.lo > u.r0 ? (u.lo - u.r0) / T : 0;
       const int qrows = u.i_last - u.i0 + 1;
-      for (int t = 0; t < ntiles; ++t, ++gt) {
+      for (int t = t0; t < ntiles; ++t, ++gt) {
         const int s = gt % kStages;
         if (gt >= kStages) {
           bool ok = true;
@@ -385,8 +393,8 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
         const int n = min(T, u.r1 - tr0);
         unsigned char* st = data + s * C::stage_bytes;
         if (lane == 0) {
-          hdr->tile[s] = make_int4(item, split, tr0, n | (t == 0 ? 1 << 16 : 0) | (t == ntiles - 1 ? 1 << 17 : 0));
-          const uint32_t qb = t == 0 ? (uint32_t)(qrows * p.GH * DK * C::ES) : 0u;
+          hdr->tile[s] = make_int4(item, split, tr0, n | (t == t0 ? 1 << 16 : 0) | (t == ntiles - 1 ? 1 << 17 : 0));
+          const uint32_t qb = t == t0 ? (uint32_t)(qrows * p.GH * DK * C::ES) : 0u;
           mbar_arrive_expect_tx(&hdr->full[s], (uint32_t)(n * C::row_bytes) + qb);
         }
         __syncwarp();
@@ -405,7 +413,11 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
           const int blk0 = tr0 / p.bs, blk1 = (tr0 + n - 1) / p.bs;
           for (int bi = blk0 + lane; bi <= blk1; bi += 32) {
             const int ra = max(tr0, bi * p.bs), rz = min(tr0 + n, (bi + 1) * p.bs);
-            const int e = __ldg(p.tables + (size_t)u.b * p.mbps + bi);
+            // A block wholly below the window may be gone from the table; its rows
+            // (masked out) are filled from the block holding the window's first
+            // key, whose entry was checked, so that they hold finite values.
+            const int bsrc = (bi + 1) * p.bs <= u.lo ? u.lo / p.bs : bi;
+            const int e = __ldg(p.tables + (size_t)u.b * p.mbps + bsrc);
             const size_t src_row = ((size_t)e * p.Hkv + u.kvh) * p.bs + (ra - bi * p.bs);
             bulk_g2s(st + (ra - tr0) * C::DN * C::ES, reinterpret_cast<const ET*>(p.k) + src_row * DK,
                      (uint32_t)((rz - ra) * DK * C::ES), &hdr->full[s], pol);
@@ -413,7 +425,7 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
                      (uint32_t)((rz - ra) * DV * C::ES), &hdr->full[s], pol);
           }
         }
-        if (t == 0 && lane < qrows) {
+        if (t == t0 && lane < qrows) {
           // query row i0 + lane: the unit's GH heads of it, contiguous
           const ET* src = reinterpret_cast<const ET*>(p.q) +
                           (((size_t)u.b * p.seq_q + u.i0 + lane) * p.H + u.kvh * p.G + u.hc * p.GH) * DK;
@@ -470,7 +482,9 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
   // output accumulators (all heads, this lane's chunks) and the owned head's state
   float2 o2[NV][H2V];
   float m_ref = -INFINITY, l_sum = 0.f;
-  int lim_own = 0;
+  int lim_own = 0;    // keys < lim_own are causal for the owned head's row
+  int lo_own = 0;     // ... and keys >= lo_own inside its window
+  float slope2 = 0.f; // the owned head's ALiBi slope in the log2 domain
   int merges = 0;
   for (int gt = 0;; ++gt) {
     const int s = gt % kStages;
@@ -492,7 +506,13 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
 #pragma unroll
         for (int e = 0; e < H2V; ++e) o2[vh][e] = make_float2(0.f, 0.f);
         const int iq = u.i0 + vh / p.GH;
-        if (vh == own) lim_own = iq <= u.i_last ? u.kv_len - p.seq_q + iq + 1 : 0;
+        if (vh == own) {
+          lim_own = iq <= u.i_last ? u.kv_len - p.seq_q + iq + 1 : 0;
+          if (ARMS) {
+            lo_own = first_visible_key(lim_own - 1, p.window);
+            slope2 = p.alibi ? __ldg(p.alibi + u.kvh * p.G + u.hc * p.GH + vh % p.GH) * kLog2e : 0.f;
+          }
+        }
       }
       m_ref = -INFINITY;
       l_sum = 0.f;
@@ -540,11 +560,20 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
           pa[vh] = acc_a[vh].x + acc_a[vh].y;
           pb[vh] = acc_b[vh].x + acc_b[vh].y;
         }
-        const float sa = reduce_own<NV, L>(pa, li);
-        const float sb = reduce_own<NV, L>(pb, li);
+        float sa = reduce_own<NV, L>(pa, li);
+        float sb = reduce_own<NV, L>(pb, li);
+        // ---- the arms: softcap on the scaled score, then the ALiBi bias
+        if (ARMS && p.softcap2 > 0.f) {
+          sa = p.softcap2 * tanhf(sa / p.softcap2);
+          sb = p.softcap2 * tanhf(sb / p.softcap2);
+        }
+        if (ARMS && p.alibi) {
+          sa = fmaf(slope2, (float)(tr0 + ra - (lim_own - 1)), sa);
+          sb = fmaf(slope2, (float)(tr0 + rb2 - (lim_own - 1)), sb);
+        }
         // ---- online softmax of the owned head over the two rows
-        const bool visa = va && tr0 + ra < lim_own;
-        const bool visb = vb && tr0 + rb2 < lim_own;
+        const bool visa = va && tr0 + ra < lim_own && (!ARMS || tr0 + ra >= lo_own);
+        const bool visb = vb && tr0 + rb2 < lim_own && (!ARMS || tr0 + rb2 >= lo_own);
         const float mx = fmaxf(visa ? sa : -INFINITY, visb ? sb : -INFINITY);
         const bool grow = mx > m_ref + kRescaleLog2;
         float f = 1.f;
@@ -663,7 +692,15 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
       }
       const size_t row = unit_out_row(p, u, vh);
       if (u.nsplit == 1) {
-        reinterpret_cast<ET*>(p.out)[row * DV + d] = Elem<ET>::from_f32(ls > 0.f ? os / ls : 0.f);
+        float res = ls > 0.f ? os / ls : 0.f;
+        if (ARMS && p.sinks) {  // the sink logit joins the denominator (once per row and head)
+          const float z2 = __ldg(p.sinks + u.kvh * p.G + u.hc * p.GH + vh % p.GH) * kLog2e;
+          const float Mx = fmaxf(M, z2);
+          const float a = M == -INFINITY ? 0.f : ex2(M - Mx);
+          const float den = fmaf(ls, a, ex2(z2 - Mx));
+          res = den > 0.f ? os * a / den : 0.f;
+        }
+        reinterpret_cast<ET*>(p.out)[row * DV + d] = Elem<ET>::from_f32(res);
       } else {
         float* P = p.partial + (row * p.max_splits + u.split) * (DV + 2);
         if (d == 0) {
@@ -678,10 +715,10 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
 
 // Host launcher of one instantiation: a persistent grid of one CTA per
 // resident slot (SMs x CTAs per SM), capped at the number of units.
-template <typename ET, int DK, int DV, int DROT, int NV>
-cudaError_t launch_rows_inst(const RowsParams& p, cudaStream_t st) {
+template <typename ET, int DK, int DV, int DROT, int NV, bool ARMS>
+cudaError_t launch_rows_inst_arms(const RowsParams& p, cudaStream_t st) {
   using C = RowsCfg<ET, DK, DV, DROT, NV>;
-  auto kern = attn_rows_kernel<ET, DK, DV, DROT, NV>;
+  auto kern = attn_rows_kernel<ET, DK, DV, DROT, NV, ARMS>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -706,6 +743,13 @@ cudaError_t launch_rows_inst(const RowsParams& p, cudaStream_t st) {
   const int grid = (int)(units < slots ? units : slots);
   kern<<<grid, kRowsThreads, C::smem_bytes, st>>>(p);
   return cudaGetLastError();
+}
+
+template <typename ET, int DK, int DV, int DROT, int NV>
+cudaError_t launch_rows_inst(const RowsParams& p, cudaStream_t st) {
+  const bool arms = p.window > 0 || p.softcap2 > 0.f || p.sinks || p.alibi;
+  return arms ? launch_rows_inst_arms<ET, DK, DV, DROT, NV, true>(p, st)
+              : launch_rows_inst_arms<ET, DK, DV, DROT, NV, false>(p, st);
 }
 
 }  // namespace gqa

@@ -42,7 +42,23 @@ struct RowsParams {
   int max_splits;
   float qscale;             // attention_scale * log2(e)
   int debug_withhold;       // test hook: withhold the first tile of every CTA
+  // The arms of the attention row (all off when zero / NULL): a row at
+  // position p sees keys first_visible_key(p, window)..p; scores s (natural
+  // units) become softcap * tanh(s / softcap), then s + alibi[h] * (j - p); the
+  // sink logit sinks[h] joins the softmax denominator only.
+  int window;               // > 0: the last `window` positions; <= 0: no window
+  float softcap2;           // softcap * log2(e) (the kernels score in the log2 domain); 0: none
+  const float* sinks;       // [H] device, natural units, or NULL
+  const float* alibi;       // [H] device, natural units, or NULL
 };
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// First key a row at position p sees: p - window + 1 (not below 0) with a
+// window, else 0.
+__host__ __device__ inline int first_visible_key(int p, int window) {
+  return (window > 0 && p - window + 1 > 0) ? p - window + 1 : 0;
+}
 
 // Dispatch of the SIMT kernel by element type and head widths; NV = GH * QR.
 // Returns cudaErrorNotSupported when there is no instantiation.

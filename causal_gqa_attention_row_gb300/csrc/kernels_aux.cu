@@ -74,7 +74,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& 
   return before;
 }
 
-__device__ __forceinline__ void item_split_counts(const RowsParams& p, int item, int& full, int& part) {
+// Splits of one item that hold a visible key: full ones s_first .. s_first +
+// full - 1 (a window hides the splits below its lower end), then one partial
+// split when split_rows does not divide the keys the last row sees.
+__device__ __forceinline__ void item_split_counts(const RowsParams& p, int item, int& full, int& part,
+                                                  int& s_first) {
   const int rb = item % p.n_rblocks;
   const int b = item / (p.n_rblocks * p.n_hchunks * p.Hkv);
   const int kv_len = p.kv_len ? p.kv_len[b] : (p.offsets ? p.offsets[b] : 0) + p.seq_q;
@@ -82,11 +86,13 @@ __device__ __forceinline__ void item_split_counts(const RowsParams& p, int item,
   if (!len_ok) {
     full = 1;
     part = 0;
+    s_first = 0;
     return;
   }
   const int i_last = min(rb * p.QR + p.QR, p.seq_q) - 1;
   const int kv_hi = kv_len - p.seq_q + i_last + 1;
-  full = kv_hi / p.split_rows;
+  s_first = first_visible_key(kv_len - p.seq_q + rb * p.QR, p.window) / p.split_rows;
+  full = max(0, kv_hi / p.split_rows - s_first);
   part = (kv_hi % p.split_rows) != 0;
 }
 
@@ -100,8 +106,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_units_kernel(const RowsPara
   const int lo = min(n_items, (int)threadIdx.x * per), hi = min(n_items, lo + per);
   int my_full = 0, my_part = 0;
   for (int item = lo; item < hi; ++item) {
-    int full, part;
-    item_split_counts(p, item, full, part);
+    int full, part, s_first;
+    item_split_counts(p, item, full, part, s_first);
     my_full += full;
     my_part += part;
   }
@@ -109,10 +115,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_units_kernel(const RowsPara
   int at_full = block_exclusive_scan(my_full, warp_sums, n_full);
   int at_part = n_full + block_exclusive_scan(my_part, warp_sums, n_part);
   for (int item = lo; item < hi; ++item) {
-    int full, part;
-    item_split_counts(p, item, full, part);
-    for (int s = 0; s < full; ++s) p.units[at_full++] = make_int2(item, s);
-    if (part) p.units[at_part++] = make_int2(item, full);
+    int full, part, s_first;
+    item_split_counts(p, item, full, part, s_first);
+    for (int s = 0; s < full; ++s) p.units[at_full++] = make_int2(item, s_first + s);
+    if (part) p.units[at_part++] = make_int2(item, s_first + full);
   }
   if (threadIdx.x == 0) {
     p.sched[0] = 0;
@@ -138,12 +144,16 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
   const int b = wid / (p.seq_q * p.H);
   const int kv_len = p.kv_len ? p.kv_len[b] : (p.offsets ? p.offsets[b] : 0) + p.seq_q;
   if (!(kv_len >= p.seq_q && kv_len >= 1 && kv_len <= p.capacity)) return;  // attention wrote zeros
-  const int n = (kv_len + p.split_rows - 1) / p.split_rows;  // seq_q == 1 whenever splitting
-  if (n <= 1) return;  // attention wrote the output itself
+  // seq_q == 1 whenever splitting: the row sits at kv_len - 1
+  const int n = (kv_len + p.split_rows - 1) / p.split_rows;
+  const int s_lo = first_visible_key(kv_len - 1, p.window) / p.split_rows;  // splits below the window hold no key
+  if (n - s_lo <= 1) return;  // attention wrote the output itself
   const int stride = DV + 2;
   const float* P = p.partial + (size_t)wid * p.max_splits * stride;
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, P[(size_t)s * stride]);
+  // the sink logit (log2 domain) joins the denominator once per row and head
+  const float z2 = p.sinks ? __ldg(p.sinks + wid % p.H) * kLog2e : -INFINITY;
+  float M = z2;
+  for (int s = s_lo + lane; s < n; s += 32) M = fmaxf(M, P[(size_t)s * stride]);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   ET* out = reinterpret_cast<ET*>(p.out) + (size_t)wid * DV;
@@ -151,15 +161,15 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
     for (int d = lane; d < DV; d += 32) out[d] = Elem<ET>::from_f32(0.f);
     return;
   }
-  float den = 0.f;
-  for (int s = 0; s < n; ++s) {
+  float den = p.sinks ? exp2f(z2 - M) : 0.f;
+  for (int s = s_lo; s < n; ++s) {
     const float ms = P[(size_t)s * stride];
     const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
     den = fmaf(w, P[(size_t)s * stride + 1], den);
   }
   for (int d = lane; d < DV; d += 32) {
     float acc = 0.f;
-    for (int s = 0; s < n; ++s) {
+    for (int s = s_lo; s < n; ++s) {
       const float ms = P[(size_t)s * stride];
       const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
       acc = fmaf(w, P[(size_t)s * stride + 2 + d], acc);

@@ -121,6 +121,50 @@ gqa_status attn_decode_paged(const void* q, const void* k_pool, const void* v_po
                              int d_k, int d_v, float attention_scale, gqa_dtype dt, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/*
+ * The arms of the attention row (frink-models src/decoder/attn_block.rs,
+ * `push_and_attend_row`: one kernel serves plain, windowed, softcapped and
+ * sink-bearing layers and takes ALiBi slopes too; the pages print no formula,
+ * so these are the readings implemented). With s_j = attention_scale * q.k_j for
+ * a row at position p:
+ *   softcap > 0        s_j <- softcap * tanh(s_j / softcap)
+ *   alibi_slopes[h]    s_j <- s_j + alibi_slopes[h] * (j - p)
+ *   window > 0         only keys p - window < j <= p are visible (causal keys
+ *                      j <= p as always); rows below the window are never read
+ *                      and their block-table entries never looked at
+ *   sinks[h]           one more term exp(sinks[h] - m) in the softmax
+ *                      denominator, none in the numerator
+ * in that order, then the softmax. The pages' own model code leaves softcap
+ * off when a layer has sinks; the library takes any combination.
+ * `gqa_arms` is read on the host during the call; sinks and alibi_slopes are
+ * device pointers to H floats (4-byte aligned) or NULL. A NULL `arms` pointer,
+ * or window <= 0, softcap <= 0 and NULL arrays, is plain attention.
+ * GQA_ERR_INVALID_ARG: softcap not finite, a misaligned array.
+ */
+typedef struct gqa_arms {
+  int window;
+  float softcap;
+  const float* sinks;
+  const float* alibi_slopes;
+} gqa_arms;
+
+/* attn_decode_contig / attn_decode_paged / attn_prefill_causal with the arms;
+ * every other argument as there. Prefill with an arm on runs on the SIMT kernel
+ * (the tensor-core kernel serves the plain arm). */
+gqa_status attn_decode_contig_ex(const void* q, const void* k_cache, const void* v_cache,
+                                 const void* k_rot_shared, int d_rot, const int32_t* seq_lens, void* out,
+                                 int B, int max_len, int H, int Hkv, int d_k, int d_v, float attention_scale,
+                                 gqa_dtype dt, void* workspace, size_t workspace_bytes, const gqa_arms* arms,
+                                 void* stream);
+gqa_status attn_decode_paged_ex(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                                const int32_t* seq_lens, void* out, int B, int max_blocks_per_seq, int num_blocks,
+                                int block_size, int H, int Hkv, int d_k, int d_v, float attention_scale,
+                                gqa_dtype dt, void* workspace, size_t workspace_bytes, const gqa_arms* arms,
+                                void* stream);
+gqa_status attn_prefill_causal_ex(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
+                                  int seq_kv_max, const int32_t* position_offset, int H, int Hkv, int d_k, int d_v,
+                                  float attention_scale, gqa_dtype dt, const gqa_arms* arms, void* stream);
+
 /* Size of the fixed device scratch behind attn_decode_paged_static_workspace. */
 #define GQA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
 

@@ -73,5 +73,13 @@ def test_bad_arguments_rejected_before_launch(lib):
     assert lib.attn_rope_interleaved(P, P, 1, 4, 2, 64, 0, 0, 64, 0.0, 1, N) == inv
     # rotated slice past the head
     assert lib.kv_append_paged(P, P, P, P, P, P, P, P, 2, 4, 10, 16, 8, 2, 64, 64, 1e4, 16, 64, 1, N) == inv
+    # the arms: a softcap that is not finite, a misaligned sink array
+    import causal_gqa_attention_row_gb300 as g
+    nan_cap = g.GqaArms(0, float("nan"), None, None)
+    assert lib.attn_decode_contig_ex(P, P, P, N, 0, P, P, 2, 64, 8, 2, 128, 128, 0.1, 1, N, 0,
+                                     ctypes.byref(nan_cap), N) == inv
+    bad_sinks = g.GqaArms(16, 0.0, 18, None)
+    assert lib.attn_decode_paged_ex(P, P, P, P, P, P, 2, 4, 10, 16, 8, 2, 128, 128, 0.1, 1, N, 0,
+                                    ctypes.byref(bad_sinks), N) == inv
     # empty batches are no-ops
     assert lib.attn_decode_contig(N, N, N, N, 0, N, N, 0, 64, 8, 2, 128, 128, 0.1, 1, N, 0, N) == 0
