@@ -55,6 +55,12 @@
 // is written as the output (one split) or as a partial (m, l, o) that the
 // combine kernel merges, again in a fixed order.
 //
+// The arms of the attention row (a template flag, so that plain calls run code
+// without them): the owner lane applies a logit softcap and then an ALiBi bias
+// to its head's score; a sliding window is a lower bound on the visible keys
+// and on the tiles a unit streams; a sink logit joins the softmax denominator
+// in the final merge (single split) or in the combine kernel.
+//
 // Determinism: split boundaries are multiples of kSplitRows, tiles multiples of
 // T rows from the split start, and the row -> row-group assignment a function of
 // the key index only. The arithmetic on a key row therefore does not depend on
