@@ -360,7 +360,15 @@ def run_prefill(args, peaks, peak_kind):
     queue_ahead(n)
     step_ms = timed(lambda k: step(3 + k), n, st, sync_first=False)
     assert g.attn_get_device_error() == g.OK
-    ms = statistics.median(evs[3 + k][0].elapsed_time(evs[3 + k][1]) for k in range(n))
+    # The kernel's average launch duration: CUDA events around a run of
+    # back-to-back launches on the step's (already rotated) inputs, queued ahead
+    # of the GPU (one event pair per microsecond-long launch would be dominated by
+    # the events' 0.5 us resolution and the launch gap in front of each).
+    n_kern = 4 * n
+    torch.cuda.synchronize()
+    queue_ahead(n_kern, us_per_group=40.0)
+    ms = timed(lambda k: g.attn_prefill_causal(qs[3], ks[3], c.v, out, c.scale), n_kern, st, sync_first=False)
+    assert g.attn_get_device_error() == g.OK
     tflops = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"workload": W.WORKLOADS["prefill"], "tflops": tflops, "kernel_ms": ms, "step_ms": step_ms,

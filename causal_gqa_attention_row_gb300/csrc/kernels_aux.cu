@@ -229,7 +229,10 @@ __device__ __forceinline__ void rotate_pair(ET* x, float c, float s) {
   x[1] = Elem<ET>::from_f32(fmaf(x0, s, x1 * c));
 }
 
-// One thread per (token, pair), looping over the heads.
+// One thread per (token, pair): the angle once, then the pair of every head,
+// eight heads' loads in flight at a time.
+constexpr int kRopeHeadsInFlight = 8;
+
 template <typename ET>
 __global__ void __launch_bounds__(256) rope_kernel(ET* x, const int32_t* positions, int B, int T, int heads, int d,
                                                    int heads_outer, int rot_offset, int rot_dim, const RopeFreqs fr) {
@@ -241,9 +244,26 @@ __global__ void __launch_bounds__(256) rope_kernel(ET* x, const int32_t* positio
   const int b = (int)(tok / T), t = (int)(tok % T);
   float c, s;
   rope_cos_sin((double)positions[tok], fr.w[pr], &c, &s);
-  for (int h = 0; h < heads; ++h) {
-    const size_t row = heads_outer ? (((size_t)b * heads + h) * T + t) : ((size_t)tok * heads + h);
-    rotate_pair(x + row * d + rot_offset + 2 * pr, c, s);
+  for (int h0 = 0; h0 < heads; h0 += kRopeHeadsInFlight) {
+    ET* px[kRopeHeadsInFlight];
+    float x0[kRopeHeadsInFlight], x1[kRopeHeadsInFlight];
+#pragma unroll
+    for (int u = 0; u < kRopeHeadsInFlight; ++u) {
+      const int h = h0 + u;
+      if (h < heads) {
+        const size_t row = heads_outer ? (((size_t)b * heads + h) * T + t) : ((size_t)tok * heads + h);
+        px[u] = x + row * d + rot_offset + 2 * pr;
+        x0[u] = Elem<ET>::to_f32(px[u][0]);
+        x1[u] = Elem<ET>::to_f32(px[u][1]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRopeHeadsInFlight; ++u) {
+      if (h0 + u < heads) {
+        px[u][0] = Elem<ET>::from_f32(fmaf(x0[u], c, -x1[u] * s));
+        px[u][1] = Elem<ET>::from_f32(fmaf(x0[u], s, x1[u] * c));
+      }
+    }
   }
 }
 

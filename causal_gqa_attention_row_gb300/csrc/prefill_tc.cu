@@ -34,10 +34,12 @@
 //
 // Softmax with lazy rescaling: p = 2^((s - m) * scale * log2 e) against a
 // reference max m that only moves when a score exceeds it by more than 2^8 in
-// p, which keeps every p <= 256 and leaves O / l unchanged. Keys past the row's
-// position (only in tiles that cross the diagonal) weigh exactly zero. In the
-// rare case the reference must move, O_w and L_w are rescaled in TMEM (after
-// every PV issued so far has completed). At the end warpgroup 0 merges the two
+// p, which keeps every p <= 256 and leaves O / l unchanged. A row's first tile
+// sets m to the tile's max; every later tile takes one pass that forms p and the
+// tile's max together, and only in the rare case the reference must move are O_w
+// and L_w rescaled in TMEM (after every PV issued so far has completed) and the
+// pass redone from the scores still in registers. Keys past the row's position
+// (only in tiles that cross the diagonal) weigh exactly zero. At the end warpgroup 0 merges the two
 // partial (m, l, O) rows and stores bf16.
 #include <cudaTypedefs.h>
 
@@ -353,26 +355,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (j0 + c * 32 + e > pos) sv[c][e] = __float_as_uint(-INFINITY);
       }
-      float mx8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // ---- rare: move the reference max and rescale O_w and L_w, once every PV
-      // issued so far (the last one, PV of tile k-1, read buffer (k-1) % 2) is done
-      const bool grow = mx > m_ref + th;
-      if (__any_sync(0xffffffffu, grow)) {
-        float f = 1.f;
-        if (grow) {
-          f = ex2f((m_ref - mx) * qs);  // 0 while m_ref = -inf
-          m_ref = mx;
+      // P buffer k % 2 is free once the PV of tile k-2 (which read it) is done
+      if (k >= kPBufs) {
+        if (!warp_wait_tc(&bars->o_done[wg][k % kPBufs], ((k - kPBufs) / kPBufs) & 1, bars, p.err)) {
+          alive = false;
+          break;
         }
-        if (k > 0) {
+      }
+      unsigned char* sP = sP0 + (k % kPBufs) * kPBytes;
+      // One pass over the row: p = 2^(s*qs - m*qs) as bf16 pairs into P (128-byte
+      // swizzle: 16-byte chunk index XOR row % 8, the K-major layout the PV MMA
+      // reads), tracking the row's max on the way when `track` is set.
+      auto exp_pass = [&](bool track) -> float {
+        const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
+        const float2 nmq2 = make_float2(-mq, -mq);
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int e = q8 * 8 + 2 * t;
+              const float s0 = __uint_as_float(sv[c][e]), s1 = __uint_as_float(sv[c][e + 1]);
+              if (track) mx8[(q8 * 4 + t) & 7] = fmax3(mx8[(q8 * 4 + t) & 7], s0, s1);
+              w4[t] = exp2_pair(s0, s1, qs2, nmq2);
+            }
+            const int cidx = c * 4 + q8;  // 16-byte chunk of the 256-byte P row
+            *reinterpret_cast<uint4*>(sP + (cidx / 8) * kTile + r * 128 + (((cidx % 8) ^ (r & 7)) * 16)) =
+                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      };
+      if (k == 0) {
+        // a row's first tile: the reference is the tile's max (nothing to rescale)
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+        m_ref = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                      fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        exp_pass(false);
+      } else {
+        // later tiles: one pass against the current reference; in the rare case a
+        // score exceeds it by more than 2^8 in p, move the reference, rescale O_w
+        // and L_w (once every PV issued so far is done) and redo the pass from the
+        // scores still in registers
+        const float mx = exp_pass(true);
+        const bool grow = mx > m_ref + th;
+        if (__any_sync(0xffffffffu, grow)) {
+          float f = 1.f;
+          if (grow) {
+            f = ex2f((m_ref - mx) * qs);  // 0 while m_ref = -inf
+            m_ref = mx;
+          }
           if (!warp_wait_tc(&bars->o_done[wg][(k - 1) % kPBufs], ((k - 1) / kPBufs) & 1, bars, p.err)) {
             alive = false;
             break;
@@ -391,34 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld_wait();
           tc::tmem_st_32x32b_x1(tL, __float_as_uint(__uint_as_float(l0) * f));
           tc::tmem_st_wait();
+          exp_pass(false);
         }
       }
-      // P buffer k % 2 is free once the PV of tile k-2 (which read it) is done
-      if (k >= kPBufs) {
-        if (!warp_wait_tc(&bars->o_done[wg][k % kPBufs], ((k - kPBufs) / kPBufs) & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
-      }
-      unsigned char* sP = sP0 + (k % kPBufs) * kPBytes;
-      // ---- p = 2^(s*qs - m*qs) as bf16 pairs into P_w (128-byte swizzle: 16-byte
-      // chunk index XOR row % 8, the K-major layout the PV MMA reads)
-      const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
-      const float2 nmq2 = make_float2(-mq, -mq);
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int e = q8 * 8 + 2 * t;
-            w4[t] = exp2_pair(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]), qs2, nmq2);
-          }
-          const int cidx = c * 4 + q8;  // 16-byte chunk of the 256-byte P row
-          *reinterpret_cast<uint4*>(sP + (cidx / 8) * kTile + r * 128 + (((cidx % 8) ^ (r & 7)) * 16)) =
-              make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
       tc::fence_before_sync();  // this thread's TMEM accesses are done
       tc::fence_async_smem();   // this thread's P_w writes visible to the tensor core
       __syncwarp();             // ... for every lane of the warp; one lane signals
