@@ -11,36 +11,38 @@
 // softmax warpgroups (setmaxnreg: 88 and 208 per thread from 168 at launch):
 //   warps 0-3   softmax warpgroup 0: key tiles 0, 2, 4, ...
 //   warps 4-7   softmax warpgroup 1: key tiles 1, 3, 5, ...
-//   warp 8      TMA producer of Q (once) and of the 128-key K tiles (two-stage
-//               ring; 128-byte swizzle, the layout the MMA reads)
+//   warp 8      initialises the barriers; TMA producer of Q (once) and of the
+//               128-key K tiles (four-stage ring; 128-byte swizzle, the layout
+//               the MMA reads)
 //   warps 9, 10 one thread each issues the tcgen05.mma of one softmax warpgroup
 //               (warp 9 also allocates and frees TMEM)
-//   warp 11     TMA producer of the V tiles (two-stage ring)
+//   warp 11     TMA producer of the V tiles (four-stage ring)
 // Warpgroup w owns, in tensor memory (TMEM), S_w = Q K^T (M=128, N=128, K=64;
-// columns 128w..) and [O_w | L_w] += P_w [V | 1] (M=128, N=64+16, K=128;
-// columns 256 + 80w..): the row sums L_w come out of the same MMAs as O_w, the
-// tensor core adding up the very bf16 p that multiply V. The ones are a
-// constant 16 KiB tile in shared memory that each stage's V descriptor reaches
-// as its second 64-column group (leading byte offset). P_w is written to shared
-// memory in the layout the PV MMA reads, in two buffers that alternate by tile.
-// Thread t of a warpgroup owns query row t (TMEM lane t).
+// columns 128w..), P_w (the bf16 probabilities, two per 32-bit column; columns
+// 384 + 64w..) and O_w += P_w V (M=128, N=64, K=128, A read from TMEM; columns
+// 256 + 64w..): the whole 512 columns. P never passes through shared memory,
+// whose bandwidth is left to the TMA tiles and the MMAs' reads of Q, K and V.
+// The softmax threads keep the row sum of exactly the bf16 p that multiply V,
+// in fp32. Thread t of a warpgroup owns query row t (TMEM lane t).
 //
 // Pipeline per warpgroup and key tile j: the softmax threads load their S_j row
 // into registers and release S_w at once, so the MMA thread issues S_{j+2}
-// while the exponentials of tile j are still being computed. P_j goes to the
-// buffer PV_{j-4} read, so the softmax never waits for the PV of the tile
-// before: PV runs behind it, off its critical path. K and V have rings of their
-// own: a K stage is free as soon as its S MMA is done, a V stage once its PV is.
+// while the exponentials of tile j are still being computed; P_j is built in
+// registers and stored into P_w once PV_{j-2} (issued a whole tile earlier) has
+// read the previous one. K and V have rings of their own: a K stage is free as
+// soon as its S MMA is done, a V stage once its PV is. K runs four tiles ahead,
+// so the load of K_{j+4} has a whole tile-period before S_{j+4} needs it.
 //
 // Softmax with lazy rescaling: p = 2^((s - m) * scale * log2 e) against a
 // reference max m that only moves when a score exceeds it by more than 2^8 in
-// p, which keeps every p <= 256 and leaves O / l unchanged. A row's first tile
-// sets m to the tile's max; every later tile takes one pass that forms p and the
-// tile's max together, and only in the rare case the reference must move are O_w
-// and L_w rescaled in TMEM (after every PV issued so far has completed) and the
-// pass redone from the scores still in registers. Keys past the row's position
-// (only in tiles that cross the diagonal) weigh exactly zero. At the end warpgroup 0 merges the two
-// partial (m, l, O) rows and stores bf16.
+// p, which keeps every p <= 256 and leaves O / l unchanged. Each tile's row max
+// is taken first; in the rare case it passes the reference by the threshold,
+// the reference moves and O_w (in TMEM, after every PV issued so far has
+// completed) and l are rescaled. Keys past the row's position (only in tiles
+// that cross the diagonal) weigh exactly zero. At the end the two warpgroups
+// exchange their (m, l), each merges half of the columns of the two partial O
+// rows into bf16 in shared memory (over the Q tile), and one TMA store writes
+// the output tile.
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
@@ -51,8 +53,8 @@ namespace {
 constexpr int kD = 64;     // head width (d_k = d_v)
 constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // keys per tile
-constexpr int kStagesKV = 2;  // per ring (K and V): stage s only ever holds key tiles of warpgroup s
-constexpr int kPBufs = 2;     // P buffers per warpgroup
+constexpr int kStagesK = 4;  // K ring: stage s only ever holds key tiles of warpgroup s % 2
+constexpr int kStagesV = 4;  // V ring: stage s only ever holds key tiles of warpgroup s % 2
 constexpr int kWG = 2;     // softmax warpgroups
 constexpr int kThreads = (kWG + 1) * 128;  // two softmax warpgroups + one control warpgroup
 constexpr int kProducerWarp = 8, kMmaWarp0 = 9, kProducerVWarp = 11;
@@ -61,24 +63,25 @@ constexpr int kProducerWarp = 8, kMmaWarp0 = 9, kProducerVWarp = 11;
 // 128 * 88 + 256 * 208 = 384 * 168.
 constexpr int kLaunchRegs = 168, kCtrlRegs = 88, kSoftmaxRegs = 208;
 static_assert(128 * kCtrlRegs + kWG * 128 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split over budget");
-static_assert(kStagesKV == kWG, "stage s must only ever hold warpgroup s's tiles");
+// A ring stage must only ever hold one warpgroup's tiles: each MMA thread then
+// waits on its stages' barriers in order and never two phases behind.
+static_assert(kStagesK % kWG == 0 && kStagesV % kWG == 0, "ring stages shared between warpgroups");
 constexpr int kTile = kBM * kD * 2;  // 16 KiB: one Q, K or V tile (128 rows x 128 bytes)
-constexpr int kSumN = 16;            // row-sum columns appended to O (the smallest N step)
-constexpr int kOW = kD + kSumN;      // 80: TMEM columns of [O_w | L_w]
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;  // S_w at 128w, [O_w | L_w] at 256 + 80w
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // S_w at 128w, O_w at 256 + 64w, P_w at 384 + 64w
+static_assert(kColP + kWG * (kBN / 2) == kTmemCols, "TMEM map");
 constexpr float kRescaleLog2 = 8.0f;
 
 // shared-memory map (from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTile;                               // K ring
-constexpr int kOffV = kOffK + kStagesKV * kTile;           // V ring
-constexpr int kOffOnes = kOffV + kStagesKV * kTile;        // columns 64..79 of every [V | 1]
-constexpr int kPBytes = 2 * kTile;                         // one P buffer: two 64-key halves
-constexpr int kOffP = kOffOnes + kTile;                    // P[w][buffer]
-constexpr int kOffML = kOffP + kWG * kPBufs * kPBytes;     // warpgroup 1's row max and sum
-constexpr int kOffBar = kOffML + 2 * kBM * 4;
+constexpr int kOffV = kOffK + kStagesK * kTile;            // V ring
+constexpr int kOffBar = kOffV + kStagesV * kTile;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;           // + alignment slack
+// At the end, once every MMA is done: the output tile over Q, and warpgroup w's
+// row max and sum over K stage w (which only ever held warpgroup w's tiles).
+constexpr int kOffOut = kOffQ;
+constexpr int kOffML = kOffK;
 static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
 
 struct TcParams {
@@ -90,12 +93,13 @@ struct TcParams {
 };
 
 struct Bars {
-  uint64_t q_full, k_full[kStagesKV], k_empty[kStagesKV], v_full[kStagesKV], v_empty[kStagesKV];
+  uint64_t q_full, k_full[kStagesK], k_empty[kStagesK], v_full[kStagesV], v_empty[kStagesV];
   uint64_t s_full[kWG], s_free[kWG], p_full[kWG], mma_final[kWG];
-  uint64_t o_done[kWG][kPBufs];  // the PV that read P buffer b of warpgroup w is done
+  uint64_t o_done[kWG];  // every PV of warpgroup w issued so far is done (a phase per PV)
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 __device__ __forceinline__ bool aborted(Bars* bars) { return *reinterpret_cast<volatile int*>(&bars->abort_flag); }
 
@@ -151,6 +155,14 @@ __device__ __forceinline__ uint32_t exp2_pair(float s0, float s1, float2 qs2, fl
   return ex2_bf16x2(pack_bf16(x.x, x.y));
 }
 
+// a += low bf16 of w, b += high bf16 of w, in fp32 (exact inputs, fp32 rounding).
+__device__ __forceinline__ void add_bf16x2(float& a, float& b, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "r"(w));
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -173,7 +185,8 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const TcParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
@@ -186,22 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = rem % p.H, b = rem / p.H;
   const int kvh = h / p.G;
   const int i0 = qt * kBM;
-  const int off = p.offsets ? p.offsets[b] : 0;
+  const int off = p.offsets ? p.offsets[b] : 0;  // in flight while the CTA sets up
   const int rows = min(kBM, p.S - i0);
 
-  if (off < 0 || (long long)off + p.S > p.S_kv) {  // the cache cannot hold these rows
-    if (threadIdx.x == 0 && qt == p.n_qtiles - 1 && h == 0) raise_error(p.err, kErrBounds);
-    for (int idx = threadIdx.x; idx < rows * kD; idx += blockDim.x)
-      p.out[(((size_t)b * p.S + i0 + idx / kD) * p.H + h) * kD + idx % kD] = __float2bfloat16_rn(0.f);
-    return;
-  }
-  const int n_kv = (off + i0 + rows - 1) / kBN + 1;  // key tiles up to the last row's position
-
-  if (threadIdx.x == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kStagesKV; ++s) {
+    for (int s = 0; s < kStagesK; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < kStagesV; ++s) {
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
@@ -210,15 +217,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_free[w], 4);  // one arrival per softmax warp
       mbar_init(&bars->p_full[w], 4);
       mbar_init(&bars->mma_final[w], 1);
-      for (int b2 = 0; b2 < kPBufs; ++b2) mbar_init(&bars->o_done[w][b2], 1);
+      mbar_init(&bars->o_done[w], 1);
     }
     bars->abort_flag = 0;
     fence_barrier_init();
+    // Q and the first K tile do not depend on the offset: they load while the
+    // rest of the CTA sets up
+    tc::prefetch_tmap(&tm_q);
+    tc::prefetch_tmap(&tm_k);
+    mbar_arrive_expect_tx(&bars->q_full, kTile);
+    tc::tma_load_4d(smem + kOffQ, &tm_q, 0, h, i0, b, &bars->q_full);
+    mbar_arrive_expect_tx(&bars->k_full[0], kTile);
+    tc::tma_load_4d(smem + kOffK, &tm_k, 0, 0, kvh, b, &bars->k_full[0]);
   }
-  // the constant all-ones tile (any swizzle of ones is ones)
-  for (int i = threadIdx.x; i < kTile / 16; i += blockDim.x)
-    *reinterpret_cast<uint4*>(smem + kOffOnes + i * 16) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-  tc::fence_async_smem();
   if (warp == kMmaWarp0) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
     tc::tmem_relinquish();
@@ -227,6 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
+
+  if (off < 0 || (long long)off + p.S > p.S_kv) {  // the cache cannot hold these rows
+    if (threadIdx.x == 0 && qt == p.n_qtiles - 1 && h == 0) raise_error(p.err, kErrBounds);
+    for (int idx = threadIdx.x; idx < rows * kD; idx += blockDim.x)
+      p.out[(((size_t)b * p.S + i0 + idx / kD) * p.H + h) * kD + idx % kD] = __float2bfloat16_rn(0.f);
+    // never exit with a load in flight
+    if (warp == kProducerWarp && lane == 0 && !(mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0)))
+      raise_error(p.err, kErrTimeout);
+    __syncthreads();
+    if (warp == kMmaWarp0) tc::tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+  const int n_kv = (off + i0 + rows - 1) / kBN + 1;  // key tiles up to the last row's position
 
   if (warp >= kProducerWarp) {
     regs_dec<kCtrlRegs>();  // the whole control warpgroup, right at the top of its branch
@@ -238,24 +262,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* full = is_k ? bars->k_full : bars->v_full;
       uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
       unsigned char* ring = smem + (is_k ? kOffK : kOffV);
-      tc::prefetch_tmap(tm);
-      if (is_k) {
-        tc::prefetch_tmap(&tm_q);
-        mbar_arrive_expect_tx(&bars->q_full, kTile);
-        tc::tma_load_4d(smem + kOffQ, &tm_q, 0, h, i0, b, &bars->q_full);
+      const int stages = is_k ? kStagesK : kStagesV;
+      if (!is_k) tc::prefetch_tmap(tm);
+      int issued_last[kStagesK];
+#pragma unroll
+      for (int st = 0; st < kStagesK; ++st) issued_last[st] = -1;
+      int j = 0;
+      if (is_k) {  // Q and K_0 went out before the setup barrier
+        issued_last[0] = 0;
+        j = 1;
       }
-      int issued_last[kStagesKV] = {-1, -1};
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % kStagesKV;
-        if (j >= kStagesKV && !wait_or_abort(&empty[st], ((j / kStagesKV) - 1) & 1, bars, p.err)) break;
+      for (; j < n_kv; ++j) {
+        const int st = j % stages;
+        if (j >= stages && !wait_or_abort(&empty[st], ((j / stages) - 1) & 1, bars, p.err)) break;
         mbar_arrive_expect_tx(&full[st], kTile);
         tc::tma_load_4d(ring + st * kTile, tm, 0, j * kBN, kvh, b, &full[st]);
         issued_last[st] = j;
       }
       // never exit with a load in flight
       if (is_k && !mbar_wait(&bars->q_full, 0)) raise_error(p.err, kErrTimeout);
-      for (int st = 0; st < kStagesKV; ++st)
-        if (issued_last[st] >= 0 && !mbar_wait(&full[st], (issued_last[st] / kStagesKV) & 1))
+      for (int st = 0; st < stages; ++st)
+        if (issued_last[st] >= 0 && !mbar_wait(&full[st], (issued_last[st] / stages) & 1))
           raise_error(p.err, kErrTimeout);
     }
   } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
@@ -264,24 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int n_mine = (n_kv - w + 1) / 2;
       const uint32_t idS = tc::idesc_bf16_f32(kBM, kBN, false);
-      const uint32_t idO = tc::idesc_bf16_f32(kBM, kOW, true);
+      const uint32_t idO = tc::idesc_bf16_f32(kBM, kD, true);
       // descriptors: constant high part + (shared address >> 4) in the low bits
       constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);
       const uint64_t dQ = kHi | (smem_u32(smem + kOffQ) >> 4);
       const uint64_t dK0 = kHi | (smem_u32(smem + kOffK) >> 4);
-      const uint64_t dP0 = kHi | (smem_u32(smem + kOffP + w * kPBufs * kPBytes) >> 4);
-      // [V | 1] of each stage: MN-major, 8-key groups 1024 bytes apart, the ones
-      // tile (columns 64..79) at the leading byte offset from the stage's V
-      uint64_t dV[kStagesKV];
-#pragma unroll
-      for (int st = 0; st < kStagesKV; ++st) {
-        const uint32_t v = smem_u32(smem + kOffV + st * kTile);
-        dV[st] = tc::desc_sw128_hi(smem_u32(smem + kOffOnes) - v, 1024) | (v >> 4);
-      }
-      const uint32_t dS = tmem + kColS + w * kBN, dO = tmem + kColO + w * kOW;
+      // V of each stage: MN-major (64 columns = one swizzle atom wide), 8-key groups 1024 bytes apart
+      const uint64_t dV0 = kHi | (smem_u32(smem + kOffV) >> 4);
+      const uint32_t dS = tmem + kColS + w * kBN, dO = tmem + kColO + w * kD, tP = tmem + kColP + w * (kBN / 2);
       auto issue_s = [&](int j) -> bool {  // S_w = Q K_j^T
-        const int st = j % kStagesKV;
-        if (!wait_or_abort(&bars->k_full[st], (j / kStagesKV) & 1, bars, p.err)) return false;
+        const int st = j % kStagesK;
+        if (!wait_or_abort(&bars->k_full[st], (j / kStagesK) & 1, bars, p.err)) return false;
         tc::fence_after_sync();
         const uint64_t dK = dK0 + (uint64_t)((st * kTile) >> 4);
 #pragma unroll
@@ -296,16 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_{j+2} as soon as the softmax threads have read S_j into registers
         if (k + 1 < n_mine) ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
         if (!ok || !wait_or_abort(&bars->p_full[w], k & 1, bars, p.err)) break;
-        const int st = j % kStagesKV;
-        if (!wait_or_abort(&bars->v_full[st], (j / kStagesKV) & 1, bars, p.err)) break;
+        const int st = j % kStagesV;
+        if (!wait_or_abort(&bars->v_full[st], (j / kStagesV) & 1, bars, p.err)) break;
         tc::fence_after_sync();
-        const uint64_t dP = dP0 + (uint64_t)(((k % kPBufs) * kPBytes) >> 4);
-        // [O_w | L_w] += P_j [V_j | 1]: 16 keys per instruction
+        // O_w += P_j V_j: 16 keys per instruction, P from TMEM (8 columns per 16 keys)
+        const uint64_t dV = dV0 + (uint64_t)((st * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_f16_ss(dO, dP + (((kk / 4) * kTile + (kk % 4) * 32) >> 4), dV[st] + kk * (2048 >> 4), idO,
-                         (k > 0 || kk > 0));
-        tc::mma_commit(&bars->o_done[w][k % kPBufs]);
+          tc::mma_f16_ts(dO, tP + kk * 8, dV + kk * (2048 >> 4), idO, (k > 0 || kk > 0));
+        tc::mma_commit(&bars->o_done[w]);
         tc::mma_commit(&bars->v_empty[st]);
       }
       // every MMA issued above has completed before TMEM is released
@@ -324,10 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float qs = p.qscale;
     const float th = kRescaleLog2 / qs;
     float m_ref = -INFINITY;
-    unsigned char* sP0 = smem + kOffP + wg * kPBufs * kPBytes;
+    float l_run = 0.f;  // the row sum of this warpgroup's p, against m_ref
     const uint32_t tS = tmem + lane_addr + kColS + wg * kBN;
-    const uint32_t tO = tmem + lane_addr + kColO + wg * kOW;
-    const uint32_t tL = tO + kD;  // L_w: the first of the 16 row-sum columns
+    const uint32_t tO = tmem + lane_addr + kColO + wg * kD;
+    const uint32_t tP = tmem + lane_addr + kColP + wg * (kBN / 2);
     const float2 qs2 = make_float2(qs, qs);
     const int n_mine = (n_kv - wg + 1) / 2;  // key tiles this warpgroup handles
     bool alive = true;
@@ -355,61 +374,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (j0 + c * 32 + e > pos) sv[c][e] = __float_as_uint(-INFINITY);
       }
-      // P buffer k % 2 is free once the PV of tile k-2 (which read it) is done
-      if (k >= kPBufs) {
-        if (!warp_wait_tc(&bars->o_done[wg][k % kPBufs], ((k - kPBufs) / kPBufs) & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
-      }
-      unsigned char* sP = sP0 + (k % kPBufs) * kPBytes;
-      // One pass over the row: p = 2^(s*qs - m*qs) as bf16 pairs into P (128-byte
-      // swizzle: 16-byte chunk index XOR row % 8, the K-major layout the PV MMA
-      // reads), tracking the row's max on the way when `track` is set.
-      auto exp_pass = [&](bool track) -> float {
-        const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
-        const float2 nmq2 = make_float2(-mq, -mq);
-        float mx8[8];
+      // ---- the tile's row max; the reference moves only past the threshold
+      float mx8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int e = q8 * 8 + 2 * t;
-              const float s0 = __uint_as_float(sv[c][e]), s1 = __uint_as_float(sv[c][e + 1]);
-              if (track) mx8[(q8 * 4 + t) & 7] = fmax3(mx8[(q8 * 4 + t) & 7], s0, s1);
-              w4[t] = exp2_pair(s0, s1, qs2, nmq2);
-            }
-            const int cidx = c * 4 + q8;  // 16-byte chunk of the 256-byte P row
-            *reinterpret_cast<uint4*>(sP + (cidx / 8) * kTile + r * 128 + (((cidx % 8) ^ (r & 7)) * 16)) =
-                make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
-        return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      };
+        for (int e = 0; e < 32; e += 2)
+          mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       if (k == 0) {
-        // a row's first tile: the reference is the tile's max (nothing to rescale)
-        float mx8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
-        m_ref = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                      fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        exp_pass(false);
+        m_ref = mx;  // a row's first tile: nothing to rescale
       } else {
-        // later tiles: one pass against the current reference; in the rare case a
-        // score exceeds it by more than 2^8 in p, move the reference, rescale O_w
-        // and L_w (once every PV issued so far is done) and redo the pass from the
-        // scores still in registers
-        const float mx = exp_pass(true);
         const bool grow = mx > m_ref + th;
         if (__any_sync(0xffffffffu, grow)) {
           float f = 1.f;
@@ -417,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             f = ex2f((m_ref - mx) * qs);  // 0 while m_ref = -inf
             m_ref = mx;
           }
-          if (!warp_wait_tc(&bars->o_done[wg][(k - 1) % kPBufs], ((k - 1) / kPBufs) & 1, bars, p.err)) {
+          // O_w holds every PV issued so far (PV_{k-1} the last): rescale it once done
+          if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
             alive = false;
             break;
           }
@@ -431,72 +410,98 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
             tc::tmem_st_32x32b_x32(tO + c * 32, o);
           }
-          const uint32_t l0 = tc::tmem_ld_32x32b_x1(tL);
-          tc::tmem_ld_wait();
-          tc::tmem_st_32x32b_x1(tL, __float_as_uint(__uint_as_float(l0) * f));
           tc::tmem_st_wait();
-          exp_pass(false);
+          l_run *= f;
         }
       }
+      // ---- p = 2^(s*qs - m*qs) as bf16 pairs, and the fp32 sum of exactly these p
+      const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
+      const float2 nmq2 = make_float2(-mq, -mq);
+      uint32_t pv[4][16];
+      float ls[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          pv[c][t] = exp2_pair(__uint_as_float(sv[c][2 * t]), __uint_as_float(sv[c][2 * t + 1]), qs2, nmq2);
+          add_bf16x2(ls[(t & 3) * 2], ls[(t & 3) * 2 + 1], pv[c][t]);
+        }
+      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      // ---- P_w is free once PV_{k-1} has read it. Every phase of o_done[w] is
+      // waited for in order, before the next PV can be issued, so the barrier is
+      // never two phases ahead of this wait (nor of the rescale's or the final one).
+      if (k >= 1) {
+        if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
+        tc::fence_after_sync();
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_st_32x32b_x16(tP + c * 16, pv[c]);
+      tc::tmem_st_wait();
       tc::fence_before_sync();  // this thread's TMEM accesses are done
-      tc::fence_async_smem();   // this thread's P_w writes visible to the tensor core
       __syncwarp();             // ... for every lane of the warp; one lane signals
       if (lane == 0) mbar_arrive(&bars->p_full[wg]);
     }
-    // ---- this warpgroup's last PV, then warpgroup 1 hands (m, l) to warpgroup 0
+    // ---- each warpgroup's last PV; the two exchange (m, l), each merges half of
+    // the columns of O_0 and O_1 into the output tile, and one TMA store writes it
     bool have_o = alive && n_mine > 0;
-    float l_sum = 0.f;
-    if (have_o) {  // the last PV (in-order completion: every earlier one too)
-      have_o = warp_wait_tc(&bars->o_done[wg][(n_mine - 1) % kPBufs], ((n_mine - 1) / kPBufs) & 1, bars, p.err);
+    if (have_o) {  // the last PV's commit covers every MMA this warpgroup's thread issued
+      have_o = warp_wait_tc(&bars->o_done[wg], (n_mine - 1) & 1, bars, p.err);
       tc::fence_after_sync();
     }
-    if (have_o) {
-      l_sum = __uint_as_float(tc::tmem_ld_32x32b_x1(tL));
-      tc::tmem_ld_wait();
-    }
-    float* sm = reinterpret_cast<float*>(smem + kOffML);
-    if (wg == 1) {
-      sm[r] = have_o ? m_ref : -INFINITY;
-      sm[kBM + r] = have_o ? l_sum : 0.f;
-    }
-    tc::fence_before_sync();  // order warpgroup 1's view of its finished O_1 before the hand-off
+    const float l_sum = l_run;
+    float* ml = reinterpret_cast<float*>(smem + kOffML + wg * kTile);  // K stage wg: consumed by now
+    ml[r] = have_o ? m_ref : -INFINITY;
+    ml[kBM + r] = have_o ? l_sum : 0.f;  // l = 0: no visible key, or no tile at all
+    tc::fence_before_sync();
     named_bar_sync(1, kWG * 128);
     tc::fence_after_sync();
-    if (wg == 0 && have_o) {
-      const float m1 = sm[r], l1 = sm[kBM + r];
-      const bool use1 = n_kv > 1 && l1 > 0.f;  // warpgroup 1 wrote O_1 and saw a visible key
-      const float M = use1 ? fmaxf(m_ref, m1) : m_ref;
-      const float a0 = (m_ref == -INFINITY) ? 0.f : ex2f((m_ref - M) * qs);
-      const float a1 = use1 ? ex2f((m1 - M) * qs) : 0.f;
-      const float l = a0 * l_sum + a1 * l1;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float c0 = a0 * inv, c1 = a1 * inv;
-      __nv_bfloat16* orow = p.out + (((size_t)b * p.S + i0 + r) * p.H + h) * kD;
+    const float* ml0 = reinterpret_cast<const float*>(smem + kOffML);
+    const float* ml1 = reinterpret_cast<const float*>(smem + kOffML + kTile);
+    const float m0 = ml0[r], l0 = ml0[kBM + r], m1 = ml1[r], l1 = ml1[kBM + r];
+    const bool use0 = l0 > 0.f, use1 = l1 > 0.f;
+    const float M = fmaxf(use0 ? m0 : -INFINITY, use1 ? m1 : -INFINITY);
+    const float a0 = use0 ? ex2f((m0 - M) * qs) : 0.f;
+    const float a1 = use1 ? ex2f((m1 - M) * qs) : 0.f;
+    const float l = a0 * l0 + a1 * l1;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float c0 = a0 * inv, c1 = a1 * inv;
+    // this warpgroup's 32 of the 64 columns; O_1 exists once warpgroup 1 had a tile
+    const int col0 = wg * (kD / 2);
+    uint32_t o0[32], o1[32];
+    tc::tmem_ld_32x32b_x32(tmem + lane_addr + kColO + col0, o0);
+    if (n_kv > 1) tc::tmem_ld_32x32b_x32(tmem + lane_addr + kColO + kD + col0, o1);
+    tc::tmem_ld_wait();
+    // the output tile over Q (every S MMA, the readers of Q, is done), in the
+    // 128-byte swizzle of the output's tensor map
+    unsigned char* so = smem + kOffOut;
 #pragma unroll
-      for (int c = 0; c < kD / 16; ++c) {
-        uint32_t o0[16], o1[16];
-        tc::tmem_ld_32x32b_x16(tmem + lane_addr + kColO + c * 16, o0);
-        if (n_kv > 1) tc::tmem_ld_32x32b_x16(tmem + lane_addr + kColO + kOW + c * 16, o1);
-        tc::tmem_ld_wait();
-        if (r < rows) {
+    for (int t = 0; t < 4; ++t) {
+      uint32_t w4[4];
 #pragma unroll
-          for (int e = 0; e < 16; e += 8) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              float x0 = __uint_as_float(o0[e + 2 * t]) * c0, x1 = __uint_as_float(o0[e + 2 * t + 1]) * c0;
-              if (use1) {
-                x0 = fmaf(__uint_as_float(o1[e + 2 * t]), c1, x0);
-                x1 = fmaf(__uint_as_float(o1[e + 2 * t + 1]), c1, x1);
-              }
-              w4[t] = pack_bf16(x0, x1);
-            }
-            *reinterpret_cast<uint4*>(orow + c * 16 + e) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
+      for (int u = 0; u < 4; ++u) {
+        const int e = t * 8 + 2 * u;
+        float x0 = __uint_as_float(o0[e]) * c0, x1 = __uint_as_float(o0[e + 1]) * c0;
+        if (use1) {
+          x0 = fmaf(__uint_as_float(o1[e]), c1, x0);
+          x1 = fmaf(__uint_as_float(o1[e + 1]), c1, x1);
         }
+        w4[u] = pack_bf16(x0, x1);
       }
-    } else if (wg == 0 && lane == 0 && !have_o) {
-      raise_error(p.err, kErrTimeout);
+      const int chunk = wg * 4 + t;  // 16-byte chunk of the 128-byte output row
+      *reinterpret_cast<uint4*>(so + r * 128 + ((chunk ^ (r & 7)) * 16)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    tc::fence_async_smem();  // the tile visible to the TMA engine
+    named_bar_sync(2, kWG * 128);
+    if (threadIdx.x == 0) {
+      // rows past the end of the sequence fall outside the tensor and are not written
+      tc::tma_store_4d(&tm_o, so, 0, h, i0, b);
+      tc::bulk_commit_group();
+      tc::bulk_wait_group_read0();  // shared memory stays valid until the store has read it
     }
   }
 
@@ -541,12 +546,14 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
                               int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv, float qscale,
                               unsigned* err, cudaStream_t st) {
   if (dk != kD || dv != kD || !(qscale > 0.f)) return cudaErrorNotSupported;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   // q [B, S, H, 64]: dims (64, H, S, B), box (64, 1, 128, 1)
   if (!make_map(&tq, q, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
   // k, v [B, Hkv, S_kv, 64]: dims (64, S_kv, Hkv, B), box (64, 128, 1, 1)
   if (!make_map(&tk, k, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
   if (!make_map(&tv, v, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
+  // out [B, S, H, 64]: as q
+  if (!make_map(&to, out, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
   TcParams p;
   p.B = B;
   p.S = seq_q;
@@ -576,7 +583,7 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
   }
   const long long ctas = (long long)B * H * p.n_qtiles;
   if (ctas <= 0) return cudaSuccess;
-  prefill_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  prefill_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
