@@ -109,10 +109,16 @@ __device__ __forceinline__ bool aborted(Bars* bars) { return *reinterpret_cast<v
 constexpr uint32_t kWaitHintNs = 20;
 
 
+// A phase that has already completed is seen by the non-blocking probe at once;
+// only a wait that has to wait goes on to the suspending probe.
+__device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity) {
+  return mbar_test_parity_nb(bar, parity) || mbar_wait_hint(bar, parity, kWaitHintNs);
+}
+
 // Single-thread wait of the producer and MMA issuers (bounded).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
   if (aborted(bars)) return false;
-  if (mbar_wait_hint(bar, parity, kWaitHintNs)) return true;
+  if (wait_fast(bar, parity)) return true;
   *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
   raise_error(err, kErrTimeout);
   return false;
@@ -120,7 +126,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 
 // Whole-warp version: every lane agrees on the outcome.
 __device__ __forceinline__ bool warp_wait_tc(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
-  bool ok = !aborted(bars) && mbar_wait_hint(bar, parity, kWaitHintNs);
+  bool ok = !aborted(bars) && wait_fast(bar, parity);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && (threadIdx.x & 31) == 0) {
     *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
