@@ -23,7 +23,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE_BOUNDS
 EXPORTS = ("attn_prefill_causal", "attn_decode_contig", "attn_decode_paged", "kv_append_paged",
            "attn_rope_interleaved", "attn_decode_workspace_bytes", "attn_get_device_error",
            "gqa_status_string", "gqa_debug_withhold_first_tile", "attn_decode_paged_static_workspace",
-           "attn_prefill_causal_ex", "attn_decode_contig_ex", "attn_decode_paged_ex")
+           "attn_prefill_causal_ex", "attn_decode_contig_ex", "attn_decode_paged_ex", "attn_prefill_paged",
+           "attn_prefill_paged_ex")
 
 
 class GqaArms(ctypes.Structure):
@@ -63,6 +64,8 @@ def load(path: str = None):
         "attn_prefill_causal_ex": [P, P, P, P, I, I, I, P, I, I, I, I, F, I, P, P],
         "attn_decode_contig_ex": [P, P, P, P, I, P, P, I, I, I, I, I, I, F, I, P, S, P, P],
         "attn_decode_paged_ex": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, S, P, P],
+        "attn_prefill_paged": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P],
+        "attn_prefill_paged_ex": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, P],
         "gqa_debug_withhold_first_tile": [I],
     }
     for name, args in sig.items():
@@ -136,6 +139,23 @@ def attn_prefill_causal(q, k, v, out, attention_scale, position_offset=None, str
         _check(load().attn_prefill_causal(*args, _stream(stream)), "attn_prefill_causal")
     else:
         _check(load().attn_prefill_causal_ex(*args, arms, _stream(stream)), "attn_prefill_causal_ex")
+    return out
+
+
+def attn_prefill_paged(q, k_pool, v_pool, block_tables, out, attention_scale, position_offset=None, stream=None,
+                       window=0, softcap=0.0, sinks=None, alibi_slopes=None):
+    """Chunked prefill against the paged pool: q [B, S, H, dk]; pools [num_blocks, Hkv, bs, d];
+    block_tables int32 [B, mbps]; position_offset int32 [B] or None; out [B, S, H, dv].
+    window / softcap / sinks / alibi_slopes: the arms (`gqa_arms`)."""
+    B, S, H, dk = q.shape
+    nb, Hkv, bs, dv = v_pool.shape
+    arms = _arms(window, softcap, sinks, alibi_slopes)
+    args = (_p(q), _p(k_pool), _p(v_pool), _i32(block_tables), _i32(position_offset), _p(out), B, S,
+            block_tables.shape[1], nb, bs, H, Hkv, dk, dv, float(attention_scale), _dtype(q, k_pool, v_pool, out))
+    if arms is None:
+        _check(load().attn_prefill_paged(*args, _stream(stream)), "attn_prefill_paged")
+    else:
+        _check(load().attn_prefill_paged_ex(*args, arms, _stream(stream)), "attn_prefill_paged_ex")
     return out
 
 

@@ -190,6 +190,32 @@ gqa_status attn_decode_paged_ex(const void* q, const void* k_pool, const void* v
   return decode_common(p, bf16, d_k, d_v, 0, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+// Prefill, contiguous or paged (p holds the pointers, shapes and arms): the
+// tcgen05 kernel for the shapes it takes, else the SIMT kernel with one split
+// per work item (every item covers its whole key range; no workspace).
+static gqa_status prefill_common(gqa::RowsParams& p, int bf16, int d_k, int d_v, float attention_scale, bool arms_on,
+                                 cudaStream_t st) {
+  p.err = error_word();
+  if (!p.err) return GQA_ERR_CUDA;
+  const float qscale = attention_scale * 1.4426950408889634f;
+  if (!arms_on && gqa::prefill_tc_supported(bf16, d_k, d_v, p.paged ? p.bs : 0) && attention_scale > 0.f)
+    return from_cuda(gqa::launch_prefill_tc(p.q, p.k, p.v, p.out, p.B, p.seq_q, p.capacity, p.offsets, p.H, p.Hkv,
+                                            d_k, d_v, qscale, p.err, st, p.paged ? p.tables : nullptr, p.mbps, p.bs,
+                                            p.num_blocks));
+  const int nvmax = gqa::rows_max_nv(bf16, d_k, d_v, 0);
+  if (nvmax == 0) return GQA_ERR_UNSUPPORTED;
+  p.G = p.H / p.Hkv;
+  p.GH = pow2_divisor(p.G, nvmax);
+  p.QR = 1;
+  while (p.GH * p.QR * 2 <= nvmax && p.QR < p.seq_q) p.QR *= 2;
+  p.n_hchunks = p.G / p.GH;
+  p.n_rblocks = ceil_div(p.seq_q, p.QR);
+  p.split_rows = p.capacity;
+  p.max_splits = 1;
+  p.qscale = qscale;
+  return launch_rows(p, bf16, d_k, d_v, 0, p.GH * p.QR, st);
+}
+
 gqa_status attn_prefill_causal_ex(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
                                   int seq_kv_max, const int32_t* position_offset, int H, int Hkv, int d_k, int d_v,
                                   float attention_scale, gqa_dtype dt, const gqa_arms* arms, void* stream) {
@@ -200,19 +226,10 @@ gqa_status attn_prefill_causal_ex(const void* q, const void* k, const void* v, v
   if (B == 0 || seq_q == 0) return GQA_OK;
   if (!q || !k || !v || !out) return GQA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GQA_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  unsigned* err = error_word();
-  if (!err) return GQA_ERR_CUDA;
-  const float qscale = attention_scale * 1.4426950408889634f;
   gqa::RowsParams p{};
   bool arms_on;
   const gqa_status sa = apply_arms(p, arms, &arms_on);
   if (sa != GQA_OK) return sa;
-  if (!arms_on && gqa::prefill_tc_supported(bf16, d_k, d_v) && attention_scale > 0.f)
-    return from_cuda(gqa::launch_prefill_tc(q, k, v, out, B, seq_q, seq_kv_max, position_offset, H, Hkv, d_k, d_v,
-                                            qscale, err, st));
-  const int nvmax = gqa::rows_max_nv(bf16, d_k, d_v, 0);
-  if (nvmax == 0) return GQA_ERR_UNSUPPORTED;
   p.q = q;
   p.k = k;
   p.v = v;
@@ -223,19 +240,45 @@ gqa_status attn_prefill_causal_ex(const void* q, const void* k, const void* v, v
   p.seq_q = seq_q;
   p.H = H;
   p.Hkv = Hkv;
-  p.G = H / Hkv;
-  p.GH = pow2_divisor(p.G, nvmax);
-  p.QR = 1;
-  while (p.GH * p.QR * 2 <= nvmax && p.QR < seq_q) p.QR *= 2;
-  p.n_hchunks = p.G / p.GH;
-  p.n_rblocks = ceil_div(seq_q, p.QR);
   p.max_len = seq_kv_max;
   p.capacity = seq_kv_max;
-  p.split_rows = seq_kv_max;  // one split: every item covers its whole key range
-  p.max_splits = 1;
-  p.qscale = qscale;
-  p.err = err;
-  return launch_rows(p, bf16, d_k, d_v, 0, p.GH * p.QR, st);
+  return prefill_common(p, bf16, d_k, d_v, attention_scale, arms_on, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status attn_prefill_paged_ex(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                                 const int32_t* position_offset, void* out, int B, int seq_q, int max_blocks_per_seq,
+                                 int num_blocks, int block_size, int H, int Hkv, int d_k, int d_v,
+                                 float attention_scale, gqa_dtype dt, const gqa_arms* arms, void* stream) {
+  const int bf16 = dtype_flag(dt);
+  if (bf16 < 0 || B < 0 || seq_q < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0 ||
+      !heads_ok(H, Hkv) || !width_ok(d_k) || !width_ok(d_v))
+    return GQA_ERR_INVALID_ARG;
+  if ((long long)max_blocks_per_seq * block_size > INT_MAX / 2) return GQA_ERR_INVALID_ARG;
+  if (seq_q > max_blocks_per_seq * block_size) return GQA_ERR_INVALID_ARG;
+  if (B == 0 || seq_q == 0) return GQA_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !out) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return GQA_ERR_INVALID_ARG;
+  gqa::RowsParams p{};
+  bool arms_on;
+  const gqa_status sa = apply_arms(p, arms, &arms_on);
+  if (sa != GQA_OK) return sa;
+  p.q = q;
+  p.k = k_pool;
+  p.v = v_pool;
+  p.out = out;
+  p.offsets = position_offset;
+  p.tables = block_tables;
+  p.paged = 1;
+  p.B = B;
+  p.seq_q = seq_q;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.max_len = 0;
+  p.capacity = max_blocks_per_seq * block_size;
+  p.mbps = max_blocks_per_seq;
+  p.bs = block_size;
+  p.num_blocks = num_blocks;
+  return prefill_common(p, bf16, d_k, d_v, attention_scale, arms_on, static_cast<cudaStream_t>(stream));
 }
 
 // The plain calls: the _ex calls with no arms.
@@ -261,6 +304,14 @@ gqa_status attn_prefill_causal(const void* q, const void* k, const void* v, void
                                float attention_scale, gqa_dtype dt, void* stream) {
   return attn_prefill_causal_ex(q, k, v, out, B, seq_q, seq_kv_max, position_offset, H, Hkv, d_k, d_v,
                                 attention_scale, dt, nullptr, stream);
+}
+
+gqa_status attn_prefill_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                              const int32_t* position_offset, void* out, int B, int seq_q, int max_blocks_per_seq,
+                              int num_blocks, int block_size, int H, int Hkv, int d_k, int d_v, float attention_scale,
+                              gqa_dtype dt, void* stream) {
+  return attn_prefill_paged_ex(q, k_pool, v_pool, block_tables, position_offset, out, B, seq_q, max_blocks_per_seq,
+                               num_blocks, block_size, H, Hkv, d_k, d_v, attention_scale, dt, nullptr, stream);
 }
 
 gqa_status kv_append_paged(void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,

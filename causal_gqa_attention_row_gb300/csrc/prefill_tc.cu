@@ -85,8 +85,12 @@ constexpr int kOffML = kOffK;
 static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
 
 struct TcParams {
-  int B, S, H, Hkv, G, S_kv, n_qtiles;
+  int B, S, H, Hkv, G, S_kv, n_qtiles;  // S_kv: keys a sequence can hold (the pool's capacity when paged)
   const int32_t* offsets;
+  // paged K/V (tables != NULL): [num_blocks, Hkv, bs, 64] pools, row j of
+  // sequence b in block tables[b * mbps + j / bs], slot j % bs; bs divides 128
+  const int32_t* tables;
+  int mbps, bs, num_blocks;
   __nv_bfloat16* out;
   float qscale;
   unsigned* err;
@@ -189,6 +193,35 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Issue the TMA loads of key tile j (128 rows of 64) of KV head kvh, sequence
+// b, into `dst`, completing 16 KiB on `bar`. Contiguous: one box. Paged: one
+// box per pool block of the tile, addressed through the block table (the
+// 128-byte swizzle is a function of the shared address, so the blocks land
+// exactly where one box would put them). A block that holds no key below
+// kv_hi, or whose table entry is out of range (flagged), loads from past the
+// end of the pool: the TMA engine fills it with zeros.
+__device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, unsigned char* dst, uint64_t* bar, int j, int kvh,
+                                             int b, const TcParams& p, int kv_hi) {
+  mbar_arrive_expect_tx(bar, kTile);
+  if (!p.tables) {
+    tc::tma_load_4d(dst, tm, 0, j * kBN, kvh, b, bar);
+    return;
+  }
+  const int per = kBN / p.bs;
+  for (int i = 0; i < per; ++i) {
+    const int t = j * per + i;  // block of the sequence
+    int blk = p.num_blocks;
+    if (t < p.mbps && t * p.bs < kv_hi) {
+      const int e = __ldg(p.tables + (size_t)b * p.mbps + t);
+      if (e >= 0 && e < p.num_blocks)
+        blk = e;
+      else
+        raise_error(p.err, kErrBounds);
+    }
+    tc::tma_load_4d(dst + i * p.bs * 128, tm, 0, 0, kvh, blk, bar);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -233,8 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::prefetch_tmap(&tm_k);
     mbar_arrive_expect_tx(&bars->q_full, kTile);
     tc::tma_load_4d(smem + kOffQ, &tm_q, 0, h, i0, b, &bars->q_full);
-    mbar_arrive_expect_tx(&bars->k_full[0], kTile);
-    tc::tma_load_4d(smem + kOffK, &tm_k, 0, 0, kvh, b, &bars->k_full[0]);
+    if (p.tables)  // the table entries of the tile wait for the offset, which bounds them
+      load_kv_tile(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, off + i0 + rows);
+    else
+      load_kv_tile(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, 0);
   }
   if (warp == kMmaWarp0) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -281,8 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; j < n_kv; ++j) {
         const int st = j % stages;
         if (j >= stages && !wait_or_abort(&empty[st], ((j / stages) - 1) & 1, bars, p.err)) break;
-        mbar_arrive_expect_tx(&full[st], kTile);
-        tc::tma_load_4d(ring + st * kTile, tm, 0, j * kBN, kvh, b, &full[st]);
+        load_kv_tile(tm, ring + st * kTile, &full[st], j, kvh, b, p, off + i0 + rows);
         issued_last[st] = j;
       }
       // never exit with a load in flight
@@ -546,18 +580,29 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64
 
 }  // namespace
 
-bool prefill_tc_supported(int bf16, int dk, int dv) { return bf16 == 1 && dk == kD && dv == kD; }
+bool prefill_tc_supported(int bf16, int dk, int dv, int bs) {
+  // paged: a pool block is a whole number of 8-row swizzle atoms and divides a 128-key tile
+  return bf16 == 1 && dk == kD && dv == kD && (bs == 0 || (bs % 8 == 0 && kBN % bs == 0));
+}
 
 cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
                               int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv, float qscale,
-                              unsigned* err, cudaStream_t st) {
+                              unsigned* err, cudaStream_t st, const int32_t* tables, int mbps, int bs,
+                              int num_blocks) {
   if (dk != kD || dv != kD || !(qscale > 0.f)) return cudaErrorNotSupported;
+  if (tables && !prefill_tc_supported(1, dk, dv, bs)) return cudaErrorNotSupported;
   CUtensorMap tq, tk, tv, to;
   // q [B, S, H, 64]: dims (64, H, S, B), box (64, 1, 128, 1)
   if (!make_map(&tq, q, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
-  // k, v [B, Hkv, S_kv, 64]: dims (64, S_kv, Hkv, B), box (64, 128, 1, 1)
-  if (!make_map(&tk, k, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
-  if (!make_map(&tv, v, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
+  if (tables) {
+    // pools [num_blocks, Hkv, bs, 64]: dims (64, bs, Hkv, num_blocks), box (64, bs, 1, 1)
+    if (!make_map(&tk, k, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
+    if (!make_map(&tv, v, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
+  } else {
+    // k, v [B, Hkv, S_kv, 64]: dims (64, S_kv, Hkv, B), box (64, 128, 1, 1)
+    if (!make_map(&tk, k, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
+    if (!make_map(&tv, v, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
+  }
   // out [B, S, H, 64]: as q
   if (!make_map(&to, out, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
   TcParams p;
@@ -569,6 +614,10 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
   p.S_kv = seq_kv_max;
   p.n_qtiles = (seq_q + kBM - 1) / kBM;
   p.offsets = offsets;
+  p.tables = tables;
+  p.mbps = mbps;
+  p.bs = bs;
+  p.num_blocks = num_blocks;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.qscale = qscale;
   p.err = err;

@@ -165,6 +165,40 @@ gqa_status attn_prefill_causal_ex(const void* q, const void* k, const void* v, v
                                   int seq_kv_max, const int32_t* position_offset, int H, int Hkv, int d_k, int d_v,
                                   float attention_scale, gqa_dtype dt, const gqa_arms* arms, void* stream);
 
+/*
+ * Chunked prefill against the paged pool: seq_q new rows of each sequence,
+ * already appended to the pool, attend to everything the sequence holds up to
+ * their own positions -- the causal rule of attn_prefill_causal (kopitiam-runtime
+ * src/attention.rs, `attention_forward`, `causal_mask`: row i at position
+ * position_offset + i sees keys 0 ..= position_offset + i) with the paged
+ * addressing of attn_decode_paged (frink-models src/decoder/attn_block.rs,
+ * `push_and_attend_row`, paged arm: paging changes where rows live and nothing
+ * else, so the result is bit-identical to attn_prefill_causal on the same
+ * history). A decode step is the case seq_q = 1.
+ *
+ *   q             [B, seq_q, H, d_k]; out [B, seq_q, H, d_v]
+ *   k_pool        [num_blocks, Hkv, block_size, d_k]
+ *   v_pool        [num_blocks, Hkv, block_size, d_v]
+ *   block_tables  int32 [B, max_blocks_per_seq], as for attn_decode_paged;
+ *                 entries of blocks that hold no key the rows see are never read
+ *   position_offset  int32 [B] on the device, or NULL for all zeros; requires
+ *                 position_offset[b] + seq_q <= max_blocks_per_seq * block_size
+ *                 (checked on the device)
+ * bf16 with d_k == d_v == 64, block_size a multiple of 8 dividing 128 and no
+ * arm runs on the tcgen05 tensor-core kernel (each 128-key tile gathered block
+ * by block with TMA); every other case on the SIMT kernel. No workspace.
+ * GQA_ERR_INVALID_ARG also for seq_q > max_blocks_per_seq * block_size.
+ */
+gqa_status attn_prefill_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                              const int32_t* position_offset, void* out, int B, int seq_q, int max_blocks_per_seq,
+                              int num_blocks, int block_size, int H, int Hkv, int d_k, int d_v, float attention_scale,
+                              gqa_dtype dt, void* stream);
+/* attn_prefill_paged with the arms (`gqa_arms`); an arm on runs on the SIMT kernel. */
+gqa_status attn_prefill_paged_ex(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                                 const int32_t* position_offset, void* out, int B, int seq_q, int max_blocks_per_seq,
+                                 int num_blocks, int block_size, int H, int Hkv, int d_k, int d_v,
+                                 float attention_scale, gqa_dtype dt, const gqa_arms* arms, void* stream);
+
 /* Size of the fixed device scratch behind attn_decode_paged_static_workspace. */
 #define GQA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
 
