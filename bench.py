@@ -377,6 +377,33 @@ def run_prefill(args, peaks, peak_kind):
                          "kernel": "prefill_tc_kernel", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
 
 
+def run_prefill_paged(args, peaks, peak_kind):
+    """Chunked prefill against the paged pool on the tcgen05 kernel (each key
+    tile gathered from the pool block by block)."""
+    import causal_gqa_attention_row_gb300 as g
+    g.load()
+    dev = torch.device("cuda")
+    offs, S, H, d = (0, 2048, 4096, 6144), 2048, 14, 64
+    q, kp, vp, tables, off, scale = W.make_prefill_paged(offsets=offs, S=S, H=H, d=d, device=dev)
+    out = torch.empty_like(q)
+    # unmasked (query, key) pairs: row i of sequence b sees off_b + i + 1 keys
+    flops = sum(2.0 * H * (d + d) * (S * o + S * (S + 1) / 2) for o in offs)
+    st = torch.cuda.current_stream()
+    call = lambda k: g.attn_prefill_paged(q, kp, vp, tables, out, scale, position_offset=off)
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    n = 4 * max(args.steps, 20)
+    queue_ahead(n, us_per_group=60.0)
+    ms = timed(call, n, st, sync_first=False)
+    assert g.attn_get_device_error() == g.OK
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"workload": W.WORKLOADS["prefill_paged"], "tflops": tflops, "kernel_ms": ms, "flops": flops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "kernel": "prefill_tc_kernel (paged)", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
+
+
 def run_contig(args, peaks, peak_kind):
     import causal_gqa_attention_row_gb300 as g
     dev = torch.device("cuda")
@@ -491,7 +518,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true", help="skip prefill, contig and mla")
-    ap.add_argument("--only", choices=["paged", "prefill", "contig", "mla"], default=None)
+    ap.add_argument("--only", choices=["paged", "prefill", "prefill_paged", "contig", "mla"], default=None)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world = dist_setup()
@@ -499,16 +526,18 @@ def main():
         reference_arm(args, rank, world)
         return
     peaks, peak_kind = measured_peaks()
-    if args.only in ("prefill", "contig", "mla"):
-        r = {"prefill": run_prefill, "contig": run_contig, "mla": run_mla}[args.only](args, peaks, peak_kind)
+    if args.only in ("prefill", "prefill_paged", "contig", "mla"):
+        r = {"prefill": run_prefill, "prefill_paged": run_prefill_paged, "contig": run_contig,
+             "mla": run_mla}[args.only](args, peaks, peak_kind)
         if rank == 0:
             print(json.dumps(r), flush=True)
         return
     res = run_paged(args, rank, world)
     secondary = {}
     if not args.no_secondary and args.only is None:
-        secondary = {"prefill": run_prefill(args, peaks, peak_kind), "contig": run_contig(args, peaks, peak_kind),
-                     "mla": run_mla(args, peaks, peak_kind)}
+        secondary = {"prefill": run_prefill(args, peaks, peak_kind),
+                     "prefill_paged": run_prefill_paged(args, peaks, peak_kind),
+                     "contig": run_contig(args, peaks, peak_kind), "mla": run_mla(args, peaks, peak_kind)}
     if res.get("arms"):
         arms = res["arms"]
         arms["roofline"].update({"peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": arms["gbs"] / peaks["hbm_gbs"],

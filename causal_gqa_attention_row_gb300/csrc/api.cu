@@ -198,7 +198,7 @@ static gqa_status prefill_common(gqa::RowsParams& p, int bf16, int d_k, int d_v,
   p.err = error_word();
   if (!p.err) return GQA_ERR_CUDA;
   const float qscale = attention_scale * 1.4426950408889634f;
-  if (!arms_on && gqa::prefill_tc_supported(bf16, d_k, d_v, p.paged ? p.bs : 0) && attention_scale > 0.f)
+  if (!arms_on && gqa::prefill_tc_supported(bf16, d_k, d_v, p.paged ? p.bs : 0, p.mbps) && attention_scale > 0.f)
     return from_cuda(gqa::launch_prefill_tc(p.q, p.k, p.v, p.out, p.B, p.seq_q, p.capacity, p.offsets, p.H, p.Hkv,
                                             d_k, d_v, qscale, p.err, st, p.paged ? p.tables : nullptr, p.mbps, p.bs,
                                             p.num_blocks));

@@ -95,7 +95,7 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
                               int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv,
                               float qscale, unsigned* err, cudaStream_t st, const int32_t* tables = nullptr,
                               int mbps = 0, int bs = 0, int num_blocks = 0);
-// bs = 0: contiguous K/V; else the pool's block size.
-bool prefill_tc_supported(int bf16, int dk, int dv, int bs = 0);
+// bs = 0: contiguous K/V; else the pool's block size and max blocks per sequence.
+bool prefill_tc_supported(int bf16, int dk, int dv, int bs = 0, int mbps = 0);
 
 }  // namespace gqa

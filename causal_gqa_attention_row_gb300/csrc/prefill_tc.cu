@@ -76,7 +76,9 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTile;                               // K ring
 constexpr int kOffV = kOffK + kStagesK * kTile;            // V ring
-constexpr int kOffBar = kOffV + kStagesV * kTile;
+constexpr int kTabEntries = 4096;                          // paged: the CTA's block-table entries
+constexpr int kOffTab = kOffV + kStagesV * kTile;
+constexpr int kOffBar = kOffTab + kTabEntries * 4;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;           // + alignment slack
 // At the end, once every MMA is done: the output tile over Q, and warpgroup w's
 // row max and sum over K stage w (which only ever held warpgroup w's tiles).
@@ -193,13 +195,22 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Issue the TMA loads of key tile j (128 rows of 64) of KV head kvh, sequence
-// b, into `dst`, completing 16 KiB on `bar`. Contiguous: one box. Paged: one
-// box per pool block of the tile, addressed through the block table (the
-// 128-byte swizzle is a function of the shared address, so the blocks land
-// exactly where one box would put them). A block that holds no key below
-// kv_hi, or whose table entry is out of range (flagged), loads from past the
-// end of the pool: the TMA engine fills it with zeros.
+// The TMA loads of key tile j (128 rows of 64) of KV head kvh, sequence b,
+// into `dst`, completing 16 KiB on `bar`. Contiguous: one box. Paged: one box
+// per pool block of the tile, addressed through the block table (the 128-byte
+// swizzle is a function of the shared address, so the blocks land exactly
+// where one box would put them). A block that holds no key below kv_hi, or
+// whose table entry is out of range (flagged), loads from past the end of the
+// pool: the TMA engine fills it with zeros.
+__device__ __forceinline__ int pool_block(const TcParams& p, int t, int kv_hi, int e) {
+  if (t >= p.mbps || t * p.bs >= kv_hi) return p.num_blocks;
+  if (e >= 0 && e < p.num_blocks) return e;
+  raise_error(p.err, kErrBounds);
+  return p.num_blocks;
+}
+
+// One thread, the table read from global memory (the first tile, before the
+// CTA's shared copy of the table exists).
 __device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, unsigned char* dst, uint64_t* bar, int j, int kvh,
                                              int b, const TcParams& p, int kv_hi) {
   mbar_arrive_expect_tx(bar, kTile);
@@ -209,17 +220,32 @@ __device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, unsigned cha
   }
   const int per = kBN / p.bs;
   for (int i = 0; i < per; ++i) {
-    const int t = j * per + i;  // block of the sequence
-    int blk = p.num_blocks;
-    if (t < p.mbps && t * p.bs < kv_hi) {
-      const int e = __ldg(p.tables + (size_t)b * p.mbps + t);
-      if (e >= 0 && e < p.num_blocks)
-        blk = e;
-      else
-        raise_error(p.err, kErrBounds);
-    }
-    tc::tma_load_4d(dst + i * p.bs * 128, tm, 0, 0, kvh, blk, bar);
+    const int t = j * per + i;
+    const int e = (t < p.mbps && t * p.bs < kv_hi) ? __ldg(p.tables + (size_t)b * p.mbps + t) : 0;
+    tc::tma_load_4d(dst + i * p.bs * 128, tm, 0, 0, kvh, pool_block(p, t, kv_hi, e), bar);
   }
+}
+
+// The whole producer warp: lane 0 sets the expected bytes, then lane i issues
+// the copy of the tile's i-th pool block (each TMA instruction holds its thread
+// for a few hundred cycles, so the blocks of a tile go out side by side), the
+// entries read from the CTA's shared copy of its table row.
+__device__ __forceinline__ void load_kv_tile_warp(const CUtensorMap* tm, unsigned char* dst, uint64_t* bar, int j,
+                                                  int kvh, int b, const TcParams& p, int kv_hi, const int* tab,
+                                                  int lane) {
+  if (lane == 0) mbar_arrive_expect_tx(bar, kTile);
+  __syncwarp();
+  if (!p.tables) {
+    if (lane == 0) tc::tma_load_4d(dst, tm, 0, j * kBN, kvh, b, bar);
+  } else {
+    const int per = kBN / p.bs;
+    if (lane < per) {
+      const int t = j * per + lane;
+      const int e = (t < p.mbps && t * p.bs < kv_hi) ? tab[t] : 0;  // the shared copy covers every such t
+      tc::tma_load_4d(dst + lane * p.bs * 128, tm, 0, 0, kvh, pool_block(p, t, kv_hi, e), bar);
+    }
+  }
+  __syncwarp();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -298,27 +324,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp || warp == kProducerVWarp) {
     // ================= TMA producers: Q and K (warp 8), V (warp 11) =================
     const bool is_k = warp == kProducerWarp;
-    if (lane == 0) {
-      const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
-      uint64_t* full = is_k ? bars->k_full : bars->v_full;
-      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
-      unsigned char* ring = smem + (is_k ? kOffK : kOffV);
-      const int stages = is_k ? kStagesK : kStagesV;
-      if (!is_k) tc::prefetch_tmap(tm);
-      int issued_last[kStagesK];
+    // Paged: the two producer warps copy the table entries of the blocks this
+    // CTA reads into shared memory first (coalesced, one round trip), so that
+    // a tile's lookups never wait on global memory. The launcher takes this
+    // kernel only when a table row fits the copy (max_blocks_per_seq <= kTabEntries).
+    const int kv_hi = off + i0 + rows;
+    const int* tab = nullptr;
+    if (p.tables) {
+      int* st_tab = reinterpret_cast<int*>(smem + kOffTab);
+      const int n_tab = min(min(p.mbps, (kv_hi + p.bs - 1) / p.bs), kTabEntries);
+      for (int i = (is_k ? 0 : 32) + lane; i < n_tab; i += 64) st_tab[i] = __ldg(p.tables + (size_t)b * p.mbps + i);
+      named_bar_sync(3, 64);
+      tab = st_tab;
+    }
+    const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+    uint64_t* full = is_k ? bars->k_full : bars->v_full;
+    uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+    unsigned char* ring = smem + (is_k ? kOffK : kOffV);
+    const int stages = is_k ? kStagesK : kStagesV;
+    if (!is_k && lane == 0) tc::prefetch_tmap(tm);
+    int issued_last[kStagesK];
 #pragma unroll
-      for (int st = 0; st < kStagesK; ++st) issued_last[st] = -1;
-      int j = 0;
-      if (is_k) {  // Q and K_0 went out before the setup barrier
-        issued_last[0] = 0;
-        j = 1;
+    for (int st = 0; st < kStagesK; ++st) issued_last[st] = -1;
+    int j = 0;
+    if (is_k) {  // Q and K_0 went out before the setup barrier
+      issued_last[0] = 0;
+      j = 1;
+    }
+    for (; j < n_kv; ++j) {
+      const int st = j % stages;
+      if (j >= stages) {
+        bool w = true;
+        if (lane == 0) w = wait_or_abort(&empty[st], ((j / stages) - 1) & 1, bars, p.err);
+        if (!__shfl_sync(0xffffffffu, w, 0)) break;
       }
-      for (; j < n_kv; ++j) {
-        const int st = j % stages;
-        if (j >= stages && !wait_or_abort(&empty[st], ((j / stages) - 1) & 1, bars, p.err)) break;
-        load_kv_tile(tm, ring + st * kTile, &full[st], j, kvh, b, p, off + i0 + rows);
-        issued_last[st] = j;
-      }
+      load_kv_tile_warp(tm, ring + st * kTile, &full[st], j, kvh, b, p, kv_hi, tab, lane);
+      issued_last[st] = j;
+    }
+    if (lane == 0) {
       // never exit with a load in flight
       if (is_k && !mbar_wait(&bars->q_full, 0)) raise_error(p.err, kErrTimeout);
       for (int st = 0; st < stages; ++st)
@@ -580,9 +623,11 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64
 
 }  // namespace
 
-bool prefill_tc_supported(int bf16, int dk, int dv, int bs) {
-  // paged: a pool block is a whole number of 8-row swizzle atoms and divides a 128-key tile
-  return bf16 == 1 && dk == kD && dv == kD && (bs == 0 || (bs % 8 == 0 && kBN % bs == 0));
+bool prefill_tc_supported(int bf16, int dk, int dv, int bs, int mbps) {
+  // paged: a pool block is a whole number of 8-row swizzle atoms and divides a
+  // 128-key tile, and a table row fits the CTA's shared copy
+  return bf16 == 1 && dk == kD && dv == kD &&
+         (bs == 0 || (bs % 8 == 0 && kBN % bs == 0 && mbps > 0 && mbps <= kTabEntries));
 }
 
 cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
@@ -590,7 +635,7 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
                               unsigned* err, cudaStream_t st, const int32_t* tables, int mbps, int bs,
                               int num_blocks) {
   if (dk != kD || dv != kD || !(qscale > 0.f)) return cudaErrorNotSupported;
-  if (tables && !prefill_tc_supported(1, dk, dv, bs)) return cudaErrorNotSupported;
+  if (tables && !prefill_tc_supported(1, dk, dv, bs, mbps)) return cudaErrorNotSupported;
   CUtensorMap tq, tk, tv, to;
   // q [B, S, H, 64]: dims (64, H, S, B), box (64, 1, 128, 1)
   if (!make_map(&tq, q, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;

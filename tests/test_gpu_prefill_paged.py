@@ -159,3 +159,32 @@ def test_bad_table_entry_and_offset_are_flagged(gpu_lib, dtype):
     g.attn_prefill_paged(c.q.to(DEV), kp.to(DEV), vp.to(DEV), tables.to(DEV), out, c.scale, position_offset=far)
     assert g.attn_get_device_error() == g.ERR_DEVICE_BOUNDS
     assert torch.all(out[1] == 0)
+
+
+def test_full_size_chunked_prefill_sampled_rows(gpu_lib):
+    """The chunked-prefill workload the bench times (4 sequences, 2048-row chunks at
+    offsets up to 6144, bs = 16): sampled rows -- first, last and seeded others of
+    each chunk, every head -- against the oracle, each row computed on its own
+    over the history gathered from the pool through the table."""
+    g = gpu_lib
+    q, kp, vp, tables, off, scale = W.make_prefill_paged()
+    B, S, H, d = q.shape
+    bs = kp.shape[2]
+    out = torch.empty(B, S, H, d, dtype=torch.bfloat16, device=DEV)
+    g.attn_prefill_paged(q.to(DEV), kp.to(DEV), vp.to(DEV), tables.to(DEV), out, scale,
+                         position_offset=off.to(DEV))
+    ok(g)
+    out = out.cpu()
+    rng = np.random.default_rng(190)
+    worst = 0.0
+    for b in range(B):
+        o = int(off[b])
+        n = o + S
+        blocks = tables[b, :(n + bs - 1) // bs].long()
+        k_hist = kp[blocks].permute(1, 0, 2, 3).reshape(1, kp.shape[1], -1, d)[:, :, :n].contiguous()
+        v_hist = vp[blocks].permute(1, 0, 2, 3).reshape(1, vp.shape[1], -1, d)[:, :, :n].contiguous()
+        for i in sorted({0, S - 1, *rng.integers(0, S, 3).tolist()}):
+            want = core.attention_arms(W.to_oracle(q[b:b + 1, i:i + 1].contiguous()), W.to_oracle(k_hist),
+                                       W.to_oracle(v_hist), [o + i + 1], scale)
+            worst = max(worst, err(out[b:b + 1, i:i + 1], want))
+    assert worst <= 2e-2, worst

@@ -168,4 +168,31 @@ WORKLOADS = {
     "paged": ("paged decode bf16: 256 seqs, H=32, Hkv=8, d=128, bs=16, 600k-block pool, "
               "history U[1,32768] + 1 appended row"),
     "mla": "MLA-shaped decode bf16: 32 seqs, 128 heads, d_k=128+64 shared rot, d_v=128, len 4096",
+    "prefill_paged": ("chunked prefill bf16 on the paged pool: 4 seqs, H=14, Hkv=2, d=64, bs=16, a 2048-row "
+                      "chunk at offsets 0/2048/4096/6144 (history already in the pool)"),
 }
+
+
+def make_prefill_paged(offsets=(0, 2048, 4096, 6144), S=2048, H=14, Hkv=2, d=64, bs=16, spare=64, seed=6,
+                       device="cpu"):
+    """Chunked-prefill case on a paged pool: sequence b holds offsets[b] + S rows
+    (its history and the chunk itself, already appended), scattered over blocks
+    of a seeded permutation of the pool; entries past a sequence's last block are
+    -1. Returns (q [B, S, H, d], k_pool, v_pool, tables, offsets, scale)."""
+    B = len(offsets)
+    need = [(o + S + bs - 1) // bs for o in offsets]
+    mbps = max(need)
+    nb = sum(need) + spare
+    gl = generator(seed + 1000)
+    perm = torch.randperm(nb, generator=gl).to(torch.int32)
+    tables = torch.full((B, mbps), -1, dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(need):
+        tables[b, :n] = perm[at:at + n]
+        at += n
+    g = generator(seed, device)
+    q = randn((B, S, H, d), g, torch.bfloat16, device)
+    k_pool = randn((nb, Hkv, bs, d), g, torch.bfloat16, device)
+    v_pool = randn((nb, Hkv, bs, d), g, torch.bfloat16, device)
+    off = torch.tensor(list(offsets), dtype=torch.int32)
+    return q, k_pool, v_pool, tables.to(device), off.to(device), 1.0 / math.sqrt(d)
