@@ -1,4 +1,4 @@
-// prefill_tc.cu -- causal prefill on the tcgen05 tensor cores (bf16, d_k = d_v = 64).
+// prefill_tc.cu -- causal prefill on the tcgen05 tensor cores (bf16, d_k = d_v = 64 or 128).
 //
 // The operation (kopitiam-runtime src/attention.rs, `attention_forward` and
 // `causal_mask`): row i of sequence b, query head h, sits at position
@@ -17,21 +17,27 @@
 //   warps 9, 10 one thread each issues the tcgen05.mma of one softmax warpgroup
 //               (warp 9 also allocates and frees TMEM)
 //   warp 11     TMA producer of the V tiles (four-stage ring)
-// Warpgroup w owns, in tensor memory (TMEM), S_w = Q K^T (M=128, N=128, K=64;
-// columns 128w..), P_w (the bf16 probabilities, two per 32-bit column; columns
-// 384 + 64w..) and O_w += P_w V (M=128, N=64, K=128, A read from TMEM; columns
-// 256 + 64w..): the whole 512 columns. P never passes through shared memory,
-// whose bandwidth is left to the TMA tiles and the MMAs' reads of Q, K and V.
-// The softmax threads keep the row sum of exactly the bf16 p that multiply V,
-// in fp32. Thread t of a warpgroup owns query row t (TMEM lane t).
+// Warpgroup w owns, in tensor memory (TMEM), S_w = Q K^T (M=128, N=128, K=d;
+// 128 columns), P_w (the bf16 probabilities, two per 32-bit column; 64 columns)
+// and O_w += P_w V (M=128, N=d, K=128, A read from TMEM; d columns). At d = 64
+// the three are separate (S 2 x 128 + O 2 x 64 + P 2 x 64 = 512 columns); at
+// d = 128 P_w sits over the first 64 columns of S_w (S 2 x 128 + O 2 x 128),
+// so the MMA thread issues the next S into S_w only once the PV that reads P_w
+// is done. P never passes through shared memory, whose bandwidth is left to
+// the TMA tiles and the MMAs' reads of Q, K and V. A row of d elements is d / 64
+// blocks of 64 columns, each in the 128-byte swizzle (one TMA box each). The
+// softmax threads keep the row sum of exactly the bf16 p that multiply V, in
+// fp32. Thread t of a warpgroup owns query row t (TMEM lane t).
 //
 // Pipeline per warpgroup and key tile j: the softmax threads load their S_j row
 // into registers and release S_w at once, so the MMA thread issues S_{j+2}
 // while the exponentials of tile j are still being computed; P_j is built in
 // registers and stored into P_w once PV_{j-2} (issued a whole tile earlier) has
-// read the previous one. K and V have rings of their own: a K stage is free as
-// soon as its S MMA is done, a V stage once its PV is. K runs four tiles ahead,
-// so the load of K_{j+4} has a whole tile-period before S_{j+4} needs it.
+// read the previous one (at d = 128, once S_w holds S_j that PV is done). K and
+// V have rings of their own: a K stage is free as soon as its S MMA is done, a
+// V stage once its PV is. At d = 64 they run four tiles ahead, so the load of
+// K_{j+4} has a whole tile-period before S_{j+4} needs it; at d = 128 (tiles
+// twice the size) two, which the later issue of S leaves enough.
 //
 // Softmax with lazy rescaling: p = 2^((s - m) * scale * log2 e) against a
 // reference max m that only moves when a score exceeds it by more than 2^8 in
@@ -50,11 +56,8 @@
 namespace gqa {
 namespace {
 
-constexpr int kD = 64;     // head width (d_k = d_v)
 constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // keys per tile
-constexpr int kStagesK = 4;  // K ring: stage s only ever holds key tiles of warpgroup s % 2
-constexpr int kStagesV = 4;  // V ring: stage s only ever holds key tiles of warpgroup s % 2
 constexpr int kWG = 2;     // softmax warpgroups
 constexpr int kThreads = (kWG + 1) * 128;  // two softmax warpgroups + one control warpgroup
 constexpr int kProducerWarp = 8, kMmaWarp0 = 9, kProducerVWarp = 11;
@@ -63,33 +66,45 @@ constexpr int kProducerWarp = 8, kMmaWarp0 = 9, kProducerVWarp = 11;
 // 128 * 88 + 256 * 208 = 384 * 168.
 constexpr int kLaunchRegs = 168, kCtrlRegs = 88, kSoftmaxRegs = 208;
 static_assert(128 * kCtrlRegs + kWG * 128 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split over budget");
-// A ring stage must only ever hold one warpgroup's tiles: each MMA thread then
-// waits on its stages' barriers in order and never two phases behind.
-static_assert(kStagesK % kWG == 0 && kStagesV % kWG == 0, "ring stages shared between warpgroups");
-constexpr int kTile = kBM * kD * 2;  // 16 KiB: one Q, K or V tile (128 rows x 128 bytes)
+constexpr int kBlk = kBM * 128;  // 16 KiB: 128 rows of one 64-column block
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // S_w at 128w, O_w at 256 + 64w, P_w at 384 + 64w
-static_assert(kColP + kWG * (kBN / 2) == kTmemCols, "TMEM map");
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kTabEntries = 4096;  // paged: the CTA's block-table entries
+constexpr int kMaxStages = 4;
 
-// shared-memory map (from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kTile;                               // K ring
-constexpr int kOffV = kOffK + kStagesK * kTile;            // V ring
-constexpr int kTabEntries = 4096;                          // paged: the CTA's block-table entries
-constexpr int kOffTab = kOffV + kStagesV * kTile;
-constexpr int kOffBar = kOffTab + kTabEntries * 4;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;           // + alignment slack
-// At the end, once every MMA is done: the output tile over Q, and warpgroup w's
-// row max and sum over K stage w (which only ever held warpgroup w's tiles).
-constexpr int kOffOut = kOffQ;
-constexpr int kOffML = kOffK;
-static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
+// Sizes and maps of the kernel for head width D (64 or 128).
+template <int D>
+struct Cfg {
+  static constexpr int kCB = D / 64;         // 64-column blocks per row
+  static constexpr int kTile = kCB * kBlk;   // one Q, K or V tile (128 rows)
+  static constexpr bool kAlias = D > 64;     // P_w over the first 64 columns of S_w
+  // rings: stage s only ever holds key tiles of warpgroup s % 2
+  static constexpr int kStagesK = kAlias ? 2 : 4, kStagesV = kAlias ? 2 : 4;
+  static_assert(kStagesK % kWG == 0 && kStagesV % kWG == 0 && kStagesK <= kMaxStages && kStagesV <= kMaxStages,
+                "ring stages shared between warpgroups");
+  // TMEM columns of S_w, O_w and P_w
+  __host__ __device__ static constexpr uint32_t col_s(int w) { return kAlias ? 256 * w : 128 * w; }
+  __host__ __device__ static constexpr uint32_t col_o(int w) { return kAlias ? 256 * w + 128 : 256 + 64 * w; }
+  __host__ __device__ static constexpr uint32_t col_p(int w) { return kAlias ? 256 * w : 384 + 64 * w; }
+  static_assert(col_o(kWG - 1) + D <= kTmemCols && col_p(kWG - 1) + 64 <= kTmemCols, "TMEM map");
+  // shared-memory map (from a 1024-byte aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kTile;                              // K ring
+  static constexpr int kOffV = kOffK + kStagesK * kTile;           // V ring
+  static constexpr int kOffTab = kOffV + kStagesV * kTile;         // paged: block-table entries
+  static constexpr int kOffBar = kOffTab + kTabEntries * 4;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;          // + alignment slack
+  // At the end, once every MMA is done: the output tile over Q, and warpgroup
+  // w's row max and sum over K stage w (which only ever held warpgroup w's tiles).
+  static constexpr int kOffOut = kOffQ;
+  static constexpr int kOffML = kOffK;
+  static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
+};
 
 struct TcParams {
   int B, S, H, Hkv, G, S_kv, n_qtiles;  // S_kv: keys a sequence can hold (the pool's capacity when paged)
   const int32_t* offsets;
-  // paged K/V (tables != NULL): [num_blocks, Hkv, bs, 64] pools, row j of
+  // paged K/V (tables != NULL): [num_blocks, Hkv, bs, d] pools, row j of
   // sequence b in block tables[b * mbps + j / bs], slot j % bs; bs divides 128
   const int32_t* tables;
   int mbps, bs, num_blocks;
@@ -99,7 +114,7 @@ struct TcParams {
 };
 
 struct Bars {
-  uint64_t q_full, k_full[kStagesK], k_empty[kStagesK], v_full[kStagesV], v_empty[kStagesV];
+  uint64_t q_full, k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
   uint64_t s_full[kWG], s_free[kWG], p_full[kWG], mma_final[kWG];
   uint64_t o_done[kWG];  // every PV of warpgroup w issued so far is done (a phase per PV)
   uint32_t tmem_base;
@@ -195,13 +210,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// The TMA loads of key tile j (128 rows of 64) of KV head kvh, sequence b,
-// into `dst`, completing 16 KiB on `bar`. Contiguous: one box. Paged: one box
-// per pool block of the tile, addressed through the block table (the 128-byte
-// swizzle is a function of the shared address, so the blocks land exactly
-// where one box would put them). A block that holds no key below kv_hi, or
-// whose table entry is out of range (flagged), loads from past the end of the
-// pool: the TMA engine fills it with zeros.
+// The TMA loads of key tile j (128 rows of D) of KV head kvh, sequence b, into
+// `dst`, completing a tile's bytes on `bar`: one box per 64-column block of the
+// rows, at that block's 16 KiB slot. Contiguous: the tile's 128 rows in one box
+// per block. Paged: one box per pool block and column block, addressed through
+// the block table (the 128-byte swizzle is a function of the shared address, so
+// the pool blocks land exactly where one box would put them). A pool block that
+// holds no key below kv_hi, or whose table entry is out of range (flagged),
+// loads from past the end of the pool: the TMA engine fills it with zeros.
 __device__ __forceinline__ int pool_block(const TcParams& p, int t, int kv_hi, int e) {
   if (t >= p.mbps || t * p.bs >= kv_hi) return p.num_blocks;
   if (e >= 0 && e < p.num_blocks) return e;
@@ -211,50 +227,64 @@ __device__ __forceinline__ int pool_block(const TcParams& p, int t, int kv_hi, i
 
 // One thread, the table read from global memory (the first tile, before the
 // CTA's shared copy of the table exists).
+template <int D>
 __device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, unsigned char* dst, uint64_t* bar, int j, int kvh,
                                              int b, const TcParams& p, int kv_hi) {
-  mbar_arrive_expect_tx(bar, kTile);
+  using C = Cfg<D>;
+  mbar_arrive_expect_tx(bar, C::kTile);
   if (!p.tables) {
-    tc::tma_load_4d(dst, tm, 0, j * kBN, kvh, b, bar);
+#pragma unroll
+    for (int cb = 0; cb < C::kCB; ++cb) tc::tma_load_4d(dst + cb * kBlk, tm, cb * 64, j * kBN, kvh, b, bar);
     return;
   }
   const int per = kBN / p.bs;
   for (int i = 0; i < per; ++i) {
     const int t = j * per + i;
     const int e = (t < p.mbps && t * p.bs < kv_hi) ? __ldg(p.tables + (size_t)b * p.mbps + t) : 0;
-    tc::tma_load_4d(dst + i * p.bs * 128, tm, 0, 0, kvh, pool_block(p, t, kv_hi, e), bar);
+    const int blk = pool_block(p, t, kv_hi, e);
+#pragma unroll
+    for (int cb = 0; cb < C::kCB; ++cb)
+      tc::tma_load_4d(dst + cb * kBlk + i * p.bs * 128, tm, cb * 64, 0, kvh, blk, bar);
   }
 }
 
-// The whole producer warp: lane 0 sets the expected bytes, then lane i issues
-// the copy of the tile's i-th pool block (each TMA instruction holds its thread
-// for a few hundred cycles, so the blocks of a tile go out side by side), the
-// entries read from the CTA's shared copy of its table row.
+// The whole producer warp: lane 0 sets the expected bytes, then each lane issues
+// one box (each TMA instruction holds its thread for a few hundred cycles, so
+// the boxes of a tile go out side by side), the entries read from the CTA's
+// shared copy of its table row.
+template <int D>
 __device__ __forceinline__ void load_kv_tile_warp(const CUtensorMap* tm, unsigned char* dst, uint64_t* bar, int j,
                                                   int kvh, int b, const TcParams& p, int kv_hi, const int* tab,
                                                   int lane) {
-  if (lane == 0) mbar_arrive_expect_tx(bar, kTile);
+  using C = Cfg<D>;
+  if (lane == 0) mbar_arrive_expect_tx(bar, C::kTile);
   __syncwarp();
   if (!p.tables) {
-    if (lane == 0) tc::tma_load_4d(dst, tm, 0, j * kBN, kvh, b, bar);
+    if (lane < C::kCB) tc::tma_load_4d(dst + lane * kBlk, tm, lane * 64, j * kBN, kvh, b, bar);
   } else {
-    const int per = kBN / p.bs;
-    if (lane < per) {
-      const int t = j * per + lane;
+    const int per = kBN / p.bs;  // per * kCB <= 32
+    if (lane < per * C::kCB) {
+      const int i = lane % per, cb = lane / per;
+      const int t = j * per + i;
       const int e = (t < p.mbps && t * p.bs < kv_hi) ? tab[t] : 0;  // the shared copy covers every such t
-      tc::tma_load_4d(dst + lane * p.bs * 128, tm, 0, 0, kvh, pool_block(p, t, kv_hi, e), bar);
+      tc::tma_load_4d(dst + cb * kBlk + i * p.bs * 128, tm, cb * 64, 0, kvh, pool_block(p, t, kv_hi, e), bar);
     }
   }
   __syncwarp();
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                       const TcParams p) {
+  using C = Cfg<D>;
+  constexpr int kTile = C::kTile, kStagesK = C::kStagesK, kStagesV = C::kStagesV;
+  constexpr int kOffQ = C::kOffQ, kOffK = C::kOffK, kOffV = C::kOffV, kOffTab = C::kOffTab;
+  constexpr int kOffOut = C::kOffOut, kOffML = C::kOffML;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item, longest first
@@ -291,11 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::prefetch_tmap(&tm_q);
     tc::prefetch_tmap(&tm_k);
     mbar_arrive_expect_tx(&bars->q_full, kTile);
-    tc::tma_load_4d(smem + kOffQ, &tm_q, 0, h, i0, b, &bars->q_full);
+#pragma unroll
+    for (int cb = 0; cb < C::kCB; ++cb) tc::tma_load_4d(smem + kOffQ + cb * kBlk, &tm_q, cb * 64, h, i0, b, &bars->q_full);
     if (p.tables)  // the table entries of the tile wait for the offset, which bounds them
-      load_kv_tile(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, off + i0 + rows);
+      load_kv_tile<D>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, off + i0 + rows);
     else
-      load_kv_tile(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, 0);
+      load_kv_tile<D>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, 0);
   }
   if (warp == kMmaWarp0) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -308,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (off < 0 || (long long)off + p.S > p.S_kv) {  // the cache cannot hold these rows
     if (threadIdx.x == 0 && qt == p.n_qtiles - 1 && h == 0) raise_error(p.err, kErrBounds);
-    for (int idx = threadIdx.x; idx < rows * kD; idx += blockDim.x)
-      p.out[(((size_t)b * p.S + i0 + idx / kD) * p.H + h) * kD + idx % kD] = __float2bfloat16_rn(0.f);
+    for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x)
+      p.out[(((size_t)b * p.S + i0 + idx / D) * p.H + h) * D + idx % D] = __float2bfloat16_rn(0.f);
     // never exit with a load in flight
     if (warp == kProducerWarp && lane == 0 && !(mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0)))
       raise_error(p.err, kErrTimeout);
@@ -358,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) w = wait_or_abort(&empty[st], ((j / stages) - 1) & 1, bars, p.err);
         if (!__shfl_sync(0xffffffffu, w, 0)) break;
       }
-      load_kv_tile_warp(tm, ring + st * kTile, &full[st], j, kvh, b, p, kv_hi, tab, lane);
+      load_kv_tile_warp<D>(tm, ring + st * kTile, &full[st], j, kvh, b, p, kv_hi, tab, lane);
       issued_last[st] = j;
     }
     if (lane == 0) {
@@ -374,21 +405,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int n_mine = (n_kv - w + 1) / 2;
       const uint32_t idS = tc::idesc_bf16_f32(kBM, kBN, false);
-      const uint32_t idO = tc::idesc_bf16_f32(kBM, kD, true);
+      const uint32_t idO = tc::idesc_bf16_f32(kBM, D, true);
       // descriptors: constant high part + (shared address >> 4) in the low bits
       constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);
       const uint64_t dQ = kHi | (smem_u32(smem + kOffQ) >> 4);
       const uint64_t dK0 = kHi | (smem_u32(smem + kOffK) >> 4);
-      // V of each stage: MN-major (64 columns = one swizzle atom wide), 8-key groups 1024 bytes apart
-      const uint64_t dV0 = kHi | (smem_u32(smem + kOffV) >> 4);
-      const uint32_t dS = tmem + kColS + w * kBN, dO = tmem + kColO + w * kD, tP = tmem + kColP + w * (kBN / 2);
+      // V of each stage: MN-major, 8-key groups 1024 bytes apart, its 64-column
+      // blocks (D > 64) a block's 16 KiB apart (the leading byte offset)
+      const uint64_t dV0 = tc::desc_sw128_hi(C::kCB > 1 ? kBlk : 0, 1024) | (smem_u32(smem + kOffV) >> 4);
+      const uint32_t dS = tmem + C::col_s(w), dO = tmem + C::col_o(w), tP = tmem + C::col_p(w);
       auto issue_s = [&](int j) -> bool {  // S_w = Q K_j^T
         const int st = j % kStagesK;
         if (!wait_or_abort(&bars->k_full[st], (j / kStagesK) & 1, bars, p.err)) return false;
         tc::fence_after_sync();
         const uint64_t dK = dK0 + (uint64_t)((st * kTile) >> 4);
+        // 16 of the D columns per instruction: block kk / 4, 32 bytes per step inside it
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) tc::mma_f16_ss(dS, dQ + kk * 2, dK + kk * 2, idS, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t at = (kk / 4) * kBlk + (kk % 4) * 32;
+          tc::mma_f16_ss(dS, dQ + (at >> 4), dK + (at >> 4), idS, kk > 0);
+        }
         tc::mma_commit(&bars->s_full[w]);
         tc::mma_commit(&bars->k_empty[st]);  // the K stage is free once S_j is done
         return true;
@@ -396,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = n_mine > 0 && wait_or_abort(&bars->q_full, 0, bars, p.err) && issue_s(w);
       for (int k = 0; ok && k < n_mine; ++k) {
         const int j = 2 * k + w;
-        // S_{j+2} as soon as the softmax threads have read S_j into registers
-        if (k + 1 < n_mine) ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
+        // d = 64: S_{j+2} as soon as the softmax threads have read S_j into registers
+        if (!C::kAlias && k + 1 < n_mine) ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
         if (!ok || !wait_or_abort(&bars->p_full[w], k & 1, bars, p.err)) break;
         const int st = j % kStagesV;
         if (!wait_or_abort(&bars->v_full[st], (j / kStagesV) & 1, bars, p.err)) break;
@@ -409,6 +445,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_f16_ts(dO, tP + kk * 8, dV + kk * (2048 >> 4), idO, (k > 0 || kk > 0));
         tc::mma_commit(&bars->o_done[w]);
         tc::mma_commit(&bars->v_empty[st]);
+        // d = 128: P_j sits in S_w, so S_{j+2} waits for PV_j (this thread waits
+        // every phase of o_done[w] in order)
+        if (C::kAlias && k + 1 < n_mine) {
+          ok = wait_or_abort(&bars->o_done[w], k & 1, bars, p.err);
+          if (ok) {
+            tc::fence_after_sync();
+            ok = issue_s(j + 2);
+          }
+        }
       }
       // every MMA issued above has completed before TMEM is released
       tc::mma_commit(&bars->mma_final[w]);
@@ -427,9 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float th = kRescaleLog2 / qs;
     float m_ref = -INFINITY;
     float l_run = 0.f;  // the row sum of this warpgroup's p, against m_ref
-    const uint32_t tS = tmem + lane_addr + kColS + wg * kBN;
-    const uint32_t tO = tmem + lane_addr + kColO + wg * kD;
-    const uint32_t tP = tmem + lane_addr + kColP + wg * (kBN / 2);
+    const uint32_t tS = tmem + lane_addr + C::col_s(wg);
+    const uint32_t tO = tmem + lane_addr + C::col_o(wg);
+    const uint32_t tP = tmem + lane_addr + C::col_p(wg);
     const float2 qs2 = make_float2(qs, qs);
     const int n_mine = (n_kv - wg + 1) / 2;  // key tiles this warpgroup handles
     bool alive = true;
@@ -478,15 +523,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             f = ex2f((m_ref - mx) * qs);  // 0 while m_ref = -inf
             m_ref = mx;
           }
-          // O_w holds every PV issued so far (PV_{k-1} the last): rescale it once done
-          if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
+          // O_w holds every PV issued so far (PV_{k-1} the last): rescale it once
+          // done (at d = 128 it is: S_k was issued after it)
+          if (!C::kAlias && !warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
             alive = false;
             break;
           }
           tc::fence_after_sync();
           uint32_t o[32];
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             tc::tmem_ld_32x32b_x32(tO + c * 32, o);
             tc::tmem_ld_wait();
 #pragma unroll
@@ -512,10 +558,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           add_bf16x2(ls[(t & 3) * 2], ls[(t & 3) * 2 + 1], pv[c][t]);
         }
       l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // ---- P_w is free once PV_{k-1} has read it. Every phase of o_done[w] is
-      // waited for in order, before the next PV can be issued, so the barrier is
-      // never two phases ahead of this wait (nor of the rescale's or the final one).
-      if (k >= 1) {
+      // ---- d = 64: P_w is free once PV_{k-1} has read it. Every phase of
+      // o_done[w] is waited for in order, before the next PV can be issued, so the
+      // barrier is never two phases ahead of this wait (nor of the rescale's or the
+      // final one). d = 128: P goes over S_k's own first columns, already read.
+      if (!C::kAlias && k >= 1) {
         if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
           alive = false;
           break;
@@ -553,36 +600,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float l = a0 * l0 + a1 * l1;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float c0 = a0 * inv, c1 = a1 * inv;
-    // this warpgroup's 32 of the 64 columns; O_1 exists once warpgroup 1 had a tile
-    const int col0 = wg * (kD / 2);
-    uint32_t o0[32], o1[32];
-    tc::tmem_ld_32x32b_x32(tmem + lane_addr + kColO + col0, o0);
-    if (n_kv > 1) tc::tmem_ld_32x32b_x32(tmem + lane_addr + kColO + kD + col0, o1);
-    tc::tmem_ld_wait();
-    // the output tile over Q (every S MMA, the readers of Q, is done), in the
-    // 128-byte swizzle of the output's tensor map
+    // this warpgroup's D / 2 of the D columns, 32 at a time; O_1 exists once
+    // warpgroup 1 had a tile. The output tile goes over Q (every S MMA, the
+    // readers of Q, is done), in the 128-byte swizzle of the output's tensor map:
+    // column c of row r in block c / 64, 16-byte chunk (c % 64) / 8 XOR r % 8.
     unsigned char* so = smem + kOffOut;
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      uint32_t w4[4];
+    for (int cc = 0; cc < D / 64; ++cc) {
+      const int col0 = wg * (D / 2) + cc * 32;
+      uint32_t o0[32], o1[32];
+      tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::col_o(0) + col0, o0);
+      if (n_kv > 1) tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::col_o(1) + col0, o1);
+      tc::tmem_ld_wait();
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = t * 8 + 2 * u;
-        float x0 = __uint_as_float(o0[e]) * c0, x1 = __uint_as_float(o0[e + 1]) * c0;
-        if (use1) {
-          x0 = fmaf(__uint_as_float(o1[e]), c1, x0);
-          x1 = fmaf(__uint_as_float(o1[e + 1]), c1, x1);
+      for (int t = 0; t < 4; ++t) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = t * 8 + 2 * u;
+          float x0 = __uint_as_float(o0[e]) * c0, x1 = __uint_as_float(o0[e + 1]) * c0;
+          if (use1) {
+            x0 = fmaf(__uint_as_float(o1[e]), c1, x0);
+            x1 = fmaf(__uint_as_float(o1[e + 1]), c1, x1);
+          }
+          w4[u] = pack_bf16(x0, x1);
         }
-        w4[u] = pack_bf16(x0, x1);
+        const int col = col0 + t * 8;
+        const int chunk = (col % 64) / 8;
+        *reinterpret_cast<uint4*>(so + (col / 64) * kBlk + r * 128 + ((chunk ^ (r & 7)) * 16)) =
+            make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
-      const int chunk = wg * 4 + t;  // 16-byte chunk of the 128-byte output row
-      *reinterpret_cast<uint4*>(so + r * 128 + ((chunk ^ (r & 7)) * 16)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
     }
     tc::fence_async_smem();  // the tile visible to the TMA engine
     named_bar_sync(2, kWG * 128);
     if (threadIdx.x == 0) {
       // rows past the end of the sequence fall outside the tensor and are not written
-      tc::tma_store_4d(&tm_o, so, 0, h, i0, b);
+#pragma unroll
+      for (int cb = 0; cb < C::kCB; ++cb) tc::tma_store_4d(&tm_o, so + cb * kBlk, cb * 64, h, i0, b);
       tc::bulk_commit_group();
       tc::bulk_wait_group_read0();  // shared memory stays valid until the store has read it
     }
@@ -608,25 +662,53 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A 4-D bf16 tensor of rows of 64 elements; box = 64 x b1 x b2 x 1, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64_t d3, uint32_t box1, uint32_t box2) {
+// A 4-D bf16 tensor of rows of d elements; box = 64 x b1 x b2 x 1 (one 64-column
+// block of the rows), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int d, uint64_t d1, uint64_t d2, uint64_t d3, uint32_t box1,
+              uint32_t box2) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[4] = {kD, d1, d2, d3};
-  const cuuint64_t strides[3] = {kD * 2, kD * 2 * d1, kD * 2 * d1 * d2};
-  const cuuint32_t box[4] = {kD, box1, box2, 1};
+  const cuuint64_t dims[4] = {(cuuint64_t)d, d1, d2, d3};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * d1, (cuuint64_t)d * 2 * d1 * d2};
+  const cuuint32_t box[4] = {64, box1, box2, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int D>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                     const TcParams& p, cudaStream_t st) {
+  using C = Cfg<D>;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static unsigned long long attr_done = 0;
+  if (dev < 64 && !(attr_done >> dev & 1ull)) {
+    // The register hand-over inside the kernel assumes exactly kLaunchRegs per
+    // thread at launch; with any other allocation it could wait forever, so
+    // such a build is refused here instead of launched.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorNotSupported;
+    e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done |= 1ull << dev;
+  }
+  const long long ctas = (long long)p.B * p.H * p.n_qtiles;
+  if (ctas <= 0) return cudaSuccess;
+  prefill_tc_kernel<D><<<(unsigned)ctas, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool prefill_tc_supported(int bf16, int dk, int dv, int bs, int mbps) {
-  // paged: a pool block is a whole number of 8-row swizzle atoms and divides a
-  // 128-key tile, and a table row fits the CTA's shared copy
-  return bf16 == 1 && dk == kD && dv == kD &&
+  // d_k = d_v = 64 or 128; paged: a pool block is a whole number of 8-row
+  // swizzle atoms and divides a 128-key tile, and a table row fits the CTA's
+  // shared copy
+  return bf16 == 1 && dk == dv && (dk == 64 || dk == 128) &&
          (bs == 0 || (bs % 8 == 0 && kBN % bs == 0 && mbps > 0 && mbps <= kTabEntries));
 }
 
@@ -634,22 +716,22 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
                               int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv, float qscale,
                               unsigned* err, cudaStream_t st, const int32_t* tables, int mbps, int bs,
                               int num_blocks) {
-  if (dk != kD || dv != kD || !(qscale > 0.f)) return cudaErrorNotSupported;
-  if (tables && !prefill_tc_supported(1, dk, dv, bs, mbps)) return cudaErrorNotSupported;
+  if (!prefill_tc_supported(1, dk, dv, tables ? bs : 0, mbps) || !(qscale > 0.f)) return cudaErrorNotSupported;
+  const int d = dk;
   CUtensorMap tq, tk, tv, to;
-  // q [B, S, H, 64]: dims (64, H, S, B), box (64, 1, 128, 1)
-  if (!make_map(&tq, q, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
+  // q [B, S, H, d]: dims (d, H, S, B), box (64, 1, 128, 1)
+  if (!make_map(&tq, q, d, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
   if (tables) {
-    // pools [num_blocks, Hkv, bs, 64]: dims (64, bs, Hkv, num_blocks), box (64, bs, 1, 1)
-    if (!make_map(&tk, k, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
-    if (!make_map(&tv, v, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
+    // pools [num_blocks, Hkv, bs, d]: dims (d, bs, Hkv, num_blocks), box (64, bs, 1, 1)
+    if (!make_map(&tk, k, d, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
+    if (!make_map(&tv, v, d, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
   } else {
-    // k, v [B, Hkv, S_kv, 64]: dims (64, S_kv, Hkv, B), box (64, 128, 1, 1)
-    if (!make_map(&tk, k, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
-    if (!make_map(&tv, v, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
+    // k, v [B, Hkv, S_kv, d]: dims (d, S_kv, Hkv, B), box (64, 128, 1, 1)
+    if (!make_map(&tk, k, d, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
+    if (!make_map(&tv, v, d, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
   }
-  // out [B, S, H, 64]: as q
-  if (!make_map(&to, out, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
+  // out [B, S, H, d]: as q
+  if (!make_map(&to, out, d, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
   TcParams p;
   p.B = B;
   p.S = seq_q;
@@ -666,25 +748,7 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
   p.out = static_cast<__nv_bfloat16*>(out);
   p.qscale = qscale;
   p.err = err;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static unsigned long long attr_done = 0;
-  if (dev < 64 && !(attr_done >> dev & 1ull)) {
-    // The register hand-over inside the kernel assumes exactly kLaunchRegs per
-    // thread at launch; with any other allocation it could wait forever, so
-    // such a build is refused here instead of launched.
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorNotSupported;
-    e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done |= 1ull << dev;
-  }
-  const long long ctas = (long long)B * H * p.n_qtiles;
-  if (ctas <= 0) return cudaSuccess;
-  prefill_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, p);
-  return cudaGetLastError();
+  return d == 64 ? launch_d<64>(tq, tk, tv, to, p, st) : launch_d<128>(tq, tk, tv, to, p, st);
 }
 
 }  // namespace gqa

@@ -1,4 +1,4 @@
-"""The tcgen05 causal prefill (bf16, d = 64) against the fp64 oracle (GPU)."""
+"""The tcgen05 causal prefill (bf16, d = 64 and d = 128) against the fp64 oracle (GPU)."""
 import numpy as np
 import pytest
 import torch
@@ -18,13 +18,14 @@ def run(g, c):
     return out
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("B,S,H,Hkv,offs", [
     (1, 128, 2, 1, [0]), (1, 256, 4, 2, [0]), (1, 300, 14, 2, [0]), (2, 200, 6, 3, [0, 37]),
     (1, 1, 2, 2, [5]), (2, 129, 8, 1, [128, 3]), (1, 520, 4, 4, [0])])
-def test_prefill_tc_matches_oracle(gpu_lib, B, S, H, Hkv, offs):
+def test_prefill_tc_matches_oracle(gpu_lib, B, S, H, Hkv, offs, d):
     g = gpu_lib
     extra = max(offs)
-    c = W.make_prefill(B=B, S=S, H=H, Hkv=Hkv, dk=64, dv=64, seed=70 + S, S_kv=S + extra + 5, offsets=offs)
+    c = W.make_prefill(B=B, S=S, H=H, Hkv=Hkv, dk=d, dv=d, seed=70 + S + d, S_kv=S + extra + 5, offsets=offs)
     out = run(g, c)
     want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
     err = np.abs(out.float().cpu().numpy() - want).max()
@@ -52,10 +53,11 @@ def test_prefill_tc_full_size_config(gpu_lib):
     assert err <= 2e-2, err
 
 
-def test_prefill_tc_zero_keys_give_prefix_mean(gpu_lib):
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_tc_zero_keys_give_prefix_mean(gpu_lib, d):
     """K = 0: every visible key scores 0, so row i is the mean of V[0..=i]."""
     g = gpu_lib
-    c = W.make_prefill(B=1, S=300, H=4, Hkv=2, dk=64, dv=64, seed=71)
+    c = W.make_prefill(B=1, S=300, H=4, Hkv=2, dk=d, dv=d, seed=71)
     c.k.zero_()
     out = run(g, c)
     v = c.v.float()[0]                                       # [Hkv, S, d]
@@ -64,11 +66,24 @@ def test_prefill_tc_zero_keys_give_prefix_mean(gpu_lib):
     assert (out[0].float().cpu() - want).abs().max().item() <= 2e-2
 
 
-def test_prefill_tc_decode_step_is_last_row(gpu_lib):
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_tc_decode_step_is_last_row(gpu_lib, d):
     g = gpu_lib
-    c = W.make_prefill(B=1, S=640, H=8, Hkv=2, dk=64, dv=64, seed=72)
+    c = W.make_prefill(B=1, S=640, H=8, Hkv=2, dk=d, dv=d, seed=72)
     out = run(g, c)
-    dec = torch.empty(1, 8, 64, dtype=torch.bfloat16, device=DEV)
+    dec = torch.empty(1, 8, d, dtype=torch.bfloat16, device=DEV)
     g.attn_decode_contig(c.q[:, 639].contiguous().to(DEV), c.k.to(DEV), c.v.to(DEV),
                          torch.tensor([640], dtype=torch.int32, device=DEV), dec, c.scale)
     assert (dec.float() - out[:, 639].float()).abs().max().item() <= 2e-2
+
+
+def test_prefill_tc_d128_model_shape(gpu_lib):
+    """d = 128 at the decode configs' head shape (H=32, Hkv=8): two sequences, one
+    at an offset inside the second key tile; every output against the oracle."""
+    g = gpu_lib
+    offs = [0, 200]
+    c = W.make_prefill(B=2, S=1024, H=32, Hkv=8, dk=128, dv=128, seed=73, S_kv=1024 + 200, offsets=offs)
+    out = run(g, c)
+    want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
+    err = np.abs(out.float().cpu().numpy() - want).max()
+    assert err <= 2e-2, err
