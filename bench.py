@@ -380,14 +380,40 @@ def run_prefill(args, peaks, peak_kind):
                          "kernel": "prefill_tc_kernel", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
 
 
-def run_prefill_paged(args, peaks, peak_kind):
+def run_prefill_d128(args, peaks, peak_kind):
+    """Causal prefill at d = 128 (the decode configs' head shape) on the tcgen05
+    kernel: the kernel's event average over back-to-back launches."""
+    import causal_gqa_attention_row_gb300 as g
+    g.load()
+    dev = torch.device("cuda")
+    S, H, Hkv, d = 2048, 32, 8, 128
+    c = W.make_prefill(B=1, S=S, H=H, Hkv=Hkv, dk=d, dv=d, seed=7, device=dev)
+    out = torch.empty_like(c.q)
+    flops = 2.0 * H * (d + d) * S * (S + 1) / 2
+    st = torch.cuda.current_stream()
+    call = lambda k: g.attn_prefill_causal(c.q, c.k, c.v, out, c.scale)
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    n = 4 * max(args.steps, 20)
+    queue_ahead(n, us_per_group=60.0)
+    ms = timed(call, n, st, sync_first=False)
+    assert g.attn_get_device_error() == g.OK
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"workload": W.WORKLOADS["prefill_d128"], "tflops": tflops, "kernel_ms": ms, "flops": flops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "kernel": "prefill_tc_kernel<128>", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
+
+
+def run_prefill_paged(args, peaks, peak_kind, H=14, Hkv=2, d=64, key="prefill_paged"):
     """Chunked prefill against the paged pool on the tcgen05 kernel (each key
     tile gathered from the pool block by block)."""
     import causal_gqa_attention_row_gb300 as g
     g.load()
     dev = torch.device("cuda")
-    offs, S, H, d = (0, 2048, 4096, 6144), 2048, 14, 64
-    q, kp, vp, tables, off, scale = W.make_prefill_paged(offsets=offs, S=S, H=H, d=d, device=dev)
+    offs, S = (0, 2048, 4096, 6144), 2048
+    q, kp, vp, tables, off, scale = W.make_prefill_paged(offsets=offs, S=S, H=H, Hkv=Hkv, d=d, device=dev)
     out = torch.empty_like(q)
     # unmasked (query, key) pairs: row i of sequence b sees off_b + i + 1 keys
     flops = sum(2.0 * H * (d + d) * (S * o + S * (S + 1) / 2) for o in offs)
@@ -402,9 +428,13 @@ def run_prefill_paged(args, peaks, peak_kind):
     assert g.attn_get_device_error() == g.OK
     tflops = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    return {"workload": W.WORKLOADS["prefill_paged"], "tflops": tflops, "kernel_ms": ms, "flops": flops,
+    return {"workload": W.WORKLOADS[key], "tflops": tflops, "kernel_ms": ms, "flops": flops,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                         "kernel": "prefill_tc_kernel (paged)", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
+                         "kernel": f"prefill_tc_kernel<{d}> (paged)", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
+
+
+def run_prefill_paged_d128(args, peaks, peak_kind):
+    return run_prefill_paged(args, peaks, peak_kind, H=32, Hkv=8, d=128, key="prefill_paged_d128")
 
 
 def run_contig(args, peaks, peak_kind):
@@ -521,7 +551,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true", help="skip prefill, contig and mla")
-    ap.add_argument("--only", choices=["paged", "prefill", "prefill_paged", "contig", "mla"], default=None)
+    ap.add_argument("--only", choices=["paged", "prefill", "prefill_paged", "prefill_d128", "prefill_paged_d128",
+                                       "contig", "mla"], default=None)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world = dist_setup()
@@ -529,9 +560,10 @@ def main():
         reference_arm(args, rank, world)
         return
     peaks, peak_kind = measured_peaks()
-    if args.only in ("prefill", "prefill_paged", "contig", "mla"):
-        r = {"prefill": run_prefill, "prefill_paged": run_prefill_paged, "contig": run_contig,
-             "mla": run_mla}[args.only](args, peaks, peak_kind)
+    only = {"prefill": run_prefill, "prefill_paged": run_prefill_paged, "prefill_d128": run_prefill_d128,
+            "prefill_paged_d128": run_prefill_paged_d128, "contig": run_contig, "mla": run_mla}
+    if args.only in only:
+        r = only[args.only](args, peaks, peak_kind)
         if rank == 0:
             print(json.dumps(r), flush=True)
         return
@@ -540,6 +572,8 @@ def main():
     if not args.no_secondary and args.only is None:
         secondary = {"prefill": run_prefill(args, peaks, peak_kind),
                      "prefill_paged": run_prefill_paged(args, peaks, peak_kind),
+                     "prefill_d128": run_prefill_d128(args, peaks, peak_kind),
+                     "prefill_paged_d128": run_prefill_paged_d128(args, peaks, peak_kind),
                      "contig": run_contig(args, peaks, peak_kind), "mla": run_mla(args, peaks, peak_kind)}
     if res.get("arms"):
         arms = res["arms"]

@@ -161,13 +161,15 @@ def test_bad_table_entry_and_offset_are_flagged(gpu_lib, dtype):
     assert torch.all(out[1] == 0)
 
 
-def test_full_size_chunked_prefill_sampled_rows(gpu_lib):
-    """The chunked-prefill workload the bench times (4 sequences, 2048-row chunks at
-    offsets up to 6144, bs = 16): sampled rows -- first, last and seeded others of
-    each chunk, every head -- against the oracle, each row computed on its own
-    over the history gathered from the pool through the table."""
+@pytest.mark.parametrize("H,Hkv,d", [(14, 2, 64), (32, 8, 128)])
+def test_full_size_chunked_prefill_sampled_rows(gpu_lib, H, Hkv, d):
+    """The chunked-prefill workloads the bench times (4 sequences, 2048-row chunks
+    at offsets up to 6144, bs = 16; d = 64 at the prefill config's heads, d = 128
+    at the decode configs'): sampled rows -- first, last and seeded others of each
+    chunk, every head -- against the oracle, each row computed on its own over the
+    history gathered from the pool through the table."""
     g = gpu_lib
-    q, kp, vp, tables, off, scale = W.make_prefill_paged()
+    q, kp, vp, tables, off, scale = W.make_prefill_paged(H=H, Hkv=Hkv, d=d)
     B, S, H, d = q.shape
     bs = kp.shape[2]
     out = torch.empty(B, S, H, d, dtype=torch.bfloat16, device=DEV)
