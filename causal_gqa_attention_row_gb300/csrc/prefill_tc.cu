@@ -1,4 +1,5 @@
-// prefill_tc.cu -- causal prefill on the tcgen05 tensor cores (bf16, d_k = d_v = 64 or 128).
+// prefill_tc.cu -- causal prefill on the tcgen05 tensor cores (bf16; (d_k, d_v) = (64, 64),
+// (128, 128) or (192, 128)).
 //
 // The operation (kopitiam-runtime src/attention.rs, `attention_forward` and
 // `causal_mask`): row i of sequence b, query head h, sits at position
@@ -17,15 +18,15 @@
 //   warps 9, 10 one thread each issues the tcgen05.mma of one softmax warpgroup
 //               (warp 9 also allocates and frees TMEM)
 //   warp 11     TMA producer of the V tiles (four-stage ring)
-// Warpgroup w owns, in tensor memory (TMEM), S_w = Q K^T (M=128, N=128, K=d;
+// Warpgroup w owns, in tensor memory (TMEM), S_w = Q K^T (M=128, N=128, K=d_k;
 // 128 columns), P_w (the bf16 probabilities, two per 32-bit column; 64 columns)
-// and O_w += P_w V (M=128, N=d, K=128, A read from TMEM; d columns). At d = 64
-// the three are separate (S 2 x 128 + O 2 x 64 + P 2 x 64 = 512 columns); at
-// d = 128 P_w sits over the first 64 columns of S_w (S 2 x 128 + O 2 x 128),
-// so the MMA thread issues the next S into S_w only once the PV that reads P_w
-// is done. P never passes through shared memory, whose bandwidth is left to
-// the TMA tiles and the MMAs' reads of Q, K and V. A row of d elements is d / 64
-// blocks of 64 columns, each in the 128-byte swizzle (one TMA box each). The
+// and O_w += P_w V (M=128, N=d_v, K=128, A read from TMEM; d_v columns). At
+// d_v = 64 the three are separate (S 2 x 128 + O 2 x 64 + P 2 x 64 = 512
+// columns); at d_v = 128 P_w sits over the first 64 columns of S_w (S 2 x 128 +
+// O 2 x 128), so the MMA thread issues the next S into S_w only once the PV that
+// reads P_w is done. P never passes through shared memory, whose bandwidth is
+// left to the TMA tiles and the MMAs' reads of Q, K and V. A row of d elements
+// is d / 64 blocks of 64 columns, each in the 128-byte swizzle (one TMA box). The
 // softmax threads keep the row sum of exactly the bf16 p that multiply V, in
 // fp32. Thread t of a warpgroup owns query row t (TMEM lane t).
 //
@@ -72,26 +73,28 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr int kTabEntries = 4096;  // paged: the CTA's block-table entries
 constexpr int kMaxStages = 4;
 
-// Sizes and maps of the kernel for head width D (64 or 128).
-template <int D>
+// Sizes and maps of the kernel for head widths DK (Q, K) and DV (V, out).
+template <int DK, int DV>
 struct Cfg {
-  static constexpr int kCB = D / 64;         // 64-column blocks per row
-  static constexpr int kTile = kCB * kBlk;   // one Q, K or V tile (128 rows)
-  static constexpr bool kAlias = D > 64;     // P_w over the first 64 columns of S_w
+  static constexpr int kCBK = DK / 64, kCBV = DV / 64;  // 64-column blocks of a Q/K row, of a V/out row
+  static constexpr int kTileK = kCBK * kBlk;            // one Q or K tile (128 rows)
+  static constexpr int kTileV = kCBV * kBlk;            // one V or output tile
+  static constexpr bool kAlias = DV > 64;               // P_w over the first 64 columns of S_w
   // rings: stage s only ever holds key tiles of warpgroup s % 2
-  static constexpr int kStagesK = kAlias ? 2 : 4, kStagesV = kAlias ? 2 : 4;
+  static constexpr int kStagesK = DK > 64 ? 2 : 4, kStagesV = DK > 64 ? 2 : 4;
   static_assert(kStagesK % kWG == 0 && kStagesV % kWG == 0 && kStagesK <= kMaxStages && kStagesV <= kMaxStages,
                 "ring stages shared between warpgroups");
+  static_assert(DV <= DK, "the output tile is staged over Q");
   // TMEM columns of S_w, O_w and P_w
-  __host__ __device__ static constexpr uint32_t col_s(int w) { return kAlias ? 256 * w : 128 * w; }
-  __host__ __device__ static constexpr uint32_t col_o(int w) { return kAlias ? 256 * w + 128 : 256 + 64 * w; }
-  __host__ __device__ static constexpr uint32_t col_p(int w) { return kAlias ? 256 * w : 384 + 64 * w; }
-  static_assert(col_o(kWG - 1) + D <= kTmemCols && col_p(kWG - 1) + 64 <= kTmemCols, "TMEM map");
+  __host__ __device__ static constexpr uint32_t col_s(int w) { return kAlias ? (128 + DV) * w : 128 * w; }
+  __host__ __device__ static constexpr uint32_t col_o(int w) { return kAlias ? (128 + DV) * w + 128 : 256 + 64 * w; }
+  __host__ __device__ static constexpr uint32_t col_p(int w) { return kAlias ? (128 + DV) * w : 384 + 64 * w; }
+  static_assert(col_o(kWG - 1) + DV <= kTmemCols && col_p(kWG - 1) + 64 <= kTmemCols, "TMEM map");
   // shared-memory map (from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kTile;                              // K ring
-  static constexpr int kOffV = kOffK + kStagesK * kTile;           // V ring
-  static constexpr int kOffTab = kOffV + kStagesV * kTile;         // paged: block-table entries
+  static constexpr int kOffK = kTileK;                             // K ring
+  static constexpr int kOffV = kOffK + kStagesK * kTileK;          // V ring
+  static constexpr int kOffTab = kOffV + kStagesV * kTileV;        // paged: block-table entries
   static constexpr int kOffBar = kOffTab + kTabEntries * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;          // + alignment slack
   // At the end, once every MMA is done: the output tile over Q, and warpgroup
@@ -227,14 +230,13 @@ __device__ __forceinline__ int pool_block(const TcParams& p, int t, int kv_hi, i
 
 // One thread, the table read from global memory (the first tile, before the
 // CTA's shared copy of the table exists).
-template <int D>
+template <int NCB>
 __device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, unsigned char* dst, uint64_t* bar, int j, int kvh,
                                              int b, const TcParams& p, int kv_hi) {
-  using C = Cfg<D>;
-  mbar_arrive_expect_tx(bar, C::kTile);
+  mbar_arrive_expect_tx(bar, NCB * kBlk);
   if (!p.tables) {
 #pragma unroll
-    for (int cb = 0; cb < C::kCB; ++cb) tc::tma_load_4d(dst + cb * kBlk, tm, cb * 64, j * kBN, kvh, b, bar);
+    for (int cb = 0; cb < NCB; ++cb) tc::tma_load_4d(dst + cb * kBlk, tm, cb * 64, j * kBN, kvh, b, bar);
     return;
   }
   const int per = kBN / p.bs;
@@ -243,7 +245,7 @@ __device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, unsigned cha
     const int e = (t < p.mbps && t * p.bs < kv_hi) ? __ldg(p.tables + (size_t)b * p.mbps + t) : 0;
     const int blk = pool_block(p, t, kv_hi, e);
 #pragma unroll
-    for (int cb = 0; cb < C::kCB; ++cb)
+    for (int cb = 0; cb < NCB; ++cb)
       tc::tma_load_4d(dst + cb * kBlk + i * p.bs * 128, tm, cb * 64, 0, kvh, blk, bar);
   }
 }
@@ -252,19 +254,18 @@ __device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, unsigned cha
 // one box (each TMA instruction holds its thread for a few hundred cycles, so
 // the boxes of a tile go out side by side), the entries read from the CTA's
 // shared copy of its table row.
-template <int D>
+template <int NCB>
 __device__ __forceinline__ void load_kv_tile_warp(const CUtensorMap* tm, unsigned char* dst, uint64_t* bar, int j,
                                                   int kvh, int b, const TcParams& p, int kv_hi, const int* tab,
                                                   int lane) {
-  using C = Cfg<D>;
-  if (lane == 0) mbar_arrive_expect_tx(bar, C::kTile);
+  if (lane == 0) mbar_arrive_expect_tx(bar, NCB * kBlk);
   __syncwarp();
   if (!p.tables) {
-    if (lane < C::kCB) tc::tma_load_4d(dst + lane * kBlk, tm, lane * 64, j * kBN, kvh, b, bar);
+    if (lane < NCB) tc::tma_load_4d(dst + lane * kBlk, tm, lane * 64, j * kBN, kvh, b, bar);
   } else {
-    const int per = kBN / p.bs;  // per * kCB <= 32
-    if (lane < per * C::kCB) {
-      const int i = lane % per, cb = lane / per;
+    const int per = kBN / p.bs;  // per * NCB boxes: one lane each while they fit the warp
+    for (int x = lane; x < per * NCB; x += 32) {
+      const int i = x % per, cb = x / per;
       const int t = j * per + i;
       const int e = (t < p.mbps && t * p.bs < kv_hi) ? tab[t] : 0;  // the shared copy covers every such t
       tc::tma_load_4d(dst + cb * kBlk + i * p.bs * 128, tm, cb * 64, 0, kvh, pool_block(p, t, kv_hi, e), bar);
@@ -273,13 +274,13 @@ __device__ __forceinline__ void load_kv_tile_warp(const CUtensorMap* tm, unsigne
   __syncwarp();
 }
 
-template <int D>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                       const TcParams p) {
-  using C = Cfg<D>;
-  constexpr int kTile = C::kTile, kStagesK = C::kStagesK, kStagesV = C::kStagesV;
+  using C = Cfg<DK, DV>;
+  constexpr int kTileK = C::kTileK, kTileV = C::kTileV, kStagesK = C::kStagesK, kStagesV = C::kStagesV;
   constexpr int kOffQ = C::kOffQ, kOffK = C::kOffK, kOffV = C::kOffV, kOffTab = C::kOffTab;
   constexpr int kOffOut = C::kOffOut, kOffML = C::kOffML;
   extern __shared__ unsigned char smem_raw[];
@@ -320,13 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rest of the CTA sets up
     tc::prefetch_tmap(&tm_q);
     tc::prefetch_tmap(&tm_k);
-    mbar_arrive_expect_tx(&bars->q_full, kTile);
+    mbar_arrive_expect_tx(&bars->q_full, kTileK);
 #pragma unroll
-    for (int cb = 0; cb < C::kCB; ++cb) tc::tma_load_4d(smem + kOffQ + cb * kBlk, &tm_q, cb * 64, h, i0, b, &bars->q_full);
+    for (int cb = 0; cb < C::kCBK; ++cb)
+      tc::tma_load_4d(smem + kOffQ + cb * kBlk, &tm_q, cb * 64, h, i0, b, &bars->q_full);
     if (p.tables)  // the table entries of the tile wait for the offset, which bounds them
-      load_kv_tile<D>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, off + i0 + rows);
+      load_kv_tile<C::kCBK>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, off + i0 + rows);
     else
-      load_kv_tile<D>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, 0);
+      load_kv_tile<C::kCBK>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, 0);
   }
   if (warp == kMmaWarp0) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -339,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (off < 0 || (long long)off + p.S > p.S_kv) {  // the cache cannot hold these rows
     if (threadIdx.x == 0 && qt == p.n_qtiles - 1 && h == 0) raise_error(p.err, kErrBounds);
-    for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x)
-      p.out[(((size_t)b * p.S + i0 + idx / D) * p.H + h) * D + idx % D] = __float2bfloat16_rn(0.f);
+    for (int idx = threadIdx.x; idx < rows * DV; idx += blockDim.x)
+      p.out[(((size_t)b * p.S + i0 + idx / DV) * p.H + h) * DV + idx % DV] = __float2bfloat16_rn(0.f);
     // never exit with a load in flight
     if (warp == kProducerWarp && lane == 0 && !(mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0)))
       raise_error(p.err, kErrTimeout);
@@ -372,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = is_k ? bars->k_full : bars->v_full;
     uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
     unsigned char* ring = smem + (is_k ? kOffK : kOffV);
+    const int tile_bytes = is_k ? kTileK : kTileV;
     const int stages = is_k ? kStagesK : kStagesV;
     if (!is_k && lane == 0) tc::prefetch_tmap(tm);
     int issued_last[kStagesK];
@@ -389,7 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) w = wait_or_abort(&empty[st], ((j / stages) - 1) & 1, bars, p.err);
         if (!__shfl_sync(0xffffffffu, w, 0)) break;
       }
-      load_kv_tile_warp<D>(tm, ring + st * kTile, &full[st], j, kvh, b, p, kv_hi, tab, lane);
+      if (is_k)
+        load_kv_tile_warp<C::kCBK>(tm, ring + st * tile_bytes, &full[st], j, kvh, b, p, kv_hi, tab, lane);
+      else
+        load_kv_tile_warp<C::kCBV>(tm, ring + st * tile_bytes, &full[st], j, kvh, b, p, kv_hi, tab, lane);
       issued_last[st] = j;
     }
     if (lane == 0) {
@@ -405,23 +411,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int n_mine = (n_kv - w + 1) / 2;
       const uint32_t idS = tc::idesc_bf16_f32(kBM, kBN, false);
-      const uint32_t idO = tc::idesc_bf16_f32(kBM, D, true);
+      const uint32_t idO = tc::idesc_bf16_f32(kBM, DV, true);
       // descriptors: constant high part + (shared address >> 4) in the low bits
       constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);
       const uint64_t dQ = kHi | (smem_u32(smem + kOffQ) >> 4);
       const uint64_t dK0 = kHi | (smem_u32(smem + kOffK) >> 4);
       // V of each stage: MN-major, 8-key groups 1024 bytes apart, its 64-column
-      // blocks (D > 64) a block's 16 KiB apart (the leading byte offset)
-      const uint64_t dV0 = tc::desc_sw128_hi(C::kCB > 1 ? kBlk : 0, 1024) | (smem_u32(smem + kOffV) >> 4);
+      // blocks (d_v > 64) a block's 16 KiB apart (the leading byte offset)
+      const uint64_t dV0 = tc::desc_sw128_hi(C::kCBV > 1 ? kBlk : 0, 1024) | (smem_u32(smem + kOffV) >> 4);
       const uint32_t dS = tmem + C::col_s(w), dO = tmem + C::col_o(w), tP = tmem + C::col_p(w);
       auto issue_s = [&](int j) -> bool {  // S_w = Q K_j^T
         const int st = j % kStagesK;
         if (!wait_or_abort(&bars->k_full[st], (j / kStagesK) & 1, bars, p.err)) return false;
         tc::fence_after_sync();
-        const uint64_t dK = dK0 + (uint64_t)((st * kTile) >> 4);
-        // 16 of the D columns per instruction: block kk / 4, 32 bytes per step inside it
+        const uint64_t dK = dK0 + (uint64_t)((st * kTileK) >> 4);
+        // 16 of the d_k columns per instruction: block kk / 4, 32 bytes per step inside it
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DK / 16; ++kk) {
           const uint32_t at = (kk / 4) * kBlk + (kk % 4) * 32;
           tc::mma_f16_ss(dS, dQ + (at >> 4), dK + (at >> 4), idS, kk > 0);
         }
@@ -439,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_or_abort(&bars->v_full[st], (j / kStagesV) & 1, bars, p.err)) break;
         tc::fence_after_sync();
         // O_w += P_j V_j: 16 keys per instruction, P from TMEM (8 columns per 16 keys)
-        const uint64_t dV = dV0 + (uint64_t)((st * kTile) >> 4);
+        const uint64_t dV = dV0 + (uint64_t)((st * kTileV) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           tc::mma_f16_ts(dO, tP + kk * 8, dV + kk * (2048 >> 4), idO, (k > 0 || kk > 0));
@@ -532,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_after_sync();
           uint32_t o[32];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < DV / 32; ++c) {
             tc::tmem_ld_32x32b_x32(tO + c * 32, o);
             tc::tmem_ld_wait();
 #pragma unroll
@@ -584,14 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
     }
     const float l_sum = l_run;
-    float* ml = reinterpret_cast<float*>(smem + kOffML + wg * kTile);  // K stage wg: consumed by now
+    float* ml = reinterpret_cast<float*>(smem + kOffML + wg * kTileK);  // K stage wg: consumed by now
     ml[r] = have_o ? m_ref : -INFINITY;
     ml[kBM + r] = have_o ? l_sum : 0.f;  // l = 0: no visible key, or no tile at all
     tc::fence_before_sync();
     named_bar_sync(1, kWG * 128);
     tc::fence_after_sync();
     const float* ml0 = reinterpret_cast<const float*>(smem + kOffML);
-    const float* ml1 = reinterpret_cast<const float*>(smem + kOffML + kTile);
+    const float* ml1 = reinterpret_cast<const float*>(smem + kOffML + kTileK);
     const float m0 = ml0[r], l0 = ml0[kBM + r], m1 = ml1[r], l1 = ml1[kBM + r];
     const bool use0 = l0 > 0.f, use1 = l1 > 0.f;
     const float M = fmaxf(use0 ? m0 : -INFINITY, use1 ? m1 : -INFINITY);
@@ -600,14 +606,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float l = a0 * l0 + a1 * l1;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float c0 = a0 * inv, c1 = a1 * inv;
-    // this warpgroup's D / 2 of the D columns, 32 at a time; O_1 exists once
+    // this warpgroup's d_v / 2 of the d_v columns, 32 at a time; O_1 exists once
     // warpgroup 1 had a tile. The output tile goes over Q (every S MMA, the
     // readers of Q, is done), in the 128-byte swizzle of the output's tensor map:
     // column c of row r in block c / 64, 16-byte chunk (c % 64) / 8 XOR r % 8.
     unsigned char* so = smem + kOffOut;
 #pragma unroll
-    for (int cc = 0; cc < D / 64; ++cc) {
-      const int col0 = wg * (D / 2) + cc * 32;
+    for (int cc = 0; cc < DV / 64; ++cc) {
+      const int col0 = wg * (DV / 2) + cc * 32;
       uint32_t o0[32], o1[32];
       tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::col_o(0) + col0, o0);
       if (n_kv > 1) tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::col_o(1) + col0, o1);
@@ -636,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
       // rows past the end of the sequence fall outside the tensor and are not written
 #pragma unroll
-      for (int cb = 0; cb < C::kCB; ++cb) tc::tma_store_4d(&tm_o, so + cb * kBlk, cb * 64, h, i0, b);
+      for (int cb = 0; cb < C::kCBV; ++cb) tc::tma_store_4d(&tm_o, so + cb * kBlk, cb * 64, h, i0, b);
       tc::bulk_commit_group();
       tc::bulk_wait_group_read0();  // shared memory stays valid until the store has read it
     }
@@ -677,10 +683,10 @@ bool make_map(CUtensorMap* m, const void* base, int d, uint64_t d1, uint64_t d2,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int DK, int DV>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                      const TcParams& p, cudaStream_t st) {
-  using C = Cfg<D>;
+  using C = Cfg<DK, DV>;
   int dev = 0;
   cudaGetDevice(&dev);
   static unsigned long long attr_done = 0;
@@ -689,26 +695,27 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     // thread at launch; with any other allocation it could wait forever, so
     // such a build is refused here instead of launched.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<DK, DV>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs) return cudaErrorNotSupported;
-    e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_tc_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << dev;
   }
   const long long ctas = (long long)p.B * p.H * p.n_qtiles;
   if (ctas <= 0) return cudaSuccess;
-  prefill_tc_kernel<D><<<(unsigned)ctas, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, p);
+  prefill_tc_kernel<DK, DV><<<(unsigned)ctas, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool prefill_tc_supported(int bf16, int dk, int dv, int bs, int mbps) {
-  // d_k = d_v = 64 or 128; paged: a pool block is a whole number of 8-row
-  // swizzle atoms and divides a 128-key tile, and a table row fits the CTA's
-  // shared copy
-  return bf16 == 1 && dk == dv && (dk == 64 || dk == 128) &&
+  // (d_k, d_v) = (64, 64), (128, 128) or (192, 128); paged: a pool block is a
+  // whole number of 8-row swizzle atoms and divides a 128-key tile, and a table
+  // row fits the CTA's shared copy
+  const bool widths = (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128);
+  return bf16 == 1 && widths &&
          (bs == 0 || (bs % 8 == 0 && kBN % bs == 0 && mbps > 0 && mbps <= kTabEntries));
 }
 
@@ -717,21 +724,20 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
                               unsigned* err, cudaStream_t st, const int32_t* tables, int mbps, int bs,
                               int num_blocks) {
   if (!prefill_tc_supported(1, dk, dv, tables ? bs : 0, mbps) || !(qscale > 0.f)) return cudaErrorNotSupported;
-  const int d = dk;
   CUtensorMap tq, tk, tv, to;
-  // q [B, S, H, d]: dims (d, H, S, B), box (64, 1, 128, 1)
-  if (!make_map(&tq, q, d, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
+  // q [B, S, H, d_k]: dims (d_k, H, S, B), box (64, 1, 128, 1)
+  if (!make_map(&tq, q, dk, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
   if (tables) {
     // pools [num_blocks, Hkv, bs, d]: dims (d, bs, Hkv, num_blocks), box (64, bs, 1, 1)
-    if (!make_map(&tk, k, d, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
-    if (!make_map(&tv, v, d, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
+    if (!make_map(&tk, k, dk, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
+    if (!make_map(&tv, v, dv, bs, Hkv, num_blocks, bs, 1)) return cudaErrorInvalidValue;
   } else {
     // k, v [B, Hkv, S_kv, d]: dims (d, S_kv, Hkv, B), box (64, 128, 1, 1)
-    if (!make_map(&tk, k, d, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
-    if (!make_map(&tv, v, d, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
+    if (!make_map(&tk, k, dk, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
+    if (!make_map(&tv, v, dv, seq_kv_max, Hkv, B, kBN, 1)) return cudaErrorInvalidValue;
   }
-  // out [B, S, H, d]: as q
-  if (!make_map(&to, out, d, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
+  // out [B, S, H, d_v]: dims (d_v, H, S, B), box (64, 1, 128, 1)
+  if (!make_map(&to, out, dv, H, seq_q, B, 1, kBM)) return cudaErrorInvalidValue;
   TcParams p;
   p.B = B;
   p.S = seq_q;
@@ -748,7 +754,9 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
   p.out = static_cast<__nv_bfloat16*>(out);
   p.qscale = qscale;
   p.err = err;
-  return d == 64 ? launch_d<64>(tq, tk, tv, to, p, st) : launch_d<128>(tq, tk, tv, to, p, st);
+  if (dk == 64) return launch_d<64, 64>(tq, tk, tv, to, p, st);
+  if (dk == 128) return launch_d<128, 128>(tq, tk, tv, to, p, st);
+  return launch_d<192, 128>(tq, tk, tv, to, p, st);
 }
 
 }  // namespace gqa

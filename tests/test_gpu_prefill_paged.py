@@ -190,3 +190,18 @@ def test_full_size_chunked_prefill_sampled_rows(gpu_lib, H, Hkv, d):
                                        W.to_oracle(v_hist), [o + i + 1], scale)
             worst = max(worst, err(out[b:b + 1, i:i + 1], want))
     assert worst <= 2e-2, worst
+
+
+@pytest.mark.parametrize("dk,dv,bs", [(128, 128, 16), (192, 128, 8), (192, 128, 32)])
+def test_tensor_core_paged_wide_heads_equal_contig_bits(gpu_lib, dk, dv, bs):
+    """d = 128 and the MLA widths (d_k = 192, d_v = 128) on the tensor cores: a
+    key tile is several 64-column blocks per pool block (bs = 8 with d_k = 192
+    needs more boxes than a warp has lanes)."""
+    g = gpu_lib
+    offs = [0, 260]
+    S = 150
+    c = W.make_prefill(B=2, S=S, H=8, Hkv=2, dk=dk, dv=dv, seed=185 + dk + bs, S_kv=S + max(offs) + 3,
+                       offsets=offs)
+    out_p, out_c = run_both(g, c, bs)
+    assert torch.equal(out_p, out_c)
+    assert err(out_p, oracle(c)) <= TOL[torch.bfloat16]

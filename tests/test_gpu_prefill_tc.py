@@ -87,3 +87,15 @@ def test_prefill_tc_d128_model_shape(gpu_lib):
     want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
     err = np.abs(out.float().cpu().numpy() - want).max()
     assert err <= 2e-2, err
+
+
+@pytest.mark.parametrize("B,S,H,Hkv,offs", [(1, 90, 4, 4, [0]), (2, 300, 8, 8, [0, 140]), (1, 257, 6, 2, [5])])
+def test_prefill_tc_mla_shape(gpu_lib, B, S, H, Hkv, offs):
+    """The MLA shape on the tensor cores: d_k = 192 (Q and K rows of three 64-column
+    blocks), d_v = 128; group size 1 as in the pages' MLA and a grouped case."""
+    g = gpu_lib
+    c = W.make_prefill(B=B, S=S, H=H, Hkv=Hkv, dk=192, dv=128, seed=75 + S, S_kv=S + max(offs) + 2, offsets=offs)
+    out = run(g, c)
+    want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
+    err = np.abs(out.float().cpu().numpy() - want).max()
+    assert err <= 2e-2, err
