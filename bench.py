@@ -380,16 +380,17 @@ def run_prefill(args, peaks, peak_kind):
                          "kernel": "prefill_tc_kernel", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
 
 
-def run_prefill_d128(args, peaks, peak_kind):
-    """Causal prefill at d = 128 (the decode configs' head shape) on the tcgen05
-    kernel: the kernel's event average over back-to-back launches."""
+def run_prefill_d128(args, peaks, peak_kind, H=32, Hkv=8, dk=128, dv=128, key="prefill_d128"):
+    """Causal prefill at d = 128 (the decode configs' head shape), or at the MLA
+    widths, on the tcgen05 kernel: the kernel's event average over back-to-back
+    launches."""
     import causal_gqa_attention_row_gb300 as g
     g.load()
     dev = torch.device("cuda")
-    S, H, Hkv, d = 2048, 32, 8, 128
-    c = W.make_prefill(B=1, S=S, H=H, Hkv=Hkv, dk=d, dv=d, seed=7, device=dev)
-    out = torch.empty_like(c.q)
-    flops = 2.0 * H * (d + d) * S * (S + 1) / 2
+    S = 2048
+    c = W.make_prefill(B=1, S=S, H=H, Hkv=Hkv, dk=dk, dv=dv, seed=7, device=dev)
+    out = torch.empty(1, S, H, dv, dtype=torch.bfloat16, device=dev)
+    flops = 2.0 * H * (dk + dv) * S * (S + 1) / 2
     st = torch.cuda.current_stream()
     call = lambda k: g.attn_prefill_causal(c.q, c.k, c.v, out, c.scale)
     for i in range(3):
@@ -401,9 +402,13 @@ def run_prefill_d128(args, peaks, peak_kind):
     assert g.attn_get_device_error() == g.OK
     tflops = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    return {"workload": W.WORKLOADS["prefill_d128"], "tflops": tflops, "kernel_ms": ms, "flops": flops,
+    return {"workload": W.WORKLOADS[key], "tflops": tflops, "kernel_ms": ms, "flops": flops,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                         "kernel": "prefill_tc_kernel<128>", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
+                         "kernel": f"prefill_tc_kernel<{dk}, {dv}>", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
+
+
+def run_prefill_mla(args, peaks, peak_kind):
+    return run_prefill_d128(args, peaks, peak_kind, H=32, Hkv=32, dk=192, dv=128, key="prefill_mla")
 
 
 def run_prefill_paged(args, peaks, peak_kind, H=14, Hkv=2, d=64, key="prefill_paged"):
@@ -552,7 +557,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true", help="skip prefill, contig and mla")
     ap.add_argument("--only", choices=["paged", "prefill", "prefill_paged", "prefill_d128", "prefill_paged_d128",
-                                       "contig", "mla"], default=None)
+                                       "prefill_mla", "contig", "mla"], default=None)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world = dist_setup()
@@ -561,7 +566,8 @@ def main():
         return
     peaks, peak_kind = measured_peaks()
     only = {"prefill": run_prefill, "prefill_paged": run_prefill_paged, "prefill_d128": run_prefill_d128,
-            "prefill_paged_d128": run_prefill_paged_d128, "contig": run_contig, "mla": run_mla}
+            "prefill_paged_d128": run_prefill_paged_d128, "prefill_mla": run_prefill_mla, "contig": run_contig,
+            "mla": run_mla}
     if args.only in only:
         r = only[args.only](args, peaks, peak_kind)
         if rank == 0:
@@ -574,6 +580,7 @@ def main():
                      "prefill_paged": run_prefill_paged(args, peaks, peak_kind),
                      "prefill_d128": run_prefill_d128(args, peaks, peak_kind),
                      "prefill_paged_d128": run_prefill_paged_d128(args, peaks, peak_kind),
+                     "prefill_mla": run_prefill_mla(args, peaks, peak_kind),
                      "contig": run_contig(args, peaks, peak_kind), "mla": run_mla(args, peaks, peak_kind)}
     if res.get("arms"):
         arms = res["arms"]

@@ -66,8 +66,9 @@ typedef enum { GQA_F32 = 0, GQA_BF16 = 1 } gqa_dtype;
  *   out  [B, seq_q, H, d_v]
  * Row i of sequence b sees keys 0..=position_offset[b] + i; it requires
  * position_offset[b] + seq_q <= seq_kv_max (checked on the device).
- * bf16 with d_k == d_v == 64 or 128 runs on the tcgen05 tensor-core kernel;
- * every other shape and f32 run on the SIMT kernel. No workspace.
+ * bf16 with (d_k, d_v) = (64, 64), (128, 128) or (192, 128) runs on the tcgen05
+ * tensor-core kernel; every other shape and f32 run on the SIMT kernel. No
+ * workspace.
  */
 gqa_status attn_prefill_causal(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
                                int seq_kv_max, const int32_t* position_offset, int H, int Hkv, int d_k,
@@ -184,8 +185,9 @@ gqa_status attn_prefill_causal_ex(const void* q, const void* k, const void* v, v
  *   position_offset  int32 [B] on the device, or NULL for all zeros; requires
  *                 position_offset[b] + seq_q <= max_blocks_per_seq * block_size
  *                 (checked on the device)
- * bf16 with d_k == d_v == 64 or 128, block_size a multiple of 8 dividing 128,
- * max_blocks_per_seq <= 4096 and no arm runs on the tcgen05 tensor-core kernel
+ * bf16 with (d_k, d_v) = (64, 64), (128, 128) or (192, 128), block_size a
+ * multiple of 8 dividing 128, max_blocks_per_seq <= 4096 and no arm runs on the
+ * tcgen05 tensor-core kernel
  * (each 128-key tile gathered block by block with TMA); every other case on the
  * SIMT kernel. No workspace.
  * GQA_ERR_INVALID_ARG also for seq_q > max_blocks_per_seq * block_size.

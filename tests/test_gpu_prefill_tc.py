@@ -99,3 +99,22 @@ def test_prefill_tc_mla_shape(gpu_lib, B, S, H, Hkv, offs):
     want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
     err = np.abs(out.float().cpu().numpy() - want).max()
     assert err <= 2e-2, err
+
+
+@pytest.mark.parametrize("H,Hkv,dk,dv", [(32, 8, 128, 128), (32, 32, 192, 128)])
+def test_prefill_tc_full_size_wide_heads_sampled_rows(gpu_lib, H, Hkv, dk, dv):
+    """The d = 128 and MLA-shaped prefill workloads the bench times (2048 rows):
+    sampled rows -- first, last and seeded others, every head -- against the
+    oracle, each row computed on its own as a one-row chunk at its position."""
+    g = gpu_lib
+    S = 2048
+    c = W.make_prefill(B=1, S=S, H=H, Hkv=Hkv, dk=dk, dv=dv, seed=7)
+    out = run(g, c).cpu()
+    rng = np.random.default_rng(76)
+    worst = 0.0
+    for i in sorted({0, 127, 128, S - 1, *rng.integers(0, S, 4).tolist()}):
+        want = core.prefill_causal(W.to_oracle(c.q[:, i:i + 1].contiguous()),
+                                   W.to_oracle(c.k[:, :, :i + 1].contiguous()),
+                                   W.to_oracle(c.v[:, :, :i + 1].contiguous()), c.scale, offsets=[i])
+        worst = max(worst, np.abs(out[:, i:i + 1].float().numpy() - want).max())
+    assert worst <= 2e-2, worst

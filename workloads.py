@@ -171,6 +171,7 @@ WORKLOADS = {
     "prefill_paged": ("chunked prefill bf16 on the paged pool: 4 seqs, H=14, Hkv=2, d=64, bs=16, a 2048-row "
                       "chunk at offsets 0/2048/4096/6144 (history already in the pool)"),
     "prefill_d128": "causal prefill bf16 at the decode configs' head shape: B=1, H=32, Hkv=8, d=128, S=2048",
+    "prefill_mla": "MLA-shaped causal prefill bf16: B=1, H=32, group 1, d_k=192 (128 + 64 rot), d_v=128, S=2048",
     "prefill_paged_d128": ("chunked prefill bf16 on the paged pool at the decode configs' head shape: 4 seqs, "
                            "H=32, Hkv=8, d=128, bs=16, a 2048-row chunk at offsets 0/2048/4096/6144"),
 }
