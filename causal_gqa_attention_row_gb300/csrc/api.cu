@@ -344,7 +344,7 @@ gqa_status attn_rope_interleaved(void* x, const int32_t* positions, int B, int T
       (heads_outer != 0 && heads_outer != 1))
     return GQA_ERR_INVALID_ARG;
   if (B == 0 || T == 0) return GQA_OK;
-  if (!x || !positions) return GQA_ERR_INVALID_ARG;
+  if (!x || !positions || !aligned16(x)) return GQA_ERR_INVALID_ARG;
   return from_cuda(gqa::launch_rope(x, positions, B, T, heads, d, heads_outer, rot_offset, rot_dim, theta, bf16,
                                     static_cast<cudaStream_t>(stream)));
 }

@@ -229,41 +229,68 @@ __device__ __forceinline__ void rotate_pair(ET* x, float c, float s) {
   x[1] = Elem<ET>::from_f32(fmaf(x0, s, x1 * c));
 }
 
+// A pair (x[2t], x[2t+1]) as one 4-byte (bf16) or 8-byte (f32) access: the
+// element offset of a pair is even and tensors are 16-byte aligned.
+template <typename ET>
+struct Pair;
+template <>
+struct Pair<__nv_bfloat16> {
+  static __device__ __forceinline__ float2 load(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+  }
+};
+template <>
+struct Pair<float> {
+  static __device__ __forceinline__ float2 load(const float* p) { return *reinterpret_cast<const float2*>(p); }
+  static __device__ __forceinline__ void store(float* p, float a, float b) {
+    *reinterpret_cast<float2*>(p) = make_float2(a, b);
+  }
+};
+
 // One thread per (token, pair): the angle once, then the pair of every head,
-// eight heads' loads in flight at a time.
-constexpr int kRopeHeadsInFlight = 8;
+// sixteen heads' loads in flight at a time (all of them for up to 16 heads),
+// so that a thread waits on memory once per sixteen heads.
+constexpr int kRopeHeadsInFlight = 16;
 
 template <typename ET>
-__global__ void __launch_bounds__(256) rope_kernel(ET* x, const int32_t* positions, int B, int T, int heads, int d,
+__global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positions, int B, int T, int heads, int d,
                                                    int heads_outer, int rot_offset, int rot_dim, const RopeFreqs fr) {
   const int npairs = rot_dim / 2;
+  // The frequencies into shared memory first: read from the parameter space at
+  // a different index in every lane, each warp's load would be serialised.
+  __shared__ double w_s[128];
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) w_s[i] = fr.w[i];
+  __syncthreads();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)B * T * npairs) return;
   const int pr = (int)(idx % npairs);
   const long long tok = idx / npairs;  // b * T + t
   const int b = (int)(tok / T), t = (int)(tok % T);
+  const int pos = positions[tok];
+  // head h's pair at p0 + h * hstride ([B, T, heads, d] or, heads outer, [B, heads, T, d])
+  const size_t hstride = heads_outer ? (size_t)T * d : (size_t)d;
+  ET* p0 = x + (heads_outer ? ((size_t)b * heads * T + t) : (size_t)tok * heads) * d + rot_offset + 2 * pr;
+  // the first heads' pairs are requested before the angle waits on the position
+  float2 xv[kRopeHeadsInFlight];
+#pragma unroll
+  for (int u = 0; u < kRopeHeadsInFlight; ++u)
+    if (u < heads) xv[u] = Pair<ET>::load(p0 + (size_t)u * hstride);
   float c, s;
-  rope_cos_sin((double)positions[tok], fr.w[pr], &c, &s);
+  rope_cos_sin((double)pos, w_s[pr], &c, &s);
   for (int h0 = 0; h0 < heads; h0 += kRopeHeadsInFlight) {
-    ET* px[kRopeHeadsInFlight];
-    float x0[kRopeHeadsInFlight], x1[kRopeHeadsInFlight];
+    if (h0 > 0) {
 #pragma unroll
-    for (int u = 0; u < kRopeHeadsInFlight; ++u) {
-      const int h = h0 + u;
-      if (h < heads) {
-        const size_t row = heads_outer ? (((size_t)b * heads + h) * T + t) : ((size_t)tok * heads + h);
-        px[u] = x + row * d + rot_offset + 2 * pr;
-        x0[u] = Elem<ET>::to_f32(px[u][0]);
-        x1[u] = Elem<ET>::to_f32(px[u][1]);
-      }
+      for (int u = 0; u < kRopeHeadsInFlight; ++u)
+        if (h0 + u < heads) xv[u] = Pair<ET>::load(p0 + (size_t)(h0 + u) * hstride);
     }
 #pragma unroll
-    for (int u = 0; u < kRopeHeadsInFlight; ++u) {
-      if (h0 + u < heads) {
-        px[u][0] = Elem<ET>::from_f32(fmaf(x0[u], c, -x1[u] * s));
-        px[u][1] = Elem<ET>::from_f32(fmaf(x0[u], s, x1[u] * c));
-      }
-    }
+    for (int u = 0; u < kRopeHeadsInFlight; ++u)
+      if (h0 + u < heads)
+        Pair<ET>::store(p0 + (size_t)(h0 + u) * hstride, fmaf(xv[u].x, c, -xv[u].y * s),
+                        fmaf(xv[u].x, s, xv[u].y * c));
   }
 }
 
@@ -272,13 +299,13 @@ cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int hea
   const long long total = (long long)B * T * (rot_dim / 2);
   if (total <= 0 || heads <= 0) return cudaSuccess;
   if (rot_dim > 256) return cudaErrorNotSupported;
-  const unsigned blocks = (unsigned)((total + 255) / 256);
+  const unsigned blocks = (unsigned)((total + 127) / 128);
   const RopeFreqs fr = rope_freqs(rot_dim, theta);
   if (bf16)
-    rope_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(x), positions, B, T, heads,
+    rope_kernel<__nv_bfloat16><<<blocks, 128, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(x), positions, B, T, heads,
                                                         d, heads_outer, rot_offset, rot_dim, fr);
   else
-    rope_kernel<float><<<blocks, 256, 0, st>>>(reinterpret_cast<float*>(x), positions, B, T, heads, d, heads_outer,
+    rope_kernel<float><<<blocks, 128, 0, st>>>(reinterpret_cast<float*>(x), positions, B, T, heads, d, heads_outer,
                                                rot_offset, rot_dim, fr);
   return cudaGetLastError();
 }
