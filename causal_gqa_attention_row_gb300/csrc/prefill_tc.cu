@@ -13,11 +13,11 @@
 //   warps 0-3   softmax warpgroup 0: key tiles 0, 2, 4, ...
 //   warps 4-7   softmax warpgroup 1: key tiles 1, 3, 5, ...
 //   warp 8      initialises the barriers; TMA producer of Q (once) and of the
-//               128-key K tiles (four-stage ring; 128-byte swizzle, the layout
-//               the MMA reads)
+//               128-key K tiles (a four-stage ring at d_k = 64, two-stage for
+//               wider heads; 128-byte swizzle, the layout the MMA reads)
 //   warps 9, 10 one thread each issues the tcgen05.mma of one softmax warpgroup
 //               (warp 9 also allocates and frees TMEM)
-//   warp 11     TMA producer of the V tiles (four-stage ring)
+//   warp 11     TMA producer of the V tiles (ring as for K)
 // Warpgroup w owns, in tensor memory (TMEM), S_w = Q K^T (M=128, N=128, K=d_k;
 // 128 columns), P_w (the bf16 probabilities, two per 32-bit column; 64 columns)
 // and O_w += P_w V (M=128, N=d_v, K=128, A read from TMEM; d_v columns). At
@@ -34,11 +34,11 @@
 // into registers and release S_w at once, so the MMA thread issues S_{j+2}
 // while the exponentials of tile j are still being computed; P_j is built in
 // registers and stored into P_w once PV_{j-2} (issued a whole tile earlier) has
-// read the previous one (at d = 128, once S_w holds S_j that PV is done). K and
-// V have rings of their own: a K stage is free as soon as its S MMA is done, a
-// V stage once its PV is. At d = 64 they run four tiles ahead, so the load of
-// K_{j+4} has a whole tile-period before S_{j+4} needs it; at d = 128 (tiles
-// twice the size) two, which the later issue of S leaves enough.
+// read the previous one (at d_v = 128, once S_w holds S_j that PV is done). K
+// and V have rings of their own: a K stage is free as soon as its S MMA is done,
+// a V stage once its PV is. At d_k = 64 they run four tiles ahead, so the load of
+// K_{j+4} has a whole tile-period before S_{j+4} needs it; for wider heads (tiles
+// two or three times the size) two, which the later issue of S leaves enough.
 //
 // Softmax with lazy rescaling: p = 2^((s - m) * scale * log2 e) against a
 // reference max m that only moves when a score exceeds it by more than 2^8 in
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = n_mine > 0 && wait_or_abort(&bars->q_full, 0, bars, p.err) && issue_s(w);
       for (int k = 0; ok && k < n_mine; ++k) {
         const int j = 2 * k + w;
-        // d = 64: S_{j+2} as soon as the softmax threads have read S_j into registers
+        // d_v = 64: S_{j+2} as soon as the softmax threads have read S_j into registers
         if (!C::kAlias && k + 1 < n_mine) ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
         if (!ok || !wait_or_abort(&bars->p_full[w], k & 1, bars, p.err)) break;
         const int st = j % kStagesV;
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_f16_ts(dO, tP + kk * 8, dV + kk * (2048 >> 4), idO, (k > 0 || kk > 0));
         tc::mma_commit(&bars->o_done[w]);
         tc::mma_commit(&bars->v_empty[st]);
-        // d = 128: P_j sits in S_w, so S_{j+2} waits for PV_j (this thread waits
+        // d_v = 128: P_j sits in S_w, so S_{j+2} waits for PV_j (this thread waits
         // every phase of o_done[w] in order)
         if (C::kAlias && k + 1 < n_mine) {
           ok = wait_or_abort(&bars->o_done[w], k & 1, bars, p.err);
@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_ref = mx;
           }
           // O_w holds every PV issued so far (PV_{k-1} the last): rescale it once
-          // done (at d = 128 it is: S_k was issued after it)
+          // done (at d_v = 128 it is: S_k was issued after it)
           if (!C::kAlias && !warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
             alive = false;
             break;
@@ -564,10 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           add_bf16x2(ls[(t & 3) * 2], ls[(t & 3) * 2 + 1], pv[c][t]);
         }
       l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // ---- d = 64: P_w is free once PV_{k-1} has read it. Every phase of
+      // ---- d_v = 64: P_w is free once PV_{k-1} has read it. Every phase of
       // o_done[w] is waited for in order, before the next PV can be issued, so the
       // barrier is never two phases ahead of this wait (nor of the rescale's or the
-      // final one). d = 128: P goes over S_k's own first columns, already read.
+      // final one). d_v = 128: P goes over S_k's own first columns, already read.
       if (!C::kAlias && k >= 1) {
         if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
           alive = false;
