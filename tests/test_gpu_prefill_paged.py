@@ -137,19 +137,21 @@ def test_decode_step_is_a_one_row_chunk(gpu_lib):
     assert (out_p[:, 0].float() - out_d.float()).abs().max().item() <= 2e-2
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_bad_table_entry_and_offset_are_flagged(gpu_lib, dtype):
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 64, 64), (torch.float32, 64, 64),
+                                         (torch.bfloat16, 128, 128), (torch.bfloat16, 192, 128)])
+def test_bad_table_entry_and_offset_are_flagged(gpu_lib, dtype, dk, dv):
     """An out-of-range entry in a block the rows read is skipped and reported; so
     is an offset that puts the chunk past the table's capacity (whose rows are
-    written as zeros). Nothing is read out of range."""
+    written as zeros). Nothing is read out of range. Both kernels, every
+    tensor-core width."""
     g = gpu_lib
     offs = [0, 150]
     S = 100
-    c = W.make_prefill(B=2, S=S, H=4, Hkv=2, dk=64, dv=64, dtype=dtype, seed=180, S_kv=S + 150, offsets=offs)
+    c = W.make_prefill(B=2, S=S, H=4, Hkv=2, dk=dk, dv=dv, dtype=dtype, seed=180, S_kv=S + 150, offsets=offs)
     kp, vp, tables = page(c, 16, seed=181)
     bad = tables.clone()
     bad[1, 2] = kp.shape[0]  # one past the pool
-    out = torch.empty(2, S, 4, 64, dtype=dtype, device=DEV)
+    out = torch.empty(2, S, 4, dv, dtype=dtype, device=DEV)
     g.attn_prefill_paged(c.q.to(DEV), kp.to(DEV), vp.to(DEV), bad.to(DEV), out, c.scale,
                          position_offset=c.offsets.to(DEV))
     assert g.attn_get_device_error() == g.ERR_DEVICE_BOUNDS
@@ -192,7 +194,7 @@ def test_full_size_chunked_prefill_sampled_rows(gpu_lib, H, Hkv, d):
     assert worst <= 2e-2, worst
 
 
-@pytest.mark.parametrize("dk,dv,bs", [(128, 128, 16), (192, 128, 8), (192, 128, 32)])
+@pytest.mark.parametrize("dk,dv,bs", [(128, 128, 16), (128, 128, 8), (192, 128, 8), (192, 128, 32)])
 def test_tensor_core_paged_wide_heads_equal_contig_bits(gpu_lib, dk, dv, bs):
     """d = 128 and the MLA widths (d_k = 192, d_v = 128) on the tensor cores: a
     key tile is several 64-column blocks per pool block (bs = 8 with d_k = 192

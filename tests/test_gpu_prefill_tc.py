@@ -118,3 +118,17 @@ def test_prefill_tc_full_size_wide_heads_sampled_rows(gpu_lib, H, Hkv, dk, dv):
                                    W.to_oracle(c.v[:, :, :i + 1].contiguous()), c.scale, offsets=[i])
         worst = max(worst, np.abs(out[:, i:i + 1].float().numpy() - want).max())
     assert worst <= 2e-2, worst
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (192, 128)])
+def test_prefill_tc_wide_zero_keys_give_prefix_mean(gpu_lib, dk, dv):
+    """K = 0 at the wide head shapes: every visible key scores 0, so row i is the
+    mean of V[0..=i] (a closed form independent of the oracle)."""
+    g = gpu_lib
+    c = W.make_prefill(B=1, S=200, H=4, Hkv=2, dk=dk, dv=dv, seed=77)
+    c.k.zero_()
+    out = run(g, c)
+    v = c.v.float()[0]                                       # [Hkv, S, dv]
+    mean = torch.cumsum(v, dim=1) / torch.arange(1, 201)[None, :, None]
+    want = mean.repeat_interleave(2, dim=0).permute(1, 0, 2)  # [S, H, dv]
+    assert (out[0].float().cpu() - want).abs().max().item() <= 2e-2
