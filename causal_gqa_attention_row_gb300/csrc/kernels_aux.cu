@@ -161,21 +161,37 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
     for (int d = lane; d < DV; d += 32) out[d] = Elem<ET>::from_f32(0.f);
     return;
   }
-  float den = p.sinks ? exp2f(z2 - M) : 0.f;
-  for (int s = s_lo; s < n; ++s) {
-    const float ms = P[(size_t)s * stride];
-    const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-    den = fmaf(w, P[(size_t)s * stride + 1], den);
-  }
-  for (int d = lane; d < DV; d += 32) {
-    float acc = 0.f;
-    for (int s = s_lo; s < n; ++s) {
+  // Each split's weight once (lane s % 32 holds split s's), the weighted row sums
+  // reduced in a fixed butterfly order; every lane then walks the splits in order,
+  // the weight broadcast, its output columns d = lane + 32 e read as coalesced rows.
+  constexpr int kMaxE = 8;  // DV <= 256
+  float acc[kMaxE];
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e) acc[e] = 0.f;
+  float den_part = 0.f;
+  for (int s0 = s_lo; s0 < n; s0 += 32) {
+    const int s = s0 + lane;
+    float w = 0.f;
+    if (s < n) {
       const float ms = P[(size_t)s * stride];
-      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      acc = fmaf(w, P[(size_t)s * stride + 2 + d], acc);
+      w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      den_part = fmaf(w, P[(size_t)s * stride + 1], den_part);
     }
-    out[d] = Elem<ET>::from_f32(den > 0.f ? acc / den : 0.f);
+    const int cnt = min(32, n - s0);
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const float* row = P + (size_t)(s0 + j) * stride + 2;
+#pragma unroll
+      for (int e = 0; e < kMaxE; ++e)
+        if (lane + 32 * e < DV) acc[e] = fmaf(wj, row[lane + 32 * e], acc[e]);
+    }
   }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) den_part += __shfl_xor_sync(0xffffffffu, den_part, off);
+  const float den = (p.sinks ? exp2f(z2 - M) : 0.f) + den_part;
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e)
+    if (lane + 32 * e < DV) out[lane + 32 * e] = Elem<ET>::from_f32(den > 0.f ? acc[e] / den : 0.f);
 }
 
 cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStream_t st) {
