@@ -173,6 +173,37 @@ def decode_mla_naive(q, k_nope, k_rot, v, seq_lens, scale, nthreads=0):
     return decode_contig(q, k_full, v, seq_lens, scale, nthreads)
 
 
+def mla_absorb_q(q, k_b, d_nope):
+    """Absorbed query of frink-models src/mla/mod.rs (`absorbed_attention`, the
+    `MlaKvB::Split` form): for every head, the nope slice q[b, h, :d_nope] is
+    mapped into the latent space by k_b[h] ([d_c, d_nope], the absorb direction),
+    and the rope slice q[b, h, d_nope:] is kept as it is. q [B, H, d_nope + d_r],
+    k_b [H, d_c, d_nope]. Returns f64 [B, H, d_c + d_r]."""
+    qd, kb = widen(np.asarray(q)), widen(np.asarray(k_b))
+    absorbed = np.einsum("hcn,bhn->bhc", kb, qd[..., :d_nope])
+    return np.concatenate([absorbed, qd[..., d_nope:]], axis=-1)
+
+
+def decode_mla_absorbed(q_abs, latent, seq_lens, d_c, scale, nthreads=0):
+    """Attention over the latent cache (frink-models src/mla/mod.rs,
+    `absorbed_attention`: MQA over rows of width kv_lora_rank + qk_rope, every
+    head attending to the same row). Row j of sequence b is latent[b, j] =
+    (c_j, k_rot_j); its key is the whole row and its value the first d_c
+    columns, c_j. q_abs [B, H, d_c + d_r], latent [B, max_len, d_c + d_r], both of
+    one storage type; seq_lens[b] rows are visible. Returns f64 [B, H, d_c]."""
+    latent = np.asarray(latent)
+    k = np.ascontiguousarray(latent[:, None, :, :])
+    v = np.ascontiguousarray(latent[:, None, :, :d_c])
+    return decode_contig(q_abs, k, v, seq_lens, scale, nthreads)
+
+
+def mla_unabsorb_out(out_lat, v_b):
+    """Output of the absorbed form (frink-models src/mla/mod.rs,
+    `absorbed_attention`): each head's weighted latent out_lat[b, h] ([d_c]) is
+    mapped to the value width by v_b[h] ([d_v, d_c]). Returns f64 [B, H, d_v]."""
+    return np.einsum("hvc,bhc->bhv", widen(np.asarray(v_b)), widen(np.asarray(out_lat)))
+
+
 def rope_interleaved(x, positions, rot_offset, rot_dim, theta):
     """Interleaved RoPE of x [B, T, heads, d] at positions [B, T]; returns a new
     array of x's storage type (f32/bf16 results rounded to nearest-even)."""

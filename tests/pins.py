@@ -284,6 +284,84 @@ def pin_shared_rot_once_equals_per_head(core):
 
 
 # ---------------------------------------------------------------------------
+# MLA, absorbed (latent) form
+
+def _mla_case(seed, B=2, H=3, dn=8, dr=4, dc=12, dv=6, L=9):
+    r = rng(seed)
+    return dict(q=r.standard_normal((B, H, dn + dr)), k_b=r.standard_normal((H, dc, dn)),
+                v_b=r.standard_normal((H, dv, dc)), c=r.standard_normal((B, L, dc)),
+                k_rot=r.standard_normal((B, L, dr)), dn=dn, dc=dc, scale=1.0 / np.sqrt(dn + dr))
+
+
+def pin_mla_absorbed_equals_naive(core):
+    """frink-models src/mla/mod.rs, `MlaKvB`: the absorbed and the naive forms
+    compute the same attention. The naive cache is the latent expanded per head:
+    k_nope[b, h, j] = k_b[h]^T c_j (k_b maps qk_nope to the latent, so its
+    transpose expands the latent into the nope key) and v[b, h, j] = v_b[h] c_j,
+    with the shared k_rot copied into every head."""
+    m = _mla_case(21)
+    k_nope = np.einsum("hcn,bjc->bhjn", m["k_b"], m["c"])
+    v = np.einsum("hvc,bjc->bhjv", m["v_b"], m["c"])
+    for lens in ([9, 5], [1, 9]):
+        naive = core.decode_mla_naive(m["q"], k_nope, m["k_rot"], v, lens, m["scale"])
+        q_abs = core.mla_absorb_q(m["q"], m["k_b"], m["dn"])
+        lat = np.concatenate([m["c"], m["k_rot"]], axis=-1)
+        out = core.mla_unabsorb_out(core.decode_mla_absorbed(q_abs, lat, lens, m["dc"], m["scale"]), m["v_b"])
+        np.testing.assert_allclose(out, naive, rtol=0, atol=1e-10)
+
+
+def pin_mla_latent_closed_forms(core):
+    """Attention over the latent rows (c_j, k_rot_j) with value c_j: (1) a zero
+    query weighs the visible rows equally, so each head gets the mean of c_j over
+    j < seq_len; (2) one visible row gives c_0 exactly; (3) two rows with c_0 =
+    e_0 and c_1 = e_1 give (p, 1 - p, 0, ...), p = 1 / (1 + e^(s_1 - s_0)), where
+    s_j = scale * (q_c . c_j + q_r . k_rot_j) takes the rope slices too."""
+    r = rng(22)
+    B, H, dc, dr, L = 2, 3, 8, 4, 7
+    lat = r.standard_normal((B, L, dc + dr))
+    lens = [7, 3]
+    zero = core.decode_mla_absorbed(np.zeros((B, H, dc + dr)), lat, lens, dc, 0.3)
+    for b, n in enumerate(lens):
+        np.testing.assert_allclose(zero[b], np.broadcast_to(lat[b, :n, :dc].mean(axis=0), (H, dc)), rtol=0,
+                                   atol=1e-12)
+    q = r.standard_normal((B, H, dc + dr))
+    one = core.decode_mla_absorbed(q, lat, [1, 1], dc, 0.3)
+    for b in range(B):
+        assert np.array_equal(one[b], np.broadcast_to(lat[b, 0, :dc], (H, dc)))
+    lat2 = np.zeros((1, 2, dc + dr))
+    lat2[0, 0, 0] = lat2[0, 1, 1] = 1.0
+    lat2[0, :, dc:] = r.standard_normal((2, dr))
+    q2 = r.standard_normal((1, H, dc + dr))
+    got = core.decode_mla_absorbed(q2, lat2, [2], dc, 0.7)
+    for h in range(H):
+        s = [0.7 * (q2[0, h, :dc] @ lat2[0, j, :dc] + q2[0, h, dc:] @ lat2[0, j, dc:]) for j in range(2)]
+        p = 1.0 / (1.0 + np.exp(s[1] - s[0]))
+        np.testing.assert_allclose(got[0, h], [p, 1.0 - p] + [0.0] * (dc - 2), rtol=0, atol=1e-12)
+
+
+def pin_mla_projections(core):
+    """The absorb and unabsorb maps on basis vectors: the absorbed nope slice of
+    q = e_n is column n of k_b[h] and the rope slice passes through unchanged;
+    out_lat = e_c maps to column c of v_b[h]."""
+    m = _mla_case(23, B=1)
+    H, dn, dc = m["k_b"].shape[0], m["dn"], m["dc"]
+    for n in (0, dn - 1):
+        q = np.zeros((1, H, dn + 4))
+        q[0, :, n] = 1.0
+        q[0, :, dn:] = [1.5, -2.0, 0.25, 3.0]
+        got = core.mla_absorb_q(q, m["k_b"], dn)
+        for h in range(H):
+            assert np.array_equal(got[0, h, :dc], m["k_b"][h, :, n])
+            assert np.array_equal(got[0, h, dc:], [1.5, -2.0, 0.25, 3.0])
+    for c in (0, dc - 1):
+        lat = np.zeros((1, H, dc))
+        lat[0, :, c] = 1.0
+        got = core.mla_unabsorb_out(lat, m["v_b"])
+        for h in range(H):
+            assert np.array_equal(got[0, h], m["v_b"][h, :, c])
+
+
+# ---------------------------------------------------------------------------
 # paged append
 
 def pin_append(core):

@@ -4,6 +4,9 @@ pinning that part of the oracle."""
 import os
 import subprocess
 import tempfile
+import types
+
+import numpy as np
 
 import pytest
 
@@ -83,3 +86,60 @@ def test_mutant_is_caught(mutant_dir, name, old, new):
         assert failed, f"planted mistake '{name}' passed every pin"
     finally:
         core.bind()
+
+
+# Planted mistakes in the absorbed-MLA functions of oracle/core.py (numpy, so
+# each is a replacement function, handed to the pins through a stand-in module).
+def _absorb_rope_dropped(q, k_b, d_nope):
+    out = core.mla_absorb_q(q, k_b, d_nope)
+    out[..., k_b.shape[1]:] = 0.0
+    return out
+
+
+def _absorb_untransposed(q, k_b, d_nope):  # k_b[h]^T applied: sums over the latent index
+    qd = core.widen(q)
+    lat = np.einsum("hcn,bhc->bhn", core.widen(k_b)[:, :d_nope, :], qd[..., :d_nope])
+    pad = np.zeros(qd.shape[:2] + (k_b.shape[1] - d_nope,))
+    return np.concatenate([lat, pad, qd[..., d_nope:]], axis=-1)
+
+
+def _latent_value_from_tail(q_abs, latent, seq_lens, d_c, scale, nthreads=0):
+    latent = np.asarray(latent)
+    k = np.ascontiguousarray(latent[:, None])
+    v = np.ascontiguousarray(latent[:, None, :, -d_c:])
+    return core.decode_contig(q_abs, k, v, seq_lens, scale, nthreads)
+
+
+def _latent_rope_ignored(q_abs, latent, seq_lens, d_c, scale, nthreads=0):
+    latent = np.asarray(latent)
+    q = np.ascontiguousarray(np.asarray(q_abs)[..., :d_c])
+    k = np.ascontiguousarray(latent[:, None, :, :d_c])
+    return core.decode_contig(q, k, k, seq_lens, scale, nthreads)
+
+
+def _unabsorb_transposed(out_lat, v_b):
+    vb = core.widen(v_b)
+    return np.einsum("hvc,bhv->bhc", vb, core.widen(out_lat)[..., :vb.shape[1]])[..., :vb.shape[1]]
+
+
+MLA_MUTANTS = [
+    ("absorb: rope slice dropped", "mla_absorb_q", _absorb_rope_dropped),
+    ("absorb: k_b transposed", "mla_absorb_q", _absorb_untransposed),
+    ("latent: value from the row's tail", "decode_mla_absorbed", _latent_value_from_tail),
+    ("latent: rope columns ignored", "decode_mla_absorbed", _latent_rope_ignored),
+    ("unabsorb: v_b transposed", "mla_unabsorb_out", _unabsorb_transposed),
+]
+
+
+@pytest.mark.parametrize("name,attr,fn", MLA_MUTANTS, ids=[m[0] for m in MLA_MUTANTS])
+def test_mla_mutant_is_caught(name, attr, fn):
+    core.bind()
+    shim = types.SimpleNamespace(**{k: getattr(core, k) for k in dir(core) if not k.startswith("__")})
+    setattr(shim, attr, fn)
+    failed = []
+    for pin in (pins.pin_mla_absorbed_equals_naive, pins.pin_mla_latent_closed_forms, pins.pin_mla_projections):
+        try:
+            pin(shim)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake '{name}' passed every absorbed-MLA pin"
