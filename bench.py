@@ -498,6 +498,61 @@ def run_mla(args, peaks, peak_kind):
                          "peak_kind": peak_kind}}
 
 
+def run_mla_absorbed(args, peaks, peak_kind):
+    """Absorbed (latent) MLA decode at the MLA-shaped config's model shape: the
+    attention over the latent rows (mla_absorbed_tc_kernel + split combine) timed
+    alone, and the whole absorbed step (absorb, attention, unabsorb). Two copies
+    of the latent cache (2 x 151 MB) alternate, so no launch finds its rows in L2."""
+    import causal_gqa_attention_row_gb300 as g
+    g.load()
+    dev = torch.device("cuda")
+    B, H, L, D_C, D_R = 32, 128, 4096, 512, 64
+    c = W.make_mla_absorbed(B=B, H=H, max_len=L, seed=9, device=dev)
+    pos = torch.arange(L, dtype=torch.int32, device=dev)[None].repeat(B, 1).contiguous()
+    # setup (untimed): RoPE theta 1e4 on each latent row's rot slice at its own
+    # position, and on every head's q rot slice at position L - 1
+    g.attn_rope_interleaved(c.latent.view(B, L, 1, D_C + D_R), pos, 1e4, rot_offset=D_C, rot_dim=D_R)
+    g.attn_rope_interleaved(c.q.view(B, 1, H, 192), pos[:, -1:].contiguous(), 1e4, rot_offset=128, rot_dim=64)
+    latents = [c.latent, c.latent.clone()]
+    q_abs = torch.empty(B, H, D_C + D_R, dtype=torch.bfloat16, device=dev)
+    out_lat = torch.empty(B, H, D_C, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(B, H, 128, dtype=torch.bfloat16, device=dev)
+    ws = g.mla_absorbed_workspace(B, H, D_C, L, device=dev)
+    k_b, v_b = c.k_b, c.v_b
+    g.mla_absorb_q(c.q, k_b, q_abs)
+    flops = 2.0 * B * H * L * (D_C + D_R + D_C)
+    nbytes = B * L * (D_C + D_R) * 2 + B * H * (D_C + D_R) * 2 + B * H * D_C * 2
+    st = torch.cuda.current_stream()
+    attend = lambda k: g.attn_decode_mla_absorbed(q_abs, latents[k % 2], c.lens, out_lat, c.scale, workspace=ws)
+
+    def step(k):
+        g.mla_absorb_q(c.q, k_b, q_abs)
+        attend(k)
+        g.mla_unabsorb_out(out_lat, v_b, out)
+
+    for i in range(4):
+        step(i)
+    torch.cuda.synchronize()
+    n = 2 * max(args.steps, 20)
+    queue_ahead(n, us_per_group=60.0)
+    ms = timed(attend, n, st, sync_first=False)
+    queue_ahead(n, us_per_group=80.0)
+    ms_step = timed(step, n, st, sync_first=False)
+    assert g.attn_get_device_error() == g.OK
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tflops = flops / (ms * 1e-3) / 1e12
+    hbm, bf = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    return {"workload": W.WORKLOADS["mla_absorbed"], "ms": ms, "gbs": gbs, "tflops": tflops, "bytes": nbytes,
+            "flops": flops, "step_ms": ms_step,
+            "step": "mla_absorb_q + attn_decode_mla_absorbed + mla_unabsorb_out",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "tensor_tflops": tflops, "tensor_frac": tflops / bf,
+                         "note": f"{flops / nbytes:.0f} flop per byte, below the ridge of {bf * 1e3 / hbm:.0f}: the "
+                                 "latent stream bounds it",
+                         "kernel": "attn_decode_mla_absorbed (mla_absorbed_tc_kernel + split_combine_kernel)",
+                         "peak_kind": f"{peak_kind} copy bandwidth; bf16 dense burst for tensor_frac"}}
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 
@@ -562,7 +617,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true", help="skip prefill, contig and mla")
     ap.add_argument("--only", choices=["paged", "prefill", "prefill_paged", "prefill_d128", "prefill_paged_d128",
-                                       "prefill_mla", "contig", "mla"], default=None)
+                                       "prefill_mla", "contig", "mla", "mla_absorbed"], default=None)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world = dist_setup()
@@ -572,7 +627,7 @@ def main():
     peaks, peak_kind = measured_peaks()
     only = {"prefill": run_prefill, "prefill_paged": run_prefill_paged, "prefill_d128": run_prefill_d128,
             "prefill_paged_d128": run_prefill_paged_d128, "prefill_mla": run_prefill_mla, "contig": run_contig,
-            "mla": run_mla}
+            "mla": run_mla, "mla_absorbed": run_mla_absorbed}
     if args.only in only:
         r = only[args.only](args, peaks, peak_kind)
         if rank == 0:
@@ -586,7 +641,8 @@ def main():
                      "prefill_d128": run_prefill_d128(args, peaks, peak_kind),
                      "prefill_paged_d128": run_prefill_paged_d128(args, peaks, peak_kind),
                      "prefill_mla": run_prefill_mla(args, peaks, peak_kind),
-                     "contig": run_contig(args, peaks, peak_kind), "mla": run_mla(args, peaks, peak_kind)}
+                     "contig": run_contig(args, peaks, peak_kind), "mla": run_mla(args, peaks, peak_kind),
+                     "mla_absorbed": run_mla_absorbed(args, peaks, peak_kind)}
     if res.get("arms"):
         arms = res["arms"]
         arms["roofline"].update({"peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": arms["gbs"] / peaks["hbm_gbs"],

@@ -24,7 +24,8 @@ EXPORTS = ("attn_prefill_causal", "attn_decode_contig", "attn_decode_paged", "kv
            "attn_rope_interleaved", "attn_decode_workspace_bytes", "attn_get_device_error",
            "gqa_status_string", "gqa_debug_withhold_first_tile", "attn_decode_paged_static_workspace",
            "attn_prefill_causal_ex", "attn_decode_contig_ex", "attn_decode_paged_ex", "attn_prefill_paged",
-           "attn_prefill_paged_ex")
+           "attn_prefill_paged_ex", "mla_absorb_q", "attn_decode_mla_absorbed",
+           "attn_decode_mla_absorbed_workspace_bytes", "mla_unabsorb_out")
 
 
 class GqaArms(ctypes.Structure):
@@ -67,6 +68,9 @@ def load(path: str = None):
         "attn_prefill_paged": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P],
         "attn_prefill_paged_ex": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, P],
         "gqa_debug_withhold_first_tile": [I],
+        "mla_absorb_q": [P, P, P, I, I, I, I, I, I, P],
+        "attn_decode_mla_absorbed": [P, P, P, P, I, I, I, I, I, F, I, P, S, P],
+        "mla_unabsorb_out": [P, P, P, I, I, I, I, I, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -74,6 +78,8 @@ def load(path: str = None):
         fn.restype = ctypes.c_int
     lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I]
     lib.attn_decode_workspace_bytes.restype = S
+    lib.attn_decode_mla_absorbed_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_decode_mla_absorbed_workspace_bytes.restype = S
     lib.gqa_status_string.argtypes = [I]
     lib.gqa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -218,6 +224,47 @@ def attn_decode_paged_static_workspace(q, k_pool, v_pool, block_tables, seq_lens
                                                      Hkv, dk, dv, float(attention_scale),
                                                      _dtype(q, k_pool, v_pool, out), _stream(stream)),
            "attn_decode_paged_static_workspace")
+    return out
+
+
+def mla_absorb_q(q, k_b, q_abs, stream=None):
+    """q [B, H, d_nope + d_rope]; k_b [H, d_c, d_nope]; q_abs [B, H, d_c + d_rope] (bf16)."""
+    B, H, dq = q.shape
+    _, d_c, d_nope = k_b.shape
+    _check(load().mla_absorb_q(_p(q), _p(k_b), _p(q_abs), B, H, d_nope, dq - d_nope, d_c, _dtype(q, k_b, q_abs),
+                               _stream(stream)), "mla_absorb_q")
+    return q_abs
+
+
+def attn_decode_mla_absorbed_workspace_bytes(B, H, d_c, max_len):
+    return int(load().attn_decode_mla_absorbed_workspace_bytes(B, H, d_c, max_len))
+
+
+def mla_absorbed_workspace(B, H, d_c, max_len, device="cuda"):
+    """A workspace tensor of the size attn_decode_mla_absorbed needs (None when none)."""
+    n = attn_decode_mla_absorbed_workspace_bytes(B, H, d_c, max_len)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def attn_decode_mla_absorbed(q_abs, latent, seq_lens, out_lat, attention_scale, workspace=None, stream=None):
+    """q_abs [B, H, d_c + d_r]; latent [B, L, d_c + d_r]; seq_lens int32 [B];
+    out_lat [B, H, d_c] (bf16)."""
+    B, H, w = q_abs.shape
+    _, L, _ = latent.shape
+    d_c = out_lat.shape[-1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().attn_decode_mla_absorbed(_p(q_abs), _p(latent), _i32(seq_lens), _p(out_lat), B, L, H, d_c, w - d_c,
+                                           float(attention_scale), _dtype(q_abs, latent, out_lat), _p(workspace), ws,
+                                           _stream(stream)), "attn_decode_mla_absorbed")
+    return out_lat
+
+
+def mla_unabsorb_out(out_lat, v_b, out, stream=None):
+    """out_lat [B, H, d_c]; v_b [H, d_v, d_c]; out [B, H, d_v] (bf16)."""
+    B, H, d_c = out_lat.shape
+    d_v = v_b.shape[1]
+    _check(load().mla_unabsorb_out(_p(out_lat), _p(v_b), _p(out), B, H, d_c, d_v, _dtype(out_lat, v_b, out),
+                                   _stream(stream)), "mla_unabsorb_out")
     return out
 
 

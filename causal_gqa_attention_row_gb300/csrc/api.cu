@@ -349,6 +349,73 @@ gqa_status attn_rope_interleaved(void* x, const int32_t* positions, int B, int T
                                     static_cast<cudaStream_t>(stream)));
 }
 
+size_t attn_decode_mla_absorbed_workspace_bytes(int B, int H, int d_c, int max_len) {
+  if (B <= 0 || H <= 0 || d_c <= 0 || max_len <= gqa::kMlaChunk) return 0;
+  const size_t splits = (size_t)ceil_div(max_len, gqa::kMlaChunk);
+  return (size_t)B * (size_t)H * splits * (size_t)(d_c + 2) * sizeof(float);
+}
+
+gqa_status attn_decode_mla_absorbed(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
+                                    int B, int max_len, int H, int d_c, int d_r, float attention_scale, gqa_dtype dt,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  const int bf16 = dtype_flag(dt);
+  if (bf16 < 0 || B < 0 || max_len <= 0 || H <= 0 || d_c <= 0 || d_r < 0 || !std::isfinite(attention_scale))
+    return GQA_ERR_INVALID_ARG;
+  if (!gqa::mla_absorbed_tc_supported(bf16, d_c, d_r) || !(attention_scale > 0.f)) return GQA_ERR_UNSUPPORTED;
+  if (B == 0) return GQA_OK;
+  if (!q_abs || !latent || !seq_lens || !out_lat) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(latent) || !aligned16(out_lat)) return GQA_ERR_INVALID_ARG;
+  const size_t need = attn_decode_mla_absorbed_workspace_bytes(B, H, d_c, max_len);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GQA_ERR_INVALID_ARG;
+  }
+  unsigned* err = error_word();
+  if (!err) return GQA_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float qscale = attention_scale * 1.4426950408889634f;
+  float* partial = need > 0 ? static_cast<float*>(workspace) : nullptr;
+  const cudaError_t e = gqa::launch_mla_absorbed_tc(q_abs, latent, seq_lens, out_lat, partial, B, max_len, H, d_c,
+                                                    d_r, gqa::kMlaChunk, qscale, err, st);
+  if (e != cudaSuccess || need == 0) return from_cuda(e);
+  // the splits of each (sequence, head) merged into out_lat
+  gqa::RowsParams p{};
+  p.out = out_lat;
+  p.partial = partial;
+  p.kv_len = seq_lens;
+  p.B = B;
+  p.seq_q = 1;
+  p.H = H;
+  p.capacity = max_len;
+  p.split_rows = gqa::kMlaChunk;
+  p.max_splits = ceil_div(max_len, gqa::kMlaChunk);
+  p.window = 0;
+  p.err = err;
+  return from_cuda(gqa::launch_split_combine(p, d_c, 1, st));
+}
+
+gqa_status mla_absorb_q(const void* q, const void* k_b, void* q_abs, int B, int H, int d_nope, int d_rope, int d_c,
+                        gqa_dtype dt, void* stream) {
+  const int bf16 = dtype_flag(dt);
+  if (bf16 < 0 || B < 0 || H <= 0 || d_nope <= 0 || d_rope < 0 || d_c <= 0) return GQA_ERR_INVALID_ARG;
+  if (bf16 != 1) return GQA_ERR_UNSUPPORTED;
+  if (B == 0) return GQA_OK;
+  if (!q || !k_b || !q_abs || q == q_abs) return GQA_ERR_INVALID_ARG;
+  return from_cuda(gqa::launch_head_matvec(k_b, q, d_nope + d_rope, q_abs, d_c + d_rope, B, H, d_c, d_nope, d_rope,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+gqa_status mla_unabsorb_out(const void* out_lat, const void* v_b, void* out, int B, int H, int d_c, int d_v,
+                            gqa_dtype dt, void* stream) {
+  const int bf16 = dtype_flag(dt);
+  if (bf16 < 0 || B < 0 || H <= 0 || d_c <= 0 || d_v <= 0) return GQA_ERR_INVALID_ARG;
+  if (bf16 != 1) return GQA_ERR_UNSUPPORTED;
+  if (B == 0) return GQA_OK;
+  if (!out_lat || !v_b || !out || out == out_lat) return GQA_ERR_INVALID_ARG;
+  return from_cuda(gqa::launch_head_matvec(v_b, out_lat, d_c, out, d_v, B, H, d_v, d_c, 0,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 gqa_status attn_get_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
   unsigned word = 0, zero = 0;

@@ -98,4 +98,22 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
 // bs = 0: contiguous K/V; else the pool's block size and max blocks per sequence.
 bool prefill_tc_supported(int bf16, int dk, int dv, int bs = 0, int mbps = 0);
 
+// Absorbed MLA decode on tcgen05 (bf16, d_c = 512, d_r = 64): attention of
+// q_abs [B, H, d_c + d_r] over the latent rows [B, max_len, d_c + d_r] (value =
+// the first d_c columns) into out_lat [B, H, d_c]; splits of `chunk` rows write
+// (m, l, o) into partial [B * H, ceil(max_len / chunk), d_c + 2] when a sequence
+// has more than one, and the split combine merges them.
+bool mla_absorbed_tc_supported(int bf16, int d_c, int d_r);
+cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
+                                   float* partial, int B, int max_len, int H, int d_c, int d_r, int chunk,
+                                   float qscale, unsigned* err, cudaStream_t st);
+// Rows of one split of the absorbed MLA decode (a fixed number, so a sequence's
+// result does not depend on the rest of the batch).
+constexpr int kMlaChunk = 1024;
+
+// y[b, h, :M] = W[h] x[b, h, :K] (bf16, fp32 accumulation), W [H, M, K]; the
+// `tail` columns of x after K are copied to y after M.
+cudaError_t launch_head_matvec(const void* W, const void* x, int x_stride, void* y, int y_stride, int B, int H, int M,
+                               int K, int tail, cudaStream_t st);
+
 }  // namespace gqa

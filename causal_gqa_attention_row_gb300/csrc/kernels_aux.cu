@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
   // Each split's weight once (lane s % 32 holds split s's), the weighted row sums
   // reduced in a fixed butterfly order; every lane then walks the splits in order,
   // the weight broadcast, its output columns d = lane + 32 e read as coalesced rows.
-  constexpr int kMaxE = 8;  // DV <= 256
+  constexpr int kMaxE = 16;  // DV <= 512 (the latent width of the absorbed MLA decode)
   float acc[kMaxE];
 #pragma unroll
   for (int e = 0; e < kMaxE; ++e) acc[e] = 0.f;

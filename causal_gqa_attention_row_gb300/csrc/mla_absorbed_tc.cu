@@ -1,0 +1,532 @@
+// mla_absorbed_tc.cu -- MLA decode in the absorbed (latent) form on the tcgen05
+// tensor cores (bf16; latent width d_c = 512, rope width d_r = 64).
+//
+// The operation (frink-models src/mla/mod.rs, `absorbed_attention` and the
+// `MlaKvB::Split` form): query head h of sequence b, already absorbed into the
+// latent space (q_abs[b, h], width d_c + d_r), attends to the cache rows
+// j < seq_len[b] of its sequence with softmax(scale * q_abs . row_j); a row is
+// (c_j, k_rot_j), its key the whole row and its value c_j, the first d_c
+// columns. Every head reads the same row (MQA with a group of H), so a row read
+// from memory serves 2 * H * (2 d_c + d_r) flops: at H = 128 this is a
+// contraction, not a stream, and it runs on the tensor cores.
+//
+// One CTA = one (sequence, tile of 128 heads, split of kChunk cache rows, half
+// of the d_c value columns). The heads are the MMA's 128 rows:
+//   S = Q_abs R^T      M = 128 heads, N = 32 rows of the cache tile, K = d_c + d_r
+//   O += P R[:, half]  M = 128 heads, N = d_c / 2 value columns,    K = 32 rows
+// The cache tile R (32 rows x 576 columns, nine 64-column blocks in the 128-byte
+// swizzle) is read by both: as K (K-major) by the S MMA and, its columns of this
+// CTA's half, as V (MN-major) by the PV MMA, so a row is loaded once per CTA.
+// Tensor memory holds O (256 columns), S (2 x 32) and P (2 x 16: bf16 pairs),
+// 352 of its 512 columns; the full 512-column O of one head tile would leave no
+// room for S, hence the two halves, which compute the same S (identical
+// arithmetic, so their row max and sum agree bit for bit). Shared memory holds
+// Q_abs for the whole CTA lifetime (128 x 576 bf16, 144 KiB) and a two-stage
+// ring of cache tiles (2 x 36 KiB).
+//
+// Roles (192 threads):
+//   warps 0-3  softmax: thread t owns head h0 + t (TMEM lane t)
+//   warp 4     initialises the barriers; TMA producer of Q_abs (once) and of
+//              the cache tiles (lane i issues the box of column block i)
+//   warp 5     allocates TMEM; one thread issues the MMAs, S_t as soon as its
+//              tile has landed and PV_t as soon as P_t is in TMEM, whichever
+//              comes first
+// Softmax as in the prefill kernel: a lazily moved reference max (threshold
+// 2^8 in p), p rounded to bf16 and the fp32 row sum taken over exactly those
+// p. Rows of the last tile at or past seq_len weigh zero; their value rows in
+// shared memory are zeroed before the PV MMA reads them, so whatever the cache
+// holds past seq_len (within its capacity) cannot reach the output. A sequence
+// with one split writes O / l as bf16; otherwise each split writes (m, l, O) in
+// fp32 (m in the log2 domain) and the split-combine kernel merges them.
+#include <cudaTypedefs.h>
+
+#include "tc_ptx.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kHeads = 128;    // query heads per CTA: the MMA's M
+constexpr int kKeys = 32;      // cache rows per tile: the S MMA's N
+constexpr int kStages = 2;     // cache-tile ring
+constexpr int kThreads = 192;  // four softmax warps, the producer, the MMA warp
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr uint32_t kWaitHintNs = 20;
+
+template <int DC, int DR>
+struct MlaCfg {
+  static constexpr int kW = DC + DR;         // row width
+  static constexpr int kCB = kW / 64;        // 64-column blocks of a row
+  static constexpr int kDVH = DC / 2;        // value columns per CTA
+  static constexpr int kCBV = kDVH / 64;     // ... in blocks
+  static constexpr int kQBlk = kHeads * 128; // one block of Q_abs: 128 rows x 128 bytes
+  static constexpr int kRBlk = kKeys * 128;  // one block of a cache tile: 32 rows x 128 bytes
+  static constexpr int kTileQ = kCB * kQBlk;
+  static constexpr int kTileR = kCB * kRBlk;
+  static constexpr int kOffQ = 0, kOffR = kTileQ, kOffBar = kOffR + kStages * kTileR;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
+  // TMEM columns
+  static constexpr uint32_t kColO = 0, kColS = kDVH, kColP = kDVH + 2 * kKeys;
+  static_assert(DC % 128 == 0 && DR % 64 == 0, "whole 64-column blocks per half");
+  static_assert(kDVH % 16 == 0 && kDVH <= 256, "one PV MMA covers the half");
+  static_assert(kColP + 2 * (kKeys / 2) <= kTmemCols, "TMEM map");
+  static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
+};
+
+struct MlaParams {
+  int B, H, max_len, chunk, max_splits, n_htiles;
+  const int32_t* seq_lens;  // [B] rows visible, >= 1 and <= max_len
+  float* partial;           // [B * H, max_splits, d_c + 2] when max_splits > 1
+  __nv_bfloat16* out;       // [B, H, d_c]
+  float qscale;             // attention_scale * log2(e)
+  unsigned* err;
+};
+
+struct MlaBars {
+  uint64_t q_full, r_full[kStages], r_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_done[2], mma_final;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(MlaBars) <= 256, "barrier block");
+
+__device__ __forceinline__ bool aborted(MlaBars* bars) {
+  return *reinterpret_cast<volatile int*>(&bars->abort_flag);
+}
+
+__device__ __forceinline__ void abort_all(MlaBars* bars, unsigned* err) {
+  *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
+  raise_error(err, kErrTimeout);
+}
+
+__device__ __forceinline__ bool wait_quick(uint64_t* bar, uint32_t parity) {
+  return mbar_test_parity_nb(bar, parity) || mbar_wait_hint(bar, parity, kWaitHintNs);
+}
+
+// One thread (producer lane 0): bounded wait, the CTA aborts on a timeout.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, MlaBars* bars, unsigned* err) {
+  if (aborted(bars)) return false;
+  if (wait_quick(bar, parity)) return true;
+  abort_all(bars, err);
+  return false;
+}
+
+// Whole warp: every lane agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, MlaBars* bars, unsigned* err) {
+  bool ok = !aborted(bars) && wait_quick(bar, parity);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0) abort_all(bars, err);
+  return ok;
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// a += low bf16 of w, b += high bf16 of w, in fp32.
+__device__ __forceinline__ void add_bf16x2(float& a, float& b, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "r"(w));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+template <int DC, int DR>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_absorbed_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
+                           const MlaParams p) {
+  using C = MlaCfg<DC, DR>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  MlaBars* bars = reinterpret_cast<MlaBars*>(smem + C::kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: the two halves of one (sequence, head tile, split) are neighbours
+  const int half = (int)(blockIdx.x & 1);
+  int rest = (int)(blockIdx.x >> 1);
+  const int split = rest % p.max_splits;
+  rest /= p.max_splits;
+  const int ht = rest % p.n_htiles;
+  const int b = rest / p.n_htiles;
+  const int h0 = ht * kHeads;
+  const int len = __ldg(p.seq_lens + b);
+  const bool len_ok = len >= 1 && len <= p.max_len;
+  const int n_split = len_ok ? (len + p.chunk - 1) / p.chunk : 1;
+  if (split >= n_split) return;  // no rows in this split: the whole CTA leaves before any set-up
+  if (!len_ok) {                 // the heads' output is zero and the error word says why
+    if (threadIdx.x == 0 && half == 0 && ht == 0) raise_error(p.err, kErrBounds);
+    for (int idx = threadIdx.x; idx < kHeads * C::kDVH; idx += blockDim.x) {
+      const int h = h0 + idx / C::kDVH;
+      if (h < p.H) p.out[((size_t)b * p.H + h) * DC + half * C::kDVH + idx % C::kDVH] = __float2bfloat16_rn(0.f);
+    }
+    return;
+  }
+  const int k0 = split * p.chunk;
+  const int k1 = min(len, k0 + p.chunk);
+  const int n_t = (k1 - k0 + kKeys - 1) / kKeys;  // >= 1
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      mbar_init(&bars->q_full, 1);
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&bars->r_full[s], 1);
+        mbar_init(&bars->r_empty[s], 1);
+      }
+      for (int x = 0; x < 2; ++x) {
+        mbar_init(&bars->s_full[x], 1);
+        mbar_init(&bars->p_full[x], 4);  // one arrival per softmax warp
+        mbar_init(&bars->o_done[x], 1);
+      }
+      mbar_init(&bars->mma_final, 1);
+      bars->abort_flag = 0;
+      fence_barrier_init();
+      tc::prefetch_tmap(&tm_q);
+      tc::prefetch_tmap(&tm_r);
+      mbar_arrive_expect_tx(&bars->q_full, C::kTileQ);
+    }
+    __syncwarp();
+    // Q_abs [B, H, W]: rows h0..h0+127 of sequence b (heads past H read as zeros)
+    if (lane < C::kCB) tc::tma_load_4d(smem + C::kOffQ + lane * C::kQBlk, &tm_q, lane * 64, h0, b, 0, &bars->q_full);
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(&bars->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ================= TMA producer of the cache tiles =================
+    int issued_last[kStages];
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) issued_last[s] = -1;
+    for (int t = 0; t < n_t; ++t) {
+      const int st = t % kStages;
+      if (t >= kStages) {  // the stage is free once PV_{t-2} is done
+        bool ok = true;
+        if (lane == 0) ok = wait_or_abort(&bars->r_empty[st], ((t / kStages) - 1) & 1, bars, p.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&bars->r_full[st], C::kTileR);
+      __syncwarp();
+      // rows k0 + 32t .. +31 of sequence b; rows past the cache's capacity read as zeros
+      if (lane < C::kCB)
+        tc::tma_load_4d(smem + C::kOffR + st * C::kTileR + lane * C::kRBlk, &tm_r, lane * 64, k0 + t * kKeys, b, 0,
+                        &bars->r_full[st]);
+      __syncwarp();
+      issued_last[st] = t;
+    }
+    if (lane == 0) {  // never exit with a load in flight
+      if (!mbar_wait(&bars->q_full, 0)) raise_error(p.err, kErrTimeout);
+      for (int s = 0; s < kStages; ++s)
+        if (issued_last[s] >= 0 && !mbar_wait(&bars->r_full[s], (issued_last[s] / kStages) & 1))
+          raise_error(p.err, kErrTimeout);
+    }
+  } else if (warp == kMmaWarp) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      const uint32_t idS = tc::idesc_bf16_f32(kHeads, kKeys, false);
+      const uint32_t idO = tc::idesc_bf16_f32(kHeads, C::kDVH, true);
+      constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);  // K-major: 8-row groups 1024 bytes apart
+      const uint64_t dQ = kHi | (smem_u32(smem + C::kOffQ) >> 4);
+      const uint64_t dR0 = kHi | (smem_u32(smem + C::kOffR) >> 4);
+      // the value half as V: MN-major, 8-row groups 1024 bytes apart, its 64-column
+      // blocks one cache-tile block (4 KiB) apart
+      const uint64_t dV0 =
+          tc::desc_sw128_hi(C::kRBlk, 1024) | (smem_u32(smem + C::kOffR + half * C::kCBV * C::kRBlk) >> 4);
+      const uint32_t tS = tmem + C::kColS, tO = tmem + C::kColO, tP = tmem + C::kColP;
+      auto issue_s = [&](int t) {  // S_{t%2} = Q_abs R_t^T, 16 of the W columns per instruction
+        const int st = t % kStages;
+        tc::fence_after_sync();
+        const uint64_t dR = dR0 + (uint64_t)((st * C::kTileR) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < C::kW / 16; ++kk) {
+          const uint32_t aq = (kk / 4) * C::kQBlk + (kk % 4) * 32;
+          const uint32_t ar = (kk / 4) * C::kRBlk + (kk % 4) * 32;
+          tc::mma_f16_ss(tS + (t & 1) * kKeys, dQ + (aq >> 4), dR + (ar >> 4), idS, kk > 0);
+        }
+        tc::mma_commit(&bars->s_full[t & 1]);
+      };
+      auto issue_pv = [&](int t) {  // O += P_{t%2} R_t[:, half], 16 rows per instruction
+        const int st = t % kStages;
+        tc::fence_after_sync();
+        const uint64_t dV = dV0 + (uint64_t)((st * C::kTileR) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc::mma_f16_ts(tO, tP + (t & 1) * (kKeys / 2) + kk * 8, dV + kk * (2048 >> 4), idO, (t > 0 || kk > 0));
+        tc::mma_commit(&bars->o_done[t & 1]);
+        tc::mma_commit(&bars->r_empty[st]);  // the tile's stage is free once PV_t is done
+      };
+      bool ok = wait_or_abort(&bars->q_full, 0, bars, p.err);
+      // S_t needs tile t in shared memory (which also means PV_{t-2} is done, so S
+      // buffer t % 2 has been read); PV_t needs P_t. Each barrier is probed for its
+      // phases in order, and neither can run two phases ahead of its probe.
+      int next_s = 0, next_pv = 0;
+      long long idle_since = clock64();
+      while (ok && next_pv < n_t) {
+        bool progressed = false;
+        if (next_s < n_t && mbar_test_parity_nb(&bars->r_full[next_s % kStages], (next_s / kStages) & 1)) {
+          issue_s(next_s++);
+          progressed = true;
+        }
+        if (next_pv < next_s && mbar_test_parity_nb(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+          issue_pv(next_pv++);
+          progressed = true;
+        }
+        if (progressed) {
+          idle_since = clock64();
+        } else if (aborted(bars)) {
+          ok = false;
+        } else if (clock64() - idle_since > kWaitLimitCycles) {
+          abort_all(bars, p.err);
+          ok = false;
+        }
+      }
+      // every MMA issued above has completed before TMEM is released
+      tc::mma_commit(&bars->mma_final);
+      if (!mbar_wait(&bars->mma_final, 0)) raise_error(p.err, kErrTimeout);
+    }
+  } else {
+    // ================= softmax: thread t owns head h0 + t =================
+    const int r = warp * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    const float qs = p.qscale;
+    const float th = kRescaleLog2 / qs;
+    const float2 qs2 = make_float2(qs, qs);
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool alive = true;
+    for (int t = 0; t < n_t; ++t) {
+      const int x = t & 1;
+      if (!warp_wait(&bars->s_full[x], (t >> 1) & 1, bars, p.err)) {
+        alive = false;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t sv[kKeys];
+      tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::kColS + x * kKeys, sv);
+      tc::tmem_ld_wait();
+      const int kt = k0 + t * kKeys;
+      const int valid = min(kKeys, k1 - kt);  // rows of this tile the heads see
+      if (valid < kKeys) {
+#pragma unroll
+        for (int e = 0; e < kKeys; ++e)
+          if (e >= valid) sv[e] = __float_as_uint(-INFINITY);
+      }
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int e = 0; e < kKeys; e += 2)
+        mx4[(e >> 1) & 3] = fmax3(mx4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      if (t == 0) {
+        m_ref = mx;  // the first tile has a visible row: mx is finite
+      } else {
+        const bool grow = mx > m_ref + th;
+        if (__any_sync(0xffffffffu, grow)) {
+          float f = 1.f;
+          if (grow) {
+            f = ex2f((m_ref - mx) * qs);
+            m_ref = mx;
+          }
+          // O holds every PV issued so far, PV_{t-1} the last: rescale it once done
+          if (!warp_wait(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, bars, p.err)) {
+            alive = false;
+            break;
+          }
+          tc::fence_after_sync();
+          uint32_t o[32];
+#pragma unroll 1
+          for (int c = 0; c < C::kDVH / 32; ++c) {
+            tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c * 32, o);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tc::tmem_st_32x32b_x32(tmem + lane_addr + C::kColO + c * 32, o);
+          }
+          tc::tmem_st_wait();
+          l_run *= f;
+        }
+      }
+      // p = 2^(s*qs - m*qs) as bf16 pairs, and the fp32 sum of exactly these p
+      const float mq = m_ref * qs;
+      const float2 nmq2 = make_float2(-mq, -mq);
+      uint32_t pv[kKeys / 2];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < kKeys / 2; ++i) {
+        const float2 xv = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), qs2, nmq2);
+        pv[i] = ex2_bf16x2(pack_bf16(xv.x, xv.y));
+        add_bf16x2(ls[(i & 1) * 2], ls[(i & 1) * 2 + 1], pv[i]);
+      }
+      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      if (valid < kKeys) {
+        // value rows valid..31 of this CTA's half: zero them (S_t, their other
+        // reader, is done) so that 0 * (whatever the cache holds) cannot be NaN
+        unsigned char* base = smem + C::kOffR + (t % kStages) * C::kTileR + half * C::kCBV * C::kRBlk;
+        const int n_chunks = (kKeys - valid) * C::kCBV * 8;  // 16-byte chunks: 8 per row and block
+        for (int i = r; i < n_chunks; i += kHeads) {
+          const int row = valid + i / (C::kCBV * 8), blk = (i / 8) % C::kCBV, ch = i % 8;
+          *reinterpret_cast<uint4*>(base + blk * C::kRBlk + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        tc::fence_async_smem();  // visible to the tensor cores' reads
+      }
+      // P buffer x was last read by PV_{t-2}
+      if (t >= 2) {
+        if (!warp_wait(&bars->o_done[x], ((t - 2) >> 1) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
+        tc::fence_after_sync();
+      }
+      tc::tmem_st_32x32b_x16(tmem + lane_addr + C::kColP + x * (kKeys / 2), pv);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[x]);
+    }
+    // ---- the last PV (its commit covers every earlier MMA), then the output
+    bool have_o = alive;
+    if (have_o) {
+      have_o = warp_wait(&bars->o_done[(n_t - 1) & 1], ((n_t - 1) >> 1) & 1, bars, p.err);
+      tc::fence_after_sync();
+    }
+    const int h = h0 + r;
+    const bool mine = h < p.H;
+    if (n_split == 1) {
+      const float inv = (have_o && l_run > 0.f) ? 1.f / l_run : 0.f;
+      __nv_bfloat16* dst = p.out + ((size_t)b * p.H + (mine ? h : 0)) * DC + half * C::kDVH;
+#pragma unroll 1
+      for (int c = 0; c < C::kDVH / 32; ++c) {
+        uint32_t o[32];
+        tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c * 32, o);
+        tc::tmem_ld_wait();
+        if (mine) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              w[u] = pack_bf16(__uint_as_float(o[q4 * 8 + 2 * u]) * inv, __uint_as_float(o[q4 * 8 + 2 * u + 1]) * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    } else {
+      float* P = p.partial + (((size_t)b * p.H + (mine ? h : 0)) * p.max_splits + split) * (DC + 2);
+      if (mine && half == 0) {
+        P[0] = have_o ? m_ref * qs : -INFINITY;
+        P[1] = have_o ? l_run : 0.f;
+      }
+      float* dst = P + 2 + half * C::kDVH;
+#pragma unroll 1
+      for (int c = 0; c < C::kDVH / 32; ++c) {
+        uint32_t o[32];
+        tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c * 32, o);
+        tc::tmem_ld_wait();
+        if (mine) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            *reinterpret_cast<float2*>(dst + c * 32 + e) = make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1]));
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// A bf16 tensor [d2, d1, w] (rows of w elements); box = 64 columns x box1 rows,
+// 128-byte swizzle; rows and columns past the tensor read as zeros.
+bool make_rows_map(CUtensorMap* m, const void* base, int w, uint64_t d1, uint64_t d2, uint32_t box1) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)w, d1, d2, 1};
+  const cuuint64_t strides[3] = {(cuuint64_t)w * 2, (cuuint64_t)w * 2 * d1, (cuuint64_t)w * 2 * d1 * d2};
+  const cuuint32_t box[4] = {64, box1, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool mla_absorbed_tc_supported(int bf16, int d_c, int d_r) { return bf16 == 1 && d_c == 512 && d_r == 64; }
+
+cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
+                                   float* partial, int B, int max_len, int H, int d_c, int d_r, int chunk,
+                                   float qscale, unsigned* err, cudaStream_t st) {
+  using C = MlaCfg<512, 64>;
+  if (!mla_absorbed_tc_supported(1, d_c, d_r) || chunk % kKeys != 0 || chunk <= 0 || !(qscale > 0.f))
+    return cudaErrorNotSupported;
+  if (B == 0) return cudaSuccess;
+  CUtensorMap tq, tr;
+  // q_abs [B, H, 576]: box of 128 heads; latent [B, max_len, 576]: box of 32 rows
+  if (!make_rows_map(&tq, q_abs, C::kW, (uint64_t)H, (uint64_t)B, kHeads)) return cudaErrorInvalidValue;
+  if (!make_rows_map(&tr, latent, C::kW, (uint64_t)max_len, (uint64_t)B, kKeys)) return cudaErrorInvalidValue;
+  MlaParams p;
+  p.B = B;
+  p.H = H;
+  p.max_len = max_len;
+  p.chunk = chunk;
+  p.max_splits = (max_len + chunk - 1) / chunk;
+  p.n_htiles = (H + kHeads - 1) / kHeads;
+  p.seq_lens = seq_lens;
+  p.partial = partial;
+  p.out = static_cast<__nv_bfloat16*>(out_lat);
+  p.qscale = qscale;
+  p.err = err;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static unsigned long long attr_done = 0;
+  if (dev < 64 && !(attr_done >> dev & 1ull)) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(mla_absorbed_tc_kernel<512, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done |= 1ull << dev;
+  }
+  const long long ctas = (long long)B * p.n_htiles * p.max_splits * 2;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  mla_absorbed_tc_kernel<512, 64><<<(unsigned)ctas, kThreads, C::kSmemBytes, st>>>(tq, tr, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

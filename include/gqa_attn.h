@@ -278,6 +278,52 @@ gqa_status attn_rope_interleaved(void* x, const int32_t* positions, int B, int T
  * then the partial results (U * (d_v + 2) floats). Host only; launches nothing. */
 size_t attn_decode_workspace_bytes(int B, int H, int d_v, int max_len_upper_bound);
 
+/* ---- MLA, absorbed (latent) form -------------------------------------------
+ * frink-models src/mla/mod.rs, `absorbed_attention` and `MlaKvB::Split`: the
+ * cache holds one latent row per position, (c_j, k_rot_j) of width d_c + d_r
+ * (kv_lora_rank + qk_rope); each query head's nope slice is absorbed into the
+ * latent space through k_b[h], every head attends to the same rows (MQA, group
+ * H) with the row as key and c_j as value, and each head's weighted latent is
+ * mapped to the value width through v_b[h]. The three steps are three calls:
+ * mla_absorb_q, attn_decode_mla_absorbed, mla_unabsorb_out. All pointers are
+ * device pointers owned by the caller; bf16 only (GQA_ERR_UNSUPPORTED for f32).
+ */
+
+/* q_abs[b, h, :d_c] = k_b[h] q[b, h, :d_nope] (fp32 accumulation, rounded to
+ * bf16) and q_abs[b, h, d_c:] = q[b, h, d_nope:] (copied).
+ *   q      [B, H, d_nope + d_rope]
+ *   k_b    [H, d_c, d_nope]   (maps qk_nope to the latent space)
+ *   q_abs  [B, H, d_c + d_rope], must not alias q. */
+gqa_status mla_absorb_q(const void* q, const void* k_b, void* q_abs, int B, int H, int d_nope, int d_rope,
+                        int d_c, gqa_dtype dt, void* stream);
+
+/* Decode attention over the latent cache:
+ *   out_lat[b, h] = sum_j w_j c_j / sum_j w_j,  w_j = exp(attention_scale * q_abs[b, h] . latent[b, j]),
+ * over the rows j < seq_lens[b] (the query's own row included, as for
+ * attn_decode_contig), c_j = latent[b, j, :d_c].
+ *   q_abs    [B, H, d_c + d_r]  (16-byte aligned)
+ *   latent   [B, max_len, d_c + d_r]  (16-byte aligned; rows at or past seq_lens[b] may hold anything)
+ *   seq_lens int32 [B], 1 <= seq_lens[b] <= max_len; a length outside that range
+ *            gives a zero output row and sets the device error word (GQA_ERR_DEVICE_BOUNDS)
+ *   out_lat  [B, H, d_c]  (16-byte aligned)
+ * Tensor-core path for (d_c, d_r) = (512, 64), any H (tiles of 128 heads);
+ * other widths return GQA_ERR_UNSUPPORTED. attention_scale > 0 (the unabsorbed
+ * head width's, 1 / sqrt(qk_nope + qk_rope)). workspace: at least
+ * attn_decode_mla_absorbed_workspace_bytes(B, H, d_c, max_len) bytes, 16-byte
+ * aligned (NULL allowed when that is 0). */
+gqa_status attn_decode_mla_absorbed(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
+                                    int B, int max_len, int H, int d_c, int d_r, float attention_scale,
+                                    gqa_dtype dt, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace of attn_decode_mla_absorbed: rows are split 1024 at a time; with S =
+ * ceil(max_len / 1024) > 1 splits, B * H * S * (d_c + 2) floats, else 0. Host only. */
+size_t attn_decode_mla_absorbed_workspace_bytes(int B, int H, int d_c, int max_len);
+
+/* out[b, h] = v_b[h] out_lat[b, h] (fp32 accumulation, rounded to bf16).
+ *   out_lat [B, H, d_c], v_b [H, d_v, d_c], out [B, H, d_v], must not alias out_lat. */
+gqa_status mla_unabsorb_out(const void* out_lat, const void* v_b, void* out, int B, int H, int d_c, int d_v,
+                            gqa_dtype dt, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device: GQA_OK, GQA_ERR_DEVICE_TIMEOUT (takes precedence) or
  * GQA_ERR_DEVICE_BOUNDS; GQA_ERR_CUDA if the stream reports a CUDA error. */

@@ -83,3 +83,28 @@ def test_bad_arguments_rejected_before_launch(lib):
                                     ctypes.byref(bad_sinks), N) == inv
     # empty batches are no-ops
     assert lib.attn_decode_contig(N, N, N, N, 0, N, N, 0, 64, 8, 2, 128, 128, 0.1, 1, N, 0, N) == 0
+
+
+def test_mla_absorbed_workspace_and_checks(lib):
+    """The absorbed-MLA calls: workspace size and host-side rejections (no launch)."""
+    import causal_gqa_attention_row_gb300 as g
+    assert g.attn_decode_mla_absorbed_workspace_bytes(32, 128, 512, 1024) == 0   # one split: none
+    assert g.attn_decode_mla_absorbed_workspace_bytes(32, 128, 512, 4096) == 32 * 128 * 4 * 514 * 4
+    assert g.attn_decode_mla_absorbed_workspace_bytes(2, 16, 512, 1025) == 2 * 16 * 2 * 514 * 4
+    P = ctypes.c_void_p(16)
+    N = None
+    # (q_abs, latent, seq_lens, out_lat, B, max_len, H, d_c, d_r, scale, dtype, workspace, bytes, stream)
+    assert lib.attn_decode_mla_absorbed(P, P, P, P, 2, 64, 16, 256, 64, 0.07, 1, N, 0, N) == 2   # widths
+    assert lib.attn_decode_mla_absorbed(P, P, P, P, 2, 64, 16, 512, 64, 0.07, 0, N, 0, N) == 2   # f32
+    assert lib.attn_decode_mla_absorbed(P, P, P, P, 2, 64, 16, 512, 64, 0.0, 1, N, 0, N) == 2    # scale
+    assert lib.attn_decode_mla_absorbed(N, P, P, P, 2, 64, 16, 512, 64, 0.07, 1, N, 0, N) == 1   # null
+    assert lib.attn_decode_mla_absorbed(ctypes.c_void_p(24), P, P, P, 2, 64, 16, 512, 64, 0.07, 1, N, 0,
+                                        N) == 1                                                   # misaligned
+    assert lib.attn_decode_mla_absorbed(P, P, P, P, 2, 4096, 16, 512, 64, 0.07, 1, N, 0, N) == 4  # workspace
+    assert lib.attn_decode_mla_absorbed(N, N, N, N, 0, 64, 16, 512, 64, 0.07, 1, N, 0, N) == 0    # empty batch
+    # (q, k_b, q_abs, B, H, d_nope, d_rope, d_c, dtype, stream)
+    assert lib.mla_absorb_q(P, P, P, 2, 16, 128, 64, 512, 1, N) == 1                              # q_abs aliases q
+    assert lib.mla_absorb_q(P, P, ctypes.c_void_p(32), 2, 16, 128, 64, 512, 0, N) == 2            # f32
+    # (out_lat, v_b, out, B, H, d_c, d_v, dtype, stream)
+    assert lib.mla_unabsorb_out(P, P, P, 2, 16, 512, 128, 1, N) == 1                              # aliasing
+    assert lib.mla_unabsorb_out(P, P, ctypes.c_void_p(32), 2, 16, 0, 128, 1, N) == 1              # d_c

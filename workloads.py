@@ -149,6 +149,31 @@ def make_paged(B=256, H=32, Hkv=8, dk=128, dv=128, block_size=16, num_blocks=600
                      1.0 / math.sqrt(dk) if scale is None else scale, theta, block_size)
 
 
+@dataclass
+class MlaAbsorbedCase:
+    q: torch.Tensor           # [B, H, d_nope + d_rope], the unabsorbed query
+    k_b: torch.Tensor         # [H, d_c, d_nope], nope slice -> latent
+    v_b: torch.Tensor         # [H, d_v, d_c], latent -> value width
+    latent: torch.Tensor      # [B, max_len, d_c + d_rope]: rows (c_j, k_rot_j)
+    lens: torch.Tensor        # int32 [B]
+    scale: float              # 1 / sqrt(d_nope + d_rope), the unabsorbed head width's
+
+
+def make_mla_absorbed(B=32, H=128, d_nope=128, d_rope=64, d_c=512, d_v=128, max_len=4096, lens=None,
+                      dtype=torch.bfloat16, seed=9, device="cpu") -> MlaAbsorbedCase:
+    """Absorbed MLA decode at the MLA-shaped config's model shape: latent rows
+    N(0, 1); synthetic projections k_b ~ N(0, 1/d_nope) and v_b ~ N(0, 1/d_c), so
+    that q_abs and the output keep unit scale; every sequence at max_len rows
+    unless `lens` is given."""
+    g = generator(seed, device)
+    q = randn((B, H, d_nope + d_rope), g, dtype, device)
+    k_b = (randn((H, d_c, d_nope), g, torch.float32, device) / math.sqrt(d_nope)).to(dtype)
+    v_b = (randn((H, d_v, d_c), g, torch.float32, device) / math.sqrt(d_c)).to(dtype)
+    latent = randn((B, max_len, d_c + d_rope), g, dtype, device)
+    lens = torch.full((B,), max_len, dtype=torch.int32) if lens is None else torch.as_tensor(lens, dtype=torch.int32)
+    return MlaAbsorbedCase(q, k_b, v_b, latent, lens.to(device), 1.0 / math.sqrt(d_nope + d_rope))
+
+
 def make_tiny(seed=0, device="cpu"):
     """The tiny fp32 case: H=4, Hkv=2, d=16, scale 1/4; an 8-row prefill and a
     ninth row (q, k, v) for the decode step after it."""
@@ -171,6 +196,8 @@ WORKLOADS = {
     "prefill_paged": ("chunked prefill bf16 on the paged pool: 4 seqs, H=14, Hkv=2, d=64, bs=16, a 2048-row "
                       "chunk at offsets 0/2048/4096/6144 (history already in the pool)"),
     "prefill_d128": "causal prefill bf16 at the decode configs' head shape: B=1, H=32, Hkv=8, d=128, S=2048",
+    "mla_absorbed": ("absorbed (latent) MLA decode bf16: 32 seqs, 128 heads, latent rows 512 + 64 rot, "
+                     "d_nope=128, d_v=128, len 4096"),
     "prefill_mla": "MLA-shaped causal prefill bf16: B=1, H=32, group 1, d_k=192 (128 + 64 rot), d_v=128, S=2048",
     "prefill_paged_d128": ("chunked prefill bf16 on the paged pool at the decode configs' head shape: 4 seqs, "
                            "H=32, Hkv=8, d=128, bs=16, a 2048-row chunk at offsets 0/2048/4096/6144"),
