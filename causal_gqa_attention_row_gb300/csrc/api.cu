@@ -401,6 +401,7 @@ gqa_status mla_absorb_q(const void* q, const void* k_b, void* q_abs, int B, int 
   if (bf16 != 1) return GQA_ERR_UNSUPPORTED;
   if (B == 0) return GQA_OK;
   if (!q || !k_b || !q_abs || q == q_abs) return GQA_ERR_INVALID_ARG;
+  if (d_nope % 8 || d_rope % 8 || !aligned16(q) || !aligned16(k_b)) return GQA_ERR_INVALID_ARG;
   return from_cuda(gqa::launch_head_matvec(k_b, q, d_nope + d_rope, q_abs, d_c + d_rope, B, H, d_c, d_nope, d_rope,
                                            static_cast<cudaStream_t>(stream)));
 }
@@ -412,6 +413,7 @@ gqa_status mla_unabsorb_out(const void* out_lat, const void* v_b, void* out, int
   if (bf16 != 1) return GQA_ERR_UNSUPPORTED;
   if (B == 0) return GQA_OK;
   if (!out_lat || !v_b || !out || out == out_lat) return GQA_ERR_INVALID_ARG;
+  if (d_c % 8 || !aligned16(out_lat) || !aligned16(v_b)) return GQA_ERR_INVALID_ARG;
   return from_cuda(gqa::launch_head_matvec(v_b, out_lat, d_c, out, d_v, B, H, d_v, d_c, 0,
                                            static_cast<cudaStream_t>(stream)));
 }

@@ -10,34 +10,41 @@
 // from memory serves 2 * H * (2 d_c + d_r) flops: at H = 128 this is a
 // contraction, not a stream, and it runs on the tensor cores.
 //
-// One CTA = one (sequence, tile of 128 heads, split of kChunk cache rows, half
-// of the d_c value columns). The heads are the MMA's 128 rows:
-//   S = Q_abs R^T      M = 128 heads, N = 32 rows of the cache tile, K = d_c + d_r
-//   O += P R[:, half]  M = 128 heads, N = d_c / 2 value columns,    K = 32 rows
-// The cache tile R (32 rows x 576 columns, nine 64-column blocks in the 128-byte
-// swizzle) is read by both: as K (K-major) by the S MMA and, its columns of this
-// CTA's half, as V (MN-major) by the PV MMA, so a row is loaded once per CTA.
-// Tensor memory holds O (256 columns), S (2 x 32) and P (2 x 16: bf16 pairs),
-// 352 of its 512 columns; the full 512-column O of one head tile would leave no
-// room for S, hence the two halves, which compute the same S (identical
-// arithmetic, so their row max and sum agree bit for bit). Shared memory holds
-// Q_abs for the whole CTA lifetime (128 x 576 bf16, 144 KiB) and a two-stage
-// ring of cache tiles (2 x 36 KiB).
+// One cluster of two CTAs = one (sequence, tile of 128 heads, split of kChunk
+// cache rows); CTA r of the pair owns value columns [r d_c / 2, (r + 1) d_c / 2)
+// and the heads are the MMA's 128 rows. Each CTA keeps the Q_abs columns of its
+// value half plus the rope columns (5 of the 9 64-column blocks) and loads the
+// same columns of each 64-row cache tile R, so the score contraction is split
+// between the pair:
+//   S_r = Q_abs[:, cols_r] R[:, cols_r]^T   M = 128 heads, N = 64 rows, K = 256 + 32
+// (the rope block's 64 columns: the first 32 to CTA 0, the last 32 to CTA 1).
+// The partial scores go through distributed shared memory: each CTA stores its
+// S_r row by row into the peer's exchange buffer (asynchronous stores that
+// complete on the peer's barrier), and both form S = S_0 + S_1
+// (one fp32 addition, the same bits on both sides), so the pair runs identical
+// softmax arithmetic and agrees on every row max and sum. Then
+//   O_r += P R[:, value half r]             M = 128 heads, N = 256, K = 64 rows
+// with P (bf16) in tensor memory over the S columns it came from. A cache row
+// is read from memory once per pair (each CTA fetches its 5 blocks), and no
+// score is computed twice.
 //
+// Per CTA: shared memory holds Q_abs's 5 blocks (80 KiB, for the CTA's whole
+// life), a two-stage ring of cache tiles (2 x 40 KiB) and two exchange buffers
+// (2 x 32 KiB); tensor memory holds O (256 columns) and two S buffers (2 x 64).
 // Roles (192 threads):
-//   warps 0-3  softmax: thread t owns head h0 + t (TMEM lane t)
+//   warps 0-3  softmax: thread t owns head h0 + t (TMEM lane t); warp w trades
+//              its 32 rows with warp w of the peer
 //   warp 4     initialises the barriers; TMA producer of Q_abs (once) and of
-//              the cache tiles (lane i issues the box of column block i)
+//              the cache tiles (lane i issues the box of local block i)
 //   warp 5     allocates TMEM; one thread issues the MMAs, S_t as soon as its
-//              tile has landed and PV_t as soon as P_t is in TMEM, whichever
-//              comes first
-// Softmax as in the prefill kernel: a lazily moved reference max (threshold
-// 2^8 in p), p rounded to bf16 and the fp32 row sum taken over exactly those
-// p. Rows of the last tile at or past seq_len weigh zero; their value rows in
-// shared memory are zeroed before the PV MMA reads them, so whatever the cache
-// holds past seq_len (within its capacity) cannot reach the output. A sequence
-// with one split writes O / l as bf16; otherwise each split writes (m, l, O) in
-// fp32 (m in the log2 domain) and the split-combine kernel merges them.
+//              tile has landed and PV_t as soon as P_t is in TMEM
+// Softmax: a lazily moved reference max (threshold 2^8 in p), p rounded to
+// bf16 and the fp32 row sum taken over exactly those p. Rows of the last tile at
+// or past seq_len weigh zero, and their value rows in shared memory are zeroed
+// before the PV MMA reads them, so whatever the cache holds past seq_len
+// (within its capacity) cannot reach the output. A sequence with one split
+// writes O / l as bf16; otherwise each split writes (m, l, O) in fp32 (m in the
+// log2 domain) and the split-combine kernel merges them.
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
@@ -45,8 +52,8 @@
 namespace gqa {
 namespace {
 
-constexpr int kHeads = 128;    // query heads per CTA: the MMA's M
-constexpr int kKeys = 32;      // cache rows per tile: the S MMA's N
+constexpr int kHeads = 128;    // query heads per cluster: the MMA's M
+constexpr int kKeys = 64;      // cache rows per tile: the S MMA's N
 constexpr int kStages = 2;     // cache-tile ring
 constexpr int kThreads = 192;  // four softmax warps, the producer, the MMA warp
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
@@ -56,21 +63,26 @@ constexpr uint32_t kWaitHintNs = 20;
 
 template <int DC, int DR>
 struct MlaCfg {
-  static constexpr int kW = DC + DR;         // row width
-  static constexpr int kCB = kW / 64;        // 64-column blocks of a row
-  static constexpr int kDVH = DC / 2;        // value columns per CTA
-  static constexpr int kCBV = kDVH / 64;     // ... in blocks
-  static constexpr int kQBlk = kHeads * 128; // one block of Q_abs: 128 rows x 128 bytes
-  static constexpr int kRBlk = kKeys * 128;  // one block of a cache tile: 32 rows x 128 bytes
-  static constexpr int kTileQ = kCB * kQBlk;
-  static constexpr int kTileR = kCB * kRBlk;
-  static constexpr int kOffQ = 0, kOffR = kTileQ, kOffBar = kOffR + kStages * kTileR;
+  static constexpr int kW = DC + DR;            // row width
+  static constexpr int kDVH = DC / 2;           // value columns per CTA
+  static constexpr int kCBV = kDVH / 64;        // ... in 64-column blocks
+  static constexpr int kCBR = DR / 64;          // rope blocks (shared by the pair)
+  static constexpr int kCBL = kCBV + kCBR;      // blocks a CTA holds of a row
+  static constexpr int kQBlk = kHeads * 128;    // one block of Q_abs: 128 rows x 128 bytes
+  static constexpr int kRBlk = kKeys * 128;     // one block of a cache tile: 64 rows x 128 bytes
+  static constexpr int kTileQ = kCBL * kQBlk;
+  static constexpr int kTileR = kCBL * kRBlk;
+  static constexpr int kXBuf = kHeads * kKeys * 4;  // one exchange buffer: 128 rows x 64 fp32
+  static constexpr int kOffQ = 0, kOffR = kTileQ, kOffX = kOffR + kStages * kTileR;
+  static constexpr int kOffBar = kOffX + 2 * kXBuf;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
-  // TMEM columns
-  static constexpr uint32_t kColO = 0, kColS = kDVH, kColP = kDVH + 2 * kKeys;
+  // K steps (16 columns) of the score MMA per CTA: its value blocks, and half of the rope blocks
+  static constexpr int kStepsV = kCBV * 4, kStepsR = kCBR * 2;
+  // TMEM columns: O, then the two S buffers (P over the first half of each)
+  static constexpr uint32_t kColO = 0, kColS = kDVH;
   static_assert(DC % 128 == 0 && DR % 64 == 0, "whole 64-column blocks per half");
   static_assert(kDVH % 16 == 0 && kDVH <= 256, "one PV MMA covers the half");
-  static_assert(kColP + 2 * (kKeys / 2) <= kTmemCols, "TMEM map");
+  static_assert(kColS + 2 * kKeys <= kTmemCols, "TMEM map");
   static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
 };
 
@@ -86,10 +98,70 @@ struct MlaParams {
 struct MlaBars {
   uint64_t q_full, r_full[kStages], r_empty[kStages];
   uint64_t s_full[2], p_full[2], o_done[2], mma_final;
+  // per exchange buffer and softmax warp:
+  // x_full: the peer's partial rows have landed in this CTA's buffer (this
+  //         warp's expected bytes, completed by the peer's asynchronous stores);
+  // x_free: the peer has read the rows this CTA wrote into its buffer (arrived
+  //         at by the peer's warp)
+  uint64_t x_full[2][4], x_free[2][4];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(MlaBars) <= 256, "barrier block");
+
+// ---- cluster helpers ---------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared-memory address, in the cluster window, of `p` (an address of this
+// CTA's shared memory) in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+// Asynchronous store of 16 bytes into a peer CTA's shared memory; when they
+// have landed they count as transaction bytes on the peer's mbarrier `bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void arrive_cluster(uint32_t bar_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Probe of a phase with cluster-scope acquire (the peer's writes into this CTA's
+// shared memory are visible once it succeeds).
+__device__ __forceinline__ bool test_parity_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitHintNs)
+      : "memory");
+  return done != 0;
+}
 
 __device__ __forceinline__ bool aborted(MlaBars* bars) {
   return *reinterpret_cast<volatile int*>(&bars->abort_flag);
@@ -104,7 +176,7 @@ __device__ __forceinline__ bool wait_quick(uint64_t* bar, uint32_t parity) {
   return mbar_test_parity_nb(bar, parity) || mbar_wait_hint(bar, parity, kWaitHintNs);
 }
 
-// One thread (producer lane 0): bounded wait, the CTA aborts on a timeout.
+// One thread: bounded wait, the CTA aborts on a timeout.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, MlaBars* bars, unsigned* err) {
   if (aborted(bars)) return false;
   if (wait_quick(bar, parity)) return true;
@@ -115,6 +187,20 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ml
 // Whole warp: every lane agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, MlaBars* bars, unsigned* err) {
   bool ok = !aborted(bars) && wait_quick(bar, parity);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0) abort_all(bars, err);
+  return ok;
+}
+
+// Whole warp, cluster-scope acquire, bounded.
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, MlaBars* bars, unsigned* err) {
+  bool ok = !aborted(bars);
+  if (ok && !test_parity_cluster(bar, parity)) {
+    const long long t0 = clock64();
+    while (!(ok = test_parity_cluster(bar, parity))) {
+      if (clock64() - t0 > kWaitLimitCycles || aborted(bars)) break;
+    }
+  }
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && (threadIdx.x & 31) == 0) abort_all(bars, err);
   return ok;
@@ -151,18 +237,24 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// Byte offset of 16-byte chunk c of row r in an exchange buffer (rows of 256
+// bytes; the chunk index XOR r % 16 spreads a warp's rows over the banks).
+__device__ __forceinline__ uint32_t xchg_off(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 15)) * 16)); }
+
 template <int DC, int DR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_absorbed_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
                            const MlaParams p) {
   using C = MlaCfg<DC, DR>;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // swizzle atoms sit on 1024-byte boundaries of the shared window
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   MlaBars* bars = reinterpret_cast<MlaBars*>(smem + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: the two halves of one (sequence, head tile, split) are neighbours
-  const int half = (int)(blockIdx.x & 1);
+  // ---- work item: the pair of one (sequence, head tile, split) is one cluster
+  const int half = (int)cluster_rank();
+  const uint32_t peer = (uint32_t)(half ^ 1);
   int rest = (int)(blockIdx.x >> 1);
   const int split = rest % p.max_splits;
   rest /= p.max_splits;
@@ -172,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int len = __ldg(p.seq_lens + b);
   const bool len_ok = len >= 1 && len <= p.max_len;
   const int n_split = len_ok ? (len + p.chunk - 1) / p.chunk : 1;
-  if (split >= n_split) return;  // no rows in this split: the whole CTA leaves before any set-up
+  if (split >= n_split) return;  // no rows in this split: both CTAs leave before any set-up
   if (!len_ok) {                 // the heads' output is zero and the error word says why
     if (threadIdx.x == 0 && half == 0 && ht == 0) raise_error(p.err, kErrBounds);
     for (int idx = threadIdx.x; idx < kHeads * C::kDVH; idx += blockDim.x) {
@@ -185,6 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int k1 = min(len, k0 + p.chunk);
   const int n_t = (k1 - k0 + kKeys - 1) / kKeys;  // >= 1
 
+  // the global column block held in local block i: the value half, then the rope blocks
+  auto global_block = [&](int i) { return i < C::kCBV ? half * C::kCBV + i : DC / 64 + (i - C::kCBV); };
+
   if (warp == kProducerWarp) {
     if (lane == 0) {
       mbar_init(&bars->q_full, 1);
@@ -196,6 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->s_full[x], 1);
         mbar_init(&bars->p_full[x], 4);  // one arrival per softmax warp
         mbar_init(&bars->o_done[x], 1);
+        for (int w = 0; w < 4; ++w) {
+          mbar_init(&bars->x_full[x][w], 1);
+          mbar_init(&bars->x_free[x][w], 1);
+        }
       }
       mbar_init(&bars->mma_final, 1);
       bars->abort_flag = 0;
@@ -205,15 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bars->q_full, C::kTileQ);
     }
     __syncwarp();
-    // Q_abs [B, H, W]: rows h0..h0+127 of sequence b (heads past H read as zeros)
-    if (lane < C::kCB) tc::tma_load_4d(smem + C::kOffQ + lane * C::kQBlk, &tm_q, lane * 64, h0, b, 0, &bars->q_full);
+    // Q_abs [B, H, W]: this CTA's blocks of rows h0..h0+127 (heads past H read as zeros)
+    if (lane < C::kCBL)
+      tc::tma_load_4d(smem + C::kOffQ + lane * C::kQBlk, &tm_q, global_block(lane) * 64, h0, b, 0, &bars->q_full);
   }
   if (warp == kMmaWarp) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either arrives at the other's
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
@@ -231,10 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) mbar_arrive_expect_tx(&bars->r_full[st], C::kTileR);
       __syncwarp();
-      // rows k0 + 32t .. +31 of sequence b; rows past the cache's capacity read as zeros
-      if (lane < C::kCB)
-        tc::tma_load_4d(smem + C::kOffR + st * C::kTileR + lane * C::kRBlk, &tm_r, lane * 64, k0 + t * kKeys, b, 0,
-                        &bars->r_full[st]);
+      // rows k0 + 64t .. +63 of sequence b; rows past the cache's capacity read as zeros
+      if (lane < C::kCBL)
+        tc::tma_load_4d(smem + C::kOffR + st * C::kTileR + lane * C::kRBlk, &tm_r, global_block(lane) * 64,
+                        k0 + t * kKeys, b, 0, &bars->r_full[st]);
       __syncwarp();
       issued_last[st] = t;
     }
@@ -250,39 +350,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idS = tc::idesc_bf16_f32(kHeads, kKeys, false);
       const uint32_t idO = tc::idesc_bf16_f32(kHeads, C::kDVH, true);
       constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);  // K-major: 8-row groups 1024 bytes apart
-      const uint64_t dQ = kHi | (smem_u32(smem + C::kOffQ) >> 4);
-      const uint64_t dR0 = kHi | (smem_u32(smem + C::kOffR) >> 4);
+      const uint64_t dQ = kHi | tc::desc_addr(smem + C::kOffQ);
+      const uint64_t dR0 = kHi | tc::desc_addr(smem + C::kOffR);
       // the value half as V: MN-major, 8-row groups 1024 bytes apart, its 64-column
-      // blocks one cache-tile block (4 KiB) apart
-      const uint64_t dV0 =
-          tc::desc_sw128_hi(C::kRBlk, 1024) | (smem_u32(smem + C::kOffR + half * C::kCBV * C::kRBlk) >> 4);
-      const uint32_t tS = tmem + C::kColS, tO = tmem + C::kColO, tP = tmem + C::kColP;
-      auto issue_s = [&](int t) {  // S_{t%2} = Q_abs R_t^T, 16 of the W columns per instruction
+      // blocks one cache-tile block (8 KiB) apart
+      const uint64_t dV0 = tc::desc_sw128_hi(C::kRBlk, 1024) | tc::desc_addr(smem + C::kOffR);
+      const uint32_t tO = tmem + C::kColO;
+      auto issue_s = [&](int t) {  // S_{t%2} = this CTA's share of Q_abs R_t^T
         const int st = t % kStages;
+        const uint32_t tS = tmem + C::kColS + (t & 1) * kKeys;
         tc::fence_after_sync();
         const uint64_t dR = dR0 + (uint64_t)((st * C::kTileR) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < C::kW / 16; ++kk) {
-          const uint32_t aq = (kk / 4) * C::kQBlk + (kk % 4) * 32;
-          const uint32_t ar = (kk / 4) * C::kRBlk + (kk % 4) * 32;
-          tc::mma_f16_ss(tS + (t & 1) * kKeys, dQ + (aq >> 4), dR + (ar >> 4), idS, kk > 0);
+        for (int kk = 0; kk < C::kStepsV + C::kStepsR; ++kk) {
+          // value blocks: all four steps of each; rope blocks: this CTA's two steps of each
+          const int blk = kk < C::kStepsV ? kk / 4 : C::kCBV + (kk - C::kStepsV) / 2;
+          const int step = kk < C::kStepsV ? kk % 4 : half * 2 + (kk - C::kStepsV) % 2;
+          const uint32_t aq = blk * C::kQBlk + step * 32;
+          const uint32_t ar = blk * C::kRBlk + step * 32;
+          tc::mma_f16_ss(tS, dQ + (aq >> 4), dR + (ar >> 4), idS, kk > 0);
         }
         tc::mma_commit(&bars->s_full[t & 1]);
       };
-      auto issue_pv = [&](int t) {  // O += P_{t%2} R_t[:, half], 16 rows per instruction
+      auto issue_pv = [&](int t) {  // O += P_t R_t[:, value half], 16 rows per instruction
         const int st = t % kStages;
+        const uint32_t tP = tmem + C::kColS + (t & 1) * kKeys;
         tc::fence_after_sync();
         const uint64_t dV = dV0 + (uint64_t)((st * C::kTileR) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          tc::mma_f16_ts(tO, tP + (t & 1) * (kKeys / 2) + kk * 8, dV + kk * (2048 >> 4), idO, (t > 0 || kk > 0));
+          tc::mma_f16_ts(tO, tP + kk * 8, dV + kk * (2048 >> 4), idO, (t > 0 || kk > 0));
         tc::mma_commit(&bars->o_done[t & 1]);
         tc::mma_commit(&bars->r_empty[st]);  // the tile's stage is free once PV_t is done
       };
       bool ok = wait_or_abort(&bars->q_full, 0, bars, p.err);
-      // S_t needs tile t in shared memory (which also means PV_{t-2} is done, so S
-      // buffer t % 2 has been read); PV_t needs P_t. Each barrier is probed for its
-      // phases in order, and neither can run two phases ahead of its probe.
+      // S_t needs tile t in shared memory, which also means PV_{t-2} is done: S
+      // buffer t % 2 (holding P_{t-2}) has been read. PV_t needs P_t. Each barrier
+      // is probed for its phases in order and cannot run two phases ahead.
       int next_s = 0, next_pv = 0;
       long long idle_since = clock64();
       while (ok && next_pv < n_t) {
@@ -324,9 +428,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
+      const uint32_t tS = tmem + lane_addr + C::kColS + x * kKeys;
       uint32_t sv[kKeys];
-      tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::kColS + x * kKeys, sv);
+      tc::tmem_ld_32x32b_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tc::tmem_ld_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tc::tmem_ld_wait();
+      // ---- trade partial scores with the peer: this row into its buffer x ...
+      if (t >= 2 && !warp_wait_cluster(&bars->x_free[x][warp], ((t - 2) >> 1) & 1, bars, p.err)) {
+        alive = false;
+        break;
+      }
+      {
+        // the 32 rows of this warp, 256 bytes each, land on the peer's x_full[x][warp]
+        unsigned char* xb = smem + C::kOffX + x * C::kXBuf;
+        const uint32_t rbase = peer_addr(xb, peer);
+        const uint32_t rbar = peer_addr(&bars->x_full[x][warp], peer);
+#pragma unroll
+        for (int c = 0; c < kKeys / 4; ++c)
+          st_async_v4(rbase + xchg_off(r, c), sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3], rbar);
+        // ... and the peer's rows into this CTA's buffer x: S = S_0 + S_1
+        if (lane == 0) mbar_arrive_expect_tx(&bars->x_full[x][warp], 32 * kKeys * 4);
+        if (!warp_wait_cluster(&bars->x_full[x][warp], (t >> 1) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
+        const uint32_t lbase = smem_u32(xb);
+#pragma unroll
+        for (int c = 0; c < kKeys / 4; ++c) {
+          const float4 o = ld_shared_v4(lbase + xchg_off(r, c));
+          sv[4 * c] = __float_as_uint(__uint_as_float(sv[4 * c]) + o.x);
+          sv[4 * c + 1] = __float_as_uint(__uint_as_float(sv[4 * c + 1]) + o.y);
+          sv[4 * c + 2] = __float_as_uint(__uint_as_float(sv[4 * c + 2]) + o.z);
+          sv[4 * c + 3] = __float_as_uint(__uint_as_float(sv[4 * c + 3]) + o.w);
+        }
+        __syncwarp();
+        if (lane == 0) arrive_cluster(peer_addr(&bars->x_free[x][warp], peer));
+      }
       const int kt = k0 + t * kKeys;
       const int valid = min(kKeys, k1 - kt);  // rows of this tile the heads see
       if (valid < kKeys) {
@@ -381,9 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (valid < kKeys) {
-        // value rows valid..31 of this CTA's half: zero them (S_t, their other
+        // value rows valid..63 of this CTA's half: zero them (S_t, their other
         // reader, is done) so that 0 * (whatever the cache holds) cannot be NaN
-        unsigned char* base = smem + C::kOffR + (t % kStages) * C::kTileR + half * C::kCBV * C::kRBlk;
+        unsigned char* base = smem + C::kOffR + (t % kStages) * C::kTileR;
         const int n_chunks = (kKeys - valid) * C::kCBV * 8;  // 16-byte chunks: 8 per row and block
         for (int i = r; i < n_chunks; i += kHeads) {
           const int row = valid + i / (C::kCBV * 8), blk = (i / 8) % C::kCBV, ch = i % 8;
@@ -391,15 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_async_smem();  // visible to the tensor cores' reads
       }
-      // P buffer x was last read by PV_{t-2}
-      if (t >= 2) {
-        if (!warp_wait(&bars->o_done[x], ((t - 2) >> 1) & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
-        tc::fence_after_sync();
-      }
-      tc::tmem_st_32x32b_x16(tmem + lane_addr + C::kColP + x * (kKeys / 2), pv);
+      // P_t over the first 32 columns of S buffer x (S_t has been read; PV_{t-2},
+      // the last reader of P_{t-2} there, completed before S_t was issued)
+      tc::tmem_st_32x32b_x16(tS, *reinterpret_cast<uint32_t(*)[16]>(&pv[0]));
+      tc::tmem_st_32x32b_x16(tS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pv[16]));
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
@@ -455,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc::fence_before_sync();
   __syncthreads();
+  cluster_sync();  // the peer's last accesses to this CTA's shared memory are done
   tc::fence_after_sync();
   if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
@@ -523,7 +656,7 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << dev;
   }
-  const long long ctas = (long long)B * p.n_htiles * p.max_splits * 2;
+  const long long ctas = (long long)B * p.n_htiles * p.max_splits * 2;  // clusters of two
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   mla_absorbed_tc_kernel<512, 64><<<(unsigned)ctas, kThreads, C::kSmemBytes, st>>>(tq, tr, p);
   return cudaGetLastError();

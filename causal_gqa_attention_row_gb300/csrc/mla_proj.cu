@@ -9,7 +9,8 @@
 // One CTA = (64 outputs m, head h, 32 batch rows b); its 256 threads each own
 // 4 outputs x 2 batch rows. The K axis goes through shared memory 64 at a time:
 // the W slice transposed to [k][m] (a thread's 4 outputs are one 16-byte read)
-// and the x slice as [k][b], both widened to fp32.
+// and the x slice as [k][b], both widened to fp32. K, the row strides and the
+// pointers are multiples of 8 elements (16 bytes), which the entry points check.
 #include "common.cuh"
 
 namespace gqa {
@@ -27,16 +28,34 @@ __global__ void __launch_bounds__(kProjThreads)
   const __nv_bfloat16* Wh = W + (size_t)h * M * K;
   float acc[2][4] = {};
   for (int kc = 0; kc < K; kc += kTK) {
-    // W[h][m0 + i][kc + j] -> ws[j][i]; x[b0 + i][h][kc + j] -> xs[j][i] (zero outside)
-    for (int e = threadIdx.x; e < kTM * kTK; e += kProjThreads) {
-      const int i = e / kTK, j = e % kTK;
-      ws[j][i] = (m0 + i < M && kc + j < K) ? __bfloat162float(Wh[(size_t)(m0 + i) * K + kc + j]) : 0.f;
+    // W[h][m0 + i][kc + 8u .. 8u + 7] -> ws[kc-relative k][i], x likewise -> xs[k][b]:
+    // one 16-byte read per task, lanes on consecutive rows (i or b), so the eight
+    // transposed stores of a task hit 32 different banks
+    for (int e = threadIdx.x; e < kTM * (kTK / 8); e += kProjThreads) {
+      const int i = e % kTM, u = e / kTM;
+      float f[8];
+      if (m0 + i < M && kc + 8 * u < K) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(Wh + (size_t)(m0 + i) * K + kc + 8 * u);
+        Elem<__nv_bfloat16>::chunk_to_f32(raw, f);
+      } else {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) f[v] = 0.f;
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v) ws[8 * u + v][i] = f[v];
     }
-    for (int e = threadIdx.x; e < kTB * kTK; e += kProjThreads) {
-      const int i = e / kTK, j = e % kTK;
-      xs[j][i] = (b0 + i < B && kc + j < K)
-                     ? __bfloat162float(x[((size_t)(b0 + i) * H + h) * x_stride + kc + j])
-                     : 0.f;
+    for (int e = threadIdx.x; e < kTB * (kTK / 8); e += kProjThreads) {
+      const int i = e % kTB, u = e / kTB;
+      float f[8];
+      if (b0 + i < B && kc + 8 * u < K) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(x + ((size_t)(b0 + i) * H + h) * x_stride + kc + 8 * u);
+        Elem<__nv_bfloat16>::chunk_to_f32(raw, f);
+      } else {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) f[v] = 0.f;
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v) xs[8 * u + v][i] = f[v];
     }
     __syncthreads();
 #pragma unroll 8

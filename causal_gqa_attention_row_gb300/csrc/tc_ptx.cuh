@@ -179,12 +179,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // The same descriptor split into a constant high part (offsets, version,
 // layout) and the start-address field, so that a loop of MMAs over one tile
-// only adds (byte offset >> 4) to a precomputed value. Valid while the start
-// address stays below 256 KiB (always true for shared memory).
+// only adds (byte offset >> 4) to a precomputed value. The start-address field
+// takes desc_addr(p): in a cluster launch a shared address carries the CTA's
+// rank above bit 18, which must not spill into the offset fields.
 __host__ __device__ constexpr uint64_t desc_sw128_hi(uint32_t lbo, uint32_t sbo) {
   return ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
          (2ull << 61);
 }
+
+// Start-address field of a shared-memory descriptor: the address within the
+// CTA's own shared memory, >> 4 (14 bits).
+__device__ __forceinline__ uint64_t desc_addr(const void* p) { return (uint64_t)((smem_u32(p) & 0x3FFFFu) >> 4); }
 
 }  // namespace tc
 }  // namespace gqa

@@ -293,7 +293,8 @@ size_t attn_decode_workspace_bytes(int B, int H, int d_v, int max_len_upper_boun
  * bf16) and q_abs[b, h, d_c:] = q[b, h, d_nope:] (copied).
  *   q      [B, H, d_nope + d_rope]
  *   k_b    [H, d_c, d_nope]   (maps qk_nope to the latent space)
- *   q_abs  [B, H, d_c + d_rope], must not alias q. */
+ *   q_abs  [B, H, d_c + d_rope], must not alias q.
+ * d_nope and d_rope multiples of 8; q and k_b 16-byte aligned. */
 gqa_status mla_absorb_q(const void* q, const void* k_b, void* q_abs, int B, int H, int d_nope, int d_rope,
                         int d_c, gqa_dtype dt, void* stream);
 
@@ -320,7 +321,8 @@ gqa_status attn_decode_mla_absorbed(const void* q_abs, const void* latent, const
 size_t attn_decode_mla_absorbed_workspace_bytes(int B, int H, int d_c, int max_len);
 
 /* out[b, h] = v_b[h] out_lat[b, h] (fp32 accumulation, rounded to bf16).
- *   out_lat [B, H, d_c], v_b [H, d_v, d_c], out [B, H, d_v], must not alias out_lat. */
+ *   out_lat [B, H, d_c], v_b [H, d_v, d_c], out [B, H, d_v], must not alias out_lat.
+ * d_c a multiple of 8; out_lat and v_b 16-byte aligned. */
 gqa_status mla_unabsorb_out(const void* out_lat, const void* v_b, void* out, int B, int H, int d_c, int d_v,
                             gqa_dtype dt, void* stream);
 
