@@ -18,9 +18,10 @@
 // between the pair:
 //   S_r = Q_abs[:, cols_r] R[:, cols_r]^T   M = 128 heads, N = 64 rows, K = 256 + 32
 // (the rope block's 64 columns: the first 32 to CTA 0, the last 32 to CTA 1).
-// The partial scores go through distributed shared memory: each CTA stores its
-// S_r row by row into the peer's exchange buffer (asynchronous stores that
-// complete on the peer's barrier), and both form S = S_0 + S_1
+// The partial scores go through distributed shared memory: each softmax warp
+// writes its rows of S_r into a local send buffer and moves them with one bulk
+// copy into the peer's receive buffer (completing on the peer's barrier), and
+// both CTAs form S = S_0 + S_1
 // (one fp32 addition, the same bits on both sides), so the pair runs identical
 // softmax arithmetic and agrees on every row max and sum. Then
 //   O_r += P R[:, value half r]             M = 128 heads, N = 256, K = 64 rows
@@ -29,8 +30,9 @@
 // score is computed twice.
 //
 // Per CTA: shared memory holds Q_abs's 5 blocks (80 KiB, for the CTA's whole
-// life), a two-stage ring of cache tiles (2 x 40 KiB) and two exchange buffers
-// (2 x 32 KiB); tensor memory holds O (256 columns) and two S buffers (2 x 64).
+// life), a two-stage ring of cache tiles (2 x 40 KiB) and the receive and send
+// buffers of the exchange (2 x 32 KiB); tensor memory holds O (256 columns) and
+// two S buffers (2 x 64).
 // Roles (192 threads):
 //   warps 0-3  softmax: thread t owns head h0 + t (TMEM lane t); warp w trades
 //              its 32 rows with warp w of the peer
@@ -72,7 +74,7 @@ struct MlaCfg {
   static constexpr int kRBlk = kKeys * 128;     // one block of a cache tile: 64 rows x 128 bytes
   static constexpr int kTileQ = kCBL * kQBlk;
   static constexpr int kTileR = kCBL * kRBlk;
-  static constexpr int kXBuf = kHeads * kKeys * 4;  // one exchange buffer: 128 rows x 64 fp32
+  static constexpr int kXBuf = kHeads * kKeys * 4;  // 128 rows x 64 fp32: the receive buffer, then the send buffer
   static constexpr int kOffQ = 0, kOffR = kTileQ, kOffX = kOffR + kStages * kTileR;
   static constexpr int kOffBar = kOffX + 2 * kXBuf;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
@@ -98,12 +100,12 @@ struct MlaParams {
 struct MlaBars {
   uint64_t q_full, r_full[kStages], r_empty[kStages];
   uint64_t s_full[2], p_full[2], o_done[2], mma_final;
-  // per exchange buffer and softmax warp:
-  // x_full: the peer's partial rows have landed in this CTA's buffer (this
-  //         warp's expected bytes, completed by the peer's asynchronous stores);
-  // x_free: the peer has read the rows this CTA wrote into its buffer (arrived
-  //         at by the peer's warp)
-  uint64_t x_full[2][4], x_free[2][4];
+  // per softmax warp (its 32 rows, 8 KiB of each buffer):
+  // x_full: the peer's partial rows have landed in this CTA's receive buffer
+  //         (this warp's expected bytes, completed by the peer's bulk copy);
+  // x_free: the peer has read the rows this CTA copied into its receive buffer
+  //         (so that copy, and the read of this CTA's send buffer, are done)
+  uint64_t x_full[4], x_free[4];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -125,13 +127,16 @@ __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
   return r;
 }
 
-// Asynchronous store of 16 bytes into a peer CTA's shared memory; when they
-// have landed they count as transaction bytes on the peer's mbarrier `bar`.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-               "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+// Bulk copy of `bytes` from this CTA's shared memory into a peer CTA's; when
+// they have landed they count as transaction bytes on the peer's mbarrier `bar`.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
@@ -291,10 +296,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bars->s_full[x], 1);
         mbar_init(&bars->p_full[x], 4);  // one arrival per softmax warp
         mbar_init(&bars->o_done[x], 1);
-        for (int w = 0; w < 4; ++w) {
-          mbar_init(&bars->x_full[x][w], 1);
-          mbar_init(&bars->x_free[x][w], 1);
-        }
+      }
+      for (int w = 0; w < 4; ++w) {
+        mbar_init(&bars->x_full[w], 1);
+        mbar_init(&bars->x_free[w], 1);
       }
       mbar_init(&bars->mma_final, 1);
       bars->abort_flag = 0;
@@ -433,26 +438,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::tmem_ld_32x32b_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
       tc::tmem_ld_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tc::tmem_ld_wait();
-      // ---- trade partial scores with the peer: this row into its buffer x ...
-      if (t >= 2 && !warp_wait_cluster(&bars->x_free[x][warp], ((t - 2) >> 1) & 1, bars, p.err)) {
+      // ---- trade partial scores with the peer. This warp's rows go into the send
+      // buffer (free once the peer has read the previous tile: that also means
+      // the copy out of it is done), one bulk copy moves them into the peer's
+      // receive buffer, and the peer's rows arrive in this CTA's.
+      if (t >= 1 && !warp_wait_cluster(&bars->x_free[warp], (t - 1) & 1, bars, p.err)) {
         alive = false;
         break;
       }
       {
-        // the 32 rows of this warp, 256 bytes each, land on the peer's x_full[x][warp]
-        unsigned char* xb = smem + C::kOffX + x * C::kXBuf;
-        const uint32_t rbase = peer_addr(xb, peer);
-        const uint32_t rbar = peer_addr(&bars->x_full[x][warp], peer);
+        unsigned char* recv = smem + C::kOffX;
+        unsigned char* send = smem + C::kOffX + C::kXBuf;
+        const uint32_t sbase = smem_u32(send);
 #pragma unroll
         for (int c = 0; c < kKeys / 4; ++c)
-          st_async_v4(rbase + xchg_off(r, c), sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3], rbar);
-        // ... and the peer's rows into this CTA's buffer x: S = S_0 + S_1
-        if (lane == 0) mbar_arrive_expect_tx(&bars->x_full[x][warp], 32 * kKeys * 4);
-        if (!warp_wait_cluster(&bars->x_full[x][warp], (t >> 1) & 1, bars, p.err)) {
+          st_shared_v4(sbase + xchg_off(r, c), sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
+        tc::fence_async_smem();  // the rows visible to the bulk copy
+        __syncwarp();
+        constexpr uint32_t kWarpBytes = 32 * kKeys * 4;
+        if (lane == 0) {
+          bulk_copy_to_peer(peer_addr(recv + warp * kWarpBytes, peer), send + warp * kWarpBytes, kWarpBytes,
+                            peer_addr(&bars->x_full[warp], peer));
+          mbar_arrive_expect_tx(&bars->x_full[warp], kWarpBytes);
+        }
+        // S = S_0 + S_1
+        if (!warp_wait_cluster(&bars->x_full[warp], t & 1, bars, p.err)) {
           alive = false;
           break;
         }
-        const uint32_t lbase = smem_u32(xb);
+        const uint32_t lbase = smem_u32(recv);
 #pragma unroll
         for (int c = 0; c < kKeys / 4; ++c) {
           const float4 o = ld_shared_v4(lbase + xchg_off(r, c));
@@ -462,7 +476,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           sv[4 * c + 3] = __float_as_uint(__uint_as_float(sv[4 * c + 3]) + o.w);
         }
         __syncwarp();
-        if (lane == 0) arrive_cluster(peer_addr(&bars->x_free[x][warp], peer));
+        if (lane == 0) arrive_cluster(peer_addr(&bars->x_free[warp], peer));
       }
       const int kt = k0 + t * kKeys;
       const int valid = min(kKeys, k1 - kt);  // rows of this tile the heads see
