@@ -10,7 +10,7 @@
 // from memory serves 2 * H * (2 d_c + d_r) flops: at H = 128 this is a
 // contraction, not a stream, and it runs on the tensor cores.
 //
-// One cluster of two CTAs = one (sequence, tile of 128 heads, split of kChunk
+// One cluster of two CTAs = one (sequence, tile of 128 heads, split of p.chunk
 // cache rows); CTA r of the pair owns value columns [r d_c / 2, (r + 1) d_c / 2)
 // and the heads are the MMA's 128 rows. Each CTA keeps the Q_abs columns of its
 // value half plus the rope columns (5 of the 9 64-column blocks) and loads the
