@@ -539,11 +539,34 @@ def run_mla_absorbed(args, peaks, peak_kind):
     queue_ahead(n, us_per_group=80.0)
     ms_step = timed(step, n, st, sync_first=False)
     assert g.attn_get_device_error() == g.OK
+    # the same rows in a paged pool of 64-row blocks (a seeded permutation of the
+    # blocks; two pools alternate), through attn_decode_mla_absorbed_paged
+    bs = 64
+    mbps = L // bs
+    gl = W.generator(10)
+    pools, tables = [], []
+    for lat in latents:
+        perm = torch.randperm(B * mbps, generator=gl).to(torch.int32)
+        tab = perm.view(B, mbps).to(dev)
+        pool = torch.empty(B * mbps, bs, D_C + D_R, dtype=torch.bfloat16, device=dev)
+        pool[tab.view(-1).long()] = lat.view(B * mbps, bs, D_C + D_R)
+        pools.append(pool)
+        tables.append(tab)
+    del pool
+    attend_paged = lambda k: g.attn_decode_mla_absorbed_paged(q_abs, pools[k % 2], tables[k % 2], c.lens, out_lat,
+                                                              c.scale, workspace=ws)
+    for i in range(3):
+        attend_paged(i)
+    torch.cuda.synchronize()
+    queue_ahead(n, us_per_group=60.0)
+    ms_paged = timed(attend_paged, n, st, sync_first=False)
+    assert g.attn_get_device_error() == g.OK
     gbs = nbytes / (ms * 1e-3) / 1e9
     tflops = flops / (ms * 1e-3) / 1e12
     hbm, bf = peaks["hbm_gbs"], peaks["bf16_tflops"]
     return {"workload": W.WORKLOADS["mla_absorbed"], "ms": ms, "gbs": gbs, "tflops": tflops, "bytes": nbytes,
-            "flops": flops, "step_ms": ms_step,
+            "flops": flops, "step_ms": ms_step, "paged_bs64_ms": ms_paged,
+            "paged_bs64_gbs": nbytes / (ms_paged * 1e-3) / 1e9,
             "step": "mla_absorb_q + attn_decode_mla_absorbed + mla_unabsorb_out",
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "tensor_tflops": tflops, "tensor_frac": tflops / bf,

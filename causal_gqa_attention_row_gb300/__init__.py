@@ -25,7 +25,7 @@ EXPORTS = ("attn_prefill_causal", "attn_decode_contig", "attn_decode_paged", "kv
            "gqa_status_string", "gqa_debug_withhold_first_tile", "attn_decode_paged_static_workspace",
            "attn_prefill_causal_ex", "attn_decode_contig_ex", "attn_decode_paged_ex", "attn_prefill_paged",
            "attn_prefill_paged_ex", "mla_absorb_q", "attn_decode_mla_absorbed",
-           "attn_decode_mla_absorbed_workspace_bytes", "mla_unabsorb_out")
+           "attn_decode_mla_absorbed_workspace_bytes", "mla_unabsorb_out", "attn_decode_mla_absorbed_paged")
 
 
 class GqaArms(ctypes.Structure):
@@ -71,6 +71,7 @@ def load(path: str = None):
         "mla_absorb_q": [P, P, P, I, I, I, I, I, I, P],
         "attn_decode_mla_absorbed": [P, P, P, P, I, I, I, I, I, F, I, P, S, P],
         "mla_unabsorb_out": [P, P, P, I, I, I, I, I, P],
+        "attn_decode_mla_absorbed_paged": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, S, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -256,6 +257,22 @@ def attn_decode_mla_absorbed(q_abs, latent, seq_lens, out_lat, attention_scale, 
     _check(load().attn_decode_mla_absorbed(_p(q_abs), _p(latent), _i32(seq_lens), _p(out_lat), B, L, H, d_c, w - d_c,
                                            float(attention_scale), _dtype(q_abs, latent, out_lat), _p(workspace), ws,
                                            _stream(stream)), "attn_decode_mla_absorbed")
+    return out_lat
+
+
+def attn_decode_mla_absorbed_paged(q_abs, latent_pool, block_tables, seq_lens, out_lat, attention_scale,
+                                   workspace=None, stream=None):
+    """q_abs [B, H, d_c + d_r]; latent_pool [num_blocks, bs, d_c + d_r]; block_tables int32
+    [B, mbps]; seq_lens int32 [B]; out_lat [B, H, d_c] (bf16)."""
+    B, H, w = q_abs.shape
+    nb, bs, _ = latent_pool.shape
+    d_c = out_lat.shape[-1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().attn_decode_mla_absorbed_paged(_p(q_abs), _p(latent_pool), _i32(block_tables), _i32(seq_lens),
+                                                 _p(out_lat), B, block_tables.shape[1], nb, bs, H, d_c, w - d_c,
+                                                 float(attention_scale), _dtype(q_abs, latent_pool, out_lat),
+                                                 _p(workspace), ws, _stream(stream)),
+           "attn_decode_mla_absorbed_paged")
     return out_lat
 
 

@@ -355,28 +355,27 @@ size_t attn_decode_mla_absorbed_workspace_bytes(int B, int H, int d_c, int max_l
   return (size_t)B * (size_t)H * splits * (size_t)(d_c + 2) * sizeof(float);
 }
 
-gqa_status attn_decode_mla_absorbed(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
-                                    int B, int max_len, int H, int d_c, int d_r, float attention_scale, gqa_dtype dt,
-                                    void* workspace, size_t workspace_bytes, void* stream) {
-  const int bf16 = dtype_flag(dt);
-  if (bf16 < 0 || B < 0 || max_len <= 0 || H <= 0 || d_c <= 0 || d_r < 0 || !std::isfinite(attention_scale))
-    return GQA_ERR_INVALID_ARG;
+// The absorbed MLA decode, contiguous latent cache (tables NULL) or paged pool.
+static gqa_status mla_absorbed_common(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
+                                      int B, int capacity, int H, int d_c, int d_r, float attention_scale, int bf16,
+                                      void* workspace, size_t workspace_bytes, cudaStream_t st,
+                                      const int32_t* tables, int mbps, int bs, int num_blocks) {
   if (!gqa::mla_absorbed_tc_supported(bf16, d_c, d_r) || !(attention_scale > 0.f)) return GQA_ERR_UNSUPPORTED;
   if (B == 0) return GQA_OK;
   if (!q_abs || !latent || !seq_lens || !out_lat) return GQA_ERR_INVALID_ARG;
   if (!aligned16(q_abs) || !aligned16(latent) || !aligned16(out_lat)) return GQA_ERR_INVALID_ARG;
-  const size_t need = attn_decode_mla_absorbed_workspace_bytes(B, H, d_c, max_len);
+  const size_t need = attn_decode_mla_absorbed_workspace_bytes(B, H, d_c, capacity);
   if (need > 0) {
     if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_INVALID_ARG;
   }
   unsigned* err = error_word();
   if (!err) return GQA_ERR_CUDA;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float qscale = attention_scale * 1.4426950408889634f;
   float* partial = need > 0 ? static_cast<float*>(workspace) : nullptr;
-  const cudaError_t e = gqa::launch_mla_absorbed_tc(q_abs, latent, seq_lens, out_lat, partial, B, max_len, H, d_c,
-                                                    d_r, gqa::kMlaChunk, qscale, err, st);
+  const cudaError_t e = gqa::launch_mla_absorbed_tc(q_abs, latent, seq_lens, out_lat, partial, B, capacity, H, d_c,
+                                                    d_r, gqa::kMlaChunk, qscale, err, st, tables, mbps, bs,
+                                                    num_blocks);
   if (e != cudaSuccess || need == 0) return from_cuda(e);
   // the splits of each (sequence, head) merged into out_lat
   gqa::RowsParams p{};
@@ -386,12 +385,39 @@ gqa_status attn_decode_mla_absorbed(const void* q_abs, const void* latent, const
   p.B = B;
   p.seq_q = 1;
   p.H = H;
-  p.capacity = max_len;
+  p.capacity = capacity;
   p.split_rows = gqa::kMlaChunk;
-  p.max_splits = ceil_div(max_len, gqa::kMlaChunk);
+  p.max_splits = ceil_div(capacity, gqa::kMlaChunk);
   p.window = 0;
   p.err = err;
   return from_cuda(gqa::launch_split_combine(p, d_c, 1, st));
+}
+
+gqa_status attn_decode_mla_absorbed(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
+                                    int B, int max_len, int H, int d_c, int d_r, float attention_scale, gqa_dtype dt,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  const int bf16 = dtype_flag(dt);
+  if (bf16 < 0 || B < 0 || max_len <= 0 || H <= 0 || d_c <= 0 || d_r < 0 || !std::isfinite(attention_scale))
+    return GQA_ERR_INVALID_ARG;
+  return mla_absorbed_common(q_abs, latent, seq_lens, out_lat, B, max_len, H, d_c, d_r, attention_scale, bf16,
+                             workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, 0, 0, 0);
+}
+
+gqa_status attn_decode_mla_absorbed_paged(const void* q_abs, const void* latent_pool, const int32_t* block_tables,
+                                          const int32_t* seq_lens, void* out_lat, int B, int max_blocks_per_seq,
+                                          int num_blocks, int block_size, int H, int d_c, int d_r,
+                                          float attention_scale, gqa_dtype dt, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  const int bf16 = dtype_flag(dt);
+  if (bf16 < 0 || B < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0 || H <= 0 || d_c <= 0 ||
+      d_r < 0 || !std::isfinite(attention_scale))
+    return GQA_ERR_INVALID_ARG;
+  if ((long long)max_blocks_per_seq * block_size > INT_MAX / 2) return GQA_ERR_INVALID_ARG;
+  if (!gqa::mla_absorbed_paged_block_ok(block_size)) return GQA_ERR_UNSUPPORTED;
+  if (B > 0 && !block_tables) return GQA_ERR_INVALID_ARG;
+  return mla_absorbed_common(q_abs, latent_pool, seq_lens, out_lat, B, max_blocks_per_seq * block_size, H, d_c, d_r,
+                             attention_scale, bf16, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                             block_tables, max_blocks_per_seq, block_size, num_blocks);
 }
 
 gqa_status mla_absorb_q(const void* q, const void* k_b, void* q_abs, int B, int H, int d_nope, int d_rope, int d_c,

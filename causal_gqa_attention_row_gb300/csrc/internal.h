@@ -104,9 +104,13 @@ bool prefill_tc_supported(int bf16, int dk, int dv, int bs = 0, int mbps = 0);
 // (m, l, o) into partial [B * H, ceil(max_len / chunk), d_c + 2] when a sequence
 // has more than one, and the split combine merges them.
 bool mla_absorbed_tc_supported(int bf16, int d_c, int d_r);
+// Paged (tables != NULL): latent is a pool [num_blocks, bs, d_c + d_r], max_len
+// is ignored (mbps * bs rows per sequence), bs one of 8, 16, 32, 64.
 cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
                                    float* partial, int B, int max_len, int H, int d_c, int d_r, int chunk,
-                                   float qscale, unsigned* err, cudaStream_t st);
+                                   float qscale, unsigned* err, cudaStream_t st, const int32_t* tables = nullptr,
+                                   int mbps = 0, int bs = 0, int num_blocks = 0);
+bool mla_absorbed_paged_block_ok(int bs);
 // Rows of one split of the absorbed MLA decode (a fixed number, so a sequence's
 // result does not depend on the rest of the batch).
 constexpr int kMlaChunk = 1024;

@@ -89,8 +89,12 @@ struct MlaCfg {
 };
 
 struct MlaParams {
-  int B, H, max_len, chunk, max_splits, n_htiles;
+  int B, H, max_len, chunk, max_splits, n_htiles;  // max_len: rows a sequence can hold
   const int32_t* seq_lens;  // [B] rows visible, >= 1 and <= max_len
+  // paged cache (tables != NULL): a pool [num_blocks, bs, d_c + d_r]; row j of
+  // sequence b in block tables[b * mbps + j / bs], slot j % bs; bs divides 64
+  const int32_t* tables;
+  int mbps, bs, num_blocks;
   float* partial;           // [B * H, max_splits, d_c + 2] when max_splits > 1
   __nv_bfloat16* out;       // [B, H, d_c]
   float qscale;             // attention_scale * log2(e)
@@ -327,8 +331,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int issued_last[kStages];
 #pragma unroll
     for (int s = 0; s < kStages; ++s) issued_last[s] = -1;
+    // paged: a tile is `per` pool blocks; lane x < per * kCBL issues the box of
+    // block x % per and column block x / per (each box a whole number of 8-row
+    // swizzle atoms, so the boxes land where one box of the tile would put them)
+    const int per = p.tables ? kKeys / p.bs : 1;
+    const int nbox = per * C::kCBL;
     for (int t = 0; t < n_t; ++t) {
       const int st = t % kStages;
+      int blk[2] = {0, 0};
+      if (p.tables) {  // the tile's table entries, fetched before waiting for the stage
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int x = lane + 32 * u;
+          if (x >= nbox) continue;
+          const int ti = (k0 + t * kKeys) / p.bs + x % per;
+          // a block past the sequence, or an entry out of range (flagged), loads
+          // from past the end of the pool: the TMA engine fills it with zeros
+          int e = p.num_blocks;
+          if (ti < p.mbps && ti * p.bs < len) {
+            e = __ldg(p.tables + (size_t)b * p.mbps + ti);
+            if (e < 0 || e >= p.num_blocks) {
+              raise_error(p.err, kErrBounds);
+              e = p.num_blocks;
+            }
+          }
+          blk[u] = e;
+        }
+      }
       if (t >= kStages) {  // the stage is free once PV_{t-2} is done
         bool ok = true;
         if (lane == 0) ok = wait_or_abort(&bars->r_empty[st], ((t / kStages) - 1) & 1, bars, p.err);
@@ -336,10 +365,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) mbar_arrive_expect_tx(&bars->r_full[st], C::kTileR);
       __syncwarp();
-      // rows k0 + 64t .. +63 of sequence b; rows past the cache's capacity read as zeros
-      if (lane < C::kCBL)
-        tc::tma_load_4d(smem + C::kOffR + st * C::kTileR + lane * C::kRBlk, &tm_r, global_block(lane) * 64,
-                        k0 + t * kKeys, b, 0, &bars->r_full[st]);
+      unsigned char* dst = smem + C::kOffR + st * C::kTileR;
+      if (!p.tables) {
+        // rows k0 + 64t .. +63 of sequence b; rows past the cache's capacity read as zeros
+        if (lane < C::kCBL)
+          tc::tma_load_4d(dst + lane * C::kRBlk, &tm_r, global_block(lane) * 64, k0 + t * kKeys, b, 0,
+                          &bars->r_full[st]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int x = lane + 32 * u;
+          if (x < nbox)
+            tc::tma_load_4d(dst + (x / per) * C::kRBlk + (x % per) * p.bs * 128, &tm_r, global_block(x / per) * 64, 0,
+                            blk[u], 0, &bars->r_full[st]);
+        }
+      }
       __syncwarp();
       issued_last[st] = t;
     }
@@ -638,18 +678,33 @@ bool make_rows_map(CUtensorMap* m, const void* base, int w, uint64_t d1, uint64_
 
 bool mla_absorbed_tc_supported(int bf16, int d_c, int d_r) { return bf16 == 1 && d_c == 512 && d_r == 64; }
 
+bool mla_absorbed_paged_block_ok(int bs) { return bs > 0 && bs % 8 == 0 && kKeys % bs == 0; }
+
 cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
                                    float* partial, int B, int max_len, int H, int d_c, int d_r, int chunk,
-                                   float qscale, unsigned* err, cudaStream_t st) {
+                                   float qscale, unsigned* err, cudaStream_t st, const int32_t* tables, int mbps,
+                                   int bs, int num_blocks) {
   using C = MlaCfg<512, 64>;
   if (!mla_absorbed_tc_supported(1, d_c, d_r) || chunk % kKeys != 0 || chunk <= 0 || !(qscale > 0.f))
     return cudaErrorNotSupported;
+  if (tables && !mla_absorbed_paged_block_ok(bs)) return cudaErrorNotSupported;
   if (B == 0) return cudaSuccess;
   CUtensorMap tq, tr;
-  // q_abs [B, H, 576]: box of 128 heads; latent [B, max_len, 576]: box of 32 rows
+  // q_abs [B, H, 576]: box of 128 heads
   if (!make_rows_map(&tq, q_abs, C::kW, (uint64_t)H, (uint64_t)B, kHeads)) return cudaErrorInvalidValue;
-  if (!make_rows_map(&tr, latent, C::kW, (uint64_t)max_len, (uint64_t)B, kKeys)) return cudaErrorInvalidValue;
+  if (tables) {
+    // pool [num_blocks, bs, 576]: box of one block
+    if (!make_rows_map(&tr, latent, C::kW, (uint64_t)bs, (uint64_t)num_blocks, (uint32_t)bs)) return cudaErrorInvalidValue;
+    max_len = mbps * bs;
+  } else {
+    // latent [B, max_len, 576]: box of one 64-row tile
+    if (!make_rows_map(&tr, latent, C::kW, (uint64_t)max_len, (uint64_t)B, kKeys)) return cudaErrorInvalidValue;
+  }
   MlaParams p;
+  p.tables = tables;
+  p.mbps = mbps;
+  p.bs = bs;
+  p.num_blocks = num_blocks;
   p.B = B;
   p.H = H;
   p.max_len = max_len;

@@ -316,6 +316,23 @@ gqa_status attn_decode_mla_absorbed(const void* q_abs, const void* latent, const
                                     int B, int max_len, int H, int d_c, int d_r, float attention_scale,
                                     gqa_dtype dt, void* workspace, size_t workspace_bytes, void* stream);
 
+/* attn_decode_mla_absorbed over a paged latent cache: row j of sequence b is
+ * latent_pool[block_tables[b * max_blocks_per_seq + j / block_size], j % block_size]
+ * (the paged addressing of attn_decode_paged with one latent row per slot).
+ *   latent_pool  [num_blocks, block_size, d_c + d_r]  (16-byte aligned)
+ *   block_tables int32 [B, max_blocks_per_seq]; entries past a sequence's rows are never read
+ *   seq_lens     1 <= seq_lens[b] <= max_blocks_per_seq * block_size
+ * block_size one of 8, 16, 32, 64 (else GQA_ERR_UNSUPPORTED). A table entry outside
+ * [0, num_blocks) for a visible row sets GQA_ERR_DEVICE_BOUNDS and its rows read as
+ * zeros. Same arithmetic as the contiguous call: the outputs are bit-identical to
+ * it on the same rows. Workspace: attn_decode_mla_absorbed_workspace_bytes(B, H, d_c,
+ * max_blocks_per_seq * block_size). */
+gqa_status attn_decode_mla_absorbed_paged(const void* q_abs, const void* latent_pool, const int32_t* block_tables,
+                                          const int32_t* seq_lens, void* out_lat, int B, int max_blocks_per_seq,
+                                          int num_blocks, int block_size, int H, int d_c, int d_r,
+                                          float attention_scale, gqa_dtype dt, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
 /* Workspace of attn_decode_mla_absorbed: rows are split 1024 at a time; with S =
  * ceil(max_len / 1024) > 1 splits, B * H * S * (d_c + 2) floats, else 0. Host only. */
 size_t attn_decode_mla_absorbed_workspace_bytes(int B, int H, int d_c, int max_len);

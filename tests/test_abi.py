@@ -108,3 +108,15 @@ def test_mla_absorbed_workspace_and_checks(lib):
     # (out_lat, v_b, out, B, H, d_c, d_v, dtype, stream)
     assert lib.mla_unabsorb_out(P, P, P, 2, 16, 512, 128, 1, N) == 1                              # aliasing
     assert lib.mla_unabsorb_out(P, P, ctypes.c_void_p(32), 2, 16, 0, 128, 1, N) == 1              # d_c
+
+
+def test_mla_absorbed_paged_checks(lib):
+    P = ctypes.c_void_p(16)
+    N = None
+    # (q_abs, pool, tables, seq_lens, out, B, mbps, num_blocks, bs, H, d_c, d_r, scale, dtype, ws, bytes, stream)
+    assert lib.attn_decode_mla_absorbed_paged(P, P, P, P, P, 2, 8, 100, 24, 16, 512, 64, 0.07, 1, N, 0, N) == 2
+    assert lib.attn_decode_mla_absorbed_paged(P, P, N, P, P, 2, 8, 100, 16, 16, 512, 64, 0.07, 1, N, 0, N) == 1
+    assert lib.attn_decode_mla_absorbed_paged(P, P, P, P, P, 2, 0, 100, 16, 16, 512, 64, 0.07, 1, N, 0, N) == 1
+    assert lib.attn_decode_mla_absorbed_paged(P, P, P, P, P, 2, 128, 100, 16, 16, 512, 64, 0.07, 1, N, 0,
+                                              N) == 4  # 2048 rows: two splits need a workspace
+    assert lib.attn_decode_mla_absorbed_paged(N, N, N, N, N, 0, 8, 100, 16, 16, 512, 64, 0.07, 1, N, 0, N) == 0

@@ -158,3 +158,65 @@ def test_full_size_sampled_sequences(gpu_lib):
         want = oracle_latent(q_abs[b:b + 1], c.latent[b:b + 1], c.lens[b:b + 1], c.scale)
         err = np.abs(out[b:b + 1].float().cpu().numpy() - want).max()
         assert err <= 2e-2, (b, err)
+
+
+def page_latent(latent, lens, bs, seed, spare=3):
+    """The latent rows of each sequence scattered over a pool of bs-row blocks in
+    a seeded permuted order; table entries past a sequence's rows are -1."""
+    B, L, w = latent.shape
+    mbps = (L + bs - 1) // bs
+    need = [(int(n) + bs - 1) // bs for n in lens]
+    nb = sum(need) + spare
+    perm = torch.randperm(nb, generator=W.generator(seed)).to(torch.int32)
+    pool = torch.full((nb, bs, w), float("nan"), dtype=latent.dtype, device=latent.device)
+    tables = torch.full((B, mbps), -1, dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(need):
+        for i in range(n):
+            blk = int(perm[at])
+            rows = latent[b, i * bs:(i + 1) * bs]
+            pool[blk, :rows.shape[0]] = rows
+            tables[b, i] = blk
+            at += 1
+    return pool, tables.to(latent.device)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+def test_paged_equals_contiguous_bit_for_bit(gpu_lib, bs):
+    """The same rows through a permuted pool of bs-row blocks give the same bits
+    as the contiguous cache (the slots past each sequence's rows hold NaN)."""
+    g = gpu_lib
+    L = 2112
+    lens = [1, 63, 1025, 2100, L]
+    c = W.make_mla_absorbed(B=5, H=128, max_len=L, lens=lens, seed=97)
+    q_abs = absorbed_q(g, c)
+    latent = c.latent.to(DEV)
+    lens_d = c.lens.to(DEV)
+    want = attend(g, q_abs, latent, lens_d, c.scale)
+    pool, tables = page_latent(latent, lens, bs, seed=98 + bs)
+    out = torch.full((5, 128, D_C), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = g.mla_absorbed_workspace(5, 128, D_C, tables.shape[1] * bs)
+    g.attn_decode_mla_absorbed_paged(q_abs, pool, tables, lens_d, out, c.scale, workspace=ws)
+    assert g.attn_get_device_error() == g.OK
+    assert torch.equal(out, want)
+    ref = oracle_latent(q_abs[3:4], latent[3:4], c.lens[3:4], c.scale)
+    assert np.abs(out[3:4].float().cpu().numpy() - ref).max() <= 2e-2
+
+
+def test_paged_bad_entry_is_flagged(gpu_lib):
+    """A table entry outside the pool for a visible row sets the bounds error; the
+    other sequences' outputs are unaffected."""
+    g = gpu_lib
+    lens = [300, 700]
+    c = W.make_mla_absorbed(B=2, H=128, max_len=704, lens=lens, seed=99)
+    q_abs = absorbed_q(g, c)
+    latent = c.latent.to(DEV)
+    pool, tables = page_latent(latent, lens, 16, seed=100)
+    good = torch.empty(2, 128, D_C, dtype=torch.bfloat16, device=DEV)
+    g.attn_decode_mla_absorbed_paged(q_abs, pool, tables, c.lens.to(DEV), good, c.scale)
+    assert g.attn_get_device_error() == g.OK
+    tables[0, 5] = pool.shape[0] + 7
+    out = torch.empty(2, 128, D_C, dtype=torch.bfloat16, device=DEV)
+    g.attn_decode_mla_absorbed_paged(q_abs, pool, tables, c.lens.to(DEV), out, c.scale)
+    assert g.attn_get_device_error() == g.ERR_DEVICE_BOUNDS
+    assert torch.equal(out[1], good[1])
