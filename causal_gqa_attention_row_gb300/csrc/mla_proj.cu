@@ -9,8 +9,9 @@
 // One CTA = (64 outputs m, head h, 32 batch rows b); its 256 threads each own
 // 4 outputs x 2 batch rows. The K axis goes through shared memory 64 at a time:
 // the W slice transposed to [k][m] (a thread's 4 outputs are one 16-byte read)
-// and the x slice as [k][b], both widened to fp32. K, the row strides and the
-// pointers are multiples of 8 elements (16 bytes), which the entry points check.
+// and the x slice as [k][b], both widened to fp32, the next slice's global reads
+// in flight during this one's FMAs. K, the row strides and the pointers are
+// multiples of 8 elements (16 bytes), which the entry points check.
 #include "common.cuh"
 
 namespace gqa {
@@ -27,37 +28,49 @@ __global__ void __launch_bounds__(kProjThreads)
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;  // outputs m0 + 4 tx .. +3, rows b0 + 2 ty, +1
   const __nv_bfloat16* Wh = W + (size_t)h * M * K;
   float acc[2][4] = {};
-  for (int kc = 0; kc < K; kc += kTK) {
-    // W[h][m0 + i][kc + 8u .. 8u + 7] -> ws[kc-relative k][i], x likewise -> xs[k][b]:
-    // one 16-byte read per task, lanes on consecutive rows (i or b), so the eight
-    // transposed stores of a task hit 32 different banks
-    for (int e = threadIdx.x; e < kTM * (kTK / 8); e += kProjThreads) {
-      const int i = e % kTM, u = e / kTM;
-      float f[8];
-      if (m0 + i < M && kc + 8 * u < K) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(Wh + (size_t)(m0 + i) * K + kc + 8 * u);
-        Elem<__nv_bfloat16>::chunk_to_f32(raw, f);
-      } else {
+  // K is staged 64 at a time: each thread moves kWTasks 16-byte pieces of W and
+  // kXTasks of x per chunk (W[h][m0 + i][kc + 8u ..] -> ws[8u ..][i], x likewise
+  // -> xs[8u ..][b]; lanes on consecutive rows, so the eight transposed stores of
+  // a piece hit 32 different banks). The next chunk's pieces are read from
+  // global memory into registers while this chunk's FMAs run.
+  constexpr int kWTasks = kTM * (kTK / 8) / kProjThreads, kXTasks = kTB * (kTK / 8) / kProjThreads;
+  static_assert(kWTasks * kProjThreads == kTM * (kTK / 8) && kXTasks * kProjThreads == kTB * (kTK / 8), "tasks");
+  uint4 wr[kWTasks], xr[kXTasks];
+  auto fetch = [&](int kc) {
 #pragma unroll
-        for (int v = 0; v < 8; ++v) f[v] = 0.f;
-      }
+    for (int q = 0; q < kWTasks; ++q) {
+      const int e = threadIdx.x + q * kProjThreads, i = e % kTM, u = e / kTM;
+      wr[q] = (m0 + i < M && kc + 8 * u < K) ? *reinterpret_cast<const uint4*>(Wh + (size_t)(m0 + i) * K + kc + 8 * u)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int q = 0; q < kXTasks; ++q) {
+      const int e = threadIdx.x + q * kProjThreads, i = e % kTB, u = e / kTB;
+      xr[q] = (b0 + i < B && kc + 8 * u < K)
+                  ? *reinterpret_cast<const uint4*>(x + ((size_t)(b0 + i) * H + h) * x_stride + kc + 8 * u)
+                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  fetch(0);
+  for (int kc = 0; kc < K; kc += kTK) {
+#pragma unroll
+    for (int q = 0; q < kWTasks; ++q) {
+      const int e = threadIdx.x + q * kProjThreads, i = e % kTM, u = e / kTM;
+      float f[8];
+      Elem<__nv_bfloat16>::chunk_to_f32(wr[q], f);
 #pragma unroll
       for (int v = 0; v < 8; ++v) ws[8 * u + v][i] = f[v];
     }
-    for (int e = threadIdx.x; e < kTB * (kTK / 8); e += kProjThreads) {
-      const int i = e % kTB, u = e / kTB;
-      float f[8];
-      if (b0 + i < B && kc + 8 * u < K) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(x + ((size_t)(b0 + i) * H + h) * x_stride + kc + 8 * u);
-        Elem<__nv_bfloat16>::chunk_to_f32(raw, f);
-      } else {
 #pragma unroll
-        for (int v = 0; v < 8; ++v) f[v] = 0.f;
-      }
+    for (int q = 0; q < kXTasks; ++q) {
+      const int e = threadIdx.x + q * kProjThreads, i = e % kTB, u = e / kTB;
+      float f[8];
+      Elem<__nv_bfloat16>::chunk_to_f32(xr[q], f);
 #pragma unroll
       for (int v = 0; v < 8; ++v) xs[8 * u + v][i] = f[v];
     }
     __syncthreads();
+    if (kc + kTK < K) fetch(kc + kTK);
 #pragma unroll 8
     for (int j = 0; j < kTK; ++j) {
       const float4 w4 = *reinterpret_cast<const float4*>(&ws[j][4 * tx]);
