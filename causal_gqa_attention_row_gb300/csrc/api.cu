@@ -420,6 +420,18 @@ gqa_status attn_decode_mla_absorbed_paged(const void* q_abs, const void* latent_
                              block_tables, max_blocks_per_seq, block_size, num_blocks);
 }
 
+// y[b, h, :M] = W[h] x[b, h, :K] (+ the tail columns copied): the tensor-core
+// kernel for the shapes it takes, else the SIMT one.
+static gqa_status head_projection(const void* W, const void* x, int x_stride, void* y, int y_stride, int B, int H,
+                                  int M, int K, int tail, cudaStream_t st) {
+  if (gqa::head_proj_tc_supported(M, K)) {
+    unsigned* err = error_word();
+    if (!err) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_head_proj_tc(W, x, x_stride, y, y_stride, B, H, M, K, tail, err, st));
+  }
+  return from_cuda(gqa::launch_head_matvec(W, x, x_stride, y, y_stride, B, H, M, K, tail, st));
+}
+
 gqa_status mla_absorb_q(const void* q, const void* k_b, void* q_abs, int B, int H, int d_nope, int d_rope, int d_c,
                         gqa_dtype dt, void* stream) {
   const int bf16 = dtype_flag(dt);
@@ -428,8 +440,8 @@ gqa_status mla_absorb_q(const void* q, const void* k_b, void* q_abs, int B, int 
   if (B == 0) return GQA_OK;
   if (!q || !k_b || !q_abs || q == q_abs) return GQA_ERR_INVALID_ARG;
   if (d_nope % 8 || d_rope % 8 || !aligned16(q) || !aligned16(k_b)) return GQA_ERR_INVALID_ARG;
-  return from_cuda(gqa::launch_head_matvec(k_b, q, d_nope + d_rope, q_abs, d_c + d_rope, B, H, d_c, d_nope, d_rope,
-                                           static_cast<cudaStream_t>(stream)));
+  return head_projection(k_b, q, d_nope + d_rope, q_abs, d_c + d_rope, B, H, d_c, d_nope, d_rope,
+                         static_cast<cudaStream_t>(stream));
 }
 
 gqa_status mla_unabsorb_out(const void* out_lat, const void* v_b, void* out, int B, int H, int d_c, int d_v,
@@ -440,8 +452,7 @@ gqa_status mla_unabsorb_out(const void* out_lat, const void* v_b, void* out, int
   if (B == 0) return GQA_OK;
   if (!out_lat || !v_b || !out || out == out_lat) return GQA_ERR_INVALID_ARG;
   if (d_c % 8 || !aligned16(out_lat) || !aligned16(v_b)) return GQA_ERR_INVALID_ARG;
-  return from_cuda(gqa::launch_head_matvec(v_b, out_lat, d_c, out, d_v, B, H, d_v, d_c, 0,
-                                           static_cast<cudaStream_t>(stream)));
+  return head_projection(v_b, out_lat, d_c, out, d_v, B, H, d_v, d_c, 0, static_cast<cudaStream_t>(stream));
 }
 
 gqa_status attn_get_device_error(void* stream) {

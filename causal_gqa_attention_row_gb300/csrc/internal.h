@@ -120,4 +120,10 @@ constexpr int kMlaChunk = 1024;
 cudaError_t launch_head_matvec(const void* W, const void* x, int x_stride, void* y, int y_stride, int B, int H, int M,
                                int K, int tail, cudaStream_t st);
 
+// The same product on tcgen05 (bf16): W's rows in tiles of 128 (M % 128 == 0),
+// K % 64 == 0 and K <= 512; cudaErrorNotSupported otherwise.
+bool head_proj_tc_supported(int M, int K);
+cudaError_t launch_head_proj_tc(const void* W, const void* x, int x_stride, void* y, int y_stride, int B, int H, int M,
+                                int K, int tail, unsigned* err, cudaStream_t st);
+
 }  // namespace gqa

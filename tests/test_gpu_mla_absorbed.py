@@ -220,3 +220,24 @@ def test_paged_bad_entry_is_flagged(gpu_lib):
     g.attn_decode_mla_absorbed_paged(q_abs, pool, tables, c.lens.to(DEV), out, c.scale)
     assert g.attn_get_device_error() == g.ERR_DEVICE_BOUNDS
     assert torch.equal(out[1], good[1])
+
+
+def test_projections_other_widths_match_oracle(gpu_lib):
+    """Widths the tensor-core projection does not take (rows not a multiple of
+    128, K not a multiple of 64) go through the SIMT kernel: same bound."""
+    g = gpu_lib
+    B, H, dn, dr, dc, dv = 5, 3, 40, 16, 96, 24
+    gen = W.generator(101)
+    q = W.randn((B, H, dn + dr), gen, torch.bfloat16)
+    k_b = (W.randn((H, dc, dn), gen) / 6.0).to(torch.bfloat16)
+    v_b = (W.randn((H, dv, dc), gen) / 10.0).to(torch.bfloat16)
+    q_abs = torch.empty(B, H, dc + dr, dtype=torch.bfloat16, device=DEV)
+    g.mla_absorb_q(q.to(DEV), k_b.to(DEV), q_abs)
+    want = core.mla_absorb_q(W.to_oracle(q), W.to_oracle(k_b), dn)
+    got = q_abs.float().cpu().numpy()
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-3)
+    out = torch.empty(B, H, dv, dtype=torch.bfloat16, device=DEV)
+    g.mla_unabsorb_out(q_abs[..., :dc].contiguous(), v_b.to(DEV), out)
+    want = core.mla_unabsorb_out(W.to_oracle(q_abs[..., :dc]), W.to_oracle(v_b))
+    assert np.all(np.abs(out.float().cpu().numpy() - want) <= 2.0 ** -8 * np.abs(want) + 1e-3)
+    assert g.attn_get_device_error() == g.OK
