@@ -241,3 +241,16 @@ def test_projections_other_widths_match_oracle(gpu_lib):
     want = core.mla_unabsorb_out(W.to_oracle(q_abs[..., :dc]), W.to_oracle(v_b))
     assert np.all(np.abs(out.float().cpu().numpy() - want) <= 2.0 ** -8 * np.abs(want) + 1e-3)
     assert g.attn_get_device_error() == g.OK
+
+
+def test_long_sequence_many_splits(gpu_lib):
+    """One 40,000-row sequence (40 splits: the combine walks its split weights in
+    two passes of 32) and a short one beside it, against the oracle."""
+    g = gpu_lib
+    c = W.make_mla_absorbed(B=2, H=128, max_len=40000, lens=[40000, 5], seed=102, device=DEV)
+    q_abs = absorbed_q(g, c)
+    out = attend(g, q_abs, c.latent, c.lens, c.scale)
+    assert g.attn_get_device_error() == g.OK
+    want = oracle_latent(q_abs, c.latent, c.lens, c.scale)
+    err = np.abs(out.float().cpu().numpy() - want).max()
+    assert err <= 2e-2, err
