@@ -96,33 +96,57 @@ __device__ __forceinline__ void item_split_counts(const RowsParams& p, int item,
   part = (kv_hi % p.split_rows) != 0;
 }
 
+// Partial units are listed longest first, in buckets of kPartBucketRows rows
+// (largest-first scheduling: the last units to be taken are the shortest, so the
+// CTAs run out of work at nearly the same time). The order inside a bucket is
+// arbitrary; it only decides which CTA takes a unit, never what a unit computes.
+constexpr int kPartBuckets = 64;
+
 __global__ void __launch_bounds__(kPlanThreads) plan_units_kernel(const RowsParams p) {
   __shared__ int warp_sums[32];
+  __shared__ int bucket_at[kPartBuckets];
   const int n_items = p.B * p.Hkv * p.n_hchunks * p.n_rblocks;
-  // thread t owns the contiguous items [lo, hi): one scan for the full units, one
-  // for the partial ones, in item order (the list order does not depend on the
-  // thread count)
+  for (int i = threadIdx.x; i < kPartBuckets; i += blockDim.x) bucket_at[i] = 0;
+  // thread t owns the contiguous items [lo, hi): one scan for the full units (in
+  // item order), a count of the partial ones per length bucket
   const int per = (n_items + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(n_items, (int)threadIdx.x * per), hi = min(n_items, lo + per);
-  int my_full = 0, my_part = 0;
+  auto bucket_of = [&](int item, int split) {
+    const int b = item / (p.n_rblocks * p.n_hchunks * p.Hkv);
+    const int rb = item % p.n_rblocks;
+    const int kv_len = p.kv_len ? p.kv_len[b] : (p.offsets ? p.offsets[b] : 0) + p.seq_q;
+    const int i_last = min(rb * p.QR + p.QR, p.seq_q) - 1;
+    const int rows = kv_len - p.seq_q + i_last + 1 - split * p.split_rows;  // 1 .. split_rows - 1
+    const int bk = (int)(((long long)(p.split_rows - rows) * kPartBuckets) / p.split_rows);
+    return min(max(bk, 0), kPartBuckets - 1);  // 0: the longest
+  };
+  __syncthreads();
+  int my_full = 0;
   for (int item = lo; item < hi; ++item) {
     int full, part, s_first;
     item_split_counts(p, item, full, part, s_first);
     my_full += full;
-    my_part += part;
+    if (part) atomicAdd(&bucket_at[bucket_of(item, s_first + full)], 1);
   }
-  int n_full, n_part;
+  int n_full;
   int at_full = block_exclusive_scan(my_full, warp_sums, n_full);
-  int at_part = n_full + block_exclusive_scan(my_part, warp_sums, n_part);
+  // bucket starts (exclusive), after the full units
+  if (threadIdx.x == 0) {
+    int at = n_full;
+    for (int i = 0; i < kPartBuckets; ++i) {
+      const int c = bucket_at[i];
+      bucket_at[i] = at;
+      at += c;
+    }
+    p.sched[1] = at;
+    p.sched[0] = 0;
+  }
+  __syncthreads();
   for (int item = lo; item < hi; ++item) {
     int full, part, s_first;
     item_split_counts(p, item, full, part, s_first);
     for (int s = 0; s < full; ++s) p.units[at_full++] = make_int2(item, s_first + s);
-    if (part) p.units[at_part++] = make_int2(item, s_first + full);
-  }
-  if (threadIdx.x == 0) {
-    p.sched[0] = 0;
-    p.sched[1] = n_full + n_part;
+    if (part) p.units[atomicAdd(&bucket_at[bucket_of(item, s_first + full)], 1)] = make_int2(item, s_first + full);
   }
 }
 
