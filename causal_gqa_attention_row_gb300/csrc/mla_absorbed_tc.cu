@@ -47,9 +47,9 @@
 // (within its capacity) cannot reach the output. A sequence with one split
 // writes O / l as bf16; otherwise each split writes (m, l, O) in fp32 (m in the
 // log2 domain) and the split-combine kernel merges them.
-#include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace gqa {
 namespace {
@@ -646,32 +646,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // A bf16 tensor [d2, d1, w] (rows of w elements); box = 64 columns x box1 rows,
 // 128-byte swizzle; rows and columns past the tensor read as zeros.
 bool make_rows_map(CUtensorMap* m, const void* base, int w, uint64_t d1, uint64_t d2, uint32_t box1) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)w, d1, d2, 1};
-  const cuuint64_t strides[3] = {(cuuint64_t)w * 2, (cuuint64_t)w * 2 * d1, (cuuint64_t)w * 2 * d1 * d2};
-  const cuuint32_t box[4] = {64, box1, 1, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[4] = {(uint64_t)w, d1, d2, 1};
+  const uint64_t strides[3] = {(uint64_t)w * 2, (uint64_t)w * 2 * d1, (uint64_t)w * 2 * d1 * d2};
+  const uint32_t box[4] = {64, box1, 1, 1};
+  return make_tmap_bf16(m, base, dims, strides, box);
 }
 
 }  // namespace

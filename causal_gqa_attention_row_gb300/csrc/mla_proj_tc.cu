@@ -11,9 +11,9 @@
 // K / 16 MMAs into a 32-column TMEM accumulator, and the four warps write their
 // 32 rows of it (thread = output row m, its 32 columns = the batch rows) to y as
 // bf16. Batch rows past B read as zeros and are not written.
-#include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace gqa {
 namespace {
@@ -105,33 +105,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, 32);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // A bf16 tensor [d2, d1, d0] with rows of `stride` elements (d0 <= stride);
 // box = 64 columns x box1 x box2, 128-byte swizzle, zeros outside.
 bool make_map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t stride, uint64_t d1, uint64_t d2,
                uint32_t box1, uint32_t box2) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {d0, d1, d2, 1};
-  const cuuint64_t strides[3] = {stride * 2, stride * 2 * d1, stride * 2 * d1 * d2};
-  const cuuint32_t box[4] = {64, box1, box2, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[4] = {d0, d1, d2, 1};
+  const uint64_t strides[3] = {stride * 2, stride * 2 * d1, stride * 2 * d1 * d2};
+  const uint32_t box[4] = {64, box1, box2, 1};
+  return make_tmap_bf16(m, base, dims, strides, box);
 }
 
 }  // namespace

@@ -50,9 +50,9 @@
 // exchange their (m, l), each merges half of the columns of the two partial O
 // rows into bf16 in shared memory (over the Q tile), and one TMA store writes
 // the output tile.
-#include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace gqa {
 namespace {
@@ -654,33 +654,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // A 4-D bf16 tensor of rows of d elements; box = 64 x b1 x b2 x 1 (one 64-column
 // block of the rows), 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int d, uint64_t d1, uint64_t d2, uint64_t d3, uint32_t box1,
               uint32_t box2) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)d, d1, d2, d3};
-  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * d1, (cuuint64_t)d * 2 * d1 * d2};
-  const cuuint32_t box[4] = {64, box1, box2, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[4] = {(uint64_t)d, d1, d2, d3};
+  const uint64_t strides[3] = {(uint64_t)d * 2, (uint64_t)d * 2 * d1, (uint64_t)d * 2 * d1 * d2};
+  const uint32_t box[4] = {64, box1, box2, 1};
+  return make_tmap_bf16(m, base, dims, strides, box);
 }
 
 template <int DK, int DV>
