@@ -21,8 +21,10 @@
  *  - Layouts are dense row-major with the shapes given below; head and row
  *    widths d_k, d_v must be multiples of 8 and every tensor pointer 16-byte
  *    aligned.
- *  - Supported head widths (d_k, d_v): (16,16), (32,32), (64,64), (128,128),
- *    (256,256), (192,128); others return GQA_ERR_UNSUPPORTED.
+ *  - Supported head widths (d_k, d_v) of the attention calls: (16,16), (32,32),
+ *    (64,64), (128,128), (256,256), (192,128); others return
+ *    GQA_ERR_UNSUPPORTED. The absorbed MLA calls (their own section below) take
+ *    a 512-wide latent with a 64-wide rotated part, bf16 only.
  *  - Errors a host check can see (null pointer, H % Hkv != 0, bad size or
  *    alignment, small workspace) are returned before anything is launched.
  *  - Errors only the device can see (a block-table entry outside
