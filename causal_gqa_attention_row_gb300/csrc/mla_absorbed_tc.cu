@@ -466,6 +466,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float2 qs2 = make_float2(qs, qs);
     float m_ref = -INFINITY, l_run = 0.f;
     bool alive = true;
+    int consumed = -1;    // the last tile whose partial rows from the peer this warp has read
+    bool posted = false;  // the expected bytes of tile consumed + 1 are on x_full
     for (int t = 0; t < n_t; ++t) {
       const int x = t & 1;
       if (!warp_wait(&bars->s_full[x], (t >> 1) & 1, bars, p.err)) {
@@ -501,6 +503,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             peer_addr(&bars->x_full[warp], peer));
           mbar_arrive_expect_tx(&bars->x_full[warp], kWarpBytes);
         }
+        posted = true;
         // S = S_0 + S_1
         if (!warp_wait_cluster(&bars->x_full[warp], t & 1, bars, p.err)) {
           alive = false;
@@ -515,6 +518,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           sv[4 * c + 2] = __float_as_uint(__uint_as_float(sv[4 * c + 2]) + o.z);
           sv[4 * c + 3] = __float_as_uint(__uint_as_float(sv[4 * c + 3]) + o.w);
         }
+        consumed = t;
+        posted = false;
         __syncwarp();
         if (lane == 0) arrive_cluster(peer_addr(&bars->x_free[warp], peer));
       }
@@ -590,6 +595,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full[x]);
+    }
+    if (!alive && consumed + 1 < n_t) {
+      // after a wait gave up: the peer may still be copying its rows of the next
+      // tile into this CTA's receive buffer (at most that one copy: it needs this
+      // warp's x_free for every earlier tile). Wait for it, bounded, so that no
+      // copy lands after the CTA has exited.
+      if (lane == 0 && !posted) mbar_arrive_expect_tx(&bars->x_full[warp], 32 * kKeys * 4);
+      __syncwarp();
+      const long long t0 = clock64();
+      while (!test_parity_cluster(&bars->x_full[warp], (consumed + 1) & 1) && clock64() - t0 < kWaitLimitCycles) {
+      }
     }
     // ---- the last PV (its commit covers every earlier MMA), then the output
     bool have_o = alive;
