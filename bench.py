@@ -196,6 +196,9 @@ def run_paged(args, rank, world):
 
     for i in range(args.warmup):
         step(i)
+        if i == 0 and sample:  # the step the CPU-baseline sample replays: keep its output rows
+            for s in sample:
+                s["gpu_out"] = out[s["b"]:s["b"] + 1].float().cpu().numpy()
     torch.cuda.synchronize()
     assert g.attn_get_device_error() == g.OK
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -299,7 +302,7 @@ def gather_paged_sample(c, q, kn, vn, nseq):
         n = int(lens[b]) + 1
         nblk = (n + bs - 1) // bs
         blocks = c.tables[b, :nblk].long()
-        seqs.append(dict(q=W.to_oracle(q[b:b + 1]), kn=W.to_oracle(kn[b:b + 1]), vn=W.to_oracle(vn[b:b + 1]),
+        seqs.append(dict(b=b, q=W.to_oracle(q[b:b + 1]), kn=W.to_oracle(kn[b:b + 1]), vn=W.to_oracle(vn[b:b + 1]),
                          kp=W.to_oracle(c.k_pool[blocks]), vp=W.to_oracle(c.v_pool[blocks]),
                          table=np.arange(nblk, dtype=np.int32)[None], len=int(lens[b])))
     return seqs
@@ -308,7 +311,8 @@ def gather_paged_sample(c, q, kn, vn, nseq):
 def oracle_paged_sample(sample, theta, scale, max_seconds, min_seconds=10.0):
     """Run the oracle's append + decode over the sampled sequences, pass after
     pass until at least min_seconds of oracle time is spent (stopping early once
-    max_seconds is); returns (algorithmic bytes, seconds, sequences run, passes)."""
+    max_seconds is); returns (algorithmic bytes, seconds, sequences run, passes).
+    The first pass leaves each sequence's oracle output in s["want"]."""
     from oracle import core
     done, t_total, n, passes = 0, 0.0, 0, 0
     while passes == 0 or t_total < min_seconds:
@@ -317,8 +321,10 @@ def oracle_paged_sample(sample, theta, scale, max_seconds, min_seconds=10.0):
             t = time.perf_counter()
             q2, kp2, vp2, l2 = core.kv_append_paged(s["q"], s["kn"], s["vn"], s["kp"], s["vp"], s["table"],
                                                     [s["len"]], theta)
-            core.decode_paged(q2, kp2, vp2, s["table"], l2, scale)
+            want = core.decode_paged(q2, kp2, vp2, s["table"], l2, scale)
             t_total += time.perf_counter() - t
+            if passes == 1:
+                s["want"] = want
             H, (Hkv, d) = s["q"].shape[1], s["kn"].shape[1:]
             dec, app = paged_bytes(np.array([s["len"] + 1]), 1, H, Hkv, d, d, s["kp"].shape[2])
             done += dec + app
@@ -681,6 +687,13 @@ def main():
                "sample": f"append + decode of {len(res['sample'])} of the {args.seqs} sequences (the shortest, the "
                          f"longest, seeded others) of the paged workload, {passes} pass(es), {n} sequence runs; "
                          f"{secs:.1f} s of oracle time"}
+        # the oracle's outputs against the GPU's for the same step (first warm-up
+        # step: same history, same new rows), element by element
+        compared = [s for s in res["sample"] if "want" in s and "gpu_out" in s]
+        err = max(float(np.abs(s["gpu_out"] - s["want"]).max()) for s in compared)
+        cpu["parity"] = {"sequences": len(compared), "max_abs_err": err, "tol": 2e-2}
+        if not err <= 2e-2:
+            raise SystemExit(f"GPU output disagrees with the oracle on the CPU-baseline sample: max abs err {err}")
     hbm = peaks["hbm_gbs"]
     line = {
         "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,

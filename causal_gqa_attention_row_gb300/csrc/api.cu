@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libgqa_attn.so (include/gqa_attn.h):
 // host-side argument checks, work decomposition, and launches. No device
 // memory is allocated here; the only device state is the error word below.
+#include <atomic>
 #include <cmath>
 #include <climits>
 #include <cstdint>
@@ -17,16 +18,19 @@ namespace {
 
 int g_withhold_first_tile = 0;
 
+// Device address of the error word on the current device, looked up once per
+// device; the cache is atomic, so concurrent first calls from several host
+// threads are safe (each stores the same value).
 unsigned* error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  static unsigned* cache[64] = {};
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_gqa_error_word) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<unsigned*>(p);
+  static std::atomic<void*> cache[64];
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_gqa_error_word) != cudaSuccess || p == nullptr) return nullptr;
+    cache[dev].store(p, std::memory_order_release);
   }
-  return cache[dev];
+  return static_cast<unsigned*>(p);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -9,9 +9,13 @@
 // Such a caller can pass the inputs and outputs it already owns, but not the
 // split-K scratch that attn_decode_paged takes as `workspace`.
 //
-// Here that scratch is a fixed array in the library's own device data. It is
-// part of the module image, so every GPU on which the library's kernels are
-// loaded holds it until the process exits; no call here allocates anything.
+// Here that scratch is a fixed array in the library's own device data. The CUDA
+// runtime places it on a device when it loads this file's module there: with
+// lazy module loading (CUDA's default) that happens at the first call on the
+// device, which looks up the array's address; with eager loading, when the
+// context is created. From then on the device holds it until the process exits,
+// and no call here allocates anything.
+#include <atomic>
 #include <climits>
 
 #include "gqa_attn.h"
@@ -26,17 +30,19 @@ static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspa
 
 // Host-side device address of g_static_workspace, per device. In host code the
 // name g_static_workspace is only a host-side stand-in, never a device address,
-// so the address is fetched once per device with that device current.
+// so the address is fetched with that device current and cached. The cache is
+// atomic: host threads making their first calls at the same time may each look
+// the address up, and they store the same value.
 void* static_workspace_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  static void* cache[64] = {};
-  if (!cache[dev]) {
-    void* ptr = nullptr;
+  static std::atomic<void*> cache[64];
+  void* ptr = cache[dev].load(std::memory_order_acquire);
+  if (!ptr) {
     if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || ptr == nullptr) return nullptr;
-    cache[dev] = ptr;
+    cache[dev].store(ptr, std::memory_order_release);
   }
-  return cache[dev];
+  return ptr;
 }
 
 }  // namespace
@@ -48,15 +54,15 @@ extern "C" gqa_status attn_decode_paged_static_workspace(const void* q, const vo
                                                          float attention_scale, gqa_dtype dt, void* stream) {
   if (max_blocks_per_seq <= 0 || block_size <= 0 || (long long)max_blocks_per_seq * block_size > INT_MAX / 2)
     return GQA_ERR_INVALID_ARG;
+  // Every call, B = 0 included, makes sure the array is on the current device
+  // first, so that a call with B = 0 is a complete set-up call.
+  void* ws = static_workspace_ptr();
+  if (!ws) return GQA_ERR_CUDA;
   const size_t need = attn_decode_workspace_bytes(B, H, d_v, max_blocks_per_seq * block_size);
   if (need > kStaticWorkspaceBytes) return GQA_ERR_WORKSPACE;  // beyond the fixed maximum
-  void* ws = nullptr;
-  if (need > 0) {
-    ws = static_workspace_ptr();
-    if (!ws) return GQA_ERR_CUDA;
-  }
-  // Nothing in the scratch needs clearing: every partial a call reads was
-  // written earlier in the same call.
+  // Nothing in the scratch needs clearing: the plan's ticket counter is reset by
+  // the call's own planning kernel, and every partial a call reads was written
+  // earlier in the same call.
   return attn_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, out, B, max_blocks_per_seq, num_blocks,
                            block_size, H, Hkv, d_k, d_v, attention_scale, dt, ws, kStaticWorkspaceBytes, stream);
 }

@@ -223,12 +223,18 @@ gqa_status attn_prefill_paged_ex(const void* q, const void* k_pool, const void* 
  * max_blocks_per_seq * block_size) > GQA_STATIC_WORKSPACE_BYTES) is rejected
  * with GQA_ERR_WORKSPACE before anything is launched.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture begins. Every call shares the one array per device: two calls whose
- * kernels overlap on the GPU (different streams, no ordering between them) race
- * on it and may return wrong results. Calls ordered on one stream are safe; no
- * contents need clearing between them.
+ * Set-up: the first call on a device (a call with B = 0 is enough, and does
+ * nothing else) looks up the array's device address with that device current.
+ * Under CUDA's lazy module loading, the default, that is also when the CUDA
+ * runtime places the array in the device's memory, so make this first call
+ * before the rest of the device's memory is reserved, and before any stream
+ * capture begins. Later calls only read the cached address; first calls from
+ * several host threads at once are safe.
+ *
+ * Every call shares the one array per device: two calls whose kernels overlap
+ * on the GPU (different streams, no ordering between them) race on it and may
+ * return wrong results. Calls ordered on one stream are safe; no contents need
+ * clearing between them (each call resets what it reads before reading it).
  */
 gqa_status attn_decode_paged_static_workspace(const void* q, const void* k_pool, const void* v_pool,
                                               const int32_t* block_tables, const int32_t* seq_lens, void* out,

@@ -120,3 +120,12 @@ def test_mla_absorbed_paged_checks(lib):
     assert lib.attn_decode_mla_absorbed_paged(P, P, P, P, P, 2, 128, 100, 16, 16, 512, 64, 0.07, 1, N, 0,
                                               N) == 4  # 2048 rows: two splits need a workspace
     assert lib.attn_decode_mla_absorbed_paged(N, N, N, N, N, 0, 8, 100, 16, 16, 512, 64, 0.07, 1, N, 0, N) == 0
+
+
+def test_static_workspace_size_matches_header():
+    """The binding's STATIC_WORKSPACE_BYTES is the header's GQA_STATIC_WORKSPACE_BYTES."""
+    import causal_gqa_attention_row_gb300 as g
+    text = open(os.path.join(ROOT, "include", "gqa_attn.h")).read()
+    m = re.search(r"#define\s+GQA_STATIC_WORKSPACE_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m, "GQA_STATIC_WORKSPACE_BYTES not found in the header"
+    assert g.STATIC_WORKSPACE_BYTES == int(m.group(1)) << int(m.group(2))

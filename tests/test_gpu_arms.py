@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import workloads as W
+from margins import check
 from oracle import core
 
 pytestmark = pytest.mark.gpu
@@ -57,7 +58,7 @@ def test_decode_contig_arms_match_oracle(gpu_lib, dtype, H, Hkv, d, arm):
                                None if sinks is None else sinks.astype(np.float64),
                                None if slopes is None else slopes.astype(np.float64))
     err = np.abs(out.float().cpu().numpy().astype(np.float64) - want).max()
-    assert err <= TOL[dtype], err
+    check(err, TOL[dtype])
 
 
 def test_paged_equals_contig_bitwise_with_every_arm(gpu_lib):
@@ -101,7 +102,7 @@ def test_paged_equals_contig_bitwise_with_every_arm(gpu_lib):
     assert torch.equal(out_p, out_c)
     want = core.attention_arms(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), lens, c.scale, window, 1.75,
                                sinks.astype(np.float64), slopes.astype(np.float64))
-    assert np.abs(out_c.float().cpu().numpy() - want).max() <= 2e-2
+    check(np.abs(out_c.float().cpu().numpy() - want).max(), 2e-2)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -118,7 +119,7 @@ def test_prefill_arms_match_oracle(gpu_lib, dtype):
     base = [o + S for o in offs]
     want = core.attention_arms(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), base, c.scale, 9, 2.5,
                                sinks.astype(np.float64), slopes.astype(np.float64))
-    assert np.abs(out.float().cpu().numpy() - want).max() <= TOL[dtype]
+    check(np.abs(out.float().cpu().numpy() - want).max(), TOL[dtype])
 
 
 def test_plain_call_equals_zero_arms(gpu_lib):

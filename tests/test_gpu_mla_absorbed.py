@@ -5,6 +5,7 @@ import pytest
 import torch
 
 import workloads as W
+from margins import check
 from oracle import core
 
 pytestmark = pytest.mark.gpu
@@ -44,7 +45,7 @@ def test_latent_attention_matches_oracle(gpu_lib, B, H, L, lens):
     assert g.attn_get_device_error() == g.OK
     want = oracle_latent(q_abs, latent, c.lens, c.scale)
     err = np.abs(out.float().cpu().numpy() - want).max()
-    assert err <= 2e-2, err
+    check(err, 2e-2)
 
 
 def test_rows_past_seq_len_never_reach_the_output(gpu_lib):
@@ -77,7 +78,7 @@ def test_zero_query_gives_prefix_mean(gpu_lib):
     for b, n in enumerate(c.lens.tolist()):
         mean = core.widen(lat[b, :n, :D_C]).mean(axis=0)
         err = np.abs(out[b].float().cpu().numpy() - mean[None]).max()
-        assert err <= 1e-2, err
+        check(err, 1e-2)
 
 
 def test_batch_composition_does_not_change_a_sequence(gpu_lib):
@@ -103,7 +104,7 @@ def test_bad_lengths_give_zero_rows_and_flag(gpu_lib):
     assert g.attn_get_device_error() == g.ERR_DEVICE_BOUNDS
     assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
     want = core.decode_mla_absorbed(W.to_oracle(q_abs[1:2]), W.to_oracle(latent[1:2]), [256], D_C, c.scale)
-    assert np.abs(out[1:2].float().cpu().numpy() - want).max() <= 2e-2
+    check(np.abs(out[1:2].float().cpu().numpy() - want).max(), 2e-2)
 
 
 def test_projections_match_oracle(gpu_lib):
@@ -142,7 +143,7 @@ def test_absorbed_chain_equals_naive_form(gpu_lib):
     want = core.decode_mla_naive(core.widen(W.to_oracle(c.q)), k_nope, np.ascontiguousarray(lat[..., D_C:]), v,
                                  c.lens.numpy(), c.scale)
     err = np.abs(out.float().cpu().numpy() - want).max()
-    assert err <= 2e-2, err
+    check(err, 2e-2)
 
 
 def test_full_size_sampled_sequences(gpu_lib):
@@ -157,7 +158,7 @@ def test_full_size_sampled_sequences(gpu_lib):
     for b in (0, 13, 31):
         want = oracle_latent(q_abs[b:b + 1], c.latent[b:b + 1], c.lens[b:b + 1], c.scale)
         err = np.abs(out[b:b + 1].float().cpu().numpy() - want).max()
-        assert err <= 2e-2, (b, err)
+        check(err, 2e-2, f"sequence {b}")
 
 
 def page_latent(latent, lens, bs, seed, spare=3):
@@ -200,7 +201,7 @@ def test_paged_equals_contiguous_bit_for_bit(gpu_lib, bs):
     assert g.attn_get_device_error() == g.OK
     assert torch.equal(out, want)
     ref = oracle_latent(q_abs[3:4], latent[3:4], c.lens[3:4], c.scale)
-    assert np.abs(out[3:4].float().cpu().numpy() - ref).max() <= 2e-2
+    check(np.abs(out[3:4].float().cpu().numpy() - ref).max(), 2e-2)
 
 
 def test_paged_bad_entry_is_flagged(gpu_lib):
@@ -253,4 +254,4 @@ def test_long_sequence_many_splits(gpu_lib):
     assert g.attn_get_device_error() == g.OK
     want = oracle_latent(q_abs, c.latent, c.lens, c.scale)
     err = np.abs(out.float().cpu().numpy() - want).max()
-    assert err <= 2e-2, err
+    check(err, 2e-2)

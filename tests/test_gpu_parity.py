@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import workloads as W
+from margins import check
 from oracle import core
 
 pytestmark = pytest.mark.gpu
@@ -38,7 +39,7 @@ def test_tiny_prefill(gpu_lib):
     want = core.prefill_causal(W.to_oracle(pre.q), W.to_oracle(pre.k)[:, :, :8], W.to_oracle(pre.v)[:, :, :8],
                                pre.scale)
     ok(g)
-    assert maxerr(out, want) <= 1e-4
+    check(maxerr(out, want), 1e-4)
 
 
 def test_tiny_decode_reading_last_prefill_row(gpu_lib):
@@ -51,7 +52,7 @@ def test_tiny_decode_reading_last_prefill_row(gpu_lib):
                          torch.tensor([8], dtype=torch.int32, device=DEV), out, pre.scale)
     want = core.prefill_causal(W.to_oracle(pre.q), W.to_oracle(k8), W.to_oracle(v8), pre.scale)[:, 7]
     ok(g)
-    assert maxerr(out, want) <= 1e-4
+    check(maxerr(out, want), 1e-4)
 
 
 def test_tiny_decode_appended_ninth_row_contig_and_paged(gpu_lib):
@@ -78,10 +79,10 @@ def test_tiny_decode_appended_ninth_row_contig_and_paged(gpu_lib):
     assert torch.equal(out_c, out_p)
     q_all = torch.cat([pre.q[0], q9], 0)[None]  # the new query is row 8 of a 9-row prefill
     want = core.prefill_causal(W.to_oracle(q_all), W.to_oracle(pre.k), W.to_oracle(pre.v), pre.scale)[:, 8]
-    assert maxerr(out_c, want) <= 1e-4
+    check(maxerr(out_c, want), 1e-4)
     want_p = core.decode_paged(W.to_oracle(q9), W.to_oracle(kp), W.to_oracle(vp), W.to_oracle(tables), [9],
                                pre.scale)
-    assert maxerr(out_p, want_p) <= 1e-4
+    check(maxerr(out_p, want_p), 1e-4)
 
 
 # ---------------------------------------------------------------------------
@@ -100,7 +101,7 @@ def test_decode_contig(gpu_lib, dtype, H, Hkv, d):
     g.attn_decode_contig(c.q.to(DEV), c.k.to(DEV), c.v.to(DEV), c.seq_lens.to(DEV), out, c.scale, workspace=ws)
     ok(g)
     want = core.decode_contig(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), lens, c.scale)
-    assert maxerr(out, want) <= TOL[dtype]
+    check(maxerr(out, want), TOL[dtype])
 
 
 @pytest.mark.parametrize("bs", [16, 4, 5, 64])
@@ -136,7 +137,7 @@ def test_decode_paged_matches_oracle_and_contig_bits(gpu_lib, bs):
     assert torch.equal(out_p, out_c), "paged and contiguous decode must be bit-identical"
     want = core.decode_paged(W.to_oracle(c.q), W.to_oracle(kp), W.to_oracle(vp), W.to_oracle(tables), lens,
                              c.scale)
-    assert maxerr(out_p, want) <= 2e-2
+    check(maxerr(out_p, want), 2e-2)
 
 
 def test_decode_mla_shared_rot(gpu_lib):
@@ -152,7 +153,7 @@ def test_decode_mla_shared_rot(gpu_lib):
     ok(g)
     want = core.decode_mla_naive(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.k_rot), W.to_oracle(c.v),
                                  [1500, 700], c.scale)
-    assert maxerr(out, want) <= 2e-2
+    check(maxerr(out, want), 2e-2)
 
 
 # ---------------------------------------------------------------------------
@@ -171,7 +172,7 @@ def test_prefill(gpu_lib, dtype, H, Hkv, d, S, off):
     ok(g)
     want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale,
                                offsets=[off, off + 3])
-    assert maxerr(out, want) <= TOL[dtype]
+    check(maxerr(out, want), TOL[dtype])
 
 
 def test_prefill_mla_shape(gpu_lib):
@@ -181,7 +182,7 @@ def test_prefill_mla_shape(gpu_lib):
     g.attn_prefill_causal(c.q.to(DEV), c.k.to(DEV), c.v.to(DEV), out, c.scale)
     ok(g)
     want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale)
-    assert maxerr(out, want) <= 2e-2
+    check(maxerr(out, want), 2e-2)
 
 
 # ---------------------------------------------------------------------------
@@ -300,7 +301,7 @@ def test_decode_equals_last_prefill_row(gpu_lib):
     g.attn_decode_contig(c.q[:, 39].contiguous().to(DEV), c.k.to(DEV), c.v.to(DEV),
                          torch.tensor([40], dtype=torch.int32, device=DEV), dec, c.scale)
     ok(g)
-    assert (dec.float() - pre[:, 39].float()).abs().max().item() <= 2e-2
+    check((dec.float() - pre[:, 39].float()).abs().max().item(), 2e-2, "decode vs prefill row")
 
 
 def test_empty_batch_is_a_no_op(gpu_lib):

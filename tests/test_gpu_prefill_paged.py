@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import workloads as W
+from margins import check
 from oracle import core
 
 pytestmark = pytest.mark.gpu
@@ -81,7 +82,7 @@ def test_tensor_core_paged_equals_contig_bits(gpu_lib, bs):
     c = W.make_prefill(B=3, S=S, H=14, Hkv=2, dk=64, dv=64, seed=150 + bs, S_kv=S + max(offs) + 5, offsets=offs)
     out_p, out_c = run_both(g, c, bs)
     assert torch.equal(out_p, out_c)
-    assert err(out_p, oracle(c)) <= TOL[torch.bfloat16]
+    check(err(out_p, oracle(c)), TOL[torch.bfloat16])
 
 
 @pytest.mark.parametrize("dtype,d,bs", [(torch.float32, 64, 16), (torch.bfloat16, 128, 16),
@@ -98,7 +99,7 @@ def test_simt_paged_equals_contig_and_oracle(gpu_lib, dtype, d, bs):
     out_p, out_c = run_both(g, c, bs)
     if not (dtype == torch.bfloat16 and d == 64):
         assert torch.equal(out_p, out_c)
-    assert err(out_p, oracle(c)) <= TOL[dtype]
+    check(err(out_p, oracle(c)), TOL[dtype])
 
 
 def test_paged_prefill_arms(gpu_lib):
@@ -115,7 +116,7 @@ def test_paged_prefill_arms(gpu_lib):
                 alibi_slopes=torch.from_numpy(slopes).to(DEV))
     out_p, out_c = run_both(g, c, 16, **arms)
     assert torch.equal(out_p, out_c)
-    assert err(out_p, oracle(c, 130, 3.0, sinks.astype(np.float64), slopes.astype(np.float64))) <= 2e-2
+    check(err(out_p, oracle(c, 130, 3.0, sinks.astype(np.float64), slopes.astype(np.float64))), 2e-2)
 
 
 def test_decode_step_is_a_one_row_chunk(gpu_lib):
@@ -134,7 +135,7 @@ def test_decode_step_is_a_one_row_chunk(gpu_lib):
     g.attn_prefill_paged(c.q.view(4, 1, 8, 64).to(DEV), c.k_pool.to(DEV), c.v_pool.to(DEV), c.tables.to(DEV), out_p,
                          c.scale, position_offset=(lens - 1).to(torch.int32))
     ok(g)
-    assert (out_p[:, 0].float() - out_d.float()).abs().max().item() <= 2e-2
+    check((out_p[:, 0].float() - out_d.float()).abs().max().item(), 2e-2)
 
 
 @pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 64, 64), (torch.float32, 64, 64),
@@ -191,7 +192,7 @@ def test_full_size_chunked_prefill_sampled_rows(gpu_lib, H, Hkv, d):
             want = core.attention_arms(W.to_oracle(q[b:b + 1, i:i + 1].contiguous()), W.to_oracle(k_hist),
                                        W.to_oracle(v_hist), [o + i + 1], scale)
             worst = max(worst, err(out[b:b + 1, i:i + 1], want))
-    assert worst <= 2e-2, worst
+    check(worst, 2e-2)
 
 
 @pytest.mark.parametrize("dk,dv,bs", [(128, 128, 16), (128, 128, 8), (192, 128, 8), (192, 128, 32)])
@@ -206,4 +207,4 @@ def test_tensor_core_paged_wide_heads_equal_contig_bits(gpu_lib, dk, dv, bs):
                        offsets=offs)
     out_p, out_c = run_both(g, c, bs)
     assert torch.equal(out_p, out_c)
-    assert err(out_p, oracle(c)) <= TOL[torch.bfloat16]
+    check(err(out_p, oracle(c)), TOL[torch.bfloat16])

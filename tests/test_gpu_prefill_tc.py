@@ -4,6 +4,7 @@ import pytest
 import torch
 
 import workloads as W
+from margins import check
 from oracle import core
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +30,7 @@ def test_prefill_tc_matches_oracle(gpu_lib, B, S, H, Hkv, offs, d):
     out = run(g, c)
     want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
     err = np.abs(out.float().cpu().numpy() - want).max()
-    assert err <= 2e-2, err
+    check(err, 2e-2)
 
 
 def test_prefill_tc_full_size_config(gpu_lib):
@@ -50,7 +51,7 @@ def test_prefill_tc_full_size_config(gpu_lib):
                                                     W.to_oracle(pos), 0, 64, 1e6).transpose(0, 2, 1, 3))
     want = core.prefill_causal(qo, ko, W.to_oracle(c.v), c.scale)
     err = np.abs(out.float().cpu().numpy() - want).max()
-    assert err <= 2e-2, err
+    check(err, 2e-2)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -63,7 +64,7 @@ def test_prefill_tc_zero_keys_give_prefix_mean(gpu_lib, d):
     v = c.v.float()[0]                                       # [Hkv, S, d]
     mean = torch.cumsum(v, dim=1) / torch.arange(1, 301)[None, :, None]
     want = mean.repeat_interleave(2, dim=0).permute(1, 0, 2)  # [S, H, d]
-    assert (out[0].float().cpu() - want).abs().max().item() <= 2e-2
+    check((out[0].float().cpu() - want).abs().max().item(), 2e-2)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -74,7 +75,7 @@ def test_prefill_tc_decode_step_is_last_row(gpu_lib, d):
     dec = torch.empty(1, 8, d, dtype=torch.bfloat16, device=DEV)
     g.attn_decode_contig(c.q[:, 639].contiguous().to(DEV), c.k.to(DEV), c.v.to(DEV),
                          torch.tensor([640], dtype=torch.int32, device=DEV), dec, c.scale)
-    assert (dec.float() - out[:, 639].float()).abs().max().item() <= 2e-2
+    check((dec.float() - out[:, 639].float()).abs().max().item(), 2e-2)
 
 
 def test_prefill_tc_d128_model_shape(gpu_lib):
@@ -86,7 +87,7 @@ def test_prefill_tc_d128_model_shape(gpu_lib):
     out = run(g, c)
     want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
     err = np.abs(out.float().cpu().numpy() - want).max()
-    assert err <= 2e-2, err
+    check(err, 2e-2)
 
 
 @pytest.mark.parametrize("B,S,H,Hkv,offs", [(1, 90, 4, 4, [0]), (2, 300, 8, 8, [0, 140]), (1, 257, 6, 2, [5])])
@@ -98,7 +99,7 @@ def test_prefill_tc_mla_shape(gpu_lib, B, S, H, Hkv, offs):
     out = run(g, c)
     want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale, offsets=offs)
     err = np.abs(out.float().cpu().numpy() - want).max()
-    assert err <= 2e-2, err
+    check(err, 2e-2)
 
 
 @pytest.mark.parametrize("H,Hkv,dk,dv", [(32, 8, 128, 128), (32, 32, 192, 128)])
@@ -117,7 +118,7 @@ def test_prefill_tc_full_size_wide_heads_sampled_rows(gpu_lib, H, Hkv, dk, dv):
                                    W.to_oracle(c.k[:, :, :i + 1].contiguous()),
                                    W.to_oracle(c.v[:, :, :i + 1].contiguous()), c.scale, offsets=[i])
         worst = max(worst, np.abs(out[:, i:i + 1].float().numpy() - want).max())
-    assert worst <= 2e-2, worst
+    check(worst, 2e-2)
 
 
 @pytest.mark.parametrize("dk,dv", [(128, 128), (192, 128)])
@@ -131,4 +132,4 @@ def test_prefill_tc_wide_zero_keys_give_prefix_mean(gpu_lib, dk, dv):
     v = c.v.float()[0]                                       # [Hkv, S, dv]
     mean = torch.cumsum(v, dim=1) / torch.arange(1, 201)[None, :, None]
     want = mean.repeat_interleave(2, dim=0).permute(1, 0, 2)  # [S, H, dv]
-    assert (out[0].float().cpu() - want).abs().max().item() <= 2e-2
+    check((out[0].float().cpu() - want).abs().max().item(), 2e-2)
