@@ -205,7 +205,7 @@ static gqa_status prefill_common(gqa::RowsParams& p, int bf16, int d_k, int d_v,
   if (!arms_on && gqa::prefill_tc_supported(bf16, d_k, d_v, p.paged ? p.bs : 0, p.mbps) && attention_scale > 0.f)
     return from_cuda(gqa::launch_prefill_tc(p.q, p.k, p.v, p.out, p.B, p.seq_q, p.capacity, p.offsets, p.H, p.Hkv,
                                             d_k, d_v, qscale, p.err, st, p.paged ? p.tables : nullptr, p.mbps, p.bs,
-                                            p.num_blocks));
+                                            p.num_blocks, g_withhold_first_tile));
   const int nvmax = gqa::rows_max_nv(bf16, d_k, d_v, 0);
   if (nvmax == 0) return GQA_ERR_UNSUPPORTED;
   p.G = p.H / p.Hkv;
@@ -379,7 +379,7 @@ static gqa_status mla_absorbed_common(const void* q_abs, const void* latent, con
   float* partial = need > 0 ? static_cast<float*>(workspace) : nullptr;
   const cudaError_t e = gqa::launch_mla_absorbed_tc(q_abs, latent, seq_lens, out_lat, partial, B, capacity, H, d_c,
                                                     d_r, gqa::kMlaChunk, qscale, err, st, tables, mbps, bs,
-                                                    num_blocks);
+                                                    num_blocks, g_withhold_first_tile);
   if (e != cudaSuccess || need == 0) return from_cuda(e);
   // the splits of each (sequence, head) merged into out_lat
   gqa::RowsParams p{};

@@ -94,7 +94,7 @@ cudaError_t launch_append(void* q, const void* k_new, const void* v_new, void* k
 cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
                               int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv,
                               float qscale, unsigned* err, cudaStream_t st, const int32_t* tables = nullptr,
-                              int mbps = 0, int bs = 0, int num_blocks = 0);
+                              int mbps = 0, int bs = 0, int num_blocks = 0, int debug_withhold = 0);
 // bs = 0: contiguous K/V; else the pool's block size and max blocks per sequence.
 bool prefill_tc_supported(int bf16, int dk, int dv, int bs = 0, int mbps = 0);
 
@@ -109,7 +109,7 @@ bool mla_absorbed_tc_supported(int bf16, int d_c, int d_r);
 cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
                                    float* partial, int B, int max_len, int H, int d_c, int d_r, int chunk,
                                    float qscale, unsigned* err, cudaStream_t st, const int32_t* tables = nullptr,
-                                   int mbps = 0, int bs = 0, int num_blocks = 0);
+                                   int mbps = 0, int bs = 0, int num_blocks = 0, int debug_withhold = 0);
 bool mla_absorbed_paged_block_ok(int bs);
 // Rows of one split of the absorbed MLA decode (a fixed number, so a sequence's
 // result does not depend on the rest of the batch).

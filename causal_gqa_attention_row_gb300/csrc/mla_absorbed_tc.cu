@@ -99,6 +99,7 @@ struct MlaParams {
   __nv_bfloat16* out;       // [B, H, d_c]
   float qscale;             // attention_scale * log2(e)
   unsigned* err;
+  int debug_withhold;       // test hook: CTA 1 of each pair never loads its first cache tile
 };
 
 struct MlaBars {
@@ -358,6 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           blk[u] = e;
         }
       }
+      if (p.debug_withhold && t == 0 && half == 1) continue;  // test hook: tile 0 is never requested
       if (t >= kStages) {  // the stage is free once PV_{t-2} is done
         bool ok = true;
         if (lane == 0) ok = wait_or_abort(&bars->r_empty[st], ((t / kStages) - 1) & 1, bars, p.err);
@@ -680,7 +682,7 @@ bool mla_absorbed_paged_block_ok(int bs) { return bs > 0 && bs % 8 == 0 && kKeys
 cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const int32_t* seq_lens, void* out_lat,
                                    float* partial, int B, int max_len, int H, int d_c, int d_r, int chunk,
                                    float qscale, unsigned* err, cudaStream_t st, const int32_t* tables, int mbps,
-                                   int bs, int num_blocks) {
+                                   int bs, int num_blocks, int debug_withhold) {
   using C = MlaCfg<512, 64>;
   if (!mla_absorbed_tc_supported(1, d_c, d_r) || chunk % kKeys != 0 || chunk <= 0 || !(qscale > 0.f))
     return cudaErrorNotSupported;
@@ -713,6 +715,7 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
   p.out = static_cast<__nv_bfloat16*>(out_lat);
   p.qscale = qscale;
   p.err = err;
+  p.debug_withhold = debug_withhold;
   int dev = 0;
   cudaGetDevice(&dev);
   static unsigned long long attr_done = 0;

@@ -27,15 +27,16 @@
 // reads P_w is done. P never passes through shared memory, whose bandwidth is
 // left to the TMA tiles and the MMAs' reads of Q, K and V. A row of d elements
 // is d / 64 blocks of 64 columns, each in the 128-byte swizzle (one TMA box). The
-// softmax threads keep the row sum of exactly the bf16 p that multiply V, in
-// fp32. Thread t of a warpgroup owns query row t (TMEM lane t).
+// softmax threads form p with fp32 exponentials, keep the fp32 row sum of these
+// p, and round P to bf16 for the PV product. Thread t of a warpgroup owns query
+// row t (TMEM lane t).
 //
 // Pipeline per warpgroup and key tile j: the softmax threads load their S_j row
 // into registers and release S_w at once, so the MMA thread issues S_{j+2}
-// while the exponentials of tile j are still being computed; P_j is built in
-// registers and stored into P_w once PV_{j-2} (issued a whole tile earlier) has
-// read the previous one (at d_v = 128, once S_w holds S_j that PV is done). K
-// and V have rings of their own: a K stage is free as soon as its S MMA is done,
+// while the exponentials of tile j are still being computed; P_j is stored into
+// P_w, chunk by chunk as it is formed, once PV_{j-2} (issued a whole tile
+// earlier) has read the previous one (at d_v = 128, once S_w holds S_j that PV
+// is done). K and V have rings of their own: a K stage is free as soon as its S MMA is done,
 // a V stage once its PV is. At d_k = 64 they run four tiles ahead, so the load of
 // K_{j+4} has a whole tile-period before S_{j+4} needs it; for wider heads (tiles
 // two or three times the size) two, which the later issue of S leaves enough.
@@ -50,6 +51,12 @@
 // exchange their (m, l), each merges half of the columns of the two partial O
 // rows into bf16 in shared memory (over the Q tile), and one TMA store writes
 // the output tile.
+//
+// Launches use programmatic stream serialization: a CTA initialises its
+// barriers, allocates TMEM and prefetches its tensor maps before waiting for
+// the previous kernel in the stream (griddepcontrol.wait), and lets the next
+// launch start once it is set up, so back-to-back launches overlap one's set-up
+// with the other's tail.
 
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -114,6 +121,7 @@ struct TcParams {
   __nv_bfloat16* out;
   float qscale;
   unsigned* err;
+  int debug_withhold;  // test hook: the first K tile is never loaded, so its waits run out
 };
 
 struct Bars {
@@ -165,32 +173,19 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// 2^x for two bf16 values at once (special-function unit, subnormals flushed;
-// 2^-inf = 0).
-__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
-  uint32_t y;
-  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
-
-// 2^(s*qs - mq) for two scores, the exponent rounded to bf16 first: the result
-// is the bf16 pair that P stores.
-__device__ __forceinline__ uint32_t exp2_pair(float s0, float s1, float2 qs2, float2 nmq2) {
+// p = 2^(s*qs - mq) for two scores: fp32 exponentials (one special-function
+// operation per score; the bf16x2 form costs the same per score and needs
+// unpacking), added to the fp32 row sum `acc`, and returned rounded to the bf16
+// pair that P stores.
+__device__ __forceinline__ uint32_t exp2_pair(float s0, float s1, float2 qs2, float2 nmq2, float2& acc) {
   const float2 x = __ffma2_rn(make_float2(s0, s1), qs2, nmq2);
-  return ex2_bf16x2(pack_bf16(x.x, x.y));
-}
-
-// a += low bf16 of w, b += high bf16 of w, in fp32 (exact inputs, fp32 rounding).
-__device__ __forceinline__ void add_bf16x2(float& a, float& b, uint32_t w) {
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
-      : "+f"(a), "+f"(b)
-      : "r"(w));
+  const float2 e = make_float2(ex2f(x.x), ex2f(x.y));
+  acc = __fadd2_rn(acc, e);
+  return pack_bf16(e.x, e.y);
 }
 
 // max(a, b, c) in one instruction.
@@ -295,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = rem % p.H, b = rem / p.H;
   const int kvh = h / p.G;
   const int i0 = qt * kBM;
-  const int off = p.offsets ? p.offsets[b] : 0;  // in flight while the CTA sets up
   const int rows = min(kBM, p.S - i0);
 
   if (warp == kProducerWarp && lane == 0) {
@@ -317,34 +311,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bars->abort_flag = 0;
     fence_barrier_init();
-    // Q and the first K tile do not depend on the offset: they load while the
-    // rest of the CTA sets up
     tc::prefetch_tmap(&tm_q);
     tc::prefetch_tmap(&tm_k);
+    // everything above may overlap the previous kernel in the stream; the loads
+    // below read memory it may have written
+    tc::grid_dep_wait();
+    // Q and the first K tile load while the rest of the CTA sets up
     mbar_arrive_expect_tx(&bars->q_full, kTileK);
 #pragma unroll
     for (int cb = 0; cb < C::kCBK; ++cb)
       tc::tma_load_4d(smem + kOffQ + cb * kBlk, &tm_q, cb * 64, h, i0, b, &bars->q_full);
-    if (p.tables)  // the table entries of the tile wait for the offset, which bounds them
-      load_kv_tile<C::kCBK>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, off + i0 + rows);
-    else
+    if (p.debug_withhold) {
+      // test hook: K_0 is never requested (nothing is left in flight), so the
+      // first wait on it runs into its bound and the CTA gives up
+    } else if (p.tables) {  // the tile's table entries are bounded by the offset
+      const int off0 = p.offsets ? p.offsets[b] : 0;
+      load_kv_tile<C::kCBK>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, off0 + i0 + rows);
+    } else {
       load_kv_tile<C::kCBK>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, 0);
+    }
   }
   if (warp == kMmaWarp0) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
+  tc::grid_dep_wait();  // before any thread touches global memory
+  const int off = p.offsets ? p.offsets[b] : 0;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
+  // the next launch in the stream may start setting up on the SMs this grid frees
+  tc::grid_dep_launch();
 
   if (off < 0 || (long long)off + p.S > p.S_kv) {  // the cache cannot hold these rows
     if (threadIdx.x == 0 && qt == p.n_qtiles - 1 && h == 0) raise_error(p.err, kErrBounds);
     for (int idx = threadIdx.x; idx < rows * DV; idx += blockDim.x)
       p.out[(((size_t)b * p.S + i0 + idx / DV) * p.H + h) * DV + idx % DV] = __float2bfloat16_rn(0.f);
     // never exit with a load in flight
-    if (warp == kProducerWarp && lane == 0 && !(mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0)))
+    if (warp == kProducerWarp && lane == 0 &&
+        !(mbar_wait(&bars->q_full, 0) && (p.debug_withhold || mbar_wait(&bars->k_full[0], 0))))
       raise_error(p.err, kErrTimeout);
     __syncthreads();
     if (warp == kMmaWarp0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int st = 0; st < kStagesK; ++st) issued_last[st] = -1;
     int j = 0;
     if (is_k) {  // Q and K_0 went out before the setup barrier
-      issued_last[0] = 0;
+      issued_last[0] = p.debug_withhold ? -1 : 0;
       j = 1;
     }
     for (; j < n_kv; ++j) {
@@ -549,25 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= f;
         }
       }
-      // ---- p = 2^(s*qs - m*qs) as bf16 pairs, and the fp32 sum of exactly these p
-      const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
-      const float2 nmq2 = make_float2(-mq, -mq);
-      uint32_t pv[4][16];
-      float ls[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ls[e] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          pv[c][t] = exp2_pair(__uint_as_float(sv[c][2 * t]), __uint_as_float(sv[c][2 * t + 1]), qs2, nmq2);
-          add_bf16x2(ls[(t & 3) * 2], ls[(t & 3) * 2 + 1], pv[c][t]);
-        }
-      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      // ---- d_v = 64: P_w is free once PV_{k-1} has read it. Every phase of
-      // o_done[w] is waited for in order, before the next PV can be issued, so the
-      // barrier is never two phases ahead of this wait (nor of the rescale's or the
-      // final one). d_v = 128: P goes over S_k's own first columns, already read.
+      // ---- d_v = 64: P_w is free once PV_{j-2} has read it (issued a whole tile
+      // earlier, so this rarely waits). Every phase of o_done[w] is waited for in
+      // order, before the next PV can be issued, so the barrier is never two
+      // phases ahead of this wait (nor of the rescale's or the final one).
+      // d_v = 128: P goes over S_j's own first columns, already read.
       if (!C::kAlias && k >= 1) {
         if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
           alive = false;
@@ -575,8 +567,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
       }
+      // ---- p = 2^(s*qs - m*qs), the fp32 row sum of these p, and P as bf16 pairs;
+      // each 16-word chunk of P goes to TMEM as soon as it is formed, so few P
+      // registers are live next to the S row
+      const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
+      const float2 nmq2 = make_float2(-mq, -mq);
+      float2 ls[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_st_32x32b_x16(tP + c * 16, pv[c]);
+      for (int e = 0; e < 4; ++e) ls[e] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pw[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          pw[t] = exp2_pair(__uint_as_float(sv[c][2 * t]), __uint_as_float(sv[c][2 * t + 1]), qs2, nmq2, ls[t & 3]);
+        tc::tmem_st_32x32b_x16(tP + c * 16, pw);
+      }
+      l_run += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
       tc::tmem_st_wait();
       tc::fence_before_sync();  // this thread's TMEM accesses are done
       __syncwarp();             // ... for every lane of the warp; one lane signals
@@ -685,8 +692,21 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   }
   const long long ctas = (long long)p.B * p.H * p.n_qtiles;
   if (ctas <= 0) return cudaSuccess;
-  prefill_tc_kernel<DK, DV><<<(unsigned)ctas, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, to, p);
-  return cudaGetLastError();
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // programmatic stream serialization: the CTAs of this launch may start their
+  // set-up while the previous kernel in the stream finishes (the kernel waits
+  // for it, grid_dep_wait, before touching global memory)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DK, DV>, tq, tk, tv, to, p);
 }
 
 }  // namespace
@@ -703,7 +723,7 @@ bool prefill_tc_supported(int bf16, int dk, int dv, int bs, int mbps) {
 cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
                               int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv, float qscale,
                               unsigned* err, cudaStream_t st, const int32_t* tables, int mbps, int bs,
-                              int num_blocks) {
+                              int num_blocks, int debug_withhold) {
   if (!prefill_tc_supported(1, dk, dv, tables ? bs : 0, mbps) || !(qscale > 0.f)) return cudaErrorNotSupported;
   CUtensorMap tq, tk, tv, to;
   // q [B, S, H, d_k]: dims (d_k, H, S, B), box (64, 1, 128, 1)
@@ -735,6 +755,7 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
   p.out = static_cast<__nv_bfloat16*>(out);
   p.qscale = qscale;
   p.err = err;
+  p.debug_withhold = debug_withhold;
   if (dk == 64) return launch_d<64, 64>(tq, tk, tv, to, p, st);
   if (dk == 128) return launch_d<128, 128>(tq, tk, tv, to, p, st);
   return launch_d<192, 128>(tq, tk, tv, to, p, st);

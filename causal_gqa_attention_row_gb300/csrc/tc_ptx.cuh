@@ -44,6 +44,19 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ----------------------------------------------
+
+// Wait until the grids this one was launched to depend on have completed and
+// their memory operations are visible. Every thread calls it before its first
+// access to global memory the previous kernel may have written (or read, for
+// outputs). A grid launched the ordinary way passes straight through.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next grid in the stream (launched with programmatic stream
+// serialization) start its CTAs once every CTA of this grid has called this or
+// exited; they run their set-up and then wait in grid_dep_wait.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- TMEM -------------------------------------------------------------------
 
 // Whole-warp operations.
@@ -151,6 +164,19 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// True in exactly one lane of the (converged) warp. A warp that issues MMAs
+// runs its loop converged and lets the elected lane issue: the descriptor
+// arithmetic then stays warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // Arrive once on `bar` when every MMA this thread issued before has completed.

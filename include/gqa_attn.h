@@ -359,11 +359,18 @@ gqa_status attn_get_device_error(void* stream);
 /* Static, NUL-terminated text of a status code. */
 const char* gqa_status_string(gqa_status status);
 
-/* Test hook for the bounded waits: while enabled, each decode launch withholds
- * the first K/V tile that every CTA of the (persistent) attention kernel would
- * stream, so that the consumers' wait on it runs out (after about one second),
- * the device error word records GQA_ERR_DEVICE_TIMEOUT and the kernel returns.
- * Outputs are then garbage.
+/* Test hook for the bounded waits: while enabled, the kernels with a TMA
+ * producer never request one of their copies, so that the wait on it runs out
+ * (after about one second), the device error word records
+ * GQA_ERR_DEVICE_TIMEOUT and the kernel returns with nothing in flight and its
+ * tensor memory released:
+ *   - the SIMT attention kernel (decode; SIMT prefill): the first K/V tile of
+ *     every CTA;
+ *   - the tensor-core prefill: the first K tile of every CTA;
+ *   - the absorbed MLA decode: the first cache tile of the second CTA of every
+ *     pair, so the first CTA also gives up waiting for its peer's partial scores
+ *     and drains the copy it sent.
+ * Outputs are then garbage. The hook is read when a call launches.
  * Never enable outside tests. Returns the previous setting. */
 int gqa_debug_withhold_first_tile(int enable);
 

@@ -1,10 +1,13 @@
 """Device-detected errors: out-of-range inputs and a bounded wait that runs out.
 Nothing here faults or hangs the GPU: bad entries are caught before any copy is
 issued, and the withheld-tile hook makes a one-second bounded wait give up."""
+import numpy as np
 import pytest
 import torch
 
 import workloads as W
+from margins import check
+from oracle import core
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -81,4 +84,53 @@ def test_withheld_tile_times_out_and_context_survives(gpu_lib):
     # the context is still usable and the same call now succeeds
     g.attn_decode_contig(*args, out, c.scale)
     assert g.attn_get_device_error() == g.OK
-    assert torch.isfinite(out.float()).all()
+    want = core.decode_contig(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), [100], c.scale)
+    check(float(np.abs(out.float().cpu().numpy() - want).max()), 2e-2, "decode after the timeout")
+
+
+def _withheld(g, call):
+    prev = g.gqa_debug_withhold_first_tile(True)
+    try:
+        call()
+    finally:
+        g.gqa_debug_withhold_first_tile(prev)
+    return g.attn_get_device_error()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_tensor_core_withheld_tile_times_out(gpu_lib, d):
+    """The tensor-core prefill's first K tile is never loaded: its one-second
+    waits give up, the call reports the timeout, and the CTA still releases its
+    tensor memory (the next call allocates it again and matches the oracle)."""
+    g = gpu_lib
+    c = W.make_prefill(B=1, S=200, H=2, Hkv=1, dk=d, dv=d, seed=64)
+    q, k, v = c.q.to(DEV), c.k.to(DEV), c.v.to(DEV)
+    out = torch.empty(1, 200, 2, d, dtype=torch.bfloat16, device=DEV)
+    assert _withheld(g, lambda: g.attn_prefill_causal(q, k, v, out, c.scale)) == g.ERR_DEVICE_TIMEOUT
+    for _ in range(2):  # every CTA of the timed-out launch freed its TMEM: these allocate it again
+        g.attn_prefill_causal(q, k, v, out, c.scale)
+        assert g.attn_get_device_error() == g.OK
+    want = core.prefill_causal(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), c.scale)
+    check(float(np.abs(out.float().cpu().numpy() - want).max()), 2e-2, "prefill after the timeout")
+
+
+def test_mla_absorbed_withheld_tile_times_out_and_pair_drains(gpu_lib):
+    """The second CTA of each absorbed-MLA pair never gets its first cache tile:
+    it gives up, its peer gives up waiting for the partial scores it would have
+    sent and waits out the copy it sent itself, and both free their tensor
+    memory. The call reports the timeout; the next call matches the oracle."""
+    g = gpu_lib
+    B, H, L, D_C, D_R = 2, 128, 100, 512, 64
+    c = W.make_mla_absorbed(B=B, H=H, max_len=L, lens=[100, 70], seed=65)
+    q_abs = torch.empty(B, H, D_C + D_R, dtype=torch.bfloat16, device=DEV)
+    g.mla_absorb_q(c.q.to(DEV), c.k_b.to(DEV), q_abs)
+    latent, lens = c.latent.to(DEV), c.lens.to(DEV)
+    out = torch.empty(B, H, D_C, dtype=torch.bfloat16, device=DEV)
+    assert g.attn_get_device_error() == g.OK
+    call = lambda: g.attn_decode_mla_absorbed(q_abs, latent, lens, out, c.scale)
+    assert _withheld(g, call) == g.ERR_DEVICE_TIMEOUT
+    for _ in range(2):
+        call()
+        assert g.attn_get_device_error() == g.OK
+    want = core.decode_mla_absorbed(W.to_oracle(q_abs), W.to_oracle(c.latent), W.to_oracle(c.lens), D_C, c.scale)
+    check(float(np.abs(out.float().cpu().numpy() - want).max()), 2e-2, "absorbed MLA after the timeout")
