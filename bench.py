@@ -8,6 +8,7 @@ working set (~17 GB per step) is far larger than L2, so steps need no flush.
 The same run also measures, as secondary objects of the one JSON line:
   prefill  -- causal prefill bf16, B=1, H=14, Hkv=2, d=64, S=2048 (tcgen05),
               with RoPE on q and k in the step; TFLOP/s against the bf16 peak
+  prefill_arms -- the same with a 512-row window, sinks, ALiBi and softcap
   contig   -- contiguous decode bf16, 64 sequences, len U[512, 8192]
   mla      -- MLA-shaped decode bf16, 32 sequences, 128 heads, d_k 128+64 shared
               rotated part, d_v 128, len 4096
@@ -386,6 +387,39 @@ def run_prefill(args, peaks, peak_kind):
                          "kernel": "prefill_tc_kernel", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
 
 
+def run_prefill_arms(args, peaks, peak_kind, window=512):
+    """The headline prefill shape with every arm on (a 512-row sliding window,
+    sink logits, ALiBi slopes, softcap 30) on the tensor-core kernel's arms
+    instantiation. Algorithmic FLOPs: the (query, key) pairs inside each row's
+    window only."""
+    import causal_gqa_attention_row_gb300 as g
+    g.load()
+    dev = torch.device("cuda")
+    B, S, H, Hkv, d = 1, 2048, 14, 2, 64
+    c = W.make_prefill(B=B, S=S, H=H, Hkv=Hkv, dk=d, dv=d, seed=1, device=dev)
+    out = torch.empty(B, S, H, d, dtype=torch.bfloat16, device=dev)
+    sinks = W.randn((H,), W.generator(123, dev), torch.float32, dev)
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32, device=dev)
+    arms = dict(window=window, softcap=30.0, sinks=sinks, alibi_slopes=slopes)
+    pairs = sum(min(i + 1, window) for i in range(S))
+    flops = 2.0 * H * (d + d) * pairs
+    st = torch.cuda.current_stream()
+    call = lambda k: g.attn_prefill_causal(c.q, c.k, c.v, out, c.scale, **arms)
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    n = 4 * max(args.steps, 20)
+    queue_ahead(n, us_per_group=40.0)
+    ms = timed(call, n, st, sync_first=False)
+    assert g.attn_get_device_error() == g.OK
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"workload": W.WORKLOADS["prefill"] + f", window {window}, sink logits, ALiBi slopes, softcap 30",
+            "tflops": tflops, "kernel_ms": ms, "flops": flops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "kernel": "prefill_tc_kernel<64, 64, arms>", "peak_kind": f"bf16 dense burst, {peak_kind}"}}
+
+
 def run_prefill_d128(args, peaks, peak_kind, H=32, Hkv=8, dk=128, dv=128, key="prefill_d128"):
     """Causal prefill at d = 128 (the decode configs' head shape), or at the MLA
     widths, on the tcgen05 kernel: the kernel's event average over back-to-back
@@ -645,8 +679,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true", help="skip prefill, contig and mla")
-    ap.add_argument("--only", choices=["paged", "prefill", "prefill_paged", "prefill_d128", "prefill_paged_d128",
-                                       "prefill_mla", "contig", "mla", "mla_absorbed"], default=None)
+    ap.add_argument("--only", choices=["paged", "prefill", "prefill_arms", "prefill_paged", "prefill_d128",
+                                       "prefill_paged_d128", "prefill_mla", "contig", "mla", "mla_absorbed"],
+                    default=None)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world = dist_setup()
@@ -654,7 +689,8 @@ def main():
         reference_arm(args, rank, world)
         return
     peaks, peak_kind = measured_peaks()
-    only = {"prefill": run_prefill, "prefill_paged": run_prefill_paged, "prefill_d128": run_prefill_d128,
+    only = {"prefill": run_prefill, "prefill_arms": run_prefill_arms, "prefill_paged": run_prefill_paged,
+            "prefill_d128": run_prefill_d128,
             "prefill_paged_d128": run_prefill_paged_d128, "prefill_mla": run_prefill_mla, "contig": run_contig,
             "mla": run_mla, "mla_absorbed": run_mla_absorbed}
     if args.only in only:
@@ -666,6 +702,7 @@ def main():
     secondary = {}
     if not args.no_secondary and args.only is None:
         secondary = {"prefill": run_prefill(args, peaks, peak_kind),
+                     "prefill_arms": run_prefill_arms(args, peaks, peak_kind),
                      "prefill_paged": run_prefill_paged(args, peaks, peak_kind),
                      "prefill_d128": run_prefill_d128(args, peaks, peak_kind),
                      "prefill_paged_d128": run_prefill_paged_d128(args, peaks, peak_kind),

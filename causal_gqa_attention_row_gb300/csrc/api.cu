@@ -202,10 +202,12 @@ static gqa_status prefill_common(gqa::RowsParams& p, int bf16, int d_k, int d_v,
   p.err = error_word();
   if (!p.err) return GQA_ERR_CUDA;
   const float qscale = attention_scale * 1.4426950408889634f;
-  if (!arms_on && gqa::prefill_tc_supported(bf16, d_k, d_v, p.paged ? p.bs : 0, p.mbps) && attention_scale > 0.f)
+  if (gqa::prefill_tc_supported(bf16, d_k, d_v, p.paged ? p.bs : 0, p.mbps) && attention_scale > 0.f) {
+    const gqa::TcArms tc_arms{p.window, p.softcap2, p.sinks, p.alibi};
     return from_cuda(gqa::launch_prefill_tc(p.q, p.k, p.v, p.out, p.B, p.seq_q, p.capacity, p.offsets, p.H, p.Hkv,
                                             d_k, d_v, qscale, p.err, st, p.paged ? p.tables : nullptr, p.mbps, p.bs,
-                                            p.num_blocks, g_withhold_first_tile));
+                                            p.num_blocks, arms_on ? &tc_arms : nullptr, g_withhold_first_tile));
+  }
   const int nvmax = gqa::rows_max_nv(bf16, d_k, d_v, 0);
   if (nvmax == 0) return GQA_ERR_UNSUPPORTED;
   p.G = p.H / p.Hkv;

@@ -87,6 +87,16 @@ cudaError_t launch_append(void* q, const void* k_new, const void* v_new, void* k
                           int num_blocks, int bs, int H, int Hkv, int dk, int dv, double theta, int rot_offset,
                           int rot_dim, int bf16, unsigned* err, cudaStream_t st);
 
+// The arms for the tensor-core prefill: window (<= 0: none), softcap * log2 e
+// (0: none), sink logits and ALiBi slopes ([H] fp32 on the device, natural
+// units, or NULL).
+struct TcArms {
+  int window;
+  float softcap2;
+  const float* sinks;
+  const float* alibi;
+};
+
 // tcgen05 causal prefill (bf16, d_k = d_v = 64). Returns cudaErrorNotSupported
 // for other shapes. Contiguous k, v [B, Hkv, seq_kv_max, 64] (tables NULL), or
 // paged pools [num_blocks, Hkv, bs, 64] with block tables [B, mbps] and
@@ -94,7 +104,8 @@ cudaError_t launch_append(void* q, const void* k_new, const void* v_new, void* k
 cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
                               int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv,
                               float qscale, unsigned* err, cudaStream_t st, const int32_t* tables = nullptr,
-                              int mbps = 0, int bs = 0, int num_blocks = 0, int debug_withhold = 0);
+                              int mbps = 0, int bs = 0, int num_blocks = 0, const TcArms* arms = nullptr,
+                              int debug_withhold = 0);
 // bs = 0: contiguous K/V; else the pool's block size and max blocks per sequence.
 bool prefill_tc_supported(int bf16, int dk, int dv, int bs = 0, int mbps = 0);
 

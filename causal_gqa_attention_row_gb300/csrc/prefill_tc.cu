@@ -122,7 +122,21 @@ struct TcParams {
   float qscale;
   unsigned* err;
   int debug_withhold;  // test hook: the first K tile is never loaded, so its waits run out
+  // The arms (the ARMS instantiation): a row at position p sees keys
+  // first_visible_key(p, window)..p; a score s (natural units) becomes
+  // softcap * tanh(s / softcap) (cap_out = softcap * log2 e, cap_in = scale /
+  // softcap applied to the raw q.k), then s + alibi[h] * (key - p); the sink
+  // logit sinks[h] joins the softmax denominator only.
+  int window;
+  float cap_in, cap_out;
+  const float* alibi;
+  const float* sinks;
 };
+
+// First key tile a row at `pos` can see under the window (0 without one).
+__device__ __forceinline__ int first_key_tile(int pos, int window) {
+  return first_visible_key(pos < 0 ? 0 : pos, window) / kBN;
+}
 
 struct Bars {
   uint64_t q_full, k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
@@ -186,6 +200,20 @@ __device__ __forceinline__ uint32_t exp2_pair(float s0, float s1, float2 qs2, fl
   const float2 e = make_float2(ex2f(x.x), ex2f(x.y));
   acc = __fadd2_rn(acc, e);
   return pack_bf16(e.x, e.y);
+}
+
+__device__ __forceinline__ float rcpf(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh(x) = 1 - 2 / (e^(2x) + 1), from the special-function unit's 2^x and
+// reciprocal: absolute error near 1e-6 over the whole range (e^(2x) -> inf
+// gives 1, -> 0 gives -1), against about 5e-4 for the tanh.approx instruction,
+// which a softcap of tens would multiply into the exponent.
+__device__ __forceinline__ float tanh_from_ex2(float x) {
+  return 1.f - 2.f * rcpf(ex2f(x * 2.8853900817779268f) + 1.f);  // 2 log2(e)
 }
 
 // max(a, b, c) in one instruction.
@@ -269,7 +297,7 @@ __device__ __forceinline__ void load_kv_tile_warp(const CUtensorMap* tm, unsigne
   __syncwarp();
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool ARMS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -324,11 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.debug_withhold) {
       // test hook: K_0 is never requested (nothing is left in flight), so the
       // first wait on it runs into its bound and the CTA gives up
-    } else if (p.tables) {  // the tile's table entries are bounded by the offset
-      const int off0 = p.offsets ? p.offsets[b] : 0;
-      load_kv_tile<C::kCBK>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, off0 + i0 + rows);
     } else {
-      load_kv_tile<C::kCBK>(&tm_k, smem + kOffK, &bars->k_full[0], 0, kvh, b, p, 0);
+      // the first key tile this query tile sees (the window's, with the arms);
+      // paged: the tile's table entries are bounded by the offset
+      const int off0 = (ARMS || p.tables) && p.offsets ? p.offsets[b] : 0;
+      const int jb0 = ARMS ? first_key_tile(off0 + i0, p.window) : 0;
+      load_kv_tile<C::kCBK>(&tm_k, smem + kOffK, &bars->k_full[0], jb0, kvh, b, p, off0 + i0 + rows);
     }
   }
   if (warp == kMmaWarp0) {
@@ -356,7 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp0) tc::tmem_dealloc(tmem, kTmemCols);
     return;
   }
-  const int n_kv = (off + i0 + rows - 1) / kBN + 1;  // key tiles up to the last row's position
+  // key tiles jb .. jb + n_kv - 1: from the first one the tile's first row sees
+  // (under the window; 0 without one) to the last row's position. Ring stages,
+  // barrier phases and the warpgroup a tile belongs to count tiles from jb.
+  const int jb = ARMS ? first_key_tile(off + i0, p.window) : 0;
+  const int n_kv = (off + i0 + rows - 1) / kBN + 1 - jb;
 
   if (warp >= kProducerWarp) {
     regs_dec<kCtrlRegs>();  // the whole control warpgroup, right at the top of its branch
@@ -399,9 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__shfl_sync(0xffffffffu, w, 0)) break;
       }
       if (is_k)
-        load_kv_tile_warp<C::kCBK>(tm, ring + st * tile_bytes, &full[st], j, kvh, b, p, kv_hi, tab, lane);
+        load_kv_tile_warp<C::kCBK>(tm, ring + st * tile_bytes, &full[st], jb + j, kvh, b, p, kv_hi, tab, lane);
       else
-        load_kv_tile_warp<C::kCBV>(tm, ring + st * tile_bytes, &full[st], j, kvh, b, p, kv_hi, tab, lane);
+        load_kv_tile_warp<C::kCBV>(tm, ring + st * tile_bytes, &full[st], jb + j, kvh, b, p, kv_hi, tab, lane);
       issued_last[st] = j;
     }
     if (lane == 0) {
@@ -480,8 +513,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;                // query row within the tile
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int pos = off + i0 + r;                     // absolute position of this row
-    const float qs = p.qscale;
+    // With the arms the scores are moved into log2 units before the max (scale,
+    // softcap, ALiBi), so the exponent's multiplier is 1; plain: the raw q.k
+    // and the scale folded into the exponent.
+    const float qs = ARMS ? 1.f : p.qscale;
     const float th = kRescaleLog2 / qs;
+    const float alibi2 = ARMS && p.alibi ? __ldg(p.alibi + h) * kLog2e : 0.f;  // slope in log2 units
+    const int lo_key = ARMS ? first_visible_key(pos, p.window) : 0;          // first key this row sees
+    const int lo_tile_end = ARMS ? first_visible_key(off + i0 + rows - 1, p.window) : 0;  // window-masked keys end below
     float m_ref = -INFINITY;
     float l_run = 0.f;  // the row sum of this warpgroup's p, against m_ref
     const uint32_t tS = tmem + lane_addr + C::col_s(wg);
@@ -491,9 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_mine = (n_kv - wg + 1) / 2;  // key tiles this warpgroup handles
     bool alive = true;
     for (int k = 0; k < n_mine; ++k) {
-      const int j = 2 * k + wg;
-      const int j0 = j * kBN;
+      const int j = 2 * k + wg;    // counted from the first visible tile jb
+      const int j0 = (jb + j) * kBN;  // the tile's first key
       const bool diag = j0 + kBN - 1 > off + i0;  // this tile crosses the diagonal of some row
+      const bool below = ARMS && j0 < lo_tile_end;  // ... or holds keys below some row's window
       if (!warp_wait_tc(&bars->s_full[wg], k & 1, bars, p.err)) {
         alive = false;
         break;
@@ -507,12 +547,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free[wg]);
-      if (diag) {  // only the tile that crosses the diagonal has keys past some row's position
+      if (ARMS) {  // scale, softcap, ALiBi: log2 units (branches uniform across the CTA, outside the loops)
+        if (p.cap_out > 0.f) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              sv[c][e] = __float_as_uint(p.cap_out * tanh_from_ex2(__uint_as_float(sv[c][e]) * p.cap_in));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[c][e] = __float_as_uint(__uint_as_float(sv[c][e]) * p.qscale);
+        }
+        if (alibi2 != 0.f) {
+          const float base = alibi2 * (float)(j0 - pos);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              sv[c][e] = __float_as_uint(fmaf(alibi2, (float)(c * 32 + e), __uint_as_float(sv[c][e]) + base));
+        }
+      }
+      if (diag || below) {  // keys past the row's position, or (arms) below its window, weigh zero
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (j0 + c * 32 + e > pos) sv[c][e] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < 32; ++e) {
+            const int key = j0 + c * 32 + e;
+            if (key > pos || key < lo_key) sv[c][e] = __float_as_uint(-INFINITY);
+          }
       }
       // ---- the tile's row max; the reference moves only past the threshold
       float mx8[8];
@@ -607,10 +671,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* ml1 = reinterpret_cast<const float*>(smem + kOffML + kTileK);
     const float m0 = ml0[r], l0 = ml0[kBM + r], m1 = ml1[r], l1 = ml1[kBM + r];
     const bool use0 = l0 > 0.f, use1 = l1 > 0.f;
-    const float M = fmaxf(use0 ? m0 : -INFINITY, use1 ? m1 : -INFINITY);
+    // the sink logit (arms) is one more term of the denominator, in log2 units
+    const bool sink = ARMS && p.sinks != nullptr;
+    const float zs = sink ? __ldg(p.sinks + h) * kLog2e : -INFINITY;
+    const float M = fmaxf(fmaxf(use0 ? m0 : -INFINITY, use1 ? m1 : -INFINITY), zs);
     const float a0 = use0 ? ex2f((m0 - M) * qs) : 0.f;
     const float a1 = use1 ? ex2f((m1 - M) * qs) : 0.f;
-    const float l = a0 * l0 + a1 * l1;
+    const float l = a0 * l0 + a1 * l1 + (sink ? ex2f(zs - M) : 0.f);
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float c0 = a0 * inv, c1 = a1 * inv;
     // this warpgroup's d_v / 2 of the d_v columns, 32 at a time; O_1 exists once
@@ -671,22 +738,22 @@ bool make_map(CUtensorMap* m, const void* base, int d, uint64_t d1, uint64_t d2,
   return make_tmap_bf16(m, base, dims, strides, box);
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool ARMS>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                      const TcParams& p, cudaStream_t st) {
   using C = Cfg<DK, DV>;
   int dev = 0;
   cudaGetDevice(&dev);
-  static unsigned long long attr_done = 0;
+  static unsigned long long attr_done = 0;  // per device, per instantiation
   if (dev < 64 && !(attr_done >> dev & 1ull)) {
     // The register hand-over inside the kernel assumes exactly kLaunchRegs per
     // thread at launch; with any other allocation it could wait forever, so
     // such a build is refused here instead of launched.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<DK, DV>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<DK, DV, ARMS>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs) return cudaErrorNotSupported;
-    e = cudaFuncSetAttribute(prefill_tc_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_tc_kernel<DK, DV, ARMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << dev;
   }
@@ -706,7 +773,7 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DK, DV>, tq, tk, tv, to, p);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DK, DV, ARMS>, tq, tk, tv, to, p);
 }
 
 }  // namespace
@@ -723,7 +790,7 @@ bool prefill_tc_supported(int bf16, int dk, int dv, int bs, int mbps) {
 cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void* out, int B, int seq_q,
                               int seq_kv_max, const int32_t* offsets, int H, int Hkv, int dk, int dv, float qscale,
                               unsigned* err, cudaStream_t st, const int32_t* tables, int mbps, int bs,
-                              int num_blocks, int debug_withhold) {
+                              int num_blocks, const TcArms* arms, int debug_withhold) {
   if (!prefill_tc_supported(1, dk, dv, tables ? bs : 0, mbps) || !(qscale > 0.f)) return cudaErrorNotSupported;
   CUtensorMap tq, tk, tv, to;
   // q [B, S, H, d_k]: dims (d_k, H, S, B), box (64, 1, 128, 1)
@@ -756,9 +823,20 @@ cudaError_t launch_prefill_tc(const void* q, const void* k, const void* v, void*
   p.qscale = qscale;
   p.err = err;
   p.debug_withhold = debug_withhold;
-  if (dk == 64) return launch_d<64, 64>(tq, tk, tv, to, p, st);
-  if (dk == 128) return launch_d<128, 128>(tq, tk, tv, to, p, st);
-  return launch_d<192, 128>(tq, tk, tv, to, p, st);
+  const bool on = arms && (arms->window > 0 || arms->softcap2 > 0.f || arms->sinks || arms->alibi);
+  p.window = on ? arms->window : 0;
+  p.cap_out = on ? arms->softcap2 : 0.f;                          // softcap * log2 e
+  p.cap_in = on && arms->softcap2 > 0.f ? qscale / arms->softcap2 : 0.f;  // scale / softcap
+  p.alibi = on ? arms->alibi : nullptr;
+  p.sinks = on ? arms->sinks : nullptr;
+  if (on) {
+    if (dk == 64) return launch_d<64, 64, true>(tq, tk, tv, to, p, st);
+    if (dk == 128) return launch_d<128, 128, true>(tq, tk, tv, to, p, st);
+    return launch_d<192, 128, true>(tq, tk, tv, to, p, st);
+  }
+  if (dk == 64) return launch_d<64, 64, false>(tq, tk, tv, to, p, st);
+  if (dk == 128) return launch_d<128, 128, false>(tq, tk, tv, to, p, st);
+  return launch_d<192, 128, false>(tq, tk, tv, to, p, st);
 }
 
 }  // namespace gqa

@@ -152,8 +152,9 @@ typedef struct gqa_arms {
 } gqa_arms;
 
 /* attn_decode_contig / attn_decode_paged / attn_prefill_causal with the arms;
- * every other argument as there. Prefill with an arm on runs on the SIMT kernel
- * (the tensor-core kernel serves the plain arm). */
+ * every other argument as there. Prefill with an arm on runs on the tensor-core
+ * kernel for the shapes it takes (bf16, (d_k, d_v) = (64, 64), (128, 128),
+ * (192, 128)) and on the SIMT kernel otherwise, like the plain call. */
 gqa_status attn_decode_contig_ex(const void* q, const void* k_cache, const void* v_cache,
                                  const void* k_rot_shared, int d_rot, const int32_t* seq_lens, void* out,
                                  int B, int max_len, int H, int Hkv, int d_k, int d_v, float attention_scale,
@@ -198,7 +199,7 @@ gqa_status attn_prefill_paged(const void* q, const void* k_pool, const void* v_p
                               const int32_t* position_offset, void* out, int B, int seq_q, int max_blocks_per_seq,
                               int num_blocks, int block_size, int H, int Hkv, int d_k, int d_v, float attention_scale,
                               gqa_dtype dt, void* stream);
-/* attn_prefill_paged with the arms (`gqa_arms`); an arm on runs on the SIMT kernel. */
+/* attn_prefill_paged with the arms (`gqa_arms`); kernel choice as attn_prefill_causal_ex. */
 gqa_status attn_prefill_paged_ex(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
                                  const int32_t* position_offset, void* out, int B, int seq_q, int max_blocks_per_seq,
                                  int num_blocks, int block_size, int H, int Hkv, int d_k, int d_v,
