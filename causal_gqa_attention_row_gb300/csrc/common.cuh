@@ -108,6 +108,27 @@ __device__ __forceinline__ bool mbar_wait_hint(uint64_t* bar, uint32_t parity, u
   return true;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+
+// Wait until the grids this one was launched to depend on have completed and
+// their memory operations are visible. Every thread calls it before its first
+// access to global memory the previous kernel may have written (or read, for
+// outputs). A grid launched the ordinary way passes straight through.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next grid in the stream (launched with programmatic stream
+// serialization) start its CTAs once every CTA of this grid has called this or
+// exited; they run their set-up and then wait in grid_dep_wait.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// The attribute a launch sets to allow it (cudaLaunchKernelEx).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // L2 eviction policy for data read exactly once (K/V streams).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;

@@ -160,8 +160,10 @@ cudaError_t launch_plan_units(const RowsParams& p, cudaStream_t st) {
 // splits of one (sequence, head), M = max_s m_s, in split order. Empty splits
 // (m = -inf) weigh zero. One warp per output row.
 
-template <typename ET>
+// kMaxE: output columns per lane (d_v <= 32 * kMaxE).
+template <typename ET, int kMaxE>
 __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, int DV) {
+  grid_dep_wait();  // the attention kernel's partials (launched as its dependent)
   const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= p.B * p.seq_q * p.H) return;
@@ -188,7 +190,6 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
   // Each split's weight once (lane s % 32 holds split s's), the weighted row sums
   // reduced in a fixed butterfly order; every lane then walks the splits in order,
   // the weight broadcast, its output columns d = lane + 32 e read as coalesced rows.
-  constexpr int kMaxE = 16;  // DV <= 512 (the latent width of the absorbed MLA decode)
   float acc[kMaxE];
 #pragma unroll
   for (int e = 0; e < kMaxE; ++e) acc[e] = 0.f;
@@ -201,13 +202,29 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
       w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
       den_part = fmaf(w, P[(size_t)s * stride + 1], den_part);
     }
+    // The rows of up to kBatch splits are loaded before any of them is
+    // accumulated, so that many loads are in flight per lane; the sum still
+    // runs over the splits in order.
+    constexpr int kBatch = 4;
     const int cnt = min(32, n - s0);
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      const float* row = P + (size_t)(s0 + j) * stride + 2;
+    for (int j0 = 0; j0 < cnt; j0 += kBatch) {
+      float v[kBatch][kMaxE];
 #pragma unroll
-      for (int e = 0; e < kMaxE; ++e)
-        if (lane + 32 * e < DV) acc[e] = fmaf(wj, row[lane + 32 * e], acc[e]);
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const float* row = P + (size_t)(s0 + j0 + jj) * stride + 2;
+#pragma unroll
+        for (int e = 0; e < kMaxE; ++e)
+          v[jj][e] = (j0 + jj < cnt && lane + 32 * e < DV) ? __ldcg(row + lane + 32 * e) : 0.f;
+      }
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j0 + jj) & 31);
+        if (j0 + jj < cnt) {
+#pragma unroll
+          for (int e = 0; e < kMaxE; ++e)
+            if (lane + 32 * e < DV) acc[e] = fmaf(wj, v[jj][e], acc[e]);
+        }
+      }
     }
   }
 #pragma unroll
@@ -223,11 +240,26 @@ cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStre
   if (rows <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const unsigned blocks = (unsigned)((rows + warps_per_block - 1) / warps_per_block);
-  if (bf16)
-    split_combine_kernel<__nv_bfloat16><<<blocks, 32 * warps_per_block, 0, st>>>(p, dv);
-  else
-    split_combine_kernel<float><<<blocks, 32 * warps_per_block, 0, st>>>(p, dv);
-  return cudaGetLastError();
+  // d_v up to 512 (the latent width of the absorbed MLA decode), in lanes' shares
+  // of 4, 8 or 16 columns. Launched as a programmatic dependent of the attention
+  // kernel before it: its CTAs may start while that kernel finishes, and wait for
+  // it (grid_dep_wait) before reading the partials.
+  if (dv > 512) return cudaErrorNotSupported;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(32 * warps_per_block);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (bf16) {
+    if (dv <= 128) return cudaLaunchKernelEx(&cfg, split_combine_kernel<__nv_bfloat16, 4>, p, dv);
+    if (dv <= 256) return cudaLaunchKernelEx(&cfg, split_combine_kernel<__nv_bfloat16, 8>, p, dv);
+    return cudaLaunchKernelEx(&cfg, split_combine_kernel<__nv_bfloat16, 16>, p, dv);
+  }
+  if (dv <= 128) return cudaLaunchKernelEx(&cfg, split_combine_kernel<float, 4>, p, dv);
+  if (dv <= 256) return cudaLaunchKernelEx(&cfg, split_combine_kernel<float, 8>, p, dv);
+  return cudaLaunchKernelEx(&cfg, split_combine_kernel<float, 16>, p, dv);
 }
 
 // ---------------------------------------------------------------------------

@@ -262,6 +262,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   MlaBars* bars = reinterpret_cast<MlaBars*>(smem + C::kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // launched as a programmatic dependent: the lengths and the query may come
+  // from the kernel before this one
+  grid_dep_wait();
   // ---- work item: the pair of one (sequence, head tile, split) is one cluster
   const int half = (int)cluster_rank();
   const uint32_t peer = (uint32_t)(half ^ 1);
@@ -657,6 +660,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
 
+  grid_dep_launch();  // the split combine may start launching on freed SMs
   tc::fence_before_sync();
   __syncthreads();
   cluster_sync();  // the peer's last accesses to this CTA's shared memory are done
@@ -727,8 +731,15 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
   }
   const long long ctas = (long long)B * p.n_htiles * p.max_splits * 2;  // clusters of two
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-  mla_absorbed_tc_kernel<512, 64><<<(unsigned)ctas, kThreads, C::kSmemBytes, st>>>(tq, tr, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);  // clusters of two (the kernel's __cluster_dims__)
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_absorbed_tc_kernel<512, 64>, tq, tr, p);
 }
 
 }  // namespace gqa

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::prefetch_tmap(&tm_k);
     // everything above may overlap the previous kernel in the stream; the loads
     // below read memory it may have written
-    tc::grid_dep_wait();
+    grid_dep_wait();
     // Q and the first K tile load while the rest of the CTA sets up
     mbar_arrive_expect_tx(&bars->q_full, kTileK);
 #pragma unroll
@@ -364,14 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
-  tc::grid_dep_wait();  // before any thread touches global memory
+  grid_dep_wait();  // before any thread touches global memory
   const int off = p.offsets ? p.offsets[b] : 0;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   // the next launch in the stream may start setting up on the SMs this grid frees
-  tc::grid_dep_launch();
+  grid_dep_launch();
 
   if (off < 0 || (long long)off + p.S > p.S_kv) {  // the cache cannot hold these rows
     if (threadIdx.x == 0 && qt == p.n_qtiles - 1 && h == 0) raise_error(p.err, kErrBounds);
@@ -768,9 +768,7 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DK, DV, ARMS>, tq, tk, tv, to, p);

@@ -44,19 +44,6 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// ---- programmatic dependent launch ----------------------------------------------
-
-// Wait until the grids this one was launched to depend on have completed and
-// their memory operations are visible. Every thread calls it before its first
-// access to global memory the previous kernel may have written (or read, for
-// outputs). A grid launched the ordinary way passes straight through.
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Let the next grid in the stream (launched with programmatic stream
-// serialization) start its CTAs once every CTA of this grid has called this or
-// exited; they run their set-up and then wait in grid_dep_wait.
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 // ---- TMEM -------------------------------------------------------------------
 
 // Whole-warp operations.
