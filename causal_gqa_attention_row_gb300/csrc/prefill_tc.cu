@@ -147,7 +147,10 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-__device__ __forceinline__ bool aborted(Bars* bars) { return *reinterpret_cast<volatile int*>(&bars->abort_flag); }
+template <typename BarsT>
+__device__ __forceinline__ bool aborted(BarsT* bars) {
+  return *reinterpret_cast<volatile int*>(&bars->abort_flag);
+}
 
 // The waits of this kernel sit on its critical path (MMA -> softmax -> MMA):
 // each probe of the mbarrier suspends a waiter for at most this long, so it
@@ -162,7 +165,8 @@ __device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity) {
 }
 
 // Single-thread wait of the producer and MMA issuers (bounded).
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
+template <typename BarsT>
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, BarsT* bars, unsigned* err) {
   if (aborted(bars)) return false;
   if (wait_fast(bar, parity)) return true;
   *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
@@ -171,7 +175,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 }
 
 // Whole-warp version: every lane agrees on the outcome.
-__device__ __forceinline__ bool warp_wait_tc(uint64_t* bar, uint32_t parity, Bars* bars, unsigned* err) {
+template <typename BarsT>
+__device__ __forceinline__ bool warp_wait_tc(uint64_t* bar, uint32_t parity, BarsT* bars, unsigned* err) {
   bool ok = !aborted(bars) && wait_fast(bar, parity);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && (threadIdx.x & 31) == 0) {
