@@ -69,6 +69,8 @@
 // results are bit-identical, and so are repeated calls.
 #pragma once
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -728,8 +730,8 @@ cudaError_t launch_rows_inst_arms(const RowsParams& p, cudaStream_t st) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static int slots_cache[64] = {};  // per device, 0 = not yet known
-  int slots = dev < 64 ? slots_cache[dev] : 0;
+  static std::atomic<int> slots_cache[64];  // per device, 0 = not yet known
+  int slots = dev < 64 ? slots_cache[dev].load(std::memory_order_acquire) : 0;
   if (slots == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes);
     if (e != cudaSuccess) return e;
@@ -740,7 +742,7 @@ cudaError_t launch_rows_inst_arms(const RowsParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
     slots = per_sm * sms;
-    if (dev < 64) slots_cache[dev] = slots;
+    if (dev < 64) slots_cache[dev].store(slots, std::memory_order_release);
   }
   const long long items = (long long)p.B * p.Hkv * p.n_hchunks * p.n_rblocks;
   if (items <= 0 || p.max_splits <= 0) return cudaSuccess;

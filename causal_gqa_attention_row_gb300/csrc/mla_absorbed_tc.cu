@@ -48,6 +48,7 @@
 // writes O / l as bf16; otherwise each split writes (m, l, O) in fp32 (m in the
 // log2 domain) and the split-combine kernel merges them.
 
+#include <atomic>
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
@@ -722,12 +723,12 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
   p.debug_withhold = debug_withhold;
   int dev = 0;
   cudaGetDevice(&dev);
-  static unsigned long long attr_done = 0;
-  if (dev < 64 && !(attr_done >> dev & 1ull)) {
+  static std::atomic<unsigned long long> attr_done{0};  // per device
+  if (dev < 64 && !(attr_done.load(std::memory_order_acquire) >> dev & 1ull)) {
     const cudaError_t e =
         cudaFuncSetAttribute(mla_absorbed_tc_kernel<512, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done |= 1ull << dev;
+    attr_done.fetch_or(1ull << dev, std::memory_order_release);
   }
   const long long ctas = (long long)B * p.n_htiles * p.max_splits * 2;  // clusters of two
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;

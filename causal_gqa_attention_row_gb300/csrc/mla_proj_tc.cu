@@ -12,6 +12,7 @@
 // 32 rows of it (thread = output row m, its 32 columns = the batch rows) to y as
 // bf16. Batch rows past B read as zeros and are not written.
 
+#include <atomic>
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
@@ -132,12 +133,12 @@ cudaError_t launch_head_proj_tc(const void* W, const void* x, int x_stride, void
   const int smem_bytes = nkb * (kPM + kPN) * 128 + (int)sizeof(ProjBars) + 1024;
   int dev = 0;
   cudaGetDevice(&dev);
-  static unsigned long long attr_done = 0;
-  if (dev < 64 && !(attr_done >> dev & 1ull)) {
+  static std::atomic<unsigned long long> attr_done{0};  // per device
+  if (dev < 64 && !(attr_done.load(std::memory_order_acquire) >> dev & 1ull)) {
     const cudaError_t e = cudaFuncSetAttribute(head_proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kMaxKBlocks * (kPM + kPN) * 128 + (int)sizeof(ProjBars) + 1024);
     if (e != cudaSuccess) return e;
-    attr_done |= 1ull << dev;
+    attr_done.fetch_or(1ull << dev, std::memory_order_release);
   }
   const dim3 grid((unsigned)(M / kPM), (unsigned)H, (unsigned)((B + kPN - 1) / kPN));
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidValue;

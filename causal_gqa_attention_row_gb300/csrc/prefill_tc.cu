@@ -58,6 +58,7 @@
 // launch start once it is set up, so back-to-back launches overlap one's set-up
 // with the other's tail.
 
+#include <atomic>
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
@@ -211,14 +212,6 @@ __device__ __forceinline__ float rcpf(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// tanh(x) = 1 - 2 / (e^(2x) + 1), from the special-function unit's 2^x and
-// reciprocal: absolute error near 1e-6 over the whole range (e^(2x) -> inf
-// gives 1, -> 0 gives -1), against about 5e-4 for the tanh.approx instruction,
-// which a softcap of tens would multiply into the exponent.
-__device__ __forceinline__ float tanh_from_ex2(float x) {
-  return 1.f - 2.f * rcpf(ex2f(x * 2.8853900817779268f) + 1.f);  // 2 log2(e)
 }
 
 // max(a, b, c) in one instruction.
@@ -553,25 +546,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free[wg]);
       if (ARMS) {  // scale, softcap, ALiBi: log2 units (branches uniform across the CTA, outside the loops)
+        // The ALiBi term splits into the tile's part, slope * (j0 - pos), added
+        // with the scale or softcap in one packed operation per pair of scores,
+        // and the column's part, slope * column, one fma with an immediate.
+        const float base = alibi2 * (float)(j0 - pos);  // 0 without ALiBi
         if (p.cap_out > 0.f) {
+          // cap * tanh(x) = cap - 2 cap / (e^(2x) + 1), from the special-function
+          // unit's 2^x and reciprocal: absolute error near 1e-6 in tanh over the
+          // whole range (e^(2x) -> inf gives cap, -> 0 gives -cap), against about
+          // 5e-4 for the tanh.approx instruction, which the cap would multiply
+          // into the exponent. The rest is packed over pairs of scores.
+          const float2 k2 = make_float2(p.cap_in * 2.8853900817779268f, p.cap_in * 2.8853900817779268f);  // 2 log2(e)
+          const float2 one2 = make_float2(1.f, 1.f);
+          const float2 m2 = make_float2(-2.f * p.cap_out, -2.f * p.cap_out);
+          const float2 a2 = make_float2(p.cap_out + base, p.cap_out + base);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              sv[c][e] = __float_as_uint(p.cap_out * tanh_from_ex2(__uint_as_float(sv[c][e]) * p.cap_in));
+            for (int e = 0; e < 32; e += 2) {
+              const float2 t = __fmul2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), k2);
+              const float2 dn = __fadd2_rn(make_float2(ex2f(t.x), ex2f(t.y)), one2);
+              const float2 y = __ffma2_rn(make_float2(rcpf(dn.x), rcpf(dn.y)), m2, a2);
+              sv[c][e] = __float_as_uint(y.x);
+              sv[c][e + 1] = __float_as_uint(y.y);
+            }
         } else {
+          const float2 q2 = make_float2(p.qscale, p.qscale), b2 = make_float2(base, base);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sv[c][e] = __float_as_uint(__uint_as_float(sv[c][e]) * p.qscale);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 y =
+                  __ffma2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), q2, b2);
+              sv[c][e] = __float_as_uint(y.x);
+              sv[c][e + 1] = __float_as_uint(y.y);
+            }
         }
         if (alibi2 != 0.f) {
-          const float base = alibi2 * (float)(j0 - pos);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              sv[c][e] = __float_as_uint(fmaf(alibi2, (float)(c * 32 + e), __uint_as_float(sv[c][e]) + base));
+              sv[c][e] = __float_as_uint(fmaf(alibi2, (float)(c * 32 + e), __uint_as_float(sv[c][e])));
         }
       }
       if (diag || below) {  // keys past the row's position, or (arms) below its window, weigh zero
@@ -749,8 +765,8 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   using C = Cfg<DK, DV>;
   int dev = 0;
   cudaGetDevice(&dev);
-  static unsigned long long attr_done = 0;  // per device, per instantiation
-  if (dev < 64 && !(attr_done >> dev & 1ull)) {
+  static std::atomic<unsigned long long> attr_done{0};  // per device, per instantiation
+  if (dev < 64 && !(attr_done.load(std::memory_order_acquire) >> dev & 1ull)) {
     // The register hand-over inside the kernel assumes exactly kLaunchRegs per
     // thread at launch; with any other allocation it could wait forever, so
     // such a build is refused here instead of launched.
@@ -760,7 +776,7 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     if (fa.numRegs != kLaunchRegs) return cudaErrorNotSupported;
     e = cudaFuncSetAttribute(prefill_tc_kernel<DK, DV, ARMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done |= 1ull << dev;
+    attr_done.fetch_or(1ull << dev, std::memory_order_release);
   }
   const long long ctas = (long long)p.B * p.H * p.n_qtiles;
   if (ctas <= 0) return cudaSuccess;
