@@ -298,6 +298,10 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
     *abort_flag = 0;
     fence_barrier_init();
   }
+  // Launched as a programmatic dependent of the kernel before it in the stream
+  // (the unit plan, or the append): the set-up above may overlap it; nothing
+  // below reads global memory before it has completed.
+  grid_dep_wait();
   __syncthreads();
 
   if (warp == kRowsWarps) {
@@ -749,8 +753,15 @@ cudaError_t launch_rows_inst_arms(const RowsParams& p, cudaStream_t st) {
   const long long units = p.sched ? items * p.max_splits : items;  // an upper bound with a plan
   if (items * p.max_splits > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const int grid = (int)(units < slots ? units : slots);
-  kern<<<grid, kRowsThreads, C::smem_bytes, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kRowsThreads);
+  cfg.dynamicSmemBytes = C::smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <typename ET, int DK, int DV, int DROT, int NV>

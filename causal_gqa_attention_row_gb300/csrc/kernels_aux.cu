@@ -105,6 +105,11 @@ constexpr int kPartBuckets = 64;
 __global__ void __launch_bounds__(kPlanThreads) plan_units_kernel(const RowsParams p) {
   __shared__ int warp_sums[32];
   __shared__ int bucket_at[kPartBuckets];
+  // The lengths may come from the kernel before this one (the append). The
+  // attention kernel after this one may launch at once: it waits for this
+  // kernel's completion before it reads the plan.
+  grid_dep_wait();
+  grid_dep_launch();
   const int n_items = p.B * p.Hkv * p.n_hchunks * p.n_rblocks;
   for (int i = threadIdx.x; i < kPartBuckets; i += blockDim.x) bucket_at[i] = 0;
   // thread t owns the contiguous items [lo, hi): one scan for the full units (in
@@ -151,8 +156,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_units_kernel(const RowsPara
 }
 
 cudaError_t launch_plan_units(const RowsParams& p, cudaStream_t st) {
-  plan_units_kernel<<<1, kPlanThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_units_kernel, p);
 }
 
 // ---------------------------------------------------------------------------
