@@ -190,6 +190,20 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 1/x on the special-function unit (the PTX rcp.approx instruction; 1/inf = 0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// cap * tanh(s / cap) for a score s and cap in the log2 domain, with k = 2 log2(e) / cap:
+// tanh(t) = 1 - 2 / (e^(2t) + 1), from 2^x and 1/x (absolute error near 1e-6 in
+// tanh over the whole range; e^(2t) -> inf gives cap, -> 0 gives -cap).
+__device__ __forceinline__ float softcap_log2(float s, float cap, float k) {
+  return fmaf(-2.f * cap, rcp_approx(ex2(s * k) + 1.f), cap);
+}
+
 template <typename ET>
 __device__ __forceinline__ void chunk_to_f2(const uint4 u, float2* f);
 
@@ -497,6 +511,7 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
   int lim_own = 0;    // keys < lim_own are causal for the owned head's row
   int lo_own = 0;     // ... and keys >= lo_own inside its window
   float slope2 = 0.f; // the owned head's ALiBi slope in the log2 domain
+  const float cap_k = ARMS && p.softcap2 > 0.f ? 2.8853900817779268f / p.softcap2 : 0.f;  // 2 log2(e) / cap
   int merges = 0;
   for (int gt = 0;; ++gt) {
     const int s = gt % kStages;
@@ -576,8 +591,8 @@ __global__ void __launch_bounds__(kRowsThreads, RowsCfg<ET, DK, DV, DROT, NV>::M
         float sb = reduce_own<NV, L>(pb, li);
         // ---- the arms: softcap on the scaled score, then the ALiBi bias
         if (ARMS && p.softcap2 > 0.f) {
-          sa = p.softcap2 * tanhf(sa / p.softcap2);
-          sb = p.softcap2 * tanhf(sb / p.softcap2);
+          sa = softcap_log2(sa, p.softcap2, cap_k);
+          sb = softcap_log2(sb, p.softcap2, cap_k);
         }
         if (ARMS && p.alibi) {
           sa = fmaf(slope2, (float)(tr0 + ra - (lim_own - 1)), sa);
