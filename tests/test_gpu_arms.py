@@ -135,3 +135,23 @@ def test_plain_call_equals_zero_arms(gpu_lib):
     g.attn_decode_contig(*args, b, c.scale, workspace=ws, window=100000, alibi_slopes=torch.zeros(32, device=DEV))
     ok(g)
     assert torch.equal(a, b)
+
+
+def test_decode_softcap_saturates(gpu_lib):
+    """Logits far beyond the softcap: q scaled so that |scale q.k| reaches the
+    hundreds with a cap of 1, so cap * tanh(s / cap) saturates to +-cap (e^(2t)
+    overflowing to infinity, or to 0) for most keys and is still checked against
+    the oracle's tanh for the rest."""
+    g = gpu_lib
+    lens = [5, 700, 2049]
+    B, H, Hkv, d, L = len(lens), 32, 8, 128, 2100
+    c = W.make_contig(B=B, H=H, Hkv=Hkv, dk=d, dv=d, max_len=L, lens=lens, seed=95)
+    q = (c.q.float() * 60.0).to(torch.bfloat16)
+    out = torch.empty(B, H, d, dtype=torch.bfloat16, device=DEV)
+    g.attn_decode_contig(q.to(DEV), c.k.to(DEV), c.v.to(DEV), c.seq_lens.to(DEV), out, c.scale,
+                         workspace=g.decode_workspace(B, H, d, L), softcap=1.0)
+    ok(g)
+    s_max = float((q.float()[2, 0] @ c.k.float()[2, 0, :lens[2]].T).abs().max() * c.scale)
+    assert s_max > 50.0  # the scores do reach far past the cap
+    want = core.attention_arms(W.to_oracle(q), W.to_oracle(c.k), W.to_oracle(c.v), lens, c.scale, 0, 1.0, None, None)
+    check(float(np.abs(out.float().cpu().numpy().astype(np.float64) - want).max()), TOL[torch.bfloat16])

@@ -92,3 +92,18 @@ def test_tc_prefill_arms_paged_equals_contig_bits(gpu_lib, bs):
     want = core.attention_arms(W.to_oracle(c.q), W.to_oracle(c.k), W.to_oracle(c.v), [o + S for o in offs], c.scale,
                                window, cap, _f64(sinks), _f64(slopes))
     check(float(np.abs(out_c.float().cpu().numpy() - want).max()), 2e-2, "paged, every arm")
+
+
+@pytest.mark.parametrize("dk,dv,H,Hkv", [(64, 64, 8, 2), (128, 128, 8, 4)])
+def test_tc_prefill_softcap_saturates(gpu_lib, dk, dv, H, Hkv):
+    """Logits far beyond the softcap (q scaled by 60, cap 1): most scores saturate
+    to +-cap, where 2^x overflows to infinity or goes to 0 inside the kernel's tanh."""
+    g = gpu_lib
+    S = 300
+    c = W.make_prefill(B=1, S=S, H=H, Hkv=Hkv, dk=dk, dv=dv, seed=310)
+    q = (c.q.float() * 60.0).to(torch.bfloat16)
+    out = torch.empty(1, S, H, dv, dtype=torch.bfloat16, device=DEV)
+    g.attn_prefill_causal(q.to(DEV), c.k.to(DEV), c.v.to(DEV), out, c.scale, softcap=1.0)
+    assert g.attn_get_device_error() == g.OK
+    want = core.attention_arms(W.to_oracle(q), W.to_oracle(c.k), W.to_oracle(c.v), [S], c.scale, 0, 1.0, None, None)
+    check(float(np.abs(out.float().cpu().numpy() - want).max()), 2e-2)
