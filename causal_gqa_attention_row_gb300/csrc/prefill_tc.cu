@@ -159,17 +159,14 @@ __device__ __forceinline__ bool aborted(BarsT* bars) {
 constexpr uint32_t kWaitHintNs = 20;
 
 
-// A phase that has already completed is seen by the non-blocking probe at once;
-// only a wait that has to wait goes on to the suspending probe.
-__device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity) {
-  return mbar_test_parity_nb(bar, parity) || mbar_wait_hint(bar, parity, kWaitHintNs);
-}
-
-// Single-thread wait of the producer and MMA issuers (bounded).
+// Single-thread wait of the producer and MMA issuers (bounded). A phase that
+// has completed is taken at once (the abort flag, a shared-memory load on the
+// critical path, is only read when the wait has to wait).
 template <typename BarsT>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, BarsT* bars, unsigned* err) {
+  if (mbar_test_parity_nb(bar, parity)) return true;
   if (aborted(bars)) return false;
-  if (wait_fast(bar, parity)) return true;
+  if (mbar_wait_hint(bar, parity, kWaitHintNs)) return true;
   *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
   raise_error(err, kErrTimeout);
   return false;
@@ -178,7 +175,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 // Whole-warp version: every lane agrees on the outcome.
 template <typename BarsT>
 __device__ __forceinline__ bool warp_wait_tc(uint64_t* bar, uint32_t parity, BarsT* bars, unsigned* err) {
-  bool ok = !aborted(bars) && wait_fast(bar, parity);
+  bool ok = mbar_test_parity_nb(bar, parity) || (!aborted(bars) && mbar_wait_hint(bar, parity, kWaitHintNs));
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && (threadIdx.x & 31) == 0) {
     *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
