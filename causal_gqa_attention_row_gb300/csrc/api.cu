@@ -356,8 +356,10 @@ gqa_status attn_rope_interleaved(void* x, const int32_t* positions, int B, int T
 }
 
 size_t attn_decode_mla_absorbed_workspace_bytes(int B, int H, int d_c, int max_len) {
-  if (B <= 0 || H <= 0 || d_c <= 0 || max_len <= gqa::kMlaChunk) return 0;
-  const size_t splits = (size_t)ceil_div(max_len, gqa::kMlaChunk);
+  if (B <= 0 || H <= 0 || d_c <= 0 || max_len <= 0) return 0;
+  const int chunk = gqa::mla_chunk_rows(B, H, max_len);
+  if (max_len <= chunk) return 0;
+  const size_t splits = (size_t)ceil_div(max_len, chunk);
   return (size_t)B * (size_t)H * splits * (size_t)(d_c + 2) * sizeof(float);
 }
 
@@ -379,8 +381,9 @@ static gqa_status mla_absorbed_common(const void* q_abs, const void* latent, con
   if (!err) return GQA_ERR_CUDA;
   const float qscale = attention_scale * 1.4426950408889634f;
   float* partial = need > 0 ? static_cast<float*>(workspace) : nullptr;
+  const int chunk = gqa::mla_chunk_rows(B, H, capacity);
   const cudaError_t e = gqa::launch_mla_absorbed_tc(q_abs, latent, seq_lens, out_lat, partial, B, capacity, H, d_c,
-                                                    d_r, gqa::kMlaChunk, qscale, err, st, tables, mbps, bs,
+                                                    d_r, chunk, qscale, err, st, tables, mbps, bs,
                                                     num_blocks, g_withhold_first_tile);
   if (e != cudaSuccess || need == 0) return from_cuda(e);
   // the splits of each (sequence, head) merged into out_lat
@@ -392,8 +395,8 @@ static gqa_status mla_absorbed_common(const void* q_abs, const void* latent, con
   p.seq_q = 1;
   p.H = H;
   p.capacity = capacity;
-  p.split_rows = gqa::kMlaChunk;
-  p.max_splits = ceil_div(capacity, gqa::kMlaChunk);
+  p.split_rows = chunk;
+  p.max_splits = ceil_div(capacity, chunk);
   p.window = 0;
   p.err = err;
   return from_cuda(gqa::launch_split_combine(p, d_c, 1, st));

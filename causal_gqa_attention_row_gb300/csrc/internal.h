@@ -122,9 +122,20 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
                                    float qscale, unsigned* err, cudaStream_t st, const int32_t* tables = nullptr,
                                    int mbps = 0, int bs = 0, int num_blocks = 0, int debug_withhold = 0);
 bool mla_absorbed_paged_block_ok(int bs);
-// Rows of one split of the absorbed MLA decode (a fixed number, so a sequence's
-// result does not depend on the rest of the batch).
+// Rows of one split of the absorbed MLA decode: 1024, doubled (up to 8192) while
+// the (sequence, head tile, split) clusters of a call at its capacity would still
+// number at least 64 (one wave of the GPU's 76 two-CTA cluster slots, nearly
+// filled), so that a batch fills the GPU with as few partial results to merge
+// as it can. A function of B, H and the capacity alone: a sequence's result does
+// not depend on the lengths of the others, and two calls with the same three
+// values split alike.
 constexpr int kMlaChunk = 1024;
+inline int mla_chunk_rows(int B, int H, int capacity) {
+  const long long clusters_per_split = (long long)B * ((H + 127) / 128);
+  int chunk = kMlaChunk;
+  while (chunk < 8192 && clusters_per_split * (((long long)capacity + 2 * chunk - 1) / (2 * chunk)) >= 64) chunk *= 2;
+  return chunk;
+}
 
 // y[b, h, :M] = W[h] x[b, h, :K] (bf16, fp32 accumulation), W [H, M, K]; the
 // `tail` columns of x after K are copied to y after M.

@@ -334,7 +334,8 @@ gqa_status attn_decode_mla_absorbed(const void* q_abs, const void* latent, const
  * block_size one of 8, 16, 32, 64 (else GQA_ERR_UNSUPPORTED). A table entry outside
  * [0, num_blocks) for a visible row sets GQA_ERR_DEVICE_BOUNDS and its rows read as
  * zeros. Same arithmetic as the contiguous call: the outputs are bit-identical to
- * it on the same rows. Workspace: attn_decode_mla_absorbed_workspace_bytes(B, H, d_c,
+ * it on the same rows when max_blocks_per_seq * block_size equals its max_len
+ * (the capacity decides the split size). Workspace: attn_decode_mla_absorbed_workspace_bytes(B, H, d_c,
  * max_blocks_per_seq * block_size). */
 gqa_status attn_decode_mla_absorbed_paged(const void* q_abs, const void* latent_pool, const int32_t* block_tables,
                                           const int32_t* seq_lens, void* out_lat, int B, int max_blocks_per_seq,
@@ -342,8 +343,11 @@ gqa_status attn_decode_mla_absorbed_paged(const void* q_abs, const void* latent_
                                           float attention_scale, gqa_dtype dt, void* workspace,
                                           size_t workspace_bytes, void* stream);
 
-/* Workspace of attn_decode_mla_absorbed: rows are split 1024 at a time; with S =
- * ceil(max_len / 1024) > 1 splits, B * H * S * (d_c + 2) floats, else 0. Host only. */
+/* Workspace of attn_decode_mla_absorbed: rows are split C at a time, C = 1024
+ * doubled (up to 8192) while B * ceil(H / 128) * ceil(max_len / (2 C)) >= 64;
+ * with S = ceil(max_len / C) > 1 splits, B * H * S * (d_c + 2) floats, else 0.
+ * C depends on B, H and max_len only (max_blocks_per_seq * block_size for the
+ * paged call). Host only. */
 size_t attn_decode_mla_absorbed_workspace_bytes(int B, int H, int d_c, int max_len);
 
 /* out[b, h] = v_b[h] out_lat[b, h] (fp32 accumulation, rounded to bf16).

@@ -88,9 +88,13 @@ def test_bad_arguments_rejected_before_launch(lib):
 def test_mla_absorbed_workspace_and_checks(lib):
     """The absorbed-MLA calls: workspace size and host-side rejections (no launch)."""
     import causal_gqa_attention_row_gb300 as g
+    # splits of C rows: C = 1024, doubled while B * ceil(H / 128) * ceil(max_len / 2C) >= 64
     assert g.attn_decode_mla_absorbed_workspace_bytes(32, 128, 512, 1024) == 0   # one split: none
-    assert g.attn_decode_mla_absorbed_workspace_bytes(32, 128, 512, 4096) == 32 * 128 * 4 * 514 * 4
-    assert g.attn_decode_mla_absorbed_workspace_bytes(2, 16, 512, 1025) == 2 * 16 * 2 * 514 * 4
+    assert g.attn_decode_mla_absorbed_workspace_bytes(32, 128, 512, 4096) == 32 * 128 * 2 * 514 * 4  # C = 2048
+    assert g.attn_decode_mla_absorbed_workspace_bytes(32, 128, 512, 1500) == 32 * 128 * 2 * 514 * 4  # C = 1024
+    assert g.attn_decode_mla_absorbed_workspace_bytes(2, 16, 512, 1025) == 2 * 16 * 2 * 514 * 4      # C = 1024
+    assert g.attn_decode_mla_absorbed_workspace_bytes(64, 256, 512, 32768) == 64 * 256 * 4 * 514 * 4  # C = 8192
+    assert g.attn_decode_mla_absorbed_workspace_bytes(1, 128, 512, 32768) == 1 * 128 * 32 * 514 * 4  # C = 1024
     P = ctypes.c_void_p(16)
     N = None
     # (q_abs, latent, seq_lens, out_lat, B, max_len, H, d_c, d_r, scale, dtype, workspace, bytes, stream)

@@ -204,6 +204,32 @@ def test_paged_equals_contiguous_bit_for_bit(gpu_lib, bs):
     check(np.abs(out[3:4].float().cpu().numpy() - ref).max(), 2e-2)
 
 
+def test_paged_equals_contiguous_at_2048_row_splits(gpu_lib):
+    """A batch large enough for 2048-row splits (32 sequences of capacity 2112:
+    32 * ceil(2112 / 2048) = 64 clusters at that size): paged equals contiguous
+    bit for bit, lengths across the 2048-row boundary, one sequence against the
+    oracle."""
+    g = gpu_lib
+    B, L = 32, 2112
+    lens = [int(x) for x in torch.randint(1, L + 1, (B,), generator=W.generator(130))]
+    lens[0], lens[1], lens[2] = 2048, 2049, L
+    c = W.make_mla_absorbed(B=B, H=128, max_len=L, lens=lens, seed=131)
+    q_abs = absorbed_q(g, c)
+    latent = c.latent.to(DEV)
+    lens_d = c.lens.to(DEV)
+    want = attend(g, q_abs, latent, lens_d, c.scale)
+    assert g.attn_get_device_error() == g.OK
+    assert g.attn_decode_mla_absorbed_workspace_bytes(B, 128, D_C, L) == B * 128 * 2 * (D_C + 2) * 4  # two splits
+    pool, tables = page_latent(latent, lens, 16, seed=132)
+    out = torch.full((B, 128, D_C), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = g.mla_absorbed_workspace(B, 128, D_C, tables.shape[1] * 16)
+    g.attn_decode_mla_absorbed_paged(q_abs, pool, tables, lens_d, out, c.scale, workspace=ws)
+    assert g.attn_get_device_error() == g.OK
+    assert torch.equal(out, want)
+    ref = oracle_latent(q_abs[1:2], latent[1:2], c.lens[1:2], c.scale)
+    check(np.abs(out[1:2].float().cpu().numpy() - ref).max(), 2e-2)
+
+
 def test_paged_bad_entry_is_flagged(gpu_lib):
     """A table entry outside the pool for a visible row sets the bounds error; the
     other sequences' outputs are unaffected."""
