@@ -658,8 +658,8 @@ def reference_arm(args, rank, world):
 
 # DRAM bytes (read + write) of the paged decode's attention kernel per algorithmic
 # byte, from an ncu capture of a 32-sequence case of the paged workload:
-# 2,086,155,008 B moved for 2,080,718,884 B of K/V rows, q, out and table entries.
-DECODE_TRAFFIC_PER_ALG_BYTE = 2086155008 / 2080718884
+# 2,085,826,048 B moved for 2,080,718,884 B of K/V rows, q, out and table entries.
+DECODE_TRAFFIC_PER_ALG_BYTE = 2085826048 / 2080718884
 
 # Kernels one paged step launches: append_kernel, then the decode's plan_units_kernel,
 # attn_rows_kernel and split_combine_kernel (the workload's caches are long enough to split).
@@ -749,7 +749,7 @@ def main():
                      "frac": res["achieved_decode_gbs"] / hbm,
                      "traffic": round(DECODE_TRAFFIC_PER_ALG_BYTE * res["decode_bytes"]) if args.seqs == 256 else None,
                      "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of attn_rows_kernel on a 32-sequence "
-                                       "case of this workload (2.086 GB for 2.081 GB of algorithmic bytes), scaled by the "
+                                       "case of this workload (2.0858 GB for 2.0807 GB of algorithmic bytes), scaled by the "
                                        "K/V rows one launch processes",
                      "kernel": "attn_decode_paged (plan_units_kernel + attn_rows_kernel + split_combine_kernel)",
                      "algorithmic_bytes_per_launch": res["decode_bytes"], "decode_ms": res["decode_ms"],
