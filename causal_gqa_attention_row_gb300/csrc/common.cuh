@@ -62,17 +62,6 @@ __device__ __forceinline__ bool mbar_test_parity_nb(uint64_t* bar, uint32_t pari
   return done != 0;
 }
 
-// Bounded spin on the non-blocking probe: reacts to a completed phase sooner
-// than mbar_wait, at the cost of issue slots while it spins.
-__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity) {
-  if (mbar_test_parity_nb(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_test_parity_nb(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
-  }
-  return true;
-}
-
 // Wait until the phase with the given parity has completed. Returns false if
 // it has not after kWaitLimitCycles; the caller records the timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
