@@ -346,6 +346,10 @@ __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positio
   // a different index in every lane, each warp's load would be serialised.
   __shared__ double w_s[128];
   for (int i = threadIdx.x; i < npairs; i += blockDim.x) w_s[i] = fr.w[i];
+  // launched as a programmatic dependent: x and the positions may come from the
+  // kernel before this one; the next launch may start setting up at once
+  grid_dep_wait();
+  grid_dep_launch();
   __syncthreads();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)B * T * npairs) return;
@@ -384,13 +388,18 @@ cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int hea
   if (rot_dim > 256) return cudaErrorNotSupported;
   const unsigned blocks = (unsigned)((total + 127) / 128);
   const RopeFreqs fr = rope_freqs(rot_dim, theta);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (bf16)
-    rope_kernel<__nv_bfloat16><<<blocks, 128, 0, st>>>(reinterpret_cast<__nv_bfloat16*>(x), positions, B, T, heads,
-                                                        d, heads_outer, rot_offset, rot_dim, fr);
-  else
-    rope_kernel<float><<<blocks, 128, 0, st>>>(reinterpret_cast<float*>(x), positions, B, T, heads, d, heads_outer,
-                                               rot_offset, rot_dim, fr);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, rope_kernel<__nv_bfloat16>, reinterpret_cast<__nv_bfloat16*>(x), positions, B, T,
+                              heads, d, heads_outer, rot_offset, rot_dim, fr);
+  return cudaLaunchKernelEx(&cfg, rope_kernel<float>, reinterpret_cast<float*>(x), positions, B, T, heads, d,
+                            heads_outer, rot_offset, rot_dim, fr);
 }
 
 // ---------------------------------------------------------------------------
@@ -406,6 +415,10 @@ __global__ void __launch_bounds__(128) append_kernel(ET* q, const ET* k_new, con
                                                      bool rope, const RopeFreqs fr, int rot_offset, int rot_dim,
                                                      unsigned* err) {
   const int b = blockIdx.x;
+  // launched as a programmatic dependent: the lengths and the rows may come from
+  // the kernel before this one; the next launch (the unit plan) may start at once
+  grid_dep_wait();
+  grid_dep_launch();
   const int p = lens_in[b];
   const bool pos_ok = p >= 0 && (long long)p < (long long)mbps * bs;
   const int blk = pos_ok ? tables[(size_t)b * mbps + p / bs] : -1;
@@ -455,18 +468,23 @@ cudaError_t launch_append(void* q, const void* k_new, const void* v_new, void* k
   const bool rope = theta > 0.0 && rot_dim > 0;
   if (rope && rot_dim > 256) return cudaErrorNotSupported;
   const RopeFreqs fr = rope_freqs(rope ? rot_dim : 0, theta);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B);
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (bf16)
-    append_kernel<__nv_bfloat16><<<B, 128, 0, st>>>(
-        reinterpret_cast<__nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k_new),
-        reinterpret_cast<const __nv_bfloat16*>(v_new), reinterpret_cast<__nv_bfloat16*>(k_pool),
-        reinterpret_cast<__nv_bfloat16*>(v_pool), tables, lens_in, lens_out, mbps, num_blocks, bs, H, Hkv, dk, dv,
-        rope, fr, rot_offset, rot_dim, err);
-  else
-    append_kernel<float><<<B, 128, 0, st>>>(reinterpret_cast<float*>(q), reinterpret_cast<const float*>(k_new),
-                                            reinterpret_cast<const float*>(v_new), reinterpret_cast<float*>(k_pool),
-                                            reinterpret_cast<float*>(v_pool), tables, lens_in, lens_out, mbps,
-                                            num_blocks, bs, H, Hkv, dk, dv, rope, fr, rot_offset, rot_dim, err);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, append_kernel<__nv_bfloat16>, reinterpret_cast<__nv_bfloat16*>(q),
+                              reinterpret_cast<const __nv_bfloat16*>(k_new), reinterpret_cast<const __nv_bfloat16*>(v_new),
+                              reinterpret_cast<__nv_bfloat16*>(k_pool), reinterpret_cast<__nv_bfloat16*>(v_pool), tables,
+                              lens_in, lens_out, mbps, num_blocks, bs, H, Hkv, dk, dv, rope, fr, rot_offset, rot_dim,
+                              err);
+  return cudaLaunchKernelEx(&cfg, append_kernel<float>, reinterpret_cast<float*>(q), reinterpret_cast<const float*>(k_new),
+                            reinterpret_cast<const float*>(v_new), reinterpret_cast<float*>(k_pool),
+                            reinterpret_cast<float*>(v_pool), tables, lens_in, lens_out, mbps, num_blocks, bs, H, Hkv,
+                            dk, dv, rope, fr, rot_offset, rot_dim, err);
 }
 
 }  // namespace gqa

@@ -26,6 +26,10 @@ __global__ void __launch_bounds__(kProjThreads)
   __shared__ __align__(16) float xs[kTK][kTB];
   const int m0 = blockIdx.x * kTM, h = blockIdx.y, b0 = blockIdx.z * kTB;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;  // outputs m0 + 4 tx .. +3, rows b0 + 2 ty, +1
+  // launched as a programmatic dependent: x may come from the kernel before this
+  // one; the next launch may start setting up at once
+  grid_dep_wait();
+  grid_dep_launch();
   const __nv_bfloat16* Wh = W + (size_t)h * M * K;
   float acc[2][4] = {};
   // K is staged 64 at a time: each thread moves kWTasks 16-byte pieces of W and
@@ -112,10 +116,16 @@ cudaError_t launch_head_matvec(const void* W, const void* x, int x_stride, void*
   if (B == 0) return cudaSuccess;
   const dim3 grid((unsigned)((M + kTM - 1) / kTM), (unsigned)H, (unsigned)((B + kTB - 1) / kTB));
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidValue;
-  head_matvec_kernel<<<grid, kProjThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(W),
-                                                    static_cast<const __nv_bfloat16*>(x), x_stride,
-                                                    static_cast<__nv_bfloat16*>(y), y_stride, B, H, M, K, tail);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kProjThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, head_matvec_kernel, static_cast<const __nv_bfloat16*>(W),
+                            static_cast<const __nv_bfloat16*>(x), x_stride, static_cast<__nv_bfloat16*>(y), y_stride, B,
+                            H, M, K, tail);
 }
 
 }  // namespace gqa

@@ -40,6 +40,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
   ProjBars* bars = reinterpret_cast<ProjBars*>(sx + nkb * kXBlk);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kPM, h = blockIdx.y, b0 = blockIdx.z * kPN;
+  // launched as a programmatic dependent: x may come from the kernel before this
+  // one; the next launch may start setting up at once
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->full, 1);
@@ -142,10 +146,16 @@ cudaError_t launch_head_proj_tc(const void* W, const void* x, int x_stride, void
   }
   const dim3 grid((unsigned)(M / kPM), (unsigned)H, (unsigned)((B + kPN - 1) / kPN));
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidValue;
-  head_proj_tc_kernel<<<grid, kPThreads, smem_bytes, st>>>(tw, tx, static_cast<const __nv_bfloat16*>(x), x_stride,
-                                                            static_cast<__nv_bfloat16*>(y), y_stride, B, H, M, K,
-                                                            tail, err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, head_proj_tc_kernel, tw, tx, static_cast<const __nv_bfloat16*>(x), x_stride,
+                            static_cast<__nv_bfloat16*>(y), y_stride, B, H, M, K, tail, err);
 }
 
 }  // namespace gqa
