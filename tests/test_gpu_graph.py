@@ -84,3 +84,36 @@ def test_prefill_step_replays_in_a_graph(gpu_lib):
         torch.cuda.synchronize()
         assert g.attn_get_device_error() == g.OK
         assert torch.equal(out, want)
+
+
+def test_absorbed_mla_step_replays_in_a_graph(gpu_lib):
+    """mla_absorb_q + attn_decode_mla_absorbed (two-CTA cluster kernel, split
+    combine) + mla_unabsorb_out captured once and replayed: equal to the eager step."""
+    g = gpu_lib
+    B, H, L = 4, 128, 2500
+    c = W.make_mla_absorbed(B=B, H=H, max_len=L, lens=[2500, 900, 1, 2049], seed=142, device=DEV)
+    q_abs = torch.empty(B, H, 576, dtype=torch.bfloat16, device=DEV)
+    out_lat = torch.empty(B, H, 512, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(B, H, 128, dtype=torch.bfloat16, device=DEV)
+    ws = g.mla_absorbed_workspace(B, H, 512, L, device=DEV)
+
+    def step():
+        g.mla_absorb_q(c.q, c.k_b, q_abs)
+        g.attn_decode_mla_absorbed(q_abs, c.latent, c.lens, out_lat, c.scale, workspace=ws)
+        g.mla_unabsorb_out(out_lat, c.v_b, out)
+
+    step()
+    torch.cuda.synchronize()
+    assert g.attn_get_device_error() == g.OK
+    want = out.clone()
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        out_lat.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert g.attn_get_device_error() == g.OK
+        assert torch.equal(out, want)
