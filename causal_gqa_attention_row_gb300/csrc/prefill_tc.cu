@@ -642,35 +642,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= f;
         }
       }
-      // ---- d_v = 64: P_w is free once PV_{j-2} has read it (issued a whole tile
-      // earlier, so this rarely waits). Every phase of o_done[w] is waited for in
-      // order, before the next PV can be issued, so the barrier is never two
-      // phases ahead of this wait (nor of the rescale's or the final one).
-      // d_v = 128: P goes over S_j's own first columns, already read.
-      if (!C::kAlias && k >= 1) {
-        if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
-        tc::fence_after_sync();
-      }
-      // ---- p = 2^(s*qs - m*qs), the fp32 row sum of these p, and P as bf16 pairs;
-      // each 16-word chunk of P goes to TMEM as soon as it is formed, so few P
-      // registers are live next to the S row
+      // ---- p = 2^(s*qs - m*qs), the fp32 row sum of these p, and P as bf16 pairs
       const float mq = m_ref == -INFINITY ? 0.f : m_ref * qs;  // no visible key yet: all p are 0
       const float2 nmq2 = make_float2(-mq, -mq);
       float2 ls[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) ls[e] = make_float2(0.f, 0.f);
+      uint32_t pw[4][16];  // each P pair replaces the two scores it came from: no more registers than S
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t pw[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t)
-          pw[t] = exp2_pair(__uint_as_float(sv[c][2 * t]), __uint_as_float(sv[c][2 * t + 1]), qs2, nmq2, ls[t & 3]);
-        tc::tmem_st_32x32b_x16(tP + c * 16, pw);
+          pw[c][t] = exp2_pair(__uint_as_float(sv[c][2 * t]), __uint_as_float(sv[c][2 * t + 1]), qs2, nmq2, ls[t & 3]);
+        // d_v = 128: P goes over S_j's own first columns, already read; each
+        // 16-word chunk is stored as soon as it is formed
+        if (C::kAlias) tc::tmem_st_32x32b_x16(tP + c * 16, pw[c]);
       }
       l_run += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
+      // ---- d_v = 64: P_w is free once this warpgroup's previous PV has read it.
+      // That PV was issued only as this tile began, so the wait comes after the
+      // exponentials, which then overlap it. Every phase of o_done[w] is waited
+      // for in order, before the next PV can be issued, so the barrier is never
+      // two phases ahead of this wait (nor of the rescale's or the final one).
+      if (!C::kAlias) {
+        if (k >= 1) {
+          if (!warp_wait_tc(&bars->o_done[wg], (k - 1) & 1, bars, p.err)) {
+            alive = false;
+            break;
+          }
+          tc::fence_after_sync();
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_st_32x32b_x16(tP + c * 16, pw[c]);
+      }
       tc::tmem_st_wait();
       tc::fence_before_sync();  // this thread's TMEM accesses are done
       __syncwarp();             // ... for every lane of the warp; one lane signals
