@@ -11,35 +11,38 @@
 // contraction, not a stream, and it runs on the tensor cores.
 //
 // One cluster of two CTAs = one (sequence, tile of 128 heads, split of p.chunk
-// cache rows); CTA r of the pair owns value columns [r d_c / 2, (r + 1) d_c / 2)
-// and the heads are the MMA's 128 rows. Each CTA keeps the Q_abs columns of its
-// value half plus the rope columns (5 of the 9 64-column blocks) and loads the
-// same columns of each 64-row cache tile R, so the score contraction is split
-// between the pair:
-//   S_r = Q_abs[:, cols_r] R[:, cols_r]^T   M = 128 heads, N = 64 rows, K = 256 + 32
-// (the rope block's 64 columns: the first 32 to CTA 0, the last 32 to CTA 1).
-// The partial scores go through distributed shared memory: each softmax warp
-// writes its rows of S_r into a local send buffer and moves them with one bulk
-// copy into the peer's receive buffer (completing on the peer's barrier), and
-// both CTAs form S = S_0 + S_1
-// (one fp32 addition, the same bits on both sides), so the pair runs identical
-// softmax arithmetic and agrees on every row max and sum. Then
-//   O_r += P R[:, value half r]             M = 128 heads, N = 256, K = 64 rows
-// with P (bf16) in tensor memory over the S columns it came from. A cache row
-// is read from memory once per pair (each CTA fetches its 5 blocks), and no
-// score is computed twice.
+// cache rows); the heads are the MMA's 128 rows. The pair walks the split in
+// tiles of 64 cache rows R_t and divides each tile two ways:
+//   - the keys: CTA r scores rows 32r .. 32r + 31 of the tile against the whole
+//     query row, S_r = Q_abs R_t[32r .. 32r + 31]^T (M = 128, N = 32, K = 576);
+//   - the values: CTA r accumulates value columns [r d_c / 2, (r + 1) d_c / 2)
+//     of all 64 rows, O_r += P R_t[:, value half r] (M = 128, N = 256, K = 64).
+// So each CTA needs the other's P. The pair agrees on one reference max per
+// head first: each CTA sends its tile row maxima (128 floats) to the other with
+// asynchronous remote stores, both take the larger, and both then move the
+// reference, rescale O and l, and form p = 2^(s*qs - m*qs) in bf16 the same
+// way. Each CTA writes its 32 columns of P_t into a shared-memory P tile and
+// copies them, one bulk copy per softmax warp and 8-key column, into the same
+// place of the peer's tile; the PV MMA reads P from there. Per tile a CTA sends
+// 8.5 KiB to its peer (the bf16 P half and the maxima) instead of a fp32 score
+// tile. Each CTA keeps the row sum of its own p; the two sums are added once,
+// at the end.
 //
-// Per CTA: shared memory holds Q_abs's 5 blocks (80 KiB, for the CTA's whole
-// life), a two-stage ring of cache tiles (2 x 40 KiB) and the receive and send
-// buffers of the exchange (2 x 32 KiB); tensor memory holds O (256 columns) and
-// two S buffers (2 x 64).
+// Per CTA: tensor memory holds O (256 columns), S (32) and the first 448 of the
+// 576 Q_abs columns (224 columns, two bf16 per column: the score MMA's A
+// operand); shared memory holds the other two Q_abs column blocks (32 KiB),
+// two P tiles (2 x 16 KiB, no swizzle: each 8-key column of all 128 heads is
+// 2 KiB, so a CTA's half is 4 contiguous pieces), and a three-stage ring of
+// cache tiles: the CTA's 32 rows in full (36 KiB) and the peer's 32 rows'
+// value half (16 KiB), 52 KiB per stage.
 // Roles (192 threads):
 //   warps 0-3  softmax: thread t owns head h0 + t (TMEM lane t); warp w trades
-//              its 32 rows with warp w of the peer
-//   warp 4     initialises the barriers; TMA producer of Q_abs (once) and of
-//              the cache tiles (lane i issues the box of local block i)
+//              maxima and P columns with warp w of the peer
+//   warp 4     initialises the barriers; TMA producer of the two Q_abs blocks
+//              (once) and of the cache tiles
 //   warp 5     allocates TMEM; one thread issues the MMAs, S_t as soon as its
-//              tile has landed and PV_t as soon as P_t is in TMEM
+//              tile has landed and S_{t-1} has been read, PV_t once both halves
+//              of P_t are in place
 // Softmax: a lazily moved reference max (threshold 2^8 in p), p rounded to
 // bf16 and the fp32 row sum taken over exactly those p. Rows of the last tile at
 // or past seq_len weigh zero, and their value rows in shared memory are zeroed
@@ -56,8 +59,9 @@ namespace gqa {
 namespace {
 
 constexpr int kHeads = 128;    // query heads per cluster: the MMA's M
-constexpr int kKeys = 64;      // cache rows per tile: the S MMA's N
-constexpr int kStages = 2;     // cache-tile ring
+constexpr int kKeys = 64;      // cache rows per tile of the pair
+constexpr int kOwn = 32;       // ... of which each CTA scores 32: the S MMA's N
+constexpr int kStages = 3;     // cache-tile ring
 constexpr int kThreads = 192;  // four softmax warps, the producer, the MMA warp
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;
@@ -67,31 +71,36 @@ constexpr uint32_t kWaitHintNs = 20;
 template <int DC, int DR>
 struct MlaCfg {
   static constexpr int kW = DC + DR;            // row width
+  static constexpr int kNB = kW / 64;           // 64-column blocks of a row
   static constexpr int kDVH = DC / 2;           // value columns per CTA
   static constexpr int kCBV = kDVH / 64;        // ... in 64-column blocks
-  static constexpr int kCBR = DR / 64;          // rope blocks (shared by the pair)
-  static constexpr int kCBL = kCBV + kCBR;      // blocks a CTA holds of a row
+  static constexpr int kQS = 2;                 // Q_abs blocks in shared memory (the last two)
+  static constexpr int kQT = kNB - kQS;         // ... and in tensor memory (the first seven)
   static constexpr int kQBlk = kHeads * 128;    // one block of Q_abs: 128 rows x 128 bytes
-  static constexpr int kRBlk = kKeys * 128;     // one block of a cache tile: 64 rows x 128 bytes
-  static constexpr int kTileQ = kCBL * kQBlk;
-  static constexpr int kTileR = kCBL * kRBlk;
-  static constexpr int kXBuf = kHeads * kKeys * 4;  // 128 rows x 64 fp32: the receive buffer, then the send buffer
-  static constexpr int kOffQ = 0, kOffR = kTileQ, kOffX = kOffR + kStages * kTileR;
-  static constexpr int kOffBar = kOffX + 2 * kXBuf;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
-  // K steps (16 columns) of the score MMA per CTA: its value blocks, and half of the rope blocks
-  static constexpr int kStepsV = kCBV * 4, kStepsR = kCBR * 2;
-  // TMEM columns: O, then the two S buffers (P over the first half of each)
-  static constexpr uint32_t kColO = 0, kColS = kDVH;
+  static constexpr int kRBlk = kOwn * 128;      // one block of a CTA's cache rows: 32 rows x 128 bytes
+  // a ring stage: this CTA's rows, every block; then the peer's rows, this CTA's value blocks
+  static constexpr int kStage = (kNB + kCBV) * kRBlk;
+  static constexpr int kPBuf = kHeads * kKeys * 2;  // a P tile: 128 heads x 64 keys, bf16
+  static constexpr int kPCol = kHeads * 16;          // ... one 8-key column of it: 2 KiB
+  // shared memory: the P tiles first (any descriptor over them stays inside
+  // the CTA's window), Q_abs's blocks, the ring, maxima and row sums, barriers
+  static constexpr int kOffP = 0, kOffQ = kOffP + 2 * kPBuf, kOffR = kOffQ + kQS * kQBlk;
+  static constexpr int kOffM = kOffR + kStages * kStage;  // [2][128] maxima by tile parity, then [128] row sums
+  static constexpr int kOffBar = kOffM + 3 * kHeads * 4;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + alignment slack
+  // TMEM columns: O, S, then Q_abs's first kQT blocks (32 columns each)
+  static constexpr uint32_t kColO = 0, kColS = kDVH, kColQ = kColS + kOwn;
   static_assert(DC % 128 == 0 && DR % 64 == 0, "whole 64-column blocks per half");
   static_assert(kDVH % 16 == 0 && kDVH <= 256, "one PV MMA covers the half");
-  static_assert(kColS + 2 * kKeys <= kTmemCols, "TMEM map");
+  static_assert(kColQ % 32 == 0 && kColQ + kQT * 32 <= kTmemCols, "TMEM map");
+  static_assert(kOffR % 1024 == 0 && kStage % 1024 == 0, "swizzle atoms on 1024-byte boundaries");
   static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
 };
 
 struct MlaParams {
   int B, H, max_len, chunk, max_splits, n_htiles;  // max_len: rows a sequence can hold
   const int32_t* seq_lens;  // [B] rows visible, >= 1 and <= max_len
+  const __nv_bfloat16* q_abs;  // [B, H, d_c + d_r]
   // paged cache (tables != NULL): a pool [num_blocks, bs, d_c + d_r]; row j of
   // sequence b in block tables[b * mbps + j / bs], slot j % bs; bs divides 64
   const int32_t* tables;
@@ -104,18 +113,22 @@ struct MlaParams {
 };
 
 struct MlaBars {
+  // q_full: Q_abs's shared-memory blocks have landed and every softmax warp has
+  // written its rows of the rest into TMEM
   uint64_t q_full, r_full[kStages], r_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_done[2], mma_final;
-  // per softmax warp (its 32 rows, 8 KiB of each buffer):
-  // x_full: the peer's partial rows have landed in this CTA's receive buffer
-  //         (this warp's expected bytes, completed by the peer's bulk copy);
-  // x_free: the peer has read the rows this CTA copied into its receive buffer
-  //         (so that copy, and the read of this CTA's send buffer, are done)
-  uint64_t x_full[4], x_free[4];
+  // s_full / s_free: S_t is in TMEM / every softmax warp has read it;
+  // p_full[x]: P tile x holds P_t (this CTA's four warps and the peer's 8 KiB);
+  // o_done[x]: PV_t done, for t of parity x
+  uint64_t s_full, s_free, p_full[2], o_done[2], mma_final;
+  // per softmax warp w (its 32 heads):
+  // m_full[w][x]: the peer's tile maxima for tile parity x have landed (128 bytes)
+  // p_free[w][x]: the peer's PV that last read its P tile x is done (a remote arrival)
+  // l_full[w]:    the peer's row sums have landed (once)
+  uint64_t m_full[4][2], p_free[4][2], l_full[4];
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(MlaBars) <= 256, "barrier block");
+static_assert(sizeof(MlaBars) <= 512, "barrier block");
 
 // ---- cluster helpers ---------------------------------------------------------
 
@@ -141,14 +154,21 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src,
                : "memory");
 }
 
+// Asynchronous 4-byte store into a peer CTA's shared memory, counted as
+// transaction bytes on the peer's mbarrier `bar`.
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+               "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
-               : "memory");
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
 
@@ -248,10 +268,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// Byte offset of 16-byte chunk c of row r in an exchange buffer (rows of 256
-// bytes; the chunk index XOR r % 16 spreads a warp's rows over the banks).
-__device__ __forceinline__ uint32_t xchg_off(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 15)) * 16)); }
-
 template <int DC, int DR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_absorbed_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
@@ -261,6 +277,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // swizzle atoms sit on 1024-byte boundaries of the shared window
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   MlaBars* bars = reinterpret_cast<MlaBars*>(smem + C::kOffBar);
+  float* mbuf = reinterpret_cast<float*>(smem + C::kOffM);  // [2][kHeads]: the peer's tile maxima
+  float* lbuf = mbuf + 2 * kHeads;                          // [kHeads]: the peer's row sums
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // launched as a programmatic dependent: the lengths and the query may come
@@ -291,36 +309,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int k1 = min(len, k0 + p.chunk);
   const int n_t = (k1 - k0 + kKeys - 1) / kKeys;  // >= 1
 
-  // the global column block held in local block i: the value half, then the rope blocks
-  auto global_block = [&](int i) { return i < C::kCBV ? half * C::kCBV + i : DC / 64 + (i - C::kCBV); };
-
   if (warp == kProducerWarp) {
     if (lane == 0) {
-      mbar_init(&bars->q_full, 1);
+      mbar_init(&bars->q_full, 5);  // the producer's expected bytes + one arrival per softmax warp
       for (int s = 0; s < kStages; ++s) {
         mbar_init(&bars->r_full[s], 1);
         mbar_init(&bars->r_empty[s], 1);
       }
+      mbar_init(&bars->s_full, 1);
+      mbar_init(&bars->s_free, 4);  // one arrival per softmax warp
       for (int x = 0; x < 2; ++x) {
-        mbar_init(&bars->s_full[x], 1);
-        mbar_init(&bars->p_full[x], 4);  // one arrival per softmax warp
+        mbar_init(&bars->p_full[x], 4);
         mbar_init(&bars->o_done[x], 1);
       }
-      for (int w = 0; w < 4; ++w) {
-        mbar_init(&bars->x_full[w], 1);
-        mbar_init(&bars->x_free[w], 1);
-      }
       mbar_init(&bars->mma_final, 1);
+      for (int w = 0; w < 4; ++w) {
+        for (int x = 0; x < 2; ++x) {
+          mbar_init(&bars->m_full[w][x], 1);
+          mbar_init(&bars->p_free[w][x], 1);
+        }
+        mbar_init(&bars->l_full[w], 1);
+      }
       bars->abort_flag = 0;
       fence_barrier_init();
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_r);
-      mbar_arrive_expect_tx(&bars->q_full, C::kTileQ);
+      mbar_arrive_expect_tx(&bars->q_full, C::kQS * C::kQBlk);
     }
     __syncwarp();
-    // Q_abs [B, H, W]: this CTA's blocks of rows h0..h0+127 (heads past H read as zeros)
-    if (lane < C::kCBL)
-      tc::tma_load_4d(smem + C::kOffQ + lane * C::kQBlk, &tm_q, global_block(lane) * 64, h0, b, 0, &bars->q_full);
+    // Q_abs [B, H, W]: its last kQS blocks of rows h0..h0+127 (heads past H read as zeros)
+    if (lane < C::kQS)
+      tc::tma_load_4d(smem + C::kOffQ + lane * C::kQBlk, &tm_q, (C::kQT + lane) * 64, h0, b, 0, &bars->q_full);
   }
   if (warp == kMmaWarp) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -336,24 +355,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int issued_last[kStages];
 #pragma unroll
     for (int s = 0; s < kStages; ++s) issued_last[s] = -1;
-    // paged: a tile is `per` pool blocks; lane x < per * kCBL issues the box of
-    // block x % per and column block x / per (each box a whole number of 8-row
-    // swizzle atoms, so the boxes land where one box of the tile would put them)
-    const int per = p.tables ? kKeys / p.bs : 1;
-    const int nbox = per * C::kCBL;
+    // Box x of a tile: this CTA's 32 rows, column block x / per (x < kNB * per),
+    // or the peer's 32 rows, value block (x - kNB * per) / per of this CTA's
+    // half; sub-box x % per covers `br` of the 32 rows (paged: one pool block or
+    // half of a 64-row one; contiguous: all 32)
+    const int br = p.tables ? min(p.bs, kOwn) : kOwn;
+    const int per = kOwn / br;
+    const int nbox = (C::kNB + C::kCBV) * per;  // <= 52
     for (int t = 0; t < n_t; ++t) {
       const int st = t % kStages;
-      int blk[2] = {0, 0};
+      const int kt = k0 + t * kKeys;
+      int blk[2] = {0, 0}, slot[2] = {0, 0};
       if (p.tables) {  // the tile's table entries, fetched before waiting for the stage
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int x = lane + 32 * u;
           if (x >= nbox) continue;
-          const int ti = (k0 + t * kKeys) / p.bs + x % per;
+          const bool own = x < C::kNB * per;
+          const int row0 = kt + kOwn * (own ? half : 1 - half) + (x % per) * br;
+          const int ti = row0 / p.bs;
           // a block past the sequence, or an entry out of range (flagged), loads
           // from past the end of the pool: the TMA engine fills it with zeros
           int e = p.num_blocks;
-          if (ti < p.mbps && ti * p.bs < len) {
+          if (ti < p.mbps && row0 < len) {
             e = __ldg(p.tables + (size_t)b * p.mbps + ti);
             if (e < 0 || e >= p.num_blocks) {
               raise_error(p.err, kErrBounds);
@@ -361,30 +385,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           blk[u] = e;
+          slot[u] = row0 % p.bs;
         }
       }
       if (p.debug_withhold && t == 0 && half == 1) continue;  // test hook: tile 0 is never requested
-      if (t >= kStages) {  // the stage is free once PV_{t-2} is done
+      if (t >= kStages) {  // the stage is free once PV_{t-kStages} is done
         bool ok = true;
         if (lane == 0) ok = wait_or_abort(&bars->r_empty[st], ((t / kStages) - 1) & 1, bars, p.err);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bars->r_full[st], C::kTileR);
+      if (lane == 0) mbar_arrive_expect_tx(&bars->r_full[st], C::kStage);
       __syncwarp();
-      unsigned char* dst = smem + C::kOffR + st * C::kTileR;
-      if (!p.tables) {
-        // rows k0 + 64t .. +63 of sequence b; rows past the cache's capacity read as zeros
-        if (lane < C::kCBL)
-          tc::tma_load_4d(dst + lane * C::kRBlk, &tm_r, global_block(lane) * 64, k0 + t * kKeys, b, 0,
-                          &bars->r_full[st]);
-      } else {
+      unsigned char* dst = smem + C::kOffR + st * C::kStage;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int x = lane + 32 * u;
-          if (x < nbox)
-            tc::tma_load_4d(dst + (x / per) * C::kRBlk + (x % per) * p.bs * 128, &tm_r, global_block(x / per) * 64, 0,
-                            blk[u], 0, &bars->r_full[st]);
-        }
+      for (int u = 0; u < 2; ++u) {
+        const int x = lane + 32 * u;
+        if (x >= nbox) continue;
+        const bool own = x < C::kNB * per;
+        const int cb = own ? x / per : (x - C::kNB * per) / per;  // block within its region
+        const int g = own ? cb : half * C::kCBV + cb;              // the row's column block
+        unsigned char* d = dst + ((own ? 0 : C::kNB) + cb) * C::kRBlk + (x % per) * br * 128;
+        if (!p.tables)  // rows past the cache's capacity read as zeros
+          tc::tma_load_4d(d, &tm_r, g * 64, kt + kOwn * (own ? half : 1 - half), b, 0, &bars->r_full[st]);
+        else
+          tc::tma_load_4d(d, &tm_r, g * 64, slot[u], blk[u], 0, &bars->r_full[st]);
       }
       __syncwarp();
       issued_last[st] = t;
@@ -398,51 +422,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      const uint32_t idS = tc::idesc_bf16_f32(kHeads, kKeys, false);
+      const uint32_t idS = tc::idesc_bf16_f32(kHeads, kOwn, false);
       const uint32_t idO = tc::idesc_bf16_f32(kHeads, C::kDVH, true);
-      constexpr uint64_t kHi = tc::desc_sw128_hi(0, 1024);  // K-major: 8-row groups 1024 bytes apart
-      const uint64_t dQ = kHi | tc::desc_addr(smem + C::kOffQ);
-      const uint64_t dR0 = kHi | tc::desc_addr(smem + C::kOffR);
-      // the value half as V: MN-major, 8-row groups 1024 bytes apart, its 64-column
-      // blocks one cache-tile block (8 KiB) apart
-      const uint64_t dV0 = tc::desc_sw128_hi(C::kRBlk, 1024) | tc::desc_addr(smem + C::kOffR);
-      const uint32_t tO = tmem + C::kColO;
-      auto issue_s = [&](int t) {  // S_{t%2} = this CTA's share of Q_abs R_t^T
+      constexpr uint64_t kHiK = tc::desc_sw128_hi(0, 1024);  // K-major: 8-row groups 1024 bytes apart
+      // V: MN-major, 8-row groups 1024 bytes apart, 64-column blocks one 32-row block apart
+      constexpr uint64_t kHiV = tc::desc_sw128_hi(C::kRBlk, 1024);
+      // P: K-major without swizzle, 8-key columns kPCol apart, 8-head groups 128 bytes apart
+      constexpr uint64_t kHiP = tc::desc_plain_hi(C::kPCol, 128);
+      const uint64_t dQ = kHiK | tc::desc_addr(smem + C::kOffQ);
+      const uint64_t dR0 = kHiK | tc::desc_addr(smem + C::kOffR);
+      const uint64_t dV0 = kHiV | tc::desc_addr(smem + C::kOffR);
+      const uint64_t dP0 = kHiP | tc::desc_addr(smem + C::kOffP);
+      const uint32_t tO = tmem + C::kColO, tS = tmem + C::kColS, tQ = tmem + C::kColQ;
+      auto issue_s = [&](int t) {  // S = Q_abs (this CTA's 32 rows of R_t)^T
         const int st = t % kStages;
-        const uint32_t tS = tmem + C::kColS + (t & 1) * kKeys;
         tc::fence_after_sync();
-        const uint64_t dR = dR0 + (uint64_t)((st * C::kTileR) >> 4);
+        const uint64_t dR = dR0 + (uint64_t)((st * C::kStage) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < C::kStepsV + C::kStepsR; ++kk) {
-          // value blocks: all four steps of each; rope blocks: this CTA's two steps of each
-          const int blk = kk < C::kStepsV ? kk / 4 : C::kCBV + (kk - C::kStepsV) / 2;
-          const int step = kk < C::kStepsV ? kk % 4 : half * 2 + (kk - C::kStepsV) % 2;
-          const uint32_t aq = blk * C::kQBlk + step * 32;
-          const uint32_t ar = blk * C::kRBlk + step * 32;
-          tc::mma_f16_ss(tS, dQ + (aq >> 4), dR + (ar >> 4), idS, kk > 0);
+        for (int kk = 0; kk < C::kW / 16; ++kk) {
+          const int g = kk / 4, step = kk % 4;  // column block, 16-column step inside it
+          const uint32_t ar = g * C::kRBlk + step * 32;
+          if (g < C::kQT)  // Q_abs from TMEM: 16 columns = 8 TMEM columns
+            tc::mma_f16_ts(tS, tQ + g * 32 + step * 8, dR + (ar >> 4), idS, kk > 0);
+          else
+            tc::mma_f16_ss(tS, dQ + (((g - C::kQT) * C::kQBlk + step * 32) >> 4), dR + (ar >> 4), idS, kk > 0);
         }
-        tc::mma_commit(&bars->s_full[t & 1]);
+        tc::mma_commit(&bars->s_full);
       };
-      auto issue_pv = [&](int t) {  // O += P_t R_t[:, value half], 16 rows per instruction
-        const int st = t % kStages;
-        const uint32_t tP = tmem + C::kColS + (t & 1) * kKeys;
+      auto issue_pv = [&](int t) {  // O += P_t R_t[:, value half], 16 keys per instruction
+        const int st = t % kStages, x = t & 1;
         tc::fence_after_sync();
-        const uint64_t dV = dV0 + (uint64_t)((st * C::kTileR) >> 4);
+        const uint64_t dP = dP0 + (uint64_t)((x * C::kPBuf) >> 4);
+        const uint64_t dV = dV0 + (uint64_t)((st * C::kStage) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          tc::mma_f16_ts(tO, tP + kk * 8, dV + kk * (2048 >> 4), idO, (t > 0 || kk > 0));
-        tc::mma_commit(&bars->o_done[t & 1]);
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          // keys 16kk .. 16kk + 15 of the tile are rows of CTA kk / 2: this CTA's
+          // own region (its value blocks) or the peer rows' region
+          const uint32_t av = (kk / 2 == half ? half * C::kCBV : C::kNB) * C::kRBlk + (kk % 2) * 16 * 128;
+          tc::mma_f16_ss(tO, dP + (uint64_t)((kk * 2 * C::kPCol) >> 4), dV + (av >> 4), idO, (t > 0 || kk > 0));
+        }
+        tc::mma_commit(&bars->o_done[x]);
         tc::mma_commit(&bars->r_empty[st]);  // the tile's stage is free once PV_t is done
       };
       bool ok = wait_or_abort(&bars->q_full, 0, bars, p.err);
-      // S_t needs tile t in shared memory, which also means PV_{t-2} is done: S
-      // buffer t % 2 (holding P_{t-2}) has been read. PV_t needs P_t. Each barrier
-      // is probed for its phases in order and cannot run two phases ahead.
+      // S_t needs tile t in shared memory and S_{t-1} read (one S buffer); PV_t
+      // needs both halves of P_t. Each barrier is probed for its phases in order
+      // and cannot run two phases ahead.
       int next_s = 0, next_pv = 0;
       long long idle_since = clock64();
       while (ok && next_pv < n_t) {
         bool progressed = false;
-        if (next_s < n_t && mbar_test_parity_nb(&bars->r_full[next_s % kStages], (next_s / kStages) & 1)) {
+        if (next_s < n_t && mbar_test_parity_nb(&bars->r_full[next_s % kStages], (next_s / kStages) & 1) &&
+            (next_s == 0 || mbar_test_parity_nb(&bars->s_free, (next_s - 1) & 1))) {
           issue_s(next_s++);
           progressed = true;
         }
@@ -467,80 +498,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ================= softmax: thread t owns head h0 + t =================
     const int r = warp * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    const int h = h0 + r;
+    const bool mine = h < p.H;
+    // ---- the head's first kQT blocks of Q_abs into TMEM (column c holds
+    // elements 2c and 2c+1), loaded in two rounds of 16-byte reads; heads past
+    // H are zeros
+    {
+      const uint4* row = reinterpret_cast<const uint4*>(p.q_abs + ((size_t)b * p.H + (mine ? h : 0)) * C::kW);
+      constexpr int kVecs = C::kQT * 8;  // 16-byte pieces: 8 per block
+      constexpr int kRound = 32;         // 4 blocks (4 x 32 TMEM columns) per round
+#pragma unroll
+      for (int v0 = 0; v0 < kVecs; v0 += kRound) {
+        uint32_t w[kRound * 4];
+#pragma unroll
+        for (int i = 0; i < kRound; ++i) {
+          const uint4 v = (mine && v0 + i < kVecs) ? __ldg(row + v0 + i) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+#pragma unroll
+        for (int c = 0; c < kRound / 8; ++c)
+          if (v0 + c * 8 < kVecs)
+            tc::tmem_st_32x32b_x32(tmem + lane_addr + C::kColQ + (v0 / 8 + c) * 32,
+                                   *reinterpret_cast<uint32_t(*)[32]>(&w[c * 32]));
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->q_full);
+    }
     const float qs = p.qscale;
     const float th = kRescaleLog2 / qs;
     const float2 qs2 = make_float2(qs, qs);
-    float m_ref = -INFINITY, l_run = 0.f;
+    const uint32_t tS = tmem + lane_addr + C::kColS;
+    unsigned char* ptile = smem + C::kOffP;
+    float m_ref = -INFINITY, l_own = 0.f;  // l_own: the row sum of this CTA's p
     bool alive = true;
-    int consumed = -1;    // the last tile whose partial rows from the peer this warp has read
-    bool posted = false;  // the expected bytes of tile consumed + 1 are on x_full
     for (int t = 0; t < n_t; ++t) {
       const int x = t & 1;
-      if (!warp_wait(&bars->s_full[x], (t >> 1) & 1, bars, p.err)) {
+      if (!warp_wait(&bars->s_full, t & 1, bars, p.err)) {
         alive = false;
         break;
       }
       tc::fence_after_sync();
-      const uint32_t tS = tmem + lane_addr + C::kColS + x * kKeys;
-      uint32_t sv[kKeys];
-      tc::tmem_ld_32x32b_x32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tc::tmem_ld_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      uint32_t sv[kOwn];
+      tc::tmem_ld_32x32b_x32(tS, sv);
       tc::tmem_ld_wait();
-      // ---- trade partial scores with the peer. This warp's rows go into the send
-      // buffer (free once the peer has read the previous tile: that also means
-      // the copy out of it is done), one bulk copy moves them into the peer's
-      // receive buffer, and the peer's rows arrive in this CTA's.
-      if (t >= 1 && !warp_wait_cluster(&bars->x_free[warp], (t - 1) & 1, bars, p.err)) {
-        alive = false;
-        break;
-      }
-      {
-        unsigned char* recv = smem + C::kOffX;
-        unsigned char* send = smem + C::kOffX + C::kXBuf;
-        const uint32_t sbase = smem_u32(send);
-#pragma unroll
-        for (int c = 0; c < kKeys / 4; ++c)
-          st_shared_v4(sbase + xchg_off(r, c), sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
-        tc::fence_async_smem();  // the rows visible to the bulk copy
-        __syncwarp();
-        constexpr uint32_t kWarpBytes = 32 * kKeys * 4;
-        if (lane == 0) {
-          bulk_copy_to_peer(peer_addr(recv + warp * kWarpBytes, peer), send + warp * kWarpBytes, kWarpBytes,
-                            peer_addr(&bars->x_full[warp], peer));
-          mbar_arrive_expect_tx(&bars->x_full[warp], kWarpBytes);
-        }
-        posted = true;
-        // S = S_0 + S_1
-        if (!warp_wait_cluster(&bars->x_full[warp], t & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
-        const uint32_t lbase = smem_u32(recv);
-#pragma unroll
-        for (int c = 0; c < kKeys / 4; ++c) {
-          const float4 o = ld_shared_v4(lbase + xchg_off(r, c));
-          sv[4 * c] = __float_as_uint(__uint_as_float(sv[4 * c]) + o.x);
-          sv[4 * c + 1] = __float_as_uint(__uint_as_float(sv[4 * c + 1]) + o.y);
-          sv[4 * c + 2] = __float_as_uint(__uint_as_float(sv[4 * c + 2]) + o.z);
-          sv[4 * c + 3] = __float_as_uint(__uint_as_float(sv[4 * c + 3]) + o.w);
-        }
-        consumed = t;
-        posted = false;
-        __syncwarp();
-        if (lane == 0) arrive_cluster(peer_addr(&bars->x_free[warp], peer));
-      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free);
+      // rows of the pair's tile the heads see: this CTA's 32 and the peer's 32
       const int kt = k0 + t * kKeys;
-      const int valid = min(kKeys, k1 - kt);  // rows of this tile the heads see
-      if (valid < kKeys) {
+      const int valid_own = max(0, min(kOwn, k1 - (kt + kOwn * half)));
+      const int valid_peer = max(0, min(kOwn, k1 - (kt + kOwn * (1 - half))));
+      if (valid_own < kOwn) {
 #pragma unroll
-        for (int e = 0; e < kKeys; ++e)
-          if (e >= valid) sv[e] = __float_as_uint(-INFINITY);
+        for (int e = 0; e < kOwn; ++e)
+          if (e >= valid_own) sv[e] = __float_as_uint(-INFINITY);
       }
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < kKeys; e += 2)
+      for (int e = 0; e < kOwn; e += 2)
         mx4[(e >> 1) & 3] = fmax3(mx4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const float mx_own = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      // ---- the tile max over both CTAs' rows: trade maxima with the peer's warp
+      if (lane == 0) mbar_arrive_expect_tx(&bars->m_full[warp][x], 32 * 4);
+      st_async_b32(peer_addr(mbuf + x * kHeads + r, peer), __float_as_uint(mx_own),
+                   peer_addr(&bars->m_full[warp][x], peer));
+      if (!warp_wait_cluster(&bars->m_full[warp][x], (t >> 1) & 1, bars, p.err)) {
+        alive = false;
+        break;
+      }
+      const float mx = fmaxf(mx_own, ld_shared_f32(smem_u32(mbuf + x * kHeads + r)));
       if (t == 0) {
         m_ref = mx;  // the first tile has a visible row: mx is finite
       } else {
@@ -567,60 +598,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc::tmem_st_32x32b_x32(tmem + lane_addr + C::kColO + c * 32, o);
           }
           tc::tmem_st_wait();
-          l_run *= f;
+          l_own *= f;
         }
       }
       // p = 2^(s*qs - m*qs) as bf16 pairs, and the fp32 sum of exactly these p
       const float mq = m_ref * qs;
       const float2 nmq2 = make_float2(-mq, -mq);
-      uint32_t pv[kKeys / 2];
+      uint32_t pw[kOwn / 2];
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < kKeys / 2; ++i) {
+      for (int i = 0; i < kOwn / 2; ++i) {
         const float2 xv = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), qs2, nmq2);
-        pv[i] = ex2_bf16x2(pack_bf16(xv.x, xv.y));
-        add_bf16x2(ls[(i & 1) * 2], ls[(i & 1) * 2 + 1], pv[i]);
+        pw[i] = ex2_bf16x2(pack_bf16(xv.x, xv.y));
+        add_bf16x2(ls[(i & 1) * 2], ls[(i & 1) * 2 + 1], pw[i]);
       }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      if (valid < kKeys) {
-        // value rows valid..63 of this CTA's half: zero them (S_t, their other
-        // reader, is done) so that 0 * (whatever the cache holds) cannot be NaN
-        unsigned char* base = smem + C::kOffR + (t % kStages) * C::kTileR;
-        const int n_chunks = (kKeys - valid) * C::kCBV * 8;  // 16-byte chunks: 8 per row and block
-        for (int i = r; i < n_chunks; i += kHeads) {
-          const int row = valid + i / (C::kCBV * 8), blk = (i / 8) % C::kCBV, ch = i % 8;
-          *reinterpret_cast<uint4*>(base + blk * C::kRBlk + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+      l_own += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      unsigned char* stage = smem + C::kOffR + (t % kStages) * C::kStage;
+      if (valid_own < kOwn || valid_peer < kOwn) {
+        // value rows of keys at or past seq_len, in this CTA's rows (its value
+        // blocks) and in the peer rows' region: zero them (S_t, the other reader
+        // of this CTA's rows, is done) so that 0 * (whatever the cache holds)
+        // cannot be NaN
+        const int n_own = (kOwn - valid_own) * C::kCBV * 8;  // 16-byte chunks: 8 per row and block
+        const int n_all = n_own + (kOwn - valid_peer) * C::kCBV * 8;
+        for (int i = r; i < n_all; i += kHeads) {
+          const bool o = i < n_own;
+          const int j = o ? i : i - n_own;
+          const int row = (o ? valid_own : valid_peer) + j / (C::kCBV * 8), blk = (j / 8) % C::kCBV, ch = j % 8;
+          const int rb = o ? half * C::kCBV + blk : C::kNB + blk;
+          *reinterpret_cast<uint4*>(stage + rb * C::kRBlk + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
-        tc::fence_async_smem();  // visible to the tensor cores' reads
       }
-      // P_t over the first 32 columns of S buffer x (S_t has been read; PV_{t-2},
-      // the last reader of P_{t-2} there, completed before S_t was issued)
-      tc::tmem_st_32x32b_x16(tS, *reinterpret_cast<uint32_t(*)[16]>(&pv[0]));
-      tc::tmem_st_32x32b_x16(tS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pv[16]));
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
+      // ---- P tile x last held P_{t-2}: free once PV_{t-2} is done here (this
+      // CTA's columns) and in the peer (the columns copied there)
+      if (t >= 2) {
+        if (!warp_wait(&bars->o_done[x], ((t - 2) >> 1) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
+        if (lane == 0) arrive_cluster(peer_addr(&bars->p_free[warp][x], peer));
+        if (!warp_wait_cluster(&bars->p_free[warp][x], ((t - 2) >> 1) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
+      }
+      // ---- this CTA's 32 keys of P_t: 8-key columns 4 half .. 4 half + 3 of
+      // the tile, each head's 16 bytes at row offset 16 r; then the warp's rows
+      // of those columns (512 bytes each) into the peer's tile
+      unsigned char* pt = ptile + x * C::kPBuf;
+      const uint32_t pbase = smem_u32(pt);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        st_shared_v4(pbase + (4 * half + i) * C::kPCol + r * 16, pw[4 * i], pw[4 * i + 1], pw[4 * i + 2],
+                     pw[4 * i + 3]);
+      tc::fence_async_smem();  // P and the zeroed rows visible to the tensor cores and the bulk copies
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[x]);
-    }
-    if (!alive && consumed + 1 < n_t) {
-      // after a wait gave up: the peer may still be copying its rows of the next
-      // tile into this CTA's receive buffer (at most that one copy: it needs this
-      // warp's x_free for every earlier tile). Wait for it, bounded, so that no
-      // copy lands after the CTA has exited.
-      if (lane == 0 && !posted) mbar_arrive_expect_tx(&bars->x_full[warp], 32 * kKeys * 4);
-      __syncwarp();
-      const long long t0 = clock64();
-      while (!test_parity_cluster(&bars->x_full[warp], (consumed + 1) & 1) && clock64() - t0 < kWaitLimitCycles) {
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          unsigned char* src = pt + (4 * half + i) * C::kPCol + warp * 32 * 16;
+          bulk_copy_to_peer(peer_addr(src, peer), src, 32 * 16, peer_addr(&bars->p_full[x], peer));
+        }
+        if (warp == 0)
+          mbar_arrive_expect_tx(&bars->p_full[x], kHeads * kOwn * 2);  // the peer's half, incoming
+        else
+          mbar_arrive(&bars->p_full[x]);
       }
     }
-    // ---- the last PV (its commit covers every earlier MMA), then the output
+    // ---- the last PV (its commit covers every earlier MMA); the pair's row sum
     bool have_o = alive;
     if (have_o) {
       have_o = warp_wait(&bars->o_done[(n_t - 1) & 1], ((n_t - 1) >> 1) & 1, bars, p.err);
       tc::fence_after_sync();
     }
-    const int h = h0 + r;
-    const bool mine = h < p.H;
+    float l_run = 0.f;
+    if (have_o) {
+      if (lane == 0) mbar_arrive_expect_tx(&bars->l_full[warp], 32 * 4);
+      st_async_b32(peer_addr(lbuf + r, peer), __float_as_uint(l_own), peer_addr(&bars->l_full[warp], peer));
+      have_o = warp_wait_cluster(&bars->l_full[warp], 0, bars, p.err);
+      if (have_o) l_run = l_own + ld_shared_f32(smem_u32(lbuf + r));  // the same sum on both sides
+    }
     if (n_split == 1) {
       const float inv = (have_o && l_run > 0.f) ? 1.f / l_run : 0.f;
       __nv_bfloat16* dst = p.out + ((size_t)b * p.H + (mine ? h : 0)) * DC + half * C::kDVH;
@@ -666,6 +723,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   cluster_sync();  // the peer's last accesses to this CTA's shared memory are done
   tc::fence_after_sync();
+  if (aborted(bars)) {
+    // after a wait gave up, a store or copy the peer issued into this CTA just
+    // before it stopped may still be landing: give it time (bounded) before the
+    // shared memory is released
+    const long long t0 = clock64();
+    while (clock64() - t0 < 200000) {
+    }
+  }
   if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -697,12 +762,13 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
   // q_abs [B, H, 576]: box of 128 heads
   if (!make_rows_map(&tq, q_abs, C::kW, (uint64_t)H, (uint64_t)B, kHeads)) return cudaErrorInvalidValue;
   if (tables) {
-    // pool [num_blocks, bs, 576]: box of one block
-    if (!make_rows_map(&tr, latent, C::kW, (uint64_t)bs, (uint64_t)num_blocks, (uint32_t)bs)) return cudaErrorInvalidValue;
+    // pool [num_blocks, bs, 576]: box of one block, or of 32 rows of a 64-row one
+    if (!make_rows_map(&tr, latent, C::kW, (uint64_t)bs, (uint64_t)num_blocks, (uint32_t)(bs < kOwn ? bs : kOwn)))
+      return cudaErrorInvalidValue;
     max_len = mbps * bs;
   } else {
-    // latent [B, max_len, 576]: box of one 64-row tile
-    if (!make_rows_map(&tr, latent, C::kW, (uint64_t)max_len, (uint64_t)B, kKeys)) return cudaErrorInvalidValue;
+    // latent [B, max_len, 576]: box of one CTA's 32 rows of a tile
+    if (!make_rows_map(&tr, latent, C::kW, (uint64_t)max_len, (uint64_t)B, kOwn)) return cudaErrorInvalidValue;
   }
   MlaParams p;
   p.tables = tables;
@@ -716,6 +782,7 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
   p.max_splits = (max_len + chunk - 1) / chunk;
   p.n_htiles = (H + kHeads - 1) / kHeads;
   p.seq_lens = seq_lens;
+  p.q_abs = static_cast<const __nv_bfloat16*>(q_abs);
   p.partial = partial;
   p.out = static_cast<__nv_bfloat16*>(out_lat);
   p.qscale = qscale;

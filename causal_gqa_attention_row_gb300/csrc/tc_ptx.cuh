@@ -161,6 +161,13 @@ __host__ __device__ constexpr uint64_t desc_sw128_hi(uint32_t lbo, uint32_t sbo)
          (2ull << 61);
 }
 
+// The same descriptor for the layout without swizzle (layout type 0), K-major:
+// core matrices of 8 rows x 16 bytes (rows 16 bytes apart), `lbo` between core
+// matrices adjacent in K, `sbo` between those adjacent in M or N.
+__host__ __device__ constexpr uint64_t desc_plain_hi(uint32_t lbo, uint32_t sbo) {
+  return ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
 // Start-address field of a shared-memory descriptor: the address within the
 // CTA's own shared memory, >> 4 (14 bits).
 __device__ __forceinline__ uint64_t desc_addr(const void* p) { return (uint64_t)((smem_u32(p) & 0x3FFFFu) >> 4); }
