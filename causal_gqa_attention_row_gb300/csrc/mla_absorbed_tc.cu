@@ -172,8 +172,12 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ void arrive_cluster(uint32_t bar_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
+// Arrival on a peer CTA's mbarrier without release ordering. It only reports
+// that a tensor-core read (seen complete through its commit barrier) is over;
+// the peer needs no data this thread wrote. (With release semantics the
+// arrival waited for this CTA's outstanding remote traffic, ~2,500 cycles.)
+__device__ __forceinline__ void arrive_cluster_relaxed(uint32_t bar_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -266,6 +270,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
+}
+
+// True in exactly one lane of the converged warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 template <int DC, int DR>
@@ -421,7 +436,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer =================
-    if (lane == 0) {
+    // The warp runs the loop converged, every decision warp-uniform, and one
+    // elected lane issues each MMA and commit: a converged warp keeps the
+    // tensor core at its rate on these short (N = 32) MMAs, a lone lane does not.
+    {
       const uint32_t idS = tc::idesc_bf16_f32(kHeads, kOwn, false);
       const uint32_t idO = tc::idesc_bf16_f32(kHeads, C::kDVH, true);
       constexpr uint64_t kHiK = tc::desc_sw128_hi(0, 1024);  // K-major: 8-row groups 1024 bytes apart
@@ -442,12 +460,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < C::kW / 16; ++kk) {
           const int g = kk / 4, step = kk % 4;  // column block, 16-column step inside it
           const uint32_t ar = g * C::kRBlk + step * 32;
-          if (g < C::kQT)  // Q_abs from TMEM: 16 columns = 8 TMEM columns
-            tc::mma_f16_ts(tS, tQ + g * 32 + step * 8, dR + (ar >> 4), idS, kk > 0);
-          else
-            tc::mma_f16_ss(tS, dQ + (((g - C::kQT) * C::kQBlk + step * 32) >> 4), dR + (ar >> 4), idS, kk > 0);
+          if (elect_one()) {
+            if (g < C::kQT)  // Q_abs from TMEM: 16 columns = 8 TMEM columns
+              tc::mma_f16_ts(tS, tQ + g * 32 + step * 8, dR + (ar >> 4), idS, kk > 0);
+            else
+              tc::mma_f16_ss(tS, dQ + (((g - C::kQT) * C::kQBlk + step * 32) >> 4), dR + (ar >> 4), idS, kk > 0);
+          }
+          __syncwarp();
         }
-        tc::mma_commit(&bars->s_full);
+        if (elect_one()) tc::mma_commit(&bars->s_full);
+        __syncwarp();
       };
       auto issue_pv = [&](int t) {  // O += P_t R_t[:, value half], 16 keys per instruction
         const int st = t % kStages, x = t & 1;
@@ -459,40 +481,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // keys 16kk .. 16kk + 15 of the tile are rows of CTA kk / 2: this CTA's
           // own region (its value blocks) or the peer rows' region
           const uint32_t av = (kk / 2 == half ? half * C::kCBV : C::kNB) * C::kRBlk + (kk % 2) * 16 * 128;
-          tc::mma_f16_ss(tO, dP + (uint64_t)((kk * 2 * C::kPCol) >> 4), dV + (av >> 4), idO, (t > 0 || kk > 0));
+          if (elect_one())
+            tc::mma_f16_ss(tO, dP + (uint64_t)((kk * 2 * C::kPCol) >> 4), dV + (av >> 4), idO, (t > 0 || kk > 0));
+          __syncwarp();
         }
-        tc::mma_commit(&bars->o_done[x]);
-        tc::mma_commit(&bars->r_empty[st]);  // the tile's stage is free once PV_t is done
+        if (elect_one()) {
+          tc::mma_commit(&bars->o_done[x]);
+          tc::mma_commit(&bars->r_empty[st]);  // the tile's stage is free once PV_t is done
+        }
+        __syncwarp();
       };
-      bool ok = wait_or_abort(&bars->q_full, 0, bars, p.err);
+      bool ok = warp_wait(&bars->q_full, 0, bars, p.err);
       // S_t needs tile t in shared memory and S_{t-1} read (one S buffer); PV_t
       // needs both halves of P_t. Each barrier is probed for its phases in order
-      // and cannot run two phases ahead.
+      // and cannot run two phases ahead. A step is taken once every lane has
+      // seen its barrier complete.
       int next_s = 0, next_pv = 0;
       long long idle_since = clock64();
       while (ok && next_pv < n_t) {
         bool progressed = false;
-        if (next_s < n_t && mbar_test_parity_nb(&bars->r_full[next_s % kStages], (next_s / kStages) & 1) &&
-            (next_s == 0 || mbar_test_parity_nb(&bars->s_free, (next_s - 1) & 1))) {
-          issue_s(next_s++);
+        // PV first: its completion frees a ring stage and a P tile
+        const bool pv_ready = next_pv < next_s && mbar_test_parity_nb(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1);
+        if (__all_sync(0xffffffffu, pv_ready)) {
+          issue_pv(next_pv++);
           progressed = true;
         }
-        if (next_pv < next_s && mbar_test_parity_nb(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1)) {
-          issue_pv(next_pv++);
+        const bool s_ready = next_s < n_t &&
+                             mbar_test_parity_nb(&bars->r_full[next_s % kStages], (next_s / kStages) & 1) &&
+                             (next_s == 0 || mbar_test_parity_nb(&bars->s_free, (next_s - 1) & 1));
+        if (__all_sync(0xffffffffu, s_ready)) {
+          issue_s(next_s++);
           progressed = true;
         }
         if (progressed) {
           idle_since = clock64();
-        } else if (aborted(bars)) {
-          ok = false;
-        } else if (clock64() - idle_since > kWaitLimitCycles) {
-          abort_all(bars, p.err);
-          ok = false;
+        } else {
+          // lane 0's view decides for the warp
+          const int stop = __shfl_sync(0xffffffffu, aborted(bars) ? 1 : (clock64() - idle_since > kWaitLimitCycles ? 2 : 0), 0);
+          if (stop == 2 && lane == 0) abort_all(bars, p.err);
+          if (stop) ok = false;
         }
       }
       // every MMA issued above has completed before TMEM is released
-      tc::mma_commit(&bars->mma_final);
-      if (!mbar_wait(&bars->mma_final, 0)) raise_error(p.err, kErrTimeout);
+      if (elect_one()) tc::mma_commit(&bars->mma_final);
+      __syncwarp();
+      if (lane == 0 && !mbar_wait(&bars->mma_final, 0)) raise_error(p.err, kErrTimeout);
+      __syncwarp();
     }
   } else {
     // ================= softmax: thread t owns head h0 + t =================
@@ -630,17 +664,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       // ---- P tile x last held P_{t-2}: free once PV_{t-2} is done here (this
-      // CTA's columns) and in the peer (the columns copied there)
-      if (t >= 2) {
-        if (!warp_wait(&bars->o_done[x], ((t - 2) >> 1) & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
-        if (lane == 0) arrive_cluster(peer_addr(&bars->p_free[warp][x], peer));
-        if (!warp_wait_cluster(&bars->p_free[warp][x], ((t - 2) >> 1) & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
+      // CTA's columns, seen at the end of tile t-1) and in the peer (the columns
+      // copied there: the peer's arrival)
+      if (t >= 2 && !warp_wait_cluster(&bars->p_free[warp][x], ((t - 2) >> 1) & 1, bars, p.err)) {
+        alive = false;
+        break;
       }
       // ---- this CTA's 32 keys of P_t: 8-key columns 4 half .. 4 half + 3 of
       // the tile, each head's 16 bytes at row offset 16 r; then the warp's rows
@@ -663,6 +691,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bars->p_full[x], kHeads * kOwn * 2);  // the peer's half, incoming
         else
           mbar_arrive(&bars->p_full[x]);
+      }
+      // ---- P tile x ^ 1 is next written at tile t + 1: tell the peer, whose
+      // columns go there, once PV_{t-1} (its last reader here) is done. Done
+      // now rather than at tile t + 1, so that the peer rarely waits for it.
+      if (t >= 1 && t + 1 < n_t) {
+        if (!warp_wait(&bars->o_done[x ^ 1], ((t - 1) >> 1) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
+        if (lane == 0) arrive_cluster_relaxed(peer_addr(&bars->p_free[warp][x ^ 1], peer));
       }
     }
     // ---- the last PV (its commit covers every earlier MMA); the pair's row sum
