@@ -21,28 +21,31 @@
 // head first: each CTA sends its tile row maxima (128 floats) to the other with
 // asynchronous remote stores, both take the larger, and both then move the
 // reference, rescale O and l, and form p = 2^(s*qs - m*qs) in bf16 the same
-// way. Each CTA writes its 32 columns of P_t into a shared-memory P tile and
-// copies them, one bulk copy per softmax warp and 8-key column, into the same
-// place of the peer's tile; the PV MMA reads P from there. Per tile a CTA sends
+// way. Each CTA writes its 32 columns of P_t into the tile's shared-memory P
+// and copies them, one bulk copy per softmax warp and 8-key column, into the
+// same place of the peer's; the PV MMA reads P from there. Per tile a CTA sends
 // 8.5 KiB to its peer (the bf16 P half and the maxima) instead of a fp32 score
 // tile. Each CTA keeps the row sum of its own p; the two sums are added once,
 // at the end.
 //
 // Per CTA: tensor memory holds O (256 columns), S (32) and the first 448 of the
 // 576 Q_abs columns (224 columns, two bf16 per column: the score MMA's A
-// operand); shared memory holds the other two Q_abs column blocks (32 KiB),
-// two P tiles (2 x 16 KiB, no swizzle: each 8-key column of all 128 heads is
-// 2 KiB, so a CTA's half is 4 contiguous pieces), and a three-stage ring of
-// cache tiles: the CTA's 32 rows in full (36 KiB) and the peer's 32 rows'
-// value half (16 KiB), 52 KiB per stage.
+// operand). Shared memory holds the other two Q_abs column blocks (32 KiB) and
+// two rings: R, four stages of the CTA's own 32 rows in full (36 KiB), and V,
+// three stages of the peer's 32 rows' value half (16 KiB), needed only by the
+// PV MMA. Once S_t is done the other half's value blocks of R stage t are
+// dead, and P_t (16 KiB, no swizzle: each 8-key column of all 128 heads is
+// 2 KiB, so a CTA's half is 4 contiguous pieces) is written over them. So P
+// needs no buffer and no hand-over of its own: the peer copies its columns in
+// only after it has this CTA's tile maxima, which are sent after S_t.
 // Roles (192 threads):
 //   warps 0-3  softmax: thread t owns head h0 + t (TMEM lane t); warp w trades
 //              maxima and P columns with warp w of the peer
 //   warp 4     initialises the barriers; TMA producer of the two Q_abs blocks
 //              (once) and of the cache tiles
-//   warp 5     allocates TMEM; one thread issues the MMAs, S_t as soon as its
-//              tile has landed and S_{t-1} has been read, PV_t once both halves
-//              of P_t are in place
+//   warp 5     allocates TMEM; issues the MMAs (one elected lane), S_t as soon
+//              as its rows have landed and S_{t-1} has been read, PV_t once both
+//              halves of P_t and the peer's rows are in place
 // Softmax: a lazily moved reference max (threshold 2^8 in p), p rounded to
 // bf16 and the fp32 row sum taken over exactly those p. Rows of the last tile at
 // or past seq_len weigh zero, and their value rows in shared memory are zeroed
@@ -61,7 +64,8 @@ namespace {
 constexpr int kHeads = 128;    // query heads per cluster: the MMA's M
 constexpr int kKeys = 64;      // cache rows per tile of the pair
 constexpr int kOwn = 32;       // ... of which each CTA scores 32: the S MMA's N
-constexpr int kStages = 3;     // cache-tile ring
+constexpr int kStagesR = 4;    // ring of this CTA's cache rows (and the P tiles)
+constexpr int kStagesV = 3;    // ring of the peer rows' value halves
 constexpr int kThreads = 192;  // four softmax warps, the producer, the MMA warp
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;
@@ -78,22 +82,25 @@ struct MlaCfg {
   static constexpr int kQT = kNB - kQS;         // ... and in tensor memory (the first seven)
   static constexpr int kQBlk = kHeads * 128;    // one block of Q_abs: 128 rows x 128 bytes
   static constexpr int kRBlk = kOwn * 128;      // one block of a CTA's cache rows: 32 rows x 128 bytes
-  // a ring stage: this CTA's rows, every block; then the peer's rows, this CTA's value blocks
-  static constexpr int kStage = (kNB + kCBV) * kRBlk;
-  static constexpr int kPBuf = kHeads * kKeys * 2;  // a P tile: 128 heads x 64 keys, bf16
-  static constexpr int kPCol = kHeads * 16;          // ... one 8-key column of it: 2 KiB
-  // shared memory: the P tiles first (any descriptor over them stays inside
-  // the CTA's window), Q_abs's blocks, the ring, maxima and row sums, barriers
-  static constexpr int kOffP = 0, kOffQ = kOffP + 2 * kPBuf, kOffR = kOffQ + kQS * kQBlk;
-  static constexpr int kOffM = kOffR + kStages * kStage;  // [2][128] maxima by tile parity, then [128] row sums
+  // a stage of the R ring: this CTA's 32 rows of a tile, every block; of the
+  // V ring: the peer's 32 rows, this CTA's value blocks
+  static constexpr int kStageR = kNB * kRBlk, kStageV = kCBV * kRBlk;
+  // A tile's P (128 heads x 64 keys, bf16) goes into its R stage over the other
+  // half's value blocks, which only the score MMA reads: kCBV blocks, 16 KiB.
+  static constexpr int kPCol = kHeads * 16;  // one 8-key column of P: 2 KiB
+  // shared memory: Q_abs's blocks, the two rings, maxima and row sums, barriers
+  static constexpr int kOffQ = 0, kOffR = kOffQ + kQS * kQBlk, kOffV = kOffR + kStagesR * kStageR;
+  static constexpr int kOffM = kOffV + kStagesV * kStageV;  // [2][128] maxima by tile parity, then [128] row sums
   static constexpr int kOffBar = kOffM + 3 * kHeads * 4;
-  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffBar + 384 + 1023;  // + alignment slack
   // TMEM columns: O, S, then Q_abs's first kQT blocks (32 columns each)
   static constexpr uint32_t kColO = 0, kColS = kDVH, kColQ = kColS + kOwn;
   static_assert(DC % 128 == 0 && DR % 64 == 0, "whole 64-column blocks per half");
   static_assert(kDVH % 16 == 0 && kDVH <= 256, "one PV MMA covers the half");
   static_assert(kColQ % 32 == 0 && kColQ + kQT * 32 <= kTmemCols, "TMEM map");
-  static_assert(kOffR % 1024 == 0 && kStage % 1024 == 0, "swizzle atoms on 1024-byte boundaries");
+  static_assert(kOffR % 1024 == 0 && kStageR % 1024 == 0 && kOffV % 1024 == 0 && kStageV % 1024 == 0,
+                "swizzle atoms on 1024-byte boundaries");
+  static_assert(kCBV * kRBlk == kHeads * kKeys * 2, "P fills the other half's value blocks");
   static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
 };
 
@@ -115,20 +122,21 @@ struct MlaParams {
 struct MlaBars {
   // q_full: Q_abs's shared-memory blocks have landed and every softmax warp has
   // written its rows of the rest into TMEM
-  uint64_t q_full, r_full[kStages], r_empty[kStages];
+  uint64_t q_full, r_full[kStagesR], v_full[kStagesV];
   // s_full / s_free: S_t is in TMEM / every softmax warp has read it;
-  // p_full[x]: P tile x holds P_t (this CTA's four warps and the peer's 8 KiB);
-  // o_done[x]: PV_t done, for t of parity x
-  uint64_t s_full, s_free, p_full[2], o_done[2], mma_final;
+  // p_full[x]: P_t is in place (this CTA's four warps and the peer's 8 KiB), t of parity x;
+  // o_done[t % kStagesR]: PV_t is done, so O may be rescaled and R stage t % kStagesR
+  // and V stage t % kStagesV refilled. One commit per PV: a second commit after
+  // the same MMAs was seen to arrive up to ~1,600 cycles after the first.
+  uint64_t s_full, s_free, p_full[2], o_done[kStagesR], mma_final;
   // per softmax warp w (its 32 heads):
   // m_full[w][x]: the peer's tile maxima for tile parity x have landed (128 bytes)
-  // p_free[w][x]: the peer's PV that last read its P tile x is done (a remote arrival)
   // l_full[w]:    the peer's row sums have landed (once)
-  uint64_t m_full[4][2], p_free[4][2], l_full[4];
+  uint64_t m_full[4][2], l_full[4];
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(MlaBars) <= 512, "barrier block");
+static_assert(sizeof(MlaBars) <= 384, "barrier block");
 
 // ---- cluster helpers ---------------------------------------------------------
 
@@ -170,14 +178,6 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
-}
-
-// Arrival on a peer CTA's mbarrier without release ordering. It only reports
-// that a tensor-core read (seen complete through its commit barrier) is over;
-// the peer needs no data this thread wrote. (With release semantics the
-// arrival waited for this CTA's outstanding remote traffic, ~2,500 cycles.)
-__device__ __forceinline__ void arrive_cluster_relaxed(uint32_t bar_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -286,7 +286,7 @@ __device__ __forceinline__ bool elect_one() {
 template <int DC, int DR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_absorbed_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
-                           const MlaParams p) {
+                           const __grid_constant__ CUtensorMap tm_v, const MlaParams p) {
   using C = MlaCfg<DC, DR>;
   extern __shared__ unsigned char smem_raw[];
   // swizzle atoms sit on 1024-byte boundaries of the shared window
@@ -327,28 +327,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     if (lane == 0) {
       mbar_init(&bars->q_full, 5);  // the producer's expected bytes + one arrival per softmax warp
-      for (int s = 0; s < kStages; ++s) {
+      for (int s = 0; s < kStagesR; ++s) {
         mbar_init(&bars->r_full[s], 1);
-        mbar_init(&bars->r_empty[s], 1);
+      }
+      for (int s = 0; s < kStagesV; ++s) {
+        mbar_init(&bars->v_full[s], 1);
       }
       mbar_init(&bars->s_full, 1);
       mbar_init(&bars->s_free, 4);  // one arrival per softmax warp
-      for (int x = 0; x < 2; ++x) {
-        mbar_init(&bars->p_full[x], 4);
-        mbar_init(&bars->o_done[x], 1);
-      }
+      for (int x = 0; x < 2; ++x) mbar_init(&bars->p_full[x], 4);
+      for (int s = 0; s < kStagesR; ++s) mbar_init(&bars->o_done[s], 1);
       mbar_init(&bars->mma_final, 1);
       for (int w = 0; w < 4; ++w) {
-        for (int x = 0; x < 2; ++x) {
-          mbar_init(&bars->m_full[w][x], 1);
-          mbar_init(&bars->p_free[w][x], 1);
-        }
+        for (int x = 0; x < 2; ++x) mbar_init(&bars->m_full[w][x], 1);
         mbar_init(&bars->l_full[w], 1);
       }
       bars->abort_flag = 0;
       fence_barrier_init();
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_r);
+      tc::prefetch_tmap(&tm_v);
       mbar_arrive_expect_tx(&bars->q_full, C::kQS * C::kQBlk);
     }
     __syncwarp();
@@ -367,72 +365,108 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ================= TMA producer of the cache tiles =================
-    int issued_last[kStages];
+    // Tile t: this CTA's 32 rows (every block) into R stage t % kStagesR, and
+    // the peer's 32 rows (this CTA's value blocks) into V stage t % kStagesV.
+    // The latent is seen as [outer][row][column block][64], so a box of 32 rows
+    // x several blocks lands block after block, as the MMAs read it: one box
+    // per part (tm_r: all 9 blocks, tm_v: 4 value blocks). A paged pool of 8-
+    // or 16-row blocks takes `per` boxes of `br` rows per column block instead
+    // (tm_r then has a box of one block).
+    int last_r[kStagesR], last_v[kStagesV];
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) issued_last[s] = -1;
-    // Box x of a tile: this CTA's 32 rows, column block x / per (x < kNB * per),
-    // or the peer's 32 rows, value block (x - kNB * per) / per of this CTA's
-    // half; sub-box x % per covers `br` of the 32 rows (paged: one pool block or
-    // half of a 64-row one; contiguous: all 32)
+    for (int s = 0; s < kStagesR; ++s) last_r[s] = -1;
+#pragma unroll
+    for (int s = 0; s < kStagesV; ++s) last_v[s] = -1;
     const int br = p.tables ? min(p.bs, kOwn) : kOwn;
     const int per = kOwn / br;
-    const int nbox = (C::kNB + C::kCBV) * per;  // <= 52
-    for (int t = 0; t < n_t; ++t) {
-      const int st = t % kStages;
-      const int kt = k0 + t * kKeys;
-      int blk[2] = {0, 0}, slot[2] = {0, 0};
-      if (p.tables) {  // the tile's table entries, fetched before waiting for the stage
+    const bool whole = per == 1;  // one box per part
+    // The tensor-map coordinates (row or slot, sequence or pool block) of this
+    // lane's boxes of tile t: [0..1] this CTA's rows, [2..3] the peer's. Paged,
+    // a tile's table entries are requested one tile ahead (`fetch`) and checked
+    // when used (`check`), so the lookups wait on nothing.
+    struct Coords {
+      int c1[4], c2[4], ti[4];
+    };
+    auto fetch = [&](int t) -> Coords {
+      Coords c;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool own = i < 2;
+        const int x = lane + 32 * (i & 1);
+        const int row_base = k0 + t * kKeys + kOwn * (own ? half : 1 - half);
+        c.c1[i] = row_base;  // contiguous: rows past the cache's capacity read as zeros
+        c.c2[i] = b;
+        c.ti[i] = -1;
+        if (!p.tables || x >= (own ? C::kNB : C::kCBV) * per) continue;
+        const int row0 = row_base + (x % per) * br;
+        c.c1[i] = row0 % p.bs;
+        c.c2[i] = p.num_blocks;  // a block past the sequence loads from past the end of the pool: zeros
+        if (row0 / p.bs < p.mbps && row0 < len) {
+          c.ti[i] = row0 / p.bs;
+          c.c2[i] = __ldg(p.tables + (size_t)b * p.mbps + c.ti[i]);
+        }
+      }
+      return c;
+    };
+    auto check = [&](Coords& c) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (c.ti[i] >= 0 && (c.c2[i] < 0 || c.c2[i] >= p.num_blocks)) {  // an entry out of range: flagged, zeros
+          raise_error(p.err, kErrBounds);
+          c.c2[i] = p.num_blocks;
+        }
+    };
+    // load one part of tile t once its stage is free; false once a wait gave up
+    auto load_part = [&](int t, bool own, const int* c1, const int* c2) -> bool {
+      const int nb = own ? C::kNB : C::kCBV;
+      const int nbox = whole ? 1 : nb * per;
+      const int stages = own ? kStagesR : kStagesV;
+      const int st = t % stages;
+      uint64_t* full = own ? &bars->r_full[st] : &bars->v_full[st];
+      if (t >= stages) {  // the stage is free once PV_{t - stages} is done
+        // (o_done[u % kStagesR] completes once per PV_u, u = t - stages; its next
+        // phase, PV_{u + kStagesR}, needs a tile this loop has not loaded yet)
+        const int u = t - stages;
+        bool ok = true;
+        if (lane == 0) ok = wait_or_abort(&bars->o_done[u % kStagesR], (u / kStagesR) & 1, bars, p.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(full, nb * C::kRBlk);
+      __syncwarp();
+      unsigned char* dst = smem + (own ? C::kOffR + st * C::kStageR : C::kOffV + st * C::kStageV);
+      if (whole) {
+        if (lane == 0) tc::tma_load_4d(dst, own ? &tm_r : &tm_v, 0, c1[0], own ? 0 : half * C::kCBV, c2[0], full);
+      } else {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int x = lane + 32 * u;
           if (x >= nbox) continue;
-          const bool own = x < C::kNB * per;
-          const int row0 = kt + kOwn * (own ? half : 1 - half) + (x % per) * br;
-          const int ti = row0 / p.bs;
-          // a block past the sequence, or an entry out of range (flagged), loads
-          // from past the end of the pool: the TMA engine fills it with zeros
-          int e = p.num_blocks;
-          if (ti < p.mbps && row0 < len) {
-            e = __ldg(p.tables + (size_t)b * p.mbps + ti);
-            if (e < 0 || e >= p.num_blocks) {
-              raise_error(p.err, kErrBounds);
-              e = p.num_blocks;
-            }
-          }
-          blk[u] = e;
-          slot[u] = row0 % p.bs;
+          const int cb = x / per;                        // block within the part
+          const int g = own ? cb : half * C::kCBV + cb;  // the row's column block
+          tc::tma_load_4d(dst + cb * C::kRBlk + (x % per) * br * 128, &tm_r, 0, c1[u], g, c2[u], full);
         }
       }
-      if (p.debug_withhold && t == 0 && half == 1) continue;  // test hook: tile 0 is never requested
-      if (t >= kStages) {  // the stage is free once PV_{t-kStages} is done
-        bool ok = true;
-        if (lane == 0) ok = wait_or_abort(&bars->r_empty[st], ((t / kStages) - 1) & 1, bars, p.err);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&bars->r_full[st], C::kStage);
       __syncwarp();
-      unsigned char* dst = smem + C::kOffR + st * C::kStage;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int x = lane + 32 * u;
-        if (x >= nbox) continue;
-        const bool own = x < C::kNB * per;
-        const int cb = own ? x / per : (x - C::kNB * per) / per;  // block within its region
-        const int g = own ? cb : half * C::kCBV + cb;              // the row's column block
-        unsigned char* d = dst + ((own ? 0 : C::kNB) + cb) * C::kRBlk + (x % per) * br * 128;
-        if (!p.tables)  // rows past the cache's capacity read as zeros
-          tc::tma_load_4d(d, &tm_r, g * 64, kt + kOwn * (own ? half : 1 - half), b, 0, &bars->r_full[st]);
-        else
-          tc::tma_load_4d(d, &tm_r, g * 64, slot[u], blk[u], 0, &bars->r_full[st]);
-      }
-      __syncwarp();
-      issued_last[st] = t;
+      if (own)
+        last_r[st] = t;
+      else
+        last_v[st] = t;
+      return true;
+    };
+    Coords cur = fetch(0);
+    for (int t = 0; t < n_t; ++t) {
+      check(cur);
+      const Coords next = fetch(min(t + 1, n_t - 1));  // in flight during this tile's waits
+      const bool skip = p.debug_withhold && t == 0 && half == 1;  // test hook: tile 0 is never requested
+      if (!skip && (!load_part(t, true, cur.c1, cur.c2) || !load_part(t, false, cur.c1 + 2, cur.c2 + 2))) break;
+      cur = next;
     }
     if (lane == 0) {  // never exit with a load in flight
       if (!mbar_wait(&bars->q_full, 0)) raise_error(p.err, kErrTimeout);
-      for (int s = 0; s < kStages; ++s)
-        if (issued_last[s] >= 0 && !mbar_wait(&bars->r_full[s], (issued_last[s] / kStages) & 1))
-          raise_error(p.err, kErrTimeout);
+      for (int s = 0; s < kStagesR; ++s)
+        if (last_r[s] >= 0 && !mbar_wait(&bars->r_full[s], (last_r[s] / kStagesR) & 1)) raise_error(p.err, kErrTimeout);
+      for (int s = 0; s < kStagesV; ++s)
+        if (last_v[s] >= 0 && !mbar_wait(&bars->v_full[s], (last_v[s] / kStagesV) & 1)) raise_error(p.err, kErrTimeout);
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer =================
@@ -449,13 +483,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint64_t kHiP = tc::desc_plain_hi(C::kPCol, 128);
       const uint64_t dQ = kHiK | tc::desc_addr(smem + C::kOffQ);
       const uint64_t dR0 = kHiK | tc::desc_addr(smem + C::kOffR);
-      const uint64_t dV0 = kHiV | tc::desc_addr(smem + C::kOffR);
-      const uint64_t dP0 = kHiP | tc::desc_addr(smem + C::kOffP);
+      // values of this CTA's keys: its value blocks of the R stage; of the peer's keys: the V stage
+      const uint64_t dVo0 = kHiV | tc::desc_addr(smem + C::kOffR + half * C::kCBV * C::kRBlk);
+      const uint64_t dVp0 = kHiV | tc::desc_addr(smem + C::kOffV);
+      const uint64_t dP0 = kHiP | tc::desc_addr(smem + C::kOffR + (1 - half) * C::kCBV * C::kRBlk);
       const uint32_t tO = tmem + C::kColO, tS = tmem + C::kColS, tQ = tmem + C::kColQ;
       auto issue_s = [&](int t) {  // S = Q_abs (this CTA's 32 rows of R_t)^T
-        const int st = t % kStages;
+        const int st = t % kStagesR;
         tc::fence_after_sync();
-        const uint64_t dR = dR0 + (uint64_t)((st * C::kStage) >> 4);
+        const uint64_t dR = dR0 + (uint64_t)((st * C::kStageR) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::kW / 16; ++kk) {
           const int g = kk / 4, step = kk % 4;  // column block, 16-column step inside it
@@ -472,28 +508,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
       auto issue_pv = [&](int t) {  // O += P_t R_t[:, value half], 16 keys per instruction
-        const int st = t % kStages, x = t & 1;
+        const int sr = t % kStagesR, sv = t % kStagesV;
         tc::fence_after_sync();
-        const uint64_t dP = dP0 + (uint64_t)((x * C::kPBuf) >> 4);
-        const uint64_t dV = dV0 + (uint64_t)((st * C::kStage) >> 4);
+        const uint64_t dP = dP0 + (uint64_t)((sr * C::kStageR) >> 4);
+        const uint64_t dVo = dVo0 + (uint64_t)((sr * C::kStageR) >> 4);
+        const uint64_t dVp = dVp0 + (uint64_t)((sv * C::kStageV) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          // keys 16kk .. 16kk + 15 of the tile are rows of CTA kk / 2: this CTA's
-          // own region (its value blocks) or the peer rows' region
-          const uint32_t av = (kk / 2 == half ? half * C::kCBV : C::kNB) * C::kRBlk + (kk % 2) * 16 * 128;
+          // keys 16kk .. 16kk + 15 of the tile are rows of CTA kk / 2
+          const uint64_t dV = (kk / 2 == half ? dVo : dVp) + (uint64_t)(((kk % 2) * 16 * 128) >> 4);
           if (elect_one())
-            tc::mma_f16_ss(tO, dP + (uint64_t)((kk * 2 * C::kPCol) >> 4), dV + (av >> 4), idO, (t > 0 || kk > 0));
+            tc::mma_f16_ss(tO, dP + (uint64_t)((kk * 2 * C::kPCol) >> 4), dV, idO, (t > 0 || kk > 0));
           __syncwarp();
         }
         if (elect_one()) {
-          tc::mma_commit(&bars->o_done[x]);
-          tc::mma_commit(&bars->r_empty[st]);  // the tile's stage is free once PV_t is done
+          tc::mma_commit(&bars->o_done[sr]);
         }
         __syncwarp();
       };
       bool ok = warp_wait(&bars->q_full, 0, bars, p.err);
-      // S_t needs tile t in shared memory and S_{t-1} read (one S buffer); PV_t
-      // needs both halves of P_t. Each barrier is probed for its phases in order
+      // S_t needs this CTA's rows of tile t and S_{t-1} read (one S buffer); PV_t
+      // needs both halves of P_t and the peer's rows. Each barrier is probed for its phases in order
       // and cannot run two phases ahead. A step is taken once every lane has
       // seen its barrier complete.
       int next_s = 0, next_pv = 0;
@@ -501,13 +536,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (ok && next_pv < n_t) {
         bool progressed = false;
         // PV first: its completion frees a ring stage and a P tile
-        const bool pv_ready = next_pv < next_s && mbar_test_parity_nb(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1);
+        const bool pv_ready = next_pv < next_s && mbar_test_parity_nb(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1) &&
+                              mbar_test_parity_nb(&bars->v_full[next_pv % kStagesV], (next_pv / kStagesV) & 1);
         if (__all_sync(0xffffffffu, pv_ready)) {
           issue_pv(next_pv++);
           progressed = true;
         }
         const bool s_ready = next_s < n_t &&
-                             mbar_test_parity_nb(&bars->r_full[next_s % kStages], (next_s / kStages) & 1) &&
+                             mbar_test_parity_nb(&bars->r_full[next_s % kStagesR], (next_s / kStagesR) & 1) &&
                              (next_s == 0 || mbar_test_parity_nb(&bars->s_free, (next_s - 1) & 1));
         if (__all_sync(0xffffffffu, s_ready)) {
           issue_s(next_s++);
@@ -567,7 +603,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float th = kRescaleLog2 / qs;
     const float2 qs2 = make_float2(qs, qs);
     const uint32_t tS = tmem + lane_addr + C::kColS;
-    unsigned char* ptile = smem + C::kOffP;
     float m_ref = -INFINITY, l_own = 0.f;  // l_own: the row sum of this CTA's p
     bool alive = true;
     for (int t = 0; t < n_t; ++t) {
@@ -597,7 +632,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int e = 0; e < kOwn; e += 2)
         mx4[(e >> 1) & 3] = fmax3(mx4[(e >> 1) & 3], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
       const float mx_own = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      // ---- the tile max over both CTAs' rows: trade maxima with the peer's warp
+      // ---- the tile max over both CTAs' rows: trade maxima with the peer's warp.
+      // The peer copies its P_t columns here only once it has these maxima, and
+      // they complete on p_full[x] like its P_{t-2} columns did: so the maxima
+      // go out only after P_{t-2} is complete here (long since, in practice).
+      if (t >= 2 && !warp_wait(&bars->p_full[x], ((t - 2) >> 1) & 1, bars, p.err)) {
+        alive = false;
+        break;
+      }
       if (lane == 0) mbar_arrive_expect_tx(&bars->m_full[warp][x], 32 * 4);
       st_async_b32(peer_addr(mbuf + x * kHeads + r, peer), __float_as_uint(mx_own),
                    peer_addr(&bars->m_full[warp][x], peer));
@@ -617,7 +659,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             m_ref = mx;
           }
           // O holds every PV issued so far, PV_{t-1} the last: rescale it once done
-          if (!warp_wait(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, bars, p.err)) {
+          if (!warp_wait(&bars->o_done[(t - 1) % kStagesR], ((t - 1) / kStagesR) & 1, bars, p.err)) {
             alive = false;
             break;
           }
@@ -647,33 +689,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         add_bf16x2(ls[(i & 1) * 2], ls[(i & 1) * 2 + 1], pw[i]);
       }
       l_own += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      unsigned char* stage = smem + C::kOffR + (t % kStages) * C::kStage;
+      unsigned char* rstage = smem + C::kOffR + (t % kStagesR) * C::kStageR;
       if (valid_own < kOwn || valid_peer < kOwn) {
         // value rows of keys at or past seq_len, in this CTA's rows (its value
-        // blocks) and in the peer rows' region: zero them (S_t, the other reader
-        // of this CTA's rows, is done) so that 0 * (whatever the cache holds)
-        // cannot be NaN
+        // blocks; S_t, their other reader, is done) and in the peer rows' V
+        // stage (once it has landed): zero them so that 0 * (whatever the cache
+        // holds) cannot be NaN
+        unsigned char* vstage = smem + C::kOffV + (t % kStagesV) * C::kStageV;
+        if (valid_peer < kOwn && !warp_wait(&bars->v_full[t % kStagesV], (t / kStagesV) & 1, bars, p.err)) {
+          alive = false;
+          break;
+        }
         const int n_own = (kOwn - valid_own) * C::kCBV * 8;  // 16-byte chunks: 8 per row and block
         const int n_all = n_own + (kOwn - valid_peer) * C::kCBV * 8;
         for (int i = r; i < n_all; i += kHeads) {
           const bool o = i < n_own;
           const int j = o ? i : i - n_own;
           const int row = (o ? valid_own : valid_peer) + j / (C::kCBV * 8), blk = (j / 8) % C::kCBV, ch = j % 8;
-          const int rb = o ? half * C::kCBV + blk : C::kNB + blk;
-          *reinterpret_cast<uint4*>(stage + rb * C::kRBlk + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+          unsigned char* base = o ? rstage + (half * C::kCBV + blk) * C::kRBlk : vstage + blk * C::kRBlk;
+          *reinterpret_cast<uint4*>(base + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      // ---- P tile x last held P_{t-2}: free once PV_{t-2} is done here (this
-      // CTA's columns, seen at the end of tile t-1) and in the peer (the columns
-      // copied there: the peer's arrival)
-      if (t >= 2 && !warp_wait_cluster(&bars->p_free[warp][x], ((t - 2) >> 1) & 1, bars, p.err)) {
-        alive = false;
-        break;
-      }
       // ---- this CTA's 32 keys of P_t: 8-key columns 4 half .. 4 half + 3 of
-      // the tile, each head's 16 bytes at row offset 16 r; then the warp's rows
-      // of those columns (512 bytes each) into the peer's tile
-      unsigned char* pt = ptile + x * C::kPBuf;
+      // the tile's P, which sits in the R stage over the other half's value
+      // blocks (only S_t read them, and S_t is done; the peer's copy of its
+      // columns comes after it has this CTA's maxima, sent after S_t too). Each
+      // head's 16 bytes at row offset 16 r; then the warp's rows of those
+      // columns (512 bytes each) into the same place of the peer's P, which
+      // sits over this CTA's value blocks there.
+      unsigned char* pt = rstage + (1 - half) * C::kCBV * C::kRBlk;
+      unsigned char* pt_peer = rstage + half * C::kCBV * C::kRBlk;
       const uint32_t pbase = smem_u32(pt);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -684,29 +729,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          unsigned char* src = pt + (4 * half + i) * C::kPCol + warp * 32 * 16;
-          bulk_copy_to_peer(peer_addr(src, peer), src, 32 * 16, peer_addr(&bars->p_full[x], peer));
+          const int off = (4 * half + i) * C::kPCol + warp * 32 * 16;
+          bulk_copy_to_peer(peer_addr(pt_peer + off, peer), pt + off, 32 * 16, peer_addr(&bars->p_full[x], peer));
         }
         if (warp == 0)
           mbar_arrive_expect_tx(&bars->p_full[x], kHeads * kOwn * 2);  // the peer's half, incoming
         else
           mbar_arrive(&bars->p_full[x]);
       }
-      // ---- P tile x ^ 1 is next written at tile t + 1: tell the peer, whose
-      // columns go there, once PV_{t-1} (its last reader here) is done. Done
-      // now rather than at tile t + 1, so that the peer rarely waits for it.
-      if (t >= 1 && t + 1 < n_t) {
-        if (!warp_wait(&bars->o_done[x ^ 1], ((t - 1) >> 1) & 1, bars, p.err)) {
-          alive = false;
-          break;
-        }
-        if (lane == 0) arrive_cluster_relaxed(peer_addr(&bars->p_free[warp][x ^ 1], peer));
-      }
     }
     // ---- the last PV (its commit covers every earlier MMA); the pair's row sum
     bool have_o = alive;
     if (have_o) {
-      have_o = warp_wait(&bars->o_done[(n_t - 1) & 1], ((n_t - 1) >> 1) & 1, bars, p.err);
+      have_o = warp_wait(&bars->o_done[(n_t - 1) % kStagesR], ((n_t - 1) / kStagesR) & 1, bars, p.err);
       tc::fence_after_sync();
     }
     float l_run = 0.f;
@@ -781,6 +816,19 @@ bool make_rows_map(CUtensorMap* m, const void* base, int w, uint64_t d1, uint64_
   return make_tmap_bf16(m, base, dims, strides, box);
 }
 
+// The same rows of w = 64 nb elements seen as [outer][row][column block][64]:
+// dimensions 64, rows, nb, outer with byte strides 2w (a row), 128 (a block),
+// 2w rows (an outer index). A box of box_rows rows x box_blk blocks lands in
+// shared memory block after block, box_rows x 128 bytes each, 128-byte swizzle;
+// rows past the tensor read as zeros.
+bool make_blocks_map(CUtensorMap* m, const void* base, int w, uint64_t rows, uint64_t outer, uint32_t box_rows,
+                     uint32_t box_blk) {
+  const uint64_t dims[4] = {64, rows, (uint64_t)(w / 64), outer};
+  const uint64_t strides[3] = {(uint64_t)w * 2, 128, (uint64_t)w * 2 * rows};
+  const uint32_t box[4] = {64, box_rows, box_blk, 1};
+  return make_tmap_bf16(m, base, dims, strides, box);
+}
+
 }  // namespace
 
 bool mla_absorbed_tc_supported(int bf16, int d_c, int d_r) { return bf16 == 1 && d_c == 512 && d_r == 64; }
@@ -796,18 +844,20 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
     return cudaErrorNotSupported;
   if (tables && !mla_absorbed_paged_block_ok(bs)) return cudaErrorNotSupported;
   if (B == 0) return cudaSuccess;
-  CUtensorMap tq, tr;
+  CUtensorMap tq, tr, tv;
   // q_abs [B, H, 576]: box of 128 heads
   if (!make_rows_map(&tq, q_abs, C::kW, (uint64_t)H, (uint64_t)B, kHeads)) return cudaErrorInvalidValue;
-  if (tables) {
-    // pool [num_blocks, bs, 576]: box of one block, or of 32 rows of a 64-row one
-    if (!make_rows_map(&tr, latent, C::kW, (uint64_t)bs, (uint64_t)num_blocks, (uint32_t)(bs < kOwn ? bs : kOwn)))
-      return cudaErrorInvalidValue;
-    max_len = mbps * bs;
-  } else {
-    // latent [B, max_len, 576]: box of one CTA's 32 rows of a tile
-    if (!make_rows_map(&tr, latent, C::kW, (uint64_t)max_len, (uint64_t)B, kOwn)) return cudaErrorInvalidValue;
-  }
+  // latent [B, max_len, 576] or pool [num_blocks, bs, 576]: boxes of one CTA's
+  // 32 rows of a tile, all blocks (tr) or a value half (tv); a pool of 8- or
+  // 16-row blocks: boxes of one pool block x one column block (tr; tv unused)
+  const uint64_t rows = tables ? (uint64_t)bs : (uint64_t)max_len;
+  const uint64_t outer = tables ? (uint64_t)num_blocks : (uint64_t)B;
+  const bool whole = !tables || bs >= kOwn;
+  const uint32_t br = whole ? kOwn : (uint32_t)bs;
+  if (!make_blocks_map(&tr, latent, C::kW, rows, outer, br, whole ? C::kNB : 1) ||
+      !make_blocks_map(&tv, latent, C::kW, rows, outer, br, whole ? C::kCBV : 1))
+    return cudaErrorInvalidValue;
+  if (tables) max_len = mbps * bs;
   MlaParams p;
   p.tables = tables;
   p.mbps = mbps;
@@ -845,7 +895,7 @@ cudaError_t launch_mla_absorbed_tc(const void* q_abs, const void* latent, const 
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_absorbed_tc_kernel<512, 64>, tq, tr, p);
+  return cudaLaunchKernelEx(&cfg, mla_absorbed_tc_kernel<512, 64>, tq, tr, tv, p);
 }
 
 }  // namespace gqa
