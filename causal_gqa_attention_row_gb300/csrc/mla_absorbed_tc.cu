@@ -453,13 +453,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         last_v[st] = t;
       return true;
     };
-    Coords cur = fetch(0);
-    for (int t = 0; t < n_t; ++t) {
-      check(cur);
-      const Coords next = fetch(min(t + 1, n_t - 1));  // in flight during this tile's waits
-      const bool skip = p.debug_withhold && t == 0 && half == 1;  // test hook: tile 0 is never requested
-      if (!skip && (!load_part(t, true, cur.c1, cur.c2) || !load_part(t, false, cur.c1 + 2, cur.c2 + 2))) break;
-      cur = next;
+    if (whole) {
+      // one box per part: lane 0 runs the loop alone
+      if (lane == 0) {
+        // paged: the pool block holding a part's 32 rows starting at `row` (bs
+        // >= 32, so one block holds them); a part past the sequence loads from
+        // past the end of the pool (zeros). Requested one tile ahead.
+        struct Entry {
+          int e;        // sequence (contiguous) or pool block
+          bool looked;  // read from the table (and so to be checked)
+        };
+        auto entry = [&](int row) -> Entry {
+          if (!p.tables) return Entry{b, false};
+          const int ti = row / p.bs;
+          if (ti < p.mbps && row < len) return Entry{__ldg(p.tables + (size_t)b * p.mbps + ti), true};
+          return Entry{p.num_blocks, false};
+        };
+        // checked when used: an entry out of range is flagged and reads zeros
+        auto use = [&](Entry x) {
+          if (x.looked && (x.e < 0 || x.e >= p.num_blocks)) {
+            raise_error(p.err, kErrBounds);
+            return p.num_blocks;
+          }
+          return x.e;
+        };
+        auto part_row = [&](int t, bool own) { return k0 + t * kKeys + kOwn * (own ? half : 1 - half); };
+        Entry x_own = entry(part_row(0, true)), x_peer = entry(part_row(0, false));
+        for (int t = 0; t < n_t; ++t) {
+          const int e_own = use(x_own), e_peer = use(x_peer);
+          const int tn = min(t + 1, n_t - 1);  // the next tile's entries, in flight during this tile's waits
+          const Entry n_own = entry(part_row(tn, true)), n_peer = entry(part_row(tn, false));
+          // contiguous: row and sequence; paged: slot in the pool block and the block
+          const int own_c1 = p.tables ? part_row(t, true) % p.bs : part_row(t, true);
+          const int peer_c1 = p.tables ? part_row(t, false) % p.bs : part_row(t, false);
+          const bool skip = p.debug_withhold && t == 0 && half == 1;  // test hook: tile 0 is never requested
+          if (!skip) {
+            const int sr = t % kStagesR, sv = t % kStagesV;
+            // a stage is free once PV_{t - stages} is done (o_done completes once per PV)
+            if (t >= kStagesR && !wait_or_abort(&bars->o_done[(t - kStagesR) % kStagesR], ((t - kStagesR) / kStagesR) & 1,
+                                                bars, p.err))
+              break;
+            mbar_arrive_expect_tx(&bars->r_full[sr], C::kStageR);
+            tc::tma_load_4d(smem + C::kOffR + sr * C::kStageR, &tm_r, 0, own_c1, 0, e_own, &bars->r_full[sr]);
+            last_r[sr] = t;
+            if (t >= kStagesV && !wait_or_abort(&bars->o_done[(t - kStagesV) % kStagesR], ((t - kStagesV) / kStagesR) & 1,
+                                                bars, p.err))
+              break;
+            mbar_arrive_expect_tx(&bars->v_full[sv], C::kStageV);
+            tc::tma_load_4d(smem + C::kOffV + sv * C::kStageV, &tm_v, 0, peer_c1, half * C::kCBV, e_peer,
+                            &bars->v_full[sv]);
+            last_v[sv] = t;
+          }
+          x_own = n_own;
+          x_peer = n_peer;
+        }
+      }
+      __syncwarp();
+    } else {
+      Coords cur = fetch(0);
+      for (int t = 0; t < n_t; ++t) {
+        check(cur);
+        const Coords next = fetch(min(t + 1, n_t - 1));  // in flight during this tile's waits
+        const bool skip = p.debug_withhold && t == 0 && half == 1;  // test hook: tile 0 is never requested
+        if (!skip && (!load_part(t, true, cur.c1, cur.c2) || !load_part(t, false, cur.c1 + 2, cur.c2 + 2))) break;
+        cur = next;
+      }
     }
     if (lane == 0) {  // never exit with a load in flight
       if (!mbar_wait(&bars->q_full, 0)) raise_error(p.err, kErrTimeout);
