@@ -116,9 +116,10 @@ def test_prefill_tensor_core_withheld_tile_times_out(gpu_lib, d):
 
 def test_mla_absorbed_withheld_tile_times_out_and_pair_drains(gpu_lib):
     """The second CTA of each absorbed-MLA pair never gets its first cache tile:
-    it gives up, its peer gives up waiting for the partial scores it would have
-    sent and waits out the copy it sent itself, and both free their tensor
-    memory. The call reports the timeout; the next call matches the oracle."""
+    it gives up, its peer gives up waiting for the tile maxima it would have
+    sent, both let what they sent each other land before leaving, and both free
+    their tensor memory. The call reports the timeout; the next call matches
+    the oracle."""
     g = gpu_lib
     B, H, L, D_C, D_R = 2, 128, 100, 512, 64
     c = W.make_mla_absorbed(B=B, H=H, max_len=L, lens=[100, 70], seed=65)
