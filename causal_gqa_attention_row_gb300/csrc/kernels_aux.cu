@@ -169,15 +169,22 @@ cudaError_t launch_plan_units(const RowsParams& p, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // Split combine: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the
 // splits of one (sequence, head), M = max_s m_s, in split order. Empty splits
-// (m = -inf) weigh zero. One warp per output row.
+// (m = -inf) weigh zero. One warp per output row and group of up to 256
+// columns (a 512-wide row takes two warps, which read the same (m, l) pairs).
 
-// kMaxE: output columns per lane (d_v <= 32 * kMaxE).
+constexpr int kCombineCols = 256;  // output columns per warp
+
+// kMaxE: output columns per lane (a warp's columns <= 32 * kMaxE <= 256).
 template <typename ET, int kMaxE>
 __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, int DV) {
   grid_dep_wait();  // the attention kernel's partials (launched as its dependent)
-  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int ncg = (DV + kCombineCols - 1) / kCombineCols;
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (wid >= p.B * p.seq_q * p.H) return;
+  if (gw >= (long long)p.B * p.seq_q * p.H * ncg) return;
+  const int wid = (int)(gw / ncg);                   // the output row
+  const int c0 = (int)(gw % ncg) * kCombineCols;     // its first column here
+  const int DW = min(kCombineCols, DV - c0);         // columns of this warp
   const int b = wid / (p.seq_q * p.H);
   const int kv_len = p.kv_len ? p.kv_len[b] : (p.offsets ? p.offsets[b] : 0) + p.seq_q;
   if (!(kv_len >= p.seq_q && kv_len >= 1 && kv_len <= p.capacity)) return;  // attention wrote zeros
@@ -189,13 +196,67 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
   const float* P = p.partial + (size_t)wid * p.max_splits * stride;
   // the sink logit (log2 domain) joins the denominator once per row and head
   const float z2 = p.sinks ? __ldg(p.sinks + wid % p.H) * kLog2e : -INFINITY;
+  ET* out = reinterpret_cast<ET*>(p.out) + (size_t)wid * DV + c0;
+  // Few splits (the common case): every load of the row is issued at once --
+  // each split's (m, l) and this lane's column pairs d = 2 lane + 64 e of its
+  // o (8-byte aligned: rows of d_v + 2 floats, d_v and c0 even) -- so the row
+  // costs one round trip; the weights and sums then run in split order as
+  // below, and the output is stored as pairs. At most 16 partial values per lane.
+  constexpr int kFast = 16 / kMaxE;
+  if (n - s_lo <= kFast && (DV & 1) == 0) {
+    const int nk = n - s_lo;
+    float2 v[kFast][kMaxE / 2];
+    float mk[kFast], lk[kFast];
+#pragma unroll
+    for (int j = 0; j < kFast; ++j) {
+      const bool ok = j < nk;
+      const float* row = P + (size_t)(s_lo + (ok ? j : 0)) * stride;
+      mk[j] = ok ? __ldcg(row) : -INFINITY;
+      lk[j] = ok ? __ldcg(row + 1) : 0.f;
+#pragma unroll
+      for (int e = 0; e < kMaxE / 2; ++e) {
+        const int d = 2 * lane + 64 * e;
+        v[j][e] = (ok && d < DW) ? __ldcg(reinterpret_cast<const float2*>(row + 2 + c0 + d)) : make_float2(0.f, 0.f);
+      }
+    }
+    float M = z2;
+#pragma unroll
+    for (int j = 0; j < kFast; ++j) M = fmaxf(M, mk[j]);
+    float2 acc[kMaxE / 2];
+#pragma unroll
+    for (int e = 0; e < kMaxE / 2; ++e) acc[e] = make_float2(0.f, 0.f);
+    float dsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < kFast; ++j) {
+        const float w = (mk[j] == -INFINITY) ? 0.f : exp2f(mk[j] - M);
+        dsum = fmaf(w, lk[j], dsum);
+#pragma unroll
+        for (int e = 0; e < kMaxE / 2; ++e) {
+          acc[e].x = fmaf(w, v[j][e].x, acc[e].x);
+          acc[e].y = fmaf(w, v[j][e].y, acc[e].y);
+        }
+      }
+    }
+    const float den = M == -INFINITY ? 0.f : (p.sinks ? exp2f(z2 - M) : 0.f) + dsum;
+#pragma unroll
+    for (int e = 0; e < kMaxE / 2; ++e) {
+      const int d = 2 * lane + 64 * e;
+      if (d >= DW) continue;
+      const float a = den > 0.f ? acc[e].x / den : 0.f, c = den > 0.f ? acc[e].y / den : 0.f;
+      if constexpr (sizeof(ET) == 2)
+        *reinterpret_cast<__nv_bfloat162*>(out + d) = __floats2bfloat162_rn(a, c);
+      else
+        *reinterpret_cast<float2*>(out + d) = make_float2(a, c);
+    }
+    return;
+  }
   float M = z2;
   for (int s = s_lo + lane; s < n; s += 32) M = fmaxf(M, P[(size_t)s * stride]);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  ET* out = reinterpret_cast<ET*>(p.out) + (size_t)wid * DV;
   if (M == -INFINITY) {
-    for (int d = lane; d < DV; d += 32) out[d] = Elem<ET>::from_f32(0.f);
+    for (int d = lane; d < DW; d += 32) out[d] = Elem<ET>::from_f32(0.f);
     return;
   }
   // Each split's weight once (lane s % 32 holds split s's), the weighted row sums
@@ -216,16 +277,16 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
     // The rows of up to kBatch splits are loaded before any of them is
     // accumulated, so that many loads are in flight per lane; the sum still
     // runs over the splits in order.
-    constexpr int kBatch = 4;
+    constexpr int kBatch = 16 / kMaxE;
     const int cnt = min(32, n - s0);
     for (int j0 = 0; j0 < cnt; j0 += kBatch) {
       float v[kBatch][kMaxE];
 #pragma unroll
       for (int jj = 0; jj < kBatch; ++jj) {
-        const float* row = P + (size_t)(s0 + j0 + jj) * stride + 2;
+        const float* row = P + (size_t)(s0 + j0 + jj) * stride + 2 + c0;
 #pragma unroll
         for (int e = 0; e < kMaxE; ++e)
-          v[jj][e] = (j0 + jj < cnt && lane + 32 * e < DV) ? __ldcg(row + lane + 32 * e) : 0.f;
+          v[jj][e] = (j0 + jj < cnt && lane + 32 * e < DW) ? __ldcg(row + lane + 32 * e) : 0.f;
       }
 #pragma unroll
       for (int jj = 0; jj < kBatch; ++jj) {
@@ -233,7 +294,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
         if (j0 + jj < cnt) {
 #pragma unroll
           for (int e = 0; e < kMaxE; ++e)
-            if (lane + 32 * e < DV) acc[e] = fmaf(wj, v[jj][e], acc[e]);
+            if (lane + 32 * e < DW) acc[e] = fmaf(wj, v[jj][e], acc[e]);
         }
       }
     }
@@ -243,21 +304,23 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const RowsParams p, 
   const float den = (p.sinks ? exp2f(z2 - M) : 0.f) + den_part;
 #pragma unroll
   for (int e = 0; e < kMaxE; ++e)
-    if (lane + 32 * e < DV) out[lane + 32 * e] = Elem<ET>::from_f32(den > 0.f ? acc[e] / den : 0.f);
+    if (lane + 32 * e < DW) out[lane + 32 * e] = Elem<ET>::from_f32(den > 0.f ? acc[e] / den : 0.f);
 }
 
 cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStream_t st) {
-  const long long rows = (long long)p.B * p.seq_q * p.H;
-  if (rows <= 0) return cudaSuccess;
-  const int warps_per_block = 8;
-  const unsigned blocks = (unsigned)((rows + warps_per_block - 1) / warps_per_block);
-  // d_v up to 512 (the latent width of the absorbed MLA decode), in lanes' shares
-  // of 4, 8 or 16 columns. Launched as a programmatic dependent of the attention
-  // kernel before it: its CTAs may start while that kernel finishes, and wait for
-  // it (grid_dep_wait) before reading the partials.
+  // d_v up to 512 (the latent width of the absorbed MLA decode): a warp per row
+  // and group of up to 256 columns, in lanes' shares of 4 or 8 columns.
   if (dv > 512) return cudaErrorNotSupported;
+  const long long warps = (long long)p.B * p.seq_q * p.H * ((dv + kCombineCols - 1) / kCombineCols);
+  if (warps <= 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  const long long blocks = (warps + warps_per_block - 1) / warps_per_block;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // Launched as a programmatic dependent of the attention kernel before it:
+  // its CTAs may start while that kernel finishes, and wait for it
+  // (grid_dep_wait) before reading the partials.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(blocks);
+  cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(32 * warps_per_block);
   cfg.stream = st;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
@@ -265,12 +328,10 @@ cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStre
   cfg.numAttrs = 1;
   if (bf16) {
     if (dv <= 128) return cudaLaunchKernelEx(&cfg, split_combine_kernel<__nv_bfloat16, 4>, p, dv);
-    if (dv <= 256) return cudaLaunchKernelEx(&cfg, split_combine_kernel<__nv_bfloat16, 8>, p, dv);
-    return cudaLaunchKernelEx(&cfg, split_combine_kernel<__nv_bfloat16, 16>, p, dv);
+    return cudaLaunchKernelEx(&cfg, split_combine_kernel<__nv_bfloat16, 8>, p, dv);
   }
   if (dv <= 128) return cudaLaunchKernelEx(&cfg, split_combine_kernel<float, 4>, p, dv);
-  if (dv <= 256) return cudaLaunchKernelEx(&cfg, split_combine_kernel<float, 8>, p, dv);
-  return cudaLaunchKernelEx(&cfg, split_combine_kernel<float, 16>, p, dv);
+  return cudaLaunchKernelEx(&cfg, split_combine_kernel<float, 8>, p, dv);
 }
 
 // ---------------------------------------------------------------------------
