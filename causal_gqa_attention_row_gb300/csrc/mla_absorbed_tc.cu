@@ -809,42 +809,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       have_o = warp_wait_cluster(&bars->l_full[warp], 0, bars, p.err);
       if (have_o) l_run = l_own + ld_shared_f32(smem_u32(lbuf + r));  // the same sum on both sides
     }
-    if (n_split == 1) {
-      const float inv = (have_o && l_run > 0.f) ? 1.f / l_run : 0.f;
-      __nv_bfloat16* dst = p.out + ((size_t)b * p.H + (mine ? h : 0)) * DC + half * C::kDVH;
+    // ---- O out. Each thread holds its head's row of this CTA's value half in
+    // TMEM; 32 columns at a time, the warp moves its 32 rows through a padded
+    // shared-memory buffer (row stride 33 words: no bank conflict either way)
+    // so that each store writes one row's 32 consecutive columns. The buffer
+    // lies in the R ring, free now: every tile is consumed and the last PV done.
+    // One sequence split: O / l as bf16; otherwise (m, l, O) in fp32.
+    float* stage = reinterpret_cast<float*>(smem + C::kOffR) + warp * 32 * 33;
+    const float inv = (have_o && l_run > 0.f) ? 1.f / l_run : 0.f;
+    if (n_split > 1 && mine && half == 0) {
+      float* P = p.partial + (((size_t)b * p.H + h) * p.max_splits + split) * (DC + 2);
+      P[0] = have_o ? m_ref * qs : -INFINITY;
+      P[1] = have_o ? l_run : 0.f;
+    }
+    const int h_w = h0 + warp * 32;  // the warp's first head
+    const int nrows = min(32, p.H - h_w);  // rows of this warp that are heads
+    // row i of the warp at dst0 + i * row_stride (elements), this lane's column within the chunk
+    const size_t row0 = (size_t)b * p.H + h_w;
+    const size_t row_stride = n_split == 1 ? (size_t)DC : (size_t)p.max_splits * (DC + 2);
+    __nv_bfloat16* out0 = p.out + row0 * DC + half * C::kDVH + lane;
+    float* part0 = p.partial + (row0 * p.max_splits + split) * (DC + 2) + 2 + half * C::kDVH + lane;
+    float inv_r[32];  // each row's 1 / l (one sequence split)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) inv_r[i] = __shfl_sync(0xffffffffu, inv, i);
 #pragma unroll 1
-      for (int c = 0; c < C::kDVH / 32; ++c) {
-        uint32_t o[32];
-        tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c * 32, o);
-        tc::tmem_ld_wait();
-        if (mine) {
+    for (int c = 0; c < C::kDVH / 32; ++c) {
+      uint32_t o[32];
+      tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c * 32, o);
+      tc::tmem_ld_wait();
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w[4];
+      for (int e = 0; e < 32; ++e) stage[lane * 33 + e] = __uint_as_float(o[e]);
+      __syncwarp();
+      float v[32];  // row i's column c * 32 + lane: every read first, then the stores
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              w[u] = pack_bf16(__uint_as_float(o[q4 * 8 + 2 * u]) * inv, __uint_as_float(o[q4 * 8 + 2 * u + 1]) * inv);
-            *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        }
-      }
-    } else {
-      float* P = p.partial + (((size_t)b * p.H + (mine ? h : 0)) * p.max_splits + split) * (DC + 2);
-      if (mine && half == 0) {
-        P[0] = have_o ? m_ref * qs : -INFINITY;
-        P[1] = have_o ? l_run : 0.f;
-      }
-      float* dst = P + 2 + half * C::kDVH;
-#pragma unroll 1
-      for (int c = 0; c < C::kDVH / 32; ++c) {
-        uint32_t o[32];
-        tc::tmem_ld_32x32b_x32(tmem + lane_addr + C::kColO + c * 32, o);
-        tc::tmem_ld_wait();
-        if (mine) {
+      for (int i = 0; i < 32; ++i) v[i] = stage[i * 33 + lane];
+      __syncwarp();  // the buffer is refilled for the next chunk
+      if (n_split == 1) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            *reinterpret_cast<float2*>(dst + c * 32 + e) = make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1]));
-        }
+        for (int i = 0; i < 32; ++i)
+          if (i < nrows) out0[i * row_stride + c * 32] = __float2bfloat16_rn(v[i] * inv_r[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nrows) part0[i * row_stride + c * 32] = v[i];
       }
     }
   }
