@@ -528,9 +528,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer =================
-    // The warp runs the loop converged, every decision warp-uniform, and one
-    // elected lane issues each MMA and commit: a converged warp keeps the
-    // tensor core at its rate on these short (N = 32) MMAs, a lone lane does not.
+    // The warp runs the loop converged, every decision warp-uniform, and an
+    // elected lane issues the MMAs two at a time, and each commit: a converged
+    // warp keeps the tensor core at its rate on these short (N = 32) MMAs, a lone
+    // lane does not (the 36 score MMAs: ~1,750 cycles of issue from one lane,
+    // ~1,100 from the warp; the whole call with one MMA per election 59.1 us,
+    // two 55.9, four 58.7).
     {
       const uint32_t idS = tc::idesc_bf16_f32(kHeads, kOwn, false);
       const uint32_t idO = tc::idesc_bf16_f32(kHeads, C::kDVH, true);
@@ -551,14 +554,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         const uint64_t dR = dR0 + (uint64_t)((st * C::kStageR) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < C::kW / 16; ++kk) {
-          const int g = kk / 4, step = kk % 4;  // column block, 16-column step inside it
-          const uint32_t ar = g * C::kRBlk + step * 32;
+        for (int k0 = 0; k0 < C::kW / 16; k0 += 2) {
           if (elect_one()) {
-            if (g < C::kQT)  // Q_abs from TMEM: 16 columns = 8 TMEM columns
-              tc::mma_f16_ts(tS, tQ + g * 32 + step * 8, dR + (ar >> 4), idS, kk > 0);
-            else
-              tc::mma_f16_ss(tS, dQ + (((g - C::kQT) * C::kQBlk + step * 32) >> 4), dR + (ar >> 4), idS, kk > 0);
+#pragma unroll
+            for (int kk = k0; kk < k0 + 2; ++kk) {
+              const int g = kk / 4, step = kk % 4;  // column block, 16-column step inside it
+              const uint32_t ar = g * C::kRBlk + step * 32;
+              if (g < C::kQT)  // Q_abs from TMEM: 16 columns = 8 TMEM columns
+                tc::mma_f16_ts(tS, tQ + g * 32 + step * 8, dR + (ar >> 4), idS, kk > 0);
+              else
+                tc::mma_f16_ss(tS, dQ + (((g - C::kQT) * C::kQBlk + step * 32) >> 4), dR + (ar >> 4), idS, kk > 0);
+            }
           }
           __syncwarp();
         }
@@ -572,11 +578,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint64_t dVo = dVo0 + (uint64_t)((sr * C::kStageR) >> 4);
         const uint64_t dVp = dVp0 + (uint64_t)((sv * C::kStageV) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          // keys 16kk .. 16kk + 15 of the tile are rows of CTA kk / 2
-          const uint64_t dV = (kk / 2 == half ? dVo : dVp) + (uint64_t)(((kk % 2) * 16 * 128) >> 4);
-          if (elect_one())
-            tc::mma_f16_ss(tO, dP + (uint64_t)((kk * 2 * C::kPCol) >> 4), dV, idO, (t > 0 || kk > 0));
+        for (int k0 = 0; k0 < kKeys / 16; k0 += 2) {
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = k0; kk < k0 + 2; ++kk) {
+              // keys 16kk .. 16kk + 15 of the tile are rows of CTA kk / 2
+              const uint64_t dV = (kk / 2 == half ? dVo : dVp) + (uint64_t)(((kk % 2) * 16 * 128) >> 4);
+              tc::mma_f16_ss(tO, dP + (uint64_t)((kk * 2 * C::kPCol) >> 4), dV, idO, (t > 0 || kk > 0));
+            }
+          }
           __syncwarp();
         }
         if (elect_one()) {
