@@ -794,12 +794,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                      pw[4 * i + 3]);
       tc::fence_async_smem();  // P and the zeroed rows visible to the tensor cores and the bulk copies
       __syncwarp();
+      if (lane < 4) {  // one 512-byte copy per lane: the four in one instruction
+        const int off = (4 * half + lane) * C::kPCol + warp * 32 * 16;
+        bulk_copy_to_peer(peer_addr(pt_peer + off, peer), pt + off, 32 * 16, peer_addr(&bars->p_full[x], peer));
+      }
       if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int off = (4 * half + i) * C::kPCol + warp * 32 * 16;
-          bulk_copy_to_peer(peer_addr(pt_peer + off, peer), pt + off, 32 * 16, peer_addr(&bars->p_full[x], peer));
-        }
         if (warp == 0)
           mbar_arrive_expect_tx(&bars->p_full[x], kHeads * kOwn * 2);  // the peer's half, incoming
         else

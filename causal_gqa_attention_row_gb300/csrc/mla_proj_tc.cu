@@ -97,11 +97,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (b < B) y[((size_t)b * H + h) * y_stride + m] = __float2bfloat16_rn(__uint_as_float(d[j]));
     }
   }
-  // the columns of x past K are copied to y past M unchanged (the query's rope slice)
+  // the columns of x past K are copied to y past M unchanged (the query's rope
+  // slice): in 16-byte pieces when the rows allow, every load of a round issued
+  // before its stores (one element at a time, each store waited for its load:
+  // ~16 round trips per thread)
   if (tail > 0 && blockIdx.x == 0) {
-    for (int e = threadIdx.x; e < kPN * tail; e += kPThreads) {
-      const int b = b0 + e / tail, c = e % tail;
-      if (b < B) y[((size_t)b * H + h) * y_stride + M + c] = x[((size_t)b * H + h) * x_stride + K + c];
+    const bool vec = (tail % 8) == 0 && (x_stride % 8) == 0 && (y_stride % 8) == 0 && (K % 8) == 0 && (M % 8) == 0 &&
+                     (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0;
+    if (vec) {
+      const int per_row = tail / 8, n = kPN * per_row;  // 16-byte pieces
+      constexpr int kRound = 4;
+      for (int e0 = threadIdx.x; e0 < n; e0 += kRound * kPThreads) {
+        uint4 v[kRound];
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+          const int e = e0 + u * kPThreads, b = b0 + e / per_row, c = (e % per_row) * 8;
+          if (e < n && b < B) v[u] = *reinterpret_cast<const uint4*>(x + ((size_t)b * H + h) * x_stride + K + c);
+        }
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+          const int e = e0 + u * kPThreads, b = b0 + e / per_row, c = (e % per_row) * 8;
+          if (e < n && b < B) *reinterpret_cast<uint4*>(y + ((size_t)b * H + h) * y_stride + M + c) = v[u];
+        }
+      }
+    } else {
+      for (int e = threadIdx.x; e < kPN * tail; e += kPThreads) {
+        const int b = b0 + e / tail, c = e % tail;
+        if (b < B) y[((size_t)b * H + h) * y_stride + M + c] = x[((size_t)b * H + h) * x_stride + K + c];
+      }
     }
   }
   tc::fence_before_sync();
