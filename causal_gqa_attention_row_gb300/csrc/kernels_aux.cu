@@ -493,29 +493,103 @@ __global__ void __launch_bounds__(128) append_kernel(ET* q, const ET* k_new, con
     return;
   }
   const int row = p % bs;
-  if (rope) {
-    for (int pr = threadIdx.x; pr < rot_dim / 2; pr += blockDim.x) {
-      float c, s;
-      rope_cos_sin((double)p, fr.w[pr], &c, &s);
-      const int e = rot_offset + 2 * pr;
-      for (int h = 0; h < H; ++h) rotate_pair(q + ((size_t)b * H + h) * dk + e, c, s);
-      for (int kh = 0; kh < Hkv; ++kh) {
-        ET pair[2] = {k_new[((size_t)b * Hkv + kh) * dk + e], k_new[((size_t)b * Hkv + kh) * dk + e + 1]};
-        rotate_pair(pair, c, s);
-        ET* dst = k_pool + (((size_t)blk * Hkv + kh) * bs + row) * dk + e;
-        dst[0] = pair[0];
-        dst[1] = pair[1];
+  // Vector path: q, k and v in 16-byte chunks (whole rotary pairs: a chunk lies
+  // wholly inside or outside the rotated columns), each pair's (cos, sin) at p
+  // computed once and shared; every chunk's load of a round issued before any
+  // rotation or store, so a thread waits on memory once per round (one element
+  // or pair at a time, the loads and stores of a CTA had been ~50 round trips).
+  constexpr int V = Elem<ET>::kPerChunk;
+  const bool vec = dk % V == 0 && dv % V == 0 && (!rope || (rot_offset % V == 0 && rot_dim % V == 0)) &&
+                   ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_new) |
+                     reinterpret_cast<uintptr_t>(v_new) | reinterpret_cast<uintptr_t>(k_pool) |
+                     reinterpret_cast<uintptr_t>(v_pool)) & 15) == 0;
+  if (vec) {
+    __shared__ float2 cs[128];  // (cos, sin) of rotary pair t at p
+    if (rope)
+      for (int pr = threadIdx.x; pr < rot_dim / 2; pr += blockDim.x) rope_cos_sin((double)p, fr.w[pr], &cs[pr].x, &cs[pr].y);
+    __syncthreads();
+    const int cpk = dk / V, cpv = dv / V;  // chunks per row
+    const int nq = H * cpk, nk = Hkv * cpk, nv = Hkv * cpv, n = nq + nk + nv;
+    // chunk i: (source, destination, first rotated pair or -1)
+    auto chunk = [&](int i, const ET*& src, ET*& dst, int& t0) {
+      t0 = -1;
+      int c0;
+      if (i < nq) {
+        const int h = i / cpk;
+        c0 = (i % cpk) * V;
+        src = dst = q + ((size_t)b * H + h) * dk + c0;
+      } else if (i < nq + nk) {
+        const int kh = (i - nq) / cpk;
+        c0 = ((i - nq) % cpk) * V;
+        src = k_new + ((size_t)b * Hkv + kh) * dk + c0;
+        dst = k_pool + (((size_t)blk * Hkv + kh) * bs + row) * dk + c0;
+      } else {
+        const int kh = (i - nq - nk) / cpv;
+        src = v_new + ((size_t)b * Hkv + kh) * dv + ((i - nq - nk) % cpv) * V;
+        dst = v_pool + (((size_t)blk * Hkv + kh) * bs + row) * dv + ((i - nq - nk) % cpv) * V;
+        return;
+      }
+      if (rope && c0 >= rot_offset && c0 < rot_offset + rot_dim) t0 = (c0 - rot_offset) / 2;
+    };
+    constexpr int kRound = 8;  // chunks per thread in flight
+    for (int i0 = threadIdx.x; i0 < n; i0 += kRound * blockDim.x) {
+      uint4 v[kRound];
+#pragma unroll
+      for (int u = 0; u < kRound; ++u) {
+        const int i = i0 + u * (int)blockDim.x;
+        if (i >= n) continue;
+        const ET* src;
+        ET* dst;
+        int t0;
+        chunk(i, src, dst, t0);
+        v[u] = *reinterpret_cast<const uint4*>(src);
+      }
+#pragma unroll
+      for (int u = 0; u < kRound; ++u) {
+        const int i = i0 + u * (int)blockDim.x;
+        if (i >= n) continue;
+        const ET* src;
+        ET* dst;
+        int t0;
+        chunk(i, src, dst, t0);
+        if (t0 >= 0) {  // rotate the chunk's V / 2 pairs as rotate_pair does
+          ET* e = reinterpret_cast<ET*>(&v[u]);
+#pragma unroll
+          for (int j = 0; j < V / 2; ++j) {
+            const float2 w = cs[t0 + j];
+            const float x0 = Elem<ET>::to_f32(e[2 * j]), x1 = Elem<ET>::to_f32(e[2 * j + 1]);
+            e[2 * j] = Elem<ET>::from_f32(fmaf(x0, w.x, -x1 * w.y));
+            e[2 * j + 1] = Elem<ET>::from_f32(fmaf(x0, w.y, x1 * w.x));
+          }
+        }
+        *reinterpret_cast<uint4*>(dst) = v[u];
       }
     }
-  }
-  for (int idx = threadIdx.x; idx < Hkv * dk; idx += blockDim.x) {
-    const int kh = idx / dk, e = idx % dk;
-    if (rope && e >= rot_offset && e < rot_offset + rot_dim) continue;  // written rotated above
-    k_pool[(((size_t)blk * Hkv + kh) * bs + row) * dk + e] = k_new[((size_t)b * Hkv + kh) * dk + e];
-  }
-  for (int idx = threadIdx.x; idx < Hkv * dv; idx += blockDim.x) {
-    const int kh = idx / dv, e = idx % dv;
-    v_pool[(((size_t)blk * Hkv + kh) * bs + row) * dv + e] = v_new[((size_t)b * Hkv + kh) * dv + e];
+  } else {
+    if (rope) {
+      for (int pr = threadIdx.x; pr < rot_dim / 2; pr += blockDim.x) {
+        float c, s;
+        rope_cos_sin((double)p, fr.w[pr], &c, &s);
+        const int e = rot_offset + 2 * pr;
+        for (int h = 0; h < H; ++h) rotate_pair(q + ((size_t)b * H + h) * dk + e, c, s);
+        for (int kh = 0; kh < Hkv; ++kh) {
+          ET pair[2] = {k_new[((size_t)b * Hkv + kh) * dk + e], k_new[((size_t)b * Hkv + kh) * dk + e + 1]};
+          rotate_pair(pair, c, s);
+          ET* dst = k_pool + (((size_t)blk * Hkv + kh) * bs + row) * dk + e;
+          dst[0] = pair[0];
+          dst[1] = pair[1];
+        }
+      }
+    }
+    for (int idx = threadIdx.x; idx < Hkv * dk; idx += blockDim.x) {
+      const int kh = idx / dk, e = idx % dk;
+      if (rope && e >= rot_offset && e < rot_offset + rot_dim) continue;  // written rotated above
+      k_pool[(((size_t)blk * Hkv + kh) * bs + row) * dk + e] = k_new[((size_t)b * Hkv + kh) * dk + e];
+    }
+    for (int idx = threadIdx.x; idx < Hkv * dv; idx += blockDim.x) {
+      const int kh = idx / dv, e = idx % dv;
+      v_pool[(((size_t)blk * Hkv + kh) * bs + row) * dv + e] = v_new[((size_t)b * Hkv + kh) * dv + e];
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) lens_out[b] = p + 1;
