@@ -256,6 +256,50 @@ def test_append_writes_only_target_slots(gpu_lib):
     assert rope_close(W.to_oracle(q), q2, W.to_oracle(c.q))
 
 
+@pytest.mark.parametrize("dtype,rot_offset,rot_dim", [
+    (torch.bfloat16, 0, None),   # every column rotated: the 16-byte chunk path
+    (torch.bfloat16, 16, 32),    # an aligned middle range: chunks rotated or copied as they fall
+    (torch.bfloat16, 2, 12),     # not on a chunk boundary: the element-wise form
+    (torch.float32, 4, 8),       # fp32 rows, 4-element chunks
+])
+def test_append_partial_rotary(gpu_lib, dtype, rot_offset, rot_dim):
+    """kv_append_paged with only part of each row rotated, through both of its
+    forms: V copied bit for bit, K and q rotated within the RoPE bound where the
+    range says and bit for bit elsewhere, no other pool slot written."""
+    g = gpu_lib
+    c = W.make_paged(B=5, H=8, Hkv=2, dk=64, dv=64, block_size=16, num_blocks=200, lens=[0, 15, 16, 300, 1],
+                     mbps=40, seed=44, dtype=dtype)
+    kp0, vp0 = W.to_oracle(c.k_pool), W.to_oracle(c.v_pool)
+    q, kp, vp = c.q.to(DEV), c.k_pool.to(DEV), c.v_pool.to(DEV)
+    lin = c.seq_lens.to(DEV)
+    lout = torch.empty_like(lin)
+    g.kv_append_paged(q, c.k_new.to(DEV), c.v_new.to(DEV), kp, vp, c.tables.to(DEV), lin, lout, c.theta,
+                      rot_offset=rot_offset, rot_dim=rot_dim)
+    ok(g)
+    q2, kp2, vp2, l2 = core.kv_append_paged(W.to_oracle(c.q), W.to_oracle(c.k_new), W.to_oracle(c.v_new), kp0, vp0,
+                                            W.to_oracle(c.tables), W.to_oracle(c.seq_lens), c.theta,
+                                            rot_offset=rot_offset, rot_dim=rot_dim)
+    assert lout.cpu().tolist() == list(l2)
+    gk, gv, gq = W.to_oracle(kp), W.to_oracle(vp), W.to_oracle(q)
+    assert np.array_equal(gv, vp2)
+    rd = 64 - rot_offset if rot_dim is None else rot_dim
+    cols = np.zeros(64, dtype=bool)
+    cols[rot_offset:rot_offset + rd] = True
+    assert np.array_equal(gk[..., ~cols], kp2[..., ~cols])   # columns outside the range: copied
+    assert np.array_equal(gq[..., ~cols], q2[..., ~cols])
+    k_in = kp2.copy()
+    for b, n in enumerate(c.seq_lens.tolist()):
+        k_in[int(c.tables[b, n // 16]), :, n % 16] = W.to_oracle(c.k_new[b])
+    if dtype == torch.bfloat16:
+        assert rope_close(gk[..., cols], kp2[..., cols], k_in[..., cols])
+        assert rope_close(gq[..., cols], q2[..., cols], W.to_oracle(c.q)[..., cols])
+    else:  # fp32: a few fp32 roundings of the pair's norm
+        for got, want, x in ((gk, kp2, k_in), (gq, q2, W.to_oracle(c.q))):
+            x = core.widen(x[..., cols])
+            norm = np.repeat(np.sqrt(x[..., 0::2] ** 2 + x[..., 1::2] ** 2), 2, axis=-1)
+            assert np.all(np.abs(core.widen(got[..., cols]) - core.widen(want[..., cols])) <= 2.0 ** -20 * norm + 1e-30)
+
+
 # ---------------------------------------------------------------------------
 # invariants
 
