@@ -272,17 +272,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// True in exactly one lane of the converged warp.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "elect.sync _|p, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 template <int DC, int DR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_absorbed_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
@@ -555,7 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint64_t dR = dR0 + (uint64_t)((st * C::kStageR) >> 4);
 #pragma unroll
         for (int k0 = 0; k0 < C::kW / 16; k0 += 2) {
-          if (elect_one()) {
+          if (tc::elect_one()) {
 #pragma unroll
             for (int kk = k0; kk < k0 + 2; ++kk) {
               const int g = kk / 4, step = kk % 4;  // column block, 16-column step inside it
@@ -568,7 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        if (elect_one()) tc::mma_commit(&bars->s_full);
+        if (tc::elect_one()) tc::mma_commit(&bars->s_full);
         __syncwarp();
       };
       auto issue_pv = [&](int t) {  // O += P_t R_t[:, value half], 16 keys per instruction
@@ -579,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint64_t dVp = dVp0 + (uint64_t)((sv * C::kStageV) >> 4);
 #pragma unroll
         for (int k0 = 0; k0 < kKeys / 16; k0 += 2) {
-          if (elect_one()) {
+          if (tc::elect_one()) {
 #pragma unroll
             for (int kk = k0; kk < k0 + 2; ++kk) {
               // keys 16kk .. 16kk + 15 of the tile are rows of CTA kk / 2
@@ -589,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        if (elect_one()) {
+        if (tc::elect_one()) {
           tc::mma_commit(&bars->o_done[sr]);
         }
         __syncwarp();
@@ -627,7 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       // every MMA issued above has completed before TMEM is released
-      if (elect_one()) tc::mma_commit(&bars->mma_final);
+      if (tc::elect_one()) tc::mma_commit(&bars->mma_final);
       __syncwarp();
       if (lane == 0 && !mbar_wait(&bars->mma_final, 0)) raise_error(p.err, kErrTimeout);
       __syncwarp();
