@@ -373,8 +373,8 @@ const char* gqa_status_string(gqa_status status);
  *     every CTA;
  *   - the tensor-core prefill: the first K tile of every CTA;
  *   - the absorbed MLA decode: the first cache tile of the second CTA of every
- *     pair, so the first CTA also gives up waiting for its peer's partial scores
- *     and drains the copy it sent.
+ *     pair, so the first CTA also gives up waiting for its peer's tile maxima;
+ *     both let what they sent each other land before releasing their memory.
  * Outputs are then garbage. The hook is read when a call launches.
  * Never enable outside tests. Returns the previous setting. */
 int gqa_debug_withhold_first_tile(int enable);
