@@ -335,8 +335,8 @@ cudaError_t launch_split_combine(const RowsParams& p, int dv, int bf16, cudaStre
 }
 
 // ---------------------------------------------------------------------------
-// Interleaved RoPE. The angle pos * theta^(-2t/rot_dim) is formed in fp64 and
-// reduced modulo 2*pi in fp64 (positions reach 32k, where an fp32 angle would
+// Interleaved RoPE. The angle pos * theta^(-2t/rot_dim) has to be reduced
+// modulo 2*pi accurately (positions reach 32k, where a plain fp32 angle would
 // be off by ~2e-3 rad); sine and cosine of the reduced angle come from the
 // fp32 sincosf, the rotation is done in fp32 and rounded once on store.
 
@@ -353,16 +353,49 @@ __device__ __forceinline__ void rope_cos_sin(double pos, double w, float* c, flo
   sincosf((float)r, s, c);
 }
 
+// The same in fp32 arithmetic, which this GPU runs far faster than fp64, for
+// |pos| < 2^24 (the position exact in a float). The frequency comes as a float
+// pair w_hi + w_lo within 2^-48 of the double; the product pos * w is formed
+// without error in a_hi + e (Dekker and Kahan's two-product: one FMA gives the
+// rounding error of pos * w_hi), and the reduction modulo 2*pi is Cody and
+// Waite's with 2*pi as the sum of three floats, one FMA per part. The reduced
+// angle is within ~3e-7 rad of the exact one (the fp64 form, which also rounds
+// it to a float before sincosf, within ~1.2e-7).
+constexpr float kTwoPiF1 = 6.2831854820251465f;       // the float nearest 2*pi
+constexpr float kTwoPiF2 = -1.7484555314695172e-07f;  // ... nearest 2*pi - kTwoPiF1
+constexpr float kTwoPiF3 = -6.8604980400235275e-15f;  // ... nearest what remains (4e-23 left)
+constexpr float kInvTwoPiF = 0.15915493667125702f;
+
+__device__ __forceinline__ void rope_cos_sin_f(int pos, float w_hi, float w_lo, double w, float* c, float* s) {
+  if (pos >= (1 << 24) || pos <= -(1 << 24)) {  // not exact as a float
+    rope_cos_sin((double)pos, w, c, s);
+    return;
+  }
+  const float p = (float)pos;
+  const float a_hi = p * w_hi;
+  const float a_lo = fmaf(p, w_lo, fmaf(p, w_hi, -a_hi));  // the rounding error of p * w_hi, plus p * w_lo
+  const float n = rintf(a_hi * kInvTwoPiF);
+  float r = fmaf(-n, kTwoPiF1, a_hi);
+  r = fmaf(-n, kTwoPiF2, r);
+  r = fmaf(-n, kTwoPiF3, r);
+  sincosf(r + a_lo, s, c);
+}
+
 // The rot_dim/2 frequencies theta^(-2t/rot_dim), t < rot_dim/2, computed once
-// per call on the host in double and passed by value (they depend only on the
-// call's scalar arguments).
+// per call on the host in double (w) and split into a float pair (w_hi + w_lo),
+// passed by value (they depend only on the call's scalar arguments).
 struct RopeFreqs {
   double w[128];
+  float w_hi[128], w_lo[128];
 };
 
 RopeFreqs rope_freqs(int rot_dim, double theta) {
   RopeFreqs f{};
-  for (int t = 0; t < rot_dim / 2 && t < 128; ++t) f.w[t] = std::pow(theta, -2.0 * t / rot_dim);
+  for (int t = 0; t < rot_dim / 2 && t < 128; ++t) {
+    f.w[t] = std::pow(theta, -2.0 * t / rot_dim);
+    f.w_hi[t] = (float)f.w[t];
+    f.w_lo[t] = (float)(f.w[t] - (double)f.w_hi[t]);
+  }
   return f;
 }
 
@@ -406,7 +439,11 @@ __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positio
   // The frequencies into shared memory first: read from the parameter space at
   // a different index in every lane, each warp's load would be serialised.
   __shared__ double w_s[128];
-  for (int i = threadIdx.x; i < npairs; i += blockDim.x) w_s[i] = fr.w[i];
+  __shared__ float2 wf_s[128];
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
+    w_s[i] = fr.w[i];
+    wf_s[i] = make_float2(fr.w_hi[i], fr.w_lo[i]);
+  }
   // launched as a programmatic dependent: x and the positions may come from the
   // kernel before this one; the next launch may start setting up at once
   grid_dep_wait();
@@ -427,7 +464,7 @@ __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positio
   for (int u = 0; u < kRopeHeadsInFlight; ++u)
     if (u < heads) xv[u] = Pair<ET>::load(p0 + (size_t)u * hstride);
   float c, s;
-  rope_cos_sin((double)pos, w_s[pr], &c, &s);
+  rope_cos_sin_f(pos, wf_s[pr].x, wf_s[pr].y, w_s[pr], &c, &s);
   for (int h0 = 0; h0 < heads; h0 += kRopeHeadsInFlight) {
     if (h0 > 0) {
 #pragma unroll

@@ -220,6 +220,21 @@ def test_rope_bf16_within_one_ulp(gpu_lib, heads_outer):
     assert rope_close(got, want, xo)
 
 
+def test_rope_positions_around_float_exactness(gpu_lib):
+    """Positions below 2^24 take the angle in fp32 arithmetic (the product formed
+    without error, Cody-Waite reduction), positions from 2^24 on (no longer exact
+    as a float) in fp64: both within the same bound as above."""
+    g = gpu_lib
+    pos = torch.tensor([[0, 1, 7, 4095, 32767, 40000, 99999, 2 ** 20, 2 ** 24 - 2, 2 ** 24 - 1, 2 ** 24, 2 ** 24 + 1,
+                         2 ** 24 + 7, 2 ** 25 + 3, 2 ** 30, 2 ** 31 - 1]], dtype=torch.int32)
+    x = W.randn((1, pos.shape[1], 2, 64), W.generator(45), torch.bfloat16)
+    xg = x.to(DEV)
+    g.attn_rope_interleaved(xg, pos.to(DEV), 1e4)
+    ok(g)
+    want = core.rope_interleaved(W.to_oracle(x), W.to_oracle(pos), 0, 64, 1e4)
+    assert rope_close(W.to_oracle(xg), want, W.to_oracle(x))
+
+
 def test_rope_f32_slice(gpu_lib):
     g = gpu_lib
     x = W.randn((1, 50, 4, 192), W.generator(42), torch.float32)
