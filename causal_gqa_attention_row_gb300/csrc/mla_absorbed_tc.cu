@@ -37,12 +37,16 @@
 // dead, and P_t (16 KiB, no swizzle: each 8-key column of all 128 heads is
 // 2 KiB, so a CTA's half is 4 contiguous pieces) is written over them. So P
 // needs no buffer and no hand-over of its own: the peer copies its columns in
-// only after it has this CTA's tile maxima, which are sent after S_t.
+// only after it has this CTA's tile maxima, which are sent after S_t. The
+// Q_abs blocks bound for TMEM arrive once, by TMA, in the part of the rings
+// that the first tiles do not use (R stages 2 and 3, the V ring); each softmax
+// thread moves its head's row from there into TMEM, and only then do tiles
+// land there. The R ring is filled one tile ahead of the V ring.
 // Roles (192 threads):
 //   warps 0-3  softmax: thread t owns head h0 + t (TMEM lane t); warp w trades
 //              maxima and P columns with warp w of the peer
-//   warp 4     initialises the barriers; TMA producer of the two Q_abs blocks
-//              (once) and of the cache tiles
+//   warp 4     initialises the barriers; TMA producer of Q_abs (once) and of
+//              the cache tiles
 //   warp 5     allocates TMEM; issues the MMAs (one elected lane), S_t as soon
 //              as its rows have landed and S_{t-1} has been read, PV_t once both
 //              halves of P_t and the peer's rows are in place
@@ -93,6 +97,10 @@ struct MlaCfg {
   static constexpr int kOffM = kOffV + kStagesV * kStageV;  // [2][128] maxima by tile parity, then [128] row sums
   static constexpr int kOffBar = kOffM + 3 * kHeads * 4;
   static constexpr int kSmemBytes = kOffBar + 384 + 1023;  // + alignment slack
+  // At the start the kQT Q_abs blocks bound for TMEM land, by TMA, over R
+  // stages 2 and 3 and the V ring; no cache tile is loaded there until every
+  // softmax thread has moved its row into TMEM
+  static constexpr int kOffStage = kOffR + 2 * kStageR;
   // TMEM columns: O, S, then Q_abs's first kQT blocks (32 columns each)
   static constexpr uint32_t kColO = 0, kColS = kDVH, kColQ = kColS + kOwn;
   static_assert(DC % 128 == 0 && DR % 64 == 0, "whole 64-column blocks per half");
@@ -102,6 +110,7 @@ struct MlaCfg {
                 "swizzle atoms on 1024-byte boundaries");
   static_assert(kCBV * kRBlk == kHeads * kKeys * 2, "P fills the other half's value blocks");
   static_assert(kSmemBytes <= 232448, "over the 227 KiB a CTA may use");
+  static_assert(kOffStage % 1024 == 0 && kOffStage + kQT * kQBlk <= kOffM, "Q_abs staging inside the rings");
 };
 
 struct MlaParams {
@@ -121,8 +130,9 @@ struct MlaParams {
 
 struct MlaBars {
   // q_full: Q_abs's shared-memory blocks have landed and every softmax warp has
-  // written its rows of the rest into TMEM
-  uint64_t q_full, r_full[kStagesR], v_full[kStagesV];
+  // written its rows of the rest into TMEM (so their staging area is free);
+  // q_stage: the rest has landed in the staging area
+  uint64_t q_full, q_stage, r_full[kStagesR], v_full[kStagesV];
   // s_full / s_free: S_t is in TMEM / every softmax warp has read it;
   // p_full[x]: P_t is in place (this CTA's four warps and the peer's 8 KiB), t of parity x;
   // o_done[t % kStagesR]: PV_t is done, so O may be rescaled and R stage t % kStagesR
@@ -172,6 +182,10 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
 
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
@@ -285,9 +299,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   float* lbuf = mbuf + 2 * kHeads;                          // [kHeads]: the peer's row sums
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // launched as a programmatic dependent: the lengths and the query may come
-  // from the kernel before this one
-  grid_dep_wait();
   // ---- work item: the pair of one (sequence, head tile, split) is one cluster
   const int half = (int)cluster_rank();
   const uint32_t peer = (uint32_t)(half ^ 1);
@@ -297,25 +308,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int ht = rest % p.n_htiles;
   const int b = rest / p.n_htiles;
   const int h0 = ht * kHeads;
-  const int len = __ldg(p.seq_lens + b);
-  const bool len_ok = len >= 1 && len <= p.max_len;
-  const int n_split = len_ok ? (len + p.chunk - 1) / p.chunk : 1;
-  if (split >= n_split) return;  // no rows in this split: both CTAs leave before any set-up
-  if (!len_ok) {                 // the heads' output is zero and the error word says why
-    if (threadIdx.x == 0 && half == 0 && ht == 0) raise_error(p.err, kErrBounds);
-    for (int idx = threadIdx.x; idx < kHeads * C::kDVH; idx += blockDim.x) {
-      const int h = h0 + idx / C::kDVH;
-      if (h < p.H) p.out[((size_t)b * p.H + h) * DC + half * C::kDVH + idx % C::kDVH] = __float2bfloat16_rn(0.f);
-    }
-    return;
-  }
-  const int k0 = split * p.chunk;
-  const int k1 = min(len, k0 + p.chunk);
-  const int n_t = (k1 - k0 + kKeys - 1) / kKeys;  // >= 1
-
   if (warp == kProducerWarp) {
     if (lane == 0) {
       mbar_init(&bars->q_full, 5);  // the producer's expected bytes + one arrival per softmax warp
+      mbar_init(&bars->q_stage, 1);
       for (int s = 0; s < kStagesR; ++s) {
         mbar_init(&bars->r_full[s], 1);
       }
@@ -336,12 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_r);
       tc::prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, C::kQS * C::kQBlk);
     }
-    __syncwarp();
-    // Q_abs [B, H, W]: its last kQS blocks of rows h0..h0+127 (heads past H read as zeros)
-    if (lane < C::kQS)
-      tc::tma_load_4d(smem + C::kOffQ + lane * C::kQBlk, &tm_q, (C::kQT + lane) * 64, h0, b, 0, &bars->q_full);
   }
   if (warp == kMmaWarp) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -351,6 +342,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers exist before either arrives at the other's
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
+
+  // Launched as a programmatic dependent: the set-up above overlaps the end of
+  // the kernel before this one, which may write the lengths, the query or the
+  // cache; nothing global is read before it is complete.
+  grid_dep_wait();
+  const int len = __ldg(p.seq_lens + b);
+  const bool len_ok = len >= 1 && len <= p.max_len;
+  const int n_split = len_ok ? (len + p.chunk - 1) / p.chunk : 1;
+  if (split >= n_split || !len_ok) {  // both CTAs of the pair (same sequence and split) leave here
+    if (!len_ok) {                     // the heads' output is zero and the error word says why
+      if (threadIdx.x == 0 && half == 0 && ht == 0) raise_error(p.err, kErrBounds);
+      for (int idx = threadIdx.x; idx < kHeads * C::kDVH; idx += blockDim.x) {
+        const int h = h0 + idx / C::kDVH;
+        if (h < p.H) p.out[((size_t)b * p.H + h) * DC + half * C::kDVH + idx % C::kDVH] = __float2bfloat16_rn(0.f);
+      }
+    }
+    if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);  // nothing was issued
+    return;
+  }
+  const int k0 = split * p.chunk;
+  const int k1 = min(len, k0 + p.chunk);
+  const int n_t = (k1 - k0 + kKeys - 1) / kKeys;  // >= 1
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->q_full, C::kQS * C::kQBlk);
+      mbar_arrive_expect_tx(&bars->q_stage, C::kQT * C::kQBlk);
+    }
+    __syncwarp();
+    // Q_abs [B, H, W], rows h0..h0+127 (heads past H read as zeros): its last
+    // kQS blocks where the score MMA reads them, the first kQT into the staging area
+    if (lane < C::kQS)
+      tc::tma_load_4d(smem + C::kOffQ + lane * C::kQBlk, &tm_q, (C::kQT + lane) * 64, h0, b, 0, &bars->q_full);
+    else if (lane < C::kQS + C::kQT)
+      tc::tma_load_4d(smem + C::kOffStage + (lane - C::kQS) * C::kQBlk, &tm_q, (lane - C::kQS) * 64, h0, b, 0,
+                      &bars->q_stage);
+  }
 
   if (warp == kProducerWarp) {
     // ================= TMA producer of the cache tiles =================
@@ -445,6 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (whole) {
       // one box per part: lane 0 runs the loop alone
       if (lane == 0) {
+        const bool skip0 = p.debug_withhold && half == 1;  // test hook: tile 0 is never requested
         // paged: the pool block holding a part's 32 rows starting at `row` (bs
         // >= 32, so one block holds them); a part past the sequence loads from
         // past the end of the pool (zeros). Requested one tile ahead.
@@ -467,49 +496,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           return x.e;
         };
         auto part_row = [&](int t, bool own) { return k0 + t * kKeys + kOwn * (own ? half : 1 - half); };
-        Entry x_own = entry(part_row(0, true)), x_peer = entry(part_row(0, false));
-        for (int t = 0; t < n_t; ++t) {
-          const int e_own = use(x_own), e_peer = use(x_peer);
-          const int tn = min(t + 1, n_t - 1);  // the next tile's entries, in flight during this tile's waits
-          const Entry n_own = entry(part_row(tn, true)), n_peer = entry(part_row(tn, false));
-          // contiguous: row and sequence; paged: slot in the pool block and the block
-          const int own_c1 = p.tables ? part_row(t, true) % p.bs : part_row(t, true);
-          const int peer_c1 = p.tables ? part_row(t, false) % p.bs : part_row(t, false);
-          const bool skip = p.debug_withhold && t == 0 && half == 1;  // test hook: tile 0 is never requested
-          if (!skip) {
-            const int sr = t % kStagesR, sv = t % kStagesV;
-            // a stage is free once PV_{t - stages} is done (o_done completes once per PV)
-            if (t >= kStagesR && !wait_or_abort(&bars->o_done[(t - kStagesR) % kStagesR], ((t - kStagesR) / kStagesR) & 1,
-                                                bars, p.err))
-              break;
-            mbar_arrive_expect_tx(&bars->r_full[sr], C::kStageR);
-            tc::tma_load_4d(smem + C::kOffR + sr * C::kStageR, &tm_r, 0, own_c1, 0, e_own, &bars->r_full[sr]);
-            last_r[sr] = t;
-            if (t >= kStagesV && !wait_or_abort(&bars->o_done[(t - kStagesV) % kStagesR], ((t - kStagesV) / kStagesR) & 1,
-                                                bars, p.err))
-              break;
-            mbar_arrive_expect_tx(&bars->v_full[sv], C::kStageV);
-            tc::tma_load_4d(smem + C::kOffV + sv * C::kStageV, &tm_v, 0, peer_c1, half * C::kCBV, e_peer,
-                            &bars->v_full[sv]);
-            last_v[sv] = t;
-          }
-          x_own = n_own;
-          x_peer = n_peer;
+        auto issue_r = [&](int t, Entry x) -> bool {  // this CTA's rows of tile t
+          const int sr = t % kStagesR;
+          // a stage is free once PV_{t - stages} is done (o_done completes once per PV)
+          if (t >= kStagesR && !wait_or_abort(&bars->o_done[(t - kStagesR) % kStagesR], ((t - kStagesR) / kStagesR) & 1,
+                                              bars, p.err))
+            return false;
+          const int c1 = p.tables ? part_row(t, true) % p.bs : part_row(t, true);
+          mbar_arrive_expect_tx(&bars->r_full[sr], C::kStageR);
+          tc::tma_load_4d(smem + C::kOffR + sr * C::kStageR, &tm_r, 0, c1, 0, use(x), &bars->r_full[sr]);
+          last_r[sr] = t;
+          return true;
+        };
+        auto issue_v = [&](int t, Entry x) -> bool {  // the peer's rows of tile t, this CTA's value blocks
+          const int sv = t % kStagesV;
+          if (t >= kStagesV && !wait_or_abort(&bars->o_done[(t - kStagesV) % kStagesR], ((t - kStagesV) / kStagesR) & 1,
+                                              bars, p.err))
+            return false;
+          const int c1 = p.tables ? part_row(t, false) % p.bs : part_row(t, false);
+          mbar_arrive_expect_tx(&bars->v_full[sv], C::kStageV);
+          tc::tma_load_4d(smem + C::kOffV + sv * C::kStageV, &tm_v, 0, c1, half * C::kCBV, use(x), &bars->v_full[sv]);
+          last_v[sv] = t;
+          return true;
+        };
+        // The R ring runs one tile ahead of the V ring: R_0 and R_1 go out at
+        // once, V_0 and then R_2 onwards land over the Q_abs staging area, so
+        // they wait for q_full. Table entries are requested a step ahead.
+        Entry x_r = entry(part_row(0, true)), x_v = entry(part_row(0, false));
+        bool ok = skip0 || issue_r(0, x_r);
+        x_r = entry(part_row(min(1, n_t - 1), true));
+        for (int t = 0; ok && t < n_t; ++t) {
+          const Entry r_next = x_r, v_cur = x_v;  // R_{t+1}, V_t
+          x_r = entry(part_row(min(t + 2, n_t - 1), true));
+          x_v = entry(part_row(min(t + 1, n_t - 1), false));
+          if (t + 1 < n_t && !issue_r(t + 1, r_next)) break;
+          if (t == 0 && !wait_or_abort(&bars->q_full, 0, bars, p.err)) break;
+          if (!(skip0 && t == 0) && !issue_v(t, v_cur)) break;
         }
       }
       __syncwarp();
     } else {
-      Coords cur = fetch(0);
-      for (int t = 0; t < n_t; ++t) {
-        check(cur);
-        const Coords next = fetch(min(t + 1, n_t - 1));  // in flight during this tile's waits
-        const bool skip = p.debug_withhold && t == 0 && half == 1;  // test hook: tile 0 is never requested
-        if (!skip && (!load_part(t, true, cur.c1, cur.c2) || !load_part(t, false, cur.c1 + 2, cur.c2 + 2))) break;
-        cur = next;
+      // the same order as above: this CTA's rows one tile ahead of the peer's
+      const bool skip0 = p.debug_withhold && half == 1;  // test hook: tile 0 is never requested
+      Coords cur = fetch(0);                     // tile t
+      Coords nxt = fetch(min(1, n_t - 1));       // tile t + 1, in flight
+      check(cur);
+      bool ok = skip0 || load_part(0, true, cur.c1, cur.c2);
+      for (int t = 0; ok && t < n_t; ++t) {
+        const Coords nn = fetch(min(t + 2, n_t - 1));  // in flight during this step's waits
+        check(nxt);
+        if (t + 1 < n_t && !load_part(t + 1, true, nxt.c1, nxt.c2)) break;
+        if (t == 0) {
+          bool g = true;
+          if (lane == 0) g = wait_or_abort(&bars->q_full, 0, bars, p.err);
+          if (!__shfl_sync(0xffffffffu, g, 0)) break;
+        }
+        if (!(skip0 && t == 0) && !load_part(t, false, cur.c1 + 2, cur.c2 + 2)) break;
+        cur = nxt;
+        nxt = nn;
       }
     }
     if (lane == 0) {  // never exit with a load in flight
       if (!mbar_wait(&bars->q_full, 0)) raise_error(p.err, kErrTimeout);
+      if (!mbar_wait(&bars->q_stage, 0)) raise_error(p.err, kErrTimeout);
       for (int s = 0; s < kStagesR; ++s)
         if (last_r[s] >= 0 && !mbar_wait(&bars->r_full[s], (last_r[s] / kStagesR) & 1)) raise_error(p.err, kErrTimeout);
       for (int s = 0; s < kStagesV; ++s)
@@ -628,41 +677,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int h = h0 + r;
     const bool mine = h < p.H;
     // ---- the head's first kQT blocks of Q_abs into TMEM (column c holds
-    // elements 2c and 2c+1), loaded in two rounds of 16-byte reads; heads past
-    // H are zeros
-    {
-      const uint4* row = reinterpret_cast<const uint4*>(p.q_abs + ((size_t)b * p.H + (mine ? h : 0)) * C::kW);
-      constexpr int kVecs = C::kQT * 8;  // 16-byte pieces: 8 per block
-      constexpr int kRound = 32;         // 4 blocks (4 x 32 TMEM columns) per round
+    // elements 2c and 2c+1), from their copies in the staging area. 128-byte
+    // swizzle: piece i (16 bytes) of row r sits at piece i ^ (r % 8) of the
+    // row, so a warp's reads of one piece spread over every bank.
+    bool alive = warp_wait(&bars->q_stage, 0, bars, p.err);
+    if (alive) {
+      const uint32_t qrow = smem_u32(smem + C::kOffStage) + r * 128;
 #pragma unroll
-      for (int v0 = 0; v0 < kVecs; v0 += kRound) {
-        uint32_t w[kRound * 4];
+      for (int g = 0; g < C::kQT; ++g) {
+        uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < kRound; ++i) {
-          const uint4 v = (mine && v0 + i < kVecs) ? __ldg(row + v0 + i) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
-        }
-#pragma unroll
-        for (int c = 0; c < kRound / 8; ++c)
-          if (v0 + c * 8 < kVecs)
-            tc::tmem_st_32x32b_x32(tmem + lane_addr + C::kColQ + (v0 / 8 + c) * 32,
-                                   *reinterpret_cast<uint32_t(*)[32]>(&w[c * 32]));
+        for (int i = 0; i < 8; ++i)
+          ld_shared_v4(qrow + g * C::kQBlk + ((i ^ (r & 7)) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        tc::tmem_st_32x32b_x32(tmem + lane_addr + C::kColQ + g * 32, w);
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->q_full);
+      if (lane == 0) mbar_arrive(&bars->q_full);  // the staging area may be refilled
     }
     const float qs = p.qscale;
     const float th = kRescaleLog2 / qs;
     const float2 qs2 = make_float2(qs, qs);
     const uint32_t tS = tmem + lane_addr + C::kColS;
     float m_ref = -INFINITY, l_own = 0.f;  // l_own: the row sum of this CTA's p
-    bool alive = true;
-    for (int t = 0; t < n_t; ++t) {
+    for (int t = 0; alive && t < n_t; ++t) {
       const int x = t & 1;
       if (!warp_wait(&bars->s_full, t & 1, bars, p.err)) {
         alive = false;
