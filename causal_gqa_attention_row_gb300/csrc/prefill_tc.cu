@@ -153,9 +153,10 @@ __device__ __forceinline__ bool aborted(BarsT* bars) {
   return *reinterpret_cast<volatile int*>(&bars->abort_flag);
 }
 
-// The waits of this kernel sit on its critical path (MMA -> softmax -> MMA):
-// each probe of the mbarrier suspends a waiter for at most this long, so it
-// resumes within tens of nanoseconds of the phase completing.
+// Each probe of an mbarrier suspends a waiter for at most this long. A waiter
+// resumes when the phase completes whatever the hint: 20, 200 and 2000 ns gave
+// the same times (prefill and absorbed MLA decode, same box), so the hint only
+// sets how often a long wait re-checks its time limit and the abort flag.
 constexpr uint32_t kWaitHintNs = 20;
 
 
