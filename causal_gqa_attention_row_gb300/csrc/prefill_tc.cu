@@ -142,6 +142,7 @@ __device__ __forceinline__ int first_key_tile(int pos, int window) {
 struct Bars {
   uint64_t q_full, k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
   uint64_t s_full[kWG], s_free[kWG], p_full[kWG], mma_final[kWG];
+  uint64_t p_half[kWG];  // P over S (d_v = 128): keys 0-63 of the warpgroup's P are in place
   uint64_t o_done[kWG];  // every PV of warpgroup w issued so far is done (a phase per PV)
   uint32_t tmem_base;
   int abort_flag;
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[w], 1);
       mbar_init(&bars->s_free[w], 4);  // one arrival per softmax warp
       mbar_init(&bars->p_full[w], 4);
+      mbar_init(&bars->p_half[w], 4);
       mbar_init(&bars->mma_final[w], 1);
       mbar_init(&bars->o_done[w], 1);
     }
@@ -475,15 +477,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = 2 * k + w;
         // d_v = 64: S_{j+2} as soon as the softmax threads have read S_j into registers
         if (!C::kAlias && k + 1 < n_mine) ok = wait_or_abort(&bars->s_free[w], k & 1, bars, p.err) && issue_s(j + 2);
-        if (!ok || !wait_or_abort(&bars->p_full[w], k & 1, bars, p.err)) break;
+        // P over S (d_v = 128): the first 64 keys' half of PV_j goes out once
+        // their P is in place, while the softmax still forms the rest
+        if (!ok || !wait_or_abort(C::kAlias ? &bars->p_half[w] : &bars->p_full[w], k & 1, bars, p.err)) break;
         const int st = j % kStagesV;
         if (!wait_or_abort(&bars->v_full[st], (j / kStagesV) & 1, bars, p.err)) break;
         tc::fence_after_sync();
         // O_w += P_j V_j: 16 keys per instruction, P from TMEM (8 columns per 16 keys)
         const uint64_t dV = dV0 + (uint64_t)((st * kTileV) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          if (C::kAlias && kk == kBN / 32) {
+            ok = wait_or_abort(&bars->p_full[w], k & 1, bars, p.err);
+            if (!ok) break;
+            tc::fence_after_sync();
+          }
           tc::mma_f16_ts(dO, tP + kk * 8, dV + kk * (2048 >> 4), idO, (k > 0 || kk > 0));
+        }
+        if (!ok) break;
         tc::mma_commit(&bars->o_done[w]);
         tc::mma_commit(&bars->v_empty[st]);
         // d_v = 128: P_j sits in S_w, so S_{j+2} waits for PV_j (this thread waits
@@ -656,8 +667,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 16; ++t)
           pw[c][t] = exp2_pair(__uint_as_float(sv[c][2 * t]), __uint_as_float(sv[c][2 * t + 1]), qs2, nmq2, ls[t & 3]);
         // d_v = 128: P goes over S_j's own first columns, already read; each
-        // 16-word chunk is stored as soon as it is formed
-        if (C::kAlias) tc::tmem_st_32x32b_x16(tP + c * 16, pw[c]);
+        // 16-word chunk is stored as soon as it is formed, and once the first
+        // two (keys 0-63) are in place their half of PV_j may start
+        if (C::kAlias) {
+          tc::tmem_st_32x32b_x16(tP + c * 16, pw[c]);
+          if (c == 1) {
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_half[wg]);
+          }
+        }
       }
       l_run += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
       // ---- d_v = 64: P_w is free once this warpgroup's previous PV has read it.
