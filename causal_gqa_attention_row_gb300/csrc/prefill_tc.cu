@@ -33,10 +33,13 @@
 //
 // Pipeline per warpgroup and key tile j: the softmax threads load their S_j row
 // into registers and release S_w at once, so the MMA thread issues S_{j+2}
-// while the exponentials of tile j are still being computed; P_j is stored into
-// P_w, chunk by chunk as it is formed, once PV_{j-2} (issued a whole tile
-// earlier) has read the previous one (at d_v = 128, once S_w holds S_j that PV
-// is done). K and V have rings of their own: a K stage is free as soon as its S MMA is done,
+// while the exponentials of tile j are still being computed. P_j goes into P_w
+// once PV_{j-2} (issued a whole tile earlier) has read the previous one: at
+// d_v = 64 all of it after the exponentials, which overlap that PV; at d_v = 128
+// (S_w holds S_j only once that PV is done) chunk by chunk as it is formed, its
+// first half (keys 0-63) signalled on a barrier of its own so that the MMA
+// thread issues that half of PV_j while the rest is formed. K and V have rings
+// of their own: a K stage is free as soon as its S MMA is done,
 // a V stage once its PV is. At d_k = 64 they run four tiles ahead, so the load of
 // K_{j+4} has a whole tile-period before S_{j+4} needs it; for wider heads (tiles
 // two or three times the size) two, which the later issue of S leaves enough.
