@@ -9,7 +9,7 @@
 // One CTA = one (sequence, query head, 128-row query tile); CTAs are ordered
 // longest-first (the causal work of a tile grows with its index). Roles, one
 // warpgroup each, with registers moved from the control warpgroup to the two
-// softmax warpgroups (setmaxnreg: 88 and 208 per thread from 168 at launch):
+// softmax warpgroups (setmaxnreg: 72 and 216 per thread from 168 at launch):
 //   warps 0-3   softmax warpgroup 0: key tiles 0, 2, 4, ...
 //   warps 4-7   softmax warpgroup 1: key tiles 1, 3, 5, ...
 //   warp 8      initialises the barriers; TMA producer of Q (once) and of the
@@ -74,9 +74,11 @@ constexpr int kWG = 2;     // softmax warpgroups
 constexpr int kThreads = (kWG + 1) * 128;  // two softmax warpgroups + one control warpgroup
 constexpr int kProducerWarp = 8, kMmaWarp0 = 9, kProducerVWarp = 11;
 // Registers per thread: 168 at launch (384 threads); the control warpgroup
-// gives up 80 per thread and the softmax warpgroups take 40 more:
-// 128 * 88 + 256 * 208 = 384 * 168.
-constexpr int kLaunchRegs = 168, kCtrlRegs = 88, kSoftmaxRegs = 208;
+// gives up 96 per thread and the softmax warpgroups take 48 more:
+// 128 * 72 + 256 * 216 = 384 * 168. (88 / 208 measured the same at d = 64 and
+// d = 128 and up to 1% slower for the arms, the MLA widths and the paged chunks;
+// 56 / 224 the same as 72 / 216.)
+constexpr int kLaunchRegs = 168, kCtrlRegs = 72, kSoftmaxRegs = 216;
 static_assert(128 * kCtrlRegs + kWG * 128 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split over budget");
 constexpr int kBlk = kBM * 128;  // 16 KiB: 128 rows of one 64-column block
 constexpr uint32_t kTmemCols = 512;
