@@ -255,35 +255,73 @@ def run_paged_arms(args, g, c, q, tables, lens, out, ws, lens_after, window=4096
 
 def run_paged_e2e(args, g, c, tables, lens_in, lens_out, out, ws, step_bytes, world):
     """The same step through the public API from pinned host buffers: q, k_new and
-    v_new copied in, the attention output copied back, every step."""
+    v_new copied in, the attention output copied back, every step. The copies run
+    on a stream of their own, pipelined with the compute as a serving loop would:
+    step i + 1's inputs come in and step i's output goes out while step i + 1 /
+    step i compute (two device buffers each, ordered by events); the timed region
+    holds every step's copies in and out."""
     B, H, d = c.q.shape
     Hkv = c.k_new.shape[1]
     gi = W.generator(99)
-    n = args.warmup + args.steps
     hq = [W.randn((B, H, d), gi, torch.bfloat16).pin_memory() for _ in range(2)]
     hk = [W.randn((B, Hkv, d), gi, torch.bfloat16).pin_memory() for _ in range(2)]
     hv = [W.randn((B, Hkv, d), gi, torch.bfloat16).pin_memory() for _ in range(2)]
-    hout = torch.empty(B, H, d, dtype=torch.bfloat16).pin_memory()
-    dq = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
-    dk = torch.empty(B, Hkv, d, dtype=torch.bfloat16, device="cuda")
-    dv = torch.empty(B, Hkv, d, dtype=torch.bfloat16, device="cuda")
+    hout = [torch.empty(B, H, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dq = [torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    dk = [torch.empty(B, Hkv, d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    dv = [torch.empty(B, Hkv, d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    outs = [out, torch.empty_like(out)]
     st = torch.cuda.current_stream()
+    cs = torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]       # step's compute finished with its buffers
+    out_read = [torch.cuda.Event() for _ in range(2)]   # its output is on the host
+    used = [False, False]
 
-    def step(i):
-        dq.copy_(hq[i % 2], non_blocking=True)
-        dk.copy_(hk[i % 2], non_blocking=True)
-        dv.copy_(hv[i % 2], non_blocking=True)
-        g.kv_append_paged(dq, dk, dv, c.k_pool, c.v_pool, tables, lens_in, lens_out, c.theta)
-        g.attn_decode_paged(dq, c.k_pool, c.v_pool, tables, lens_out, out, c.scale, workspace=ws)
-        hout.copy_(out, non_blocking=True)
+    def inputs(i):  # step i's inputs into buffer i % 2, once the step before that used it is done
+        b = i % 2
+        with torch.cuda.stream(cs):
+            if used[b]:
+                cs.wait_event(done[b])
+            dq[b].copy_(hq[b], non_blocking=True)
+            dk[b].copy_(hk[b], non_blocking=True)
+            dv[b].copy_(hv[b], non_blocking=True)
+            in_ready[b].record(cs)
 
-    for i in range(args.warmup):
-        step(i)
+    def steps(first, count):
+        inputs(first)
+        for i in range(first, first + count):
+            b = i % 2
+            st.wait_event(in_ready[b])
+            if used[b]:
+                st.wait_event(out_read[b])  # the output buffer's last copy out is done
+            g.kv_append_paged(dq[b], dk[b], dv[b], c.k_pool, c.v_pool, tables, lens_in, lens_out, c.theta)
+            g.attn_decode_paged(dq[b], c.k_pool, c.v_pool, tables, lens_out, outs[b], c.scale, workspace=ws)
+            done[b].record(st)
+            used[b] = True
+            if i + 1 < first + count:
+                inputs(i + 1)
+            with torch.cuda.stream(cs):
+                cs.wait_event(done[b])
+                hout[b].copy_(outs[b], non_blocking=True)
+                out_read[b].record(cs)
+        st.wait_stream(cs)  # the last output is on the host
+
+    steps(0, args.warmup)
+    torch.cuda.synchronize()
     barrier(world)
-    ms = reduce_over_ranks(timed(step, args.steps, st), world, "max")
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(st)
+    cs.wait_stream(st)  # no copy of the timed steps starts before t0
+    steps(args.warmup, args.steps)
+    t1.record(st)
+    torch.cuda.synchronize()
+    ms = reduce_over_ranks(t0.elapsed_time(t1) / args.steps, world, "max")
     total = reduce_over_ranks(step_bytes, world, "sum")
     return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": (dq.numel() + dk.numel() + dv.numel()) * 2, "d2h_bytes_per_step": out.numel() * 2}
+            "h2d_bytes_per_step": (dq[0].numel() + dk[0].numel() + dv[0].numel()) * 2,
+            "d2h_bytes_per_step": out.numel() * 2,
+            "copies": "own stream, pipelined with the compute (step i+1 in, step i out)"}
 
 
 def gather_paged_sample(c, q, kn, vn, nseq):
