@@ -391,9 +391,8 @@ def run_prefill(args, peaks, peak_kind):
     flops = 2.0 * H * (d + d) * S * (S + 1) / 2  # unmasked (query, key) pairs only
     st = torch.cuda.current_stream()
 
-    def step(i):
-        g.attn_rope_interleaved(qs[i], pos, 1e6)
-        g.attn_rope_interleaved(ks[i], pos, 1e6, heads_outer=True)
+    def step(i):  # RoPE of q and k (one launch), then the prefill
+        g.attn_rope_interleaved_qk(qs[i], ks[i], pos, 1e6, k_heads_outer=True)
         g.attn_prefill_causal(qs[i], ks[i], c.v, out, c.scale)
 
     for i in range(3):

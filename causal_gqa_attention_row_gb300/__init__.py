@@ -25,7 +25,8 @@ EXPORTS = ("attn_prefill_causal", "attn_decode_contig", "attn_decode_paged", "kv
            "gqa_status_string", "gqa_debug_withhold_first_tile", "attn_decode_paged_static_workspace",
            "attn_prefill_causal_ex", "attn_decode_contig_ex", "attn_decode_paged_ex", "attn_prefill_paged",
            "attn_prefill_paged_ex", "mla_absorb_q", "attn_decode_mla_absorbed",
-           "attn_decode_mla_absorbed_workspace_bytes", "mla_unabsorb_out", "attn_decode_mla_absorbed_paged")
+           "attn_decode_mla_absorbed_workspace_bytes", "mla_unabsorb_out", "attn_decode_mla_absorbed_paged",
+           "attn_rope_interleaved_qk")
 
 
 class GqaArms(ctypes.Structure):
@@ -61,6 +62,7 @@ def load(path: str = None):
         "attn_decode_paged_static_workspace": [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P],
         "kv_append_paged": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, I, I, I, P],
         "attn_rope_interleaved": [P, P, I, I, I, I, I, I, I, D, I, P],
+        "attn_rope_interleaved_qk": [P, P, P, I, I, I, I, I, I, I, I, I, D, I, P],
         "attn_get_device_error": [P],
         "attn_prefill_causal_ex": [P, P, P, P, I, I, I, P, I, I, I, I, F, I, P, P],
         "attn_decode_contig_ex": [P, P, P, P, I, P, P, I, I, I, I, I, I, F, I, P, S, P, P],
@@ -309,6 +311,22 @@ def attn_rope_interleaved(x, positions, theta, rot_offset=0, rot_dim=None, heads
                                         rot_offset, rot_dim, float(theta), _dtype(x), _stream(stream)),
            "attn_rope_interleaved")
     return x
+
+
+def attn_rope_interleaved_qk(q, k, positions, theta, rot_offset=0, rot_dim=None, q_heads_outer=False,
+                             k_heads_outer=False, stream=None):
+    """In place, one launch. q [B, T, heads_q, d] (or [B, heads_q, T, d] with
+    q_heads_outer), k likewise; positions int32 [B, T]."""
+    if q_heads_outer:
+        B, hq, T, d = q.shape
+    else:
+        B, T, hq, d = q.shape
+    hk = k.shape[1] if k_heads_outer else k.shape[2]
+    rot_dim = d - rot_offset if rot_dim is None else rot_dim
+    _check(load().attn_rope_interleaved_qk(_p(q), _p(k), _i32(positions), B, T, hq, hk, d, int(bool(q_heads_outer)),
+                                           int(bool(k_heads_outer)), rot_offset, rot_dim, float(theta), _dtype(q),
+                                           _stream(stream)), "attn_rope_interleaved_qk")
+    return q, k
 
 
 def attn_get_device_error(stream=None):

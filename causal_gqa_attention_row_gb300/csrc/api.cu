@@ -355,6 +355,20 @@ gqa_status attn_rope_interleaved(void* x, const int32_t* positions, int B, int T
                                     static_cast<cudaStream_t>(stream)));
 }
 
+gqa_status attn_rope_interleaved_qk(void* q, void* k, const int32_t* positions, int B, int T, int heads_q, int heads_k,
+                                    int d, int q_heads_outer, int k_heads_outer, int rot_offset, int rot_dim,
+                                    double theta, gqa_dtype dt, void* stream) {
+  const int bf16 = dtype_flag(dt);
+  if (bf16 < 0 || B < 0 || T < 0 || heads_q <= 0 || heads_k <= 0 || d <= 0 || d % 2 || rot_dim <= 0 ||
+      rot_dim % 2 || rot_offset < 0 || rot_offset % 2 || rot_offset + rot_dim > d || !(theta > 0.0) ||
+      (q_heads_outer != 0 && q_heads_outer != 1) || (k_heads_outer != 0 && k_heads_outer != 1))
+    return GQA_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return GQA_OK;
+  if (!q || !k || !positions || !aligned16(q) || !aligned16(k)) return GQA_ERR_INVALID_ARG;
+  return from_cuda(gqa::launch_rope(q, positions, B, T, heads_q, d, q_heads_outer, rot_offset, rot_dim, theta, bf16,
+                                    static_cast<cudaStream_t>(stream), k, heads_k, k_heads_outer));
+}
+
 size_t attn_decode_mla_absorbed_workspace_bytes(int B, int H, int d_c, int max_len) {
   if (B <= 0 || H <= 0 || d_c <= 0 || max_len <= 0) return 0;
   const int chunk = gqa::mla_chunk_rows(B, H, max_len);

@@ -79,8 +79,11 @@ constexpr size_t kPlanHeaderBytes = 256;
 inline size_t round_up256(size_t n) { return (n + 255) / 256 * 256; }
 inline size_t plan_bytes(size_t units_max) { return kPlanHeaderBytes + round_up256(units_max * 8); }
 
+// x2 != NULL: a second tensor of the same tokens (heads2 heads, its own layout)
+// turned by the same angles in the same launch.
 cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int heads, int d, int heads_outer,
-                        int rot_offset, int rot_dim, double theta, int bf16, cudaStream_t st);
+                        int rot_offset, int rot_dim, double theta, int bf16, cudaStream_t st, void* x2 = nullptr,
+                        int heads2 = 0, int heads_outer2 = 0);
 
 cudaError_t launch_append(void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                           const int32_t* tables, const int32_t* lens_in, int32_t* lens_out, int B, int mbps,

@@ -431,10 +431,12 @@ struct Pair<float> {
 // sixteen heads' loads in flight at a time (all of them for up to 16 heads),
 // so that a thread waits on memory once per sixteen heads.
 constexpr int kRopeHeadsInFlight = 16;
+constexpr int kRopeHeadsInFlight2 = 4;  // of the second tensor (the k heads of a GQA pair)
 
 template <typename ET>
 __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positions, int B, int T, int heads, int d,
-                                                   int heads_outer, int rot_offset, int rot_dim, const RopeFreqs fr) {
+                                                   int heads_outer, int rot_offset, int rot_dim, const RopeFreqs fr,
+                                                   ET* x2, int heads2, int heads_outer2) {
   const int npairs = rot_dim / 2;
   // The frequencies into shared memory first: read from the parameter space at
   // a different index in every lane, each warp's load would be serialised.
@@ -458,11 +460,19 @@ __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positio
   // head h's pair at p0 + h * hstride ([B, T, heads, d] or, heads outer, [B, heads, T, d])
   const size_t hstride = heads_outer ? (size_t)T * d : (size_t)d;
   ET* p0 = x + (heads_outer ? ((size_t)b * heads * T + t) : (size_t)tok * heads) * d + rot_offset + 2 * pr;
-  // the first heads' pairs are requested before the angle waits on the position
-  float2 xv[kRopeHeadsInFlight];
+  // a second tensor of the same tokens (x2 != NULL) turns by the same angle
+  const size_t hstride2 = heads_outer2 ? (size_t)T * d : (size_t)d;
+  ET* q0 = x2 ? x2 + (heads_outer2 ? ((size_t)b * heads2 * T + t) : (size_t)tok * heads2) * d + rot_offset + 2 * pr
+              : nullptr;
+  // the first heads' pairs (of both tensors) are requested before the angle
+  // waits on the position
+  float2 xv[kRopeHeadsInFlight], xv2[kRopeHeadsInFlight2];
 #pragma unroll
   for (int u = 0; u < kRopeHeadsInFlight; ++u)
     if (u < heads) xv[u] = Pair<ET>::load(p0 + (size_t)u * hstride);
+#pragma unroll
+  for (int u = 0; u < kRopeHeadsInFlight2; ++u)
+    if (q0 && u < heads2) xv2[u] = Pair<ET>::load(q0 + (size_t)u * hstride2);
   float c, s;
   rope_cos_sin_f(pos, wf_s[pr].x, wf_s[pr].y, w_s[pr], &c, &s);
   for (int h0 = 0; h0 < heads; h0 += kRopeHeadsInFlight) {
@@ -477,10 +487,24 @@ __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positio
         Pair<ET>::store(p0 + (size_t)(h0 + u) * hstride, fmaf(xv[u].x, c, -xv[u].y * s),
                         fmaf(xv[u].x, s, xv[u].y * c));
   }
+  if (!q0) return;
+  for (int h0 = 0; h0 < heads2; h0 += kRopeHeadsInFlight2) {
+    if (h0 > 0) {
+#pragma unroll
+      for (int u = 0; u < kRopeHeadsInFlight2; ++u)
+        if (h0 + u < heads2) xv2[u] = Pair<ET>::load(q0 + (size_t)(h0 + u) * hstride2);
+    }
+#pragma unroll
+    for (int u = 0; u < kRopeHeadsInFlight2; ++u)
+      if (h0 + u < heads2)
+        Pair<ET>::store(q0 + (size_t)(h0 + u) * hstride2, fmaf(xv2[u].x, c, -xv2[u].y * s),
+                        fmaf(xv2[u].x, s, xv2[u].y * c));
+  }
 }
 
 cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int heads, int d, int heads_outer,
-                        int rot_offset, int rot_dim, double theta, int bf16, cudaStream_t st) {
+                        int rot_offset, int rot_dim, double theta, int bf16, cudaStream_t st, void* x2, int heads2,
+                        int heads_outer2) {
   const long long total = (long long)B * T * (rot_dim / 2);
   if (total <= 0 || heads <= 0) return cudaSuccess;
   if (rot_dim > 256) return cudaErrorNotSupported;
@@ -495,9 +519,10 @@ cudaError_t launch_rope(void* x, const int32_t* positions, int B, int T, int hea
   cfg.numAttrs = 1;
   if (bf16)
     return cudaLaunchKernelEx(&cfg, rope_kernel<__nv_bfloat16>, reinterpret_cast<__nv_bfloat16*>(x), positions, B, T,
-                              heads, d, heads_outer, rot_offset, rot_dim, fr);
+                              heads, d, heads_outer, rot_offset, rot_dim, fr, reinterpret_cast<__nv_bfloat16*>(x2),
+                              heads2, heads_outer2);
   return cudaLaunchKernelEx(&cfg, rope_kernel<float>, reinterpret_cast<float*>(x), positions, B, T, heads, d,
-                            heads_outer, rot_offset, rot_dim, fr);
+                            heads_outer, rot_offset, rot_dim, fr, reinterpret_cast<float*>(x2), heads2, heads_outer2);
 }
 
 // ---------------------------------------------------------------------------

@@ -280,6 +280,19 @@ gqa_status attn_rope_interleaved(void* x, const int32_t* positions, int B, int T
                                  int heads_outer, int rot_offset, int rot_dim, double theta,
                                  gqa_dtype dt, void* stream);
 
+/*
+ * attn_rope_interleaved on the queries and the keys of the same tokens in one
+ * launch (the prefill's "RoPE on q and k first"): each pair's angle is formed
+ * once and turns every head of both. The results are bit-identical to two
+ * attn_rope_interleaved calls with the same arguments.
+ *   q  q_heads_outer == 0: [B, T, heads_q, d]; 1: [B, heads_q, T, d]  (16-byte aligned)
+ *   k  k_heads_outer == 0: [B, T, heads_k, d]; 1: [B, heads_k, T, d]  (16-byte aligned)
+ * Same positions, slice, theta and dtype for both; q and k must not overlap.
+ */
+gqa_status attn_rope_interleaved_qk(void* q, void* k, const int32_t* positions, int B, int T, int heads_q,
+                                    int heads_k, int d, int q_heads_outer, int k_heads_outer, int rot_offset,
+                                    int rot_dim, double theta, gqa_dtype dt, void* stream);
+
 /* Bytes of workspace attn_decode_contig / attn_decode_paged need for B
  * sequences of at most max_len_upper_bound rows (0 when no sequence that long
  * is split). With S = ceil(max_len_upper_bound / 2048) splits and U = B*H*S:

@@ -246,6 +246,41 @@ def test_rope_f32_slice(gpu_lib):
     assert np.abs(xg.cpu().numpy() - want).max() <= 2e-5
 
 
+@pytest.mark.parametrize("dt,hq,hk,q_outer,k_outer,off,rot", [
+    (torch.bfloat16, 14, 2, False, True, 0, 64),    # the 2048-row prefill's layout and heads
+    (torch.bfloat16, 5, 7, True, False, 0, 64),     # more k heads than in flight at once, both layouts swapped
+    (torch.bfloat16, 20, 1, False, False, 16, 32),  # a partial slice; q heads past the in-flight group
+    (torch.float32, 3, 2, False, True, 128, 64),    # fp32, the MLA-style rope slice of a 192-wide head
+])
+def test_rope_qk_equals_two_calls(gpu_lib, dt, hq, hk, q_outer, k_outer, off, rot):
+    """One launch over q and k gives bit for bit what two attn_rope_interleaved
+    calls give (the same angle per pair and token, the same arithmetic); the k
+    result is also checked against the oracle."""
+    g = gpu_lib
+    B, T = 2, 333
+    d = off + rot if off else 64
+    d = max(d, 64)
+    shape = lambda h, outer: (B, h, T, d) if outer else (B, T, h, d)
+    q = W.randn(shape(hq, q_outer), W.generator(46), dt)
+    k = W.randn(shape(hk, k_outer), W.generator(47), dt)
+    pos = torch.randint(0, 50000, (B, T), generator=W.generator(48), dtype=torch.int32)
+    q1, k1, q2, k2 = q.to(DEV), k.to(DEV), q.to(DEV), k.to(DEV)
+    g.attn_rope_interleaved(q1, pos.to(DEV), 1e6, rot_offset=off, rot_dim=rot, heads_outer=q_outer)
+    g.attn_rope_interleaved(k1, pos.to(DEV), 1e6, rot_offset=off, rot_dim=rot, heads_outer=k_outer)
+    g.attn_rope_interleaved_qk(q2, k2, pos.to(DEV), 1e6, rot_offset=off, rot_dim=rot, q_heads_outer=q_outer,
+                               k_heads_outer=k_outer)
+    ok(g)
+    assert torch.equal(q1, q2) and torch.equal(k1, k2)
+    tok = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3)) if k_outer else a  # to [B, T, heads, d]
+    if dt == torch.bfloat16:  # the oracle's bf16 values, as bits
+        ko = tok(W.to_oracle(k))
+        want = core.rope_interleaved(ko, W.to_oracle(pos), off, rot, 1e6)
+        assert rope_close(tok(W.to_oracle(k2)), want, ko)
+    else:
+        want = core.rope_interleaved(tok(W.to_oracle(k).astype(np.float64)), W.to_oracle(pos), off, rot, 1e6)
+        assert np.abs(tok(k2.cpu().numpy()) - want).max() <= 2e-5
+
+
 def test_append_writes_only_target_slots(gpu_lib):
     g = gpu_lib
     c = W.make_paged(B=6, H=8, Hkv=2, dk=128, dv=128, block_size=16, num_blocks=300, lens=[0, 15, 16, 17, 700, 1],
