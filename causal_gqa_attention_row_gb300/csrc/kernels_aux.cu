@@ -429,7 +429,9 @@ struct Pair<float> {
 
 // One thread per (token, pair): the angle once, then the pair of every head,
 // sixteen heads' loads in flight at a time (all of them for up to 16 heads),
-// so that a thread waits on memory once per sixteen heads.
+// so that a thread waits on memory once per sixteen heads; with a second
+// tensor of the same tokens (the keys beside the queries), its heads' pairs
+// next, turned by the same angle.
 constexpr int kRopeHeadsInFlight = 16;
 constexpr int kRopeHeadsInFlight2 = 4;  // of the second tensor (the k heads of a GQA pair)
 
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positio
   ET* p0 = x + (heads_outer ? ((size_t)b * heads * T + t) : (size_t)tok * heads) * d + rot_offset + 2 * pr;
   // a second tensor of the same tokens (x2 != NULL) turns by the same angle
   const size_t hstride2 = heads_outer2 ? (size_t)T * d : (size_t)d;
-  ET* q0 = x2 ? x2 + (heads_outer2 ? ((size_t)b * heads2 * T + t) : (size_t)tok * heads2) * d + rot_offset + 2 * pr
+  ET* p2 = x2 ? x2 + (heads_outer2 ? ((size_t)b * heads2 * T + t) : (size_t)tok * heads2) * d + rot_offset + 2 * pr
               : nullptr;
   // the first heads' pairs (of both tensors) are requested before the angle
   // waits on the position
@@ -472,7 +474,7 @@ __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positio
     if (u < heads) xv[u] = Pair<ET>::load(p0 + (size_t)u * hstride);
 #pragma unroll
   for (int u = 0; u < kRopeHeadsInFlight2; ++u)
-    if (q0 && u < heads2) xv2[u] = Pair<ET>::load(q0 + (size_t)u * hstride2);
+    if (p2 && u < heads2) xv2[u] = Pair<ET>::load(p2 + (size_t)u * hstride2);
   float c, s;
   rope_cos_sin_f(pos, wf_s[pr].x, wf_s[pr].y, w_s[pr], &c, &s);
   for (int h0 = 0; h0 < heads; h0 += kRopeHeadsInFlight) {
@@ -487,17 +489,17 @@ __global__ void __launch_bounds__(128) rope_kernel(ET* x, const int32_t* positio
         Pair<ET>::store(p0 + (size_t)(h0 + u) * hstride, fmaf(xv[u].x, c, -xv[u].y * s),
                         fmaf(xv[u].x, s, xv[u].y * c));
   }
-  if (!q0) return;
+  if (!p2) return;
   for (int h0 = 0; h0 < heads2; h0 += kRopeHeadsInFlight2) {
     if (h0 > 0) {
 #pragma unroll
       for (int u = 0; u < kRopeHeadsInFlight2; ++u)
-        if (h0 + u < heads2) xv2[u] = Pair<ET>::load(q0 + (size_t)(h0 + u) * hstride2);
+        if (h0 + u < heads2) xv2[u] = Pair<ET>::load(p2 + (size_t)(h0 + u) * hstride2);
     }
 #pragma unroll
     for (int u = 0; u < kRopeHeadsInFlight2; ++u)
       if (h0 + u < heads2)
-        Pair<ET>::store(q0 + (size_t)(h0 + u) * hstride2, fmaf(xv2[u].x, c, -xv2[u].y * s),
+        Pair<ET>::store(p2 + (size_t)(h0 + u) * hstride2, fmaf(xv2[u].x, c, -xv2[u].y * s),
                         fmaf(xv2[u].x, s, xv2[u].y * c));
   }
 }
